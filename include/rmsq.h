@@ -1,0 +1,190 @@
+/*
+ * rmsq.h -- C ABI of librmsq: fused (residual add +) RMSNorm + dynamic
+ * per-token-group activation quantisation on NVIDIA GB300 (sm_103a).
+ *
+ * What a call computes, per row m of an [M, H] bf16 activation:
+ *
+ *   r = bf16(x + residual)            written to out_residual (when a
+ *                                     residual is given; otherwise r = x)
+ *   inv = f32(1 / sqrt(mean(r^2) + eps))
+ *   y = bf16((r * inv) * gamma)       written to out_bf16 when non-NULL
+ *   FP8:   per 1x128 group  scale = amax|y| / 448 (fp32),
+ *          q = e4m3_saturate(y / scale)   (OCP E4M3, round to nearest even)
+ *   MXFP4: per 1x32 group   X = clamp(floor(log2 amax|y|) - 2, -127, 127),
+ *          scale byte = X + 127 (E8M0), q = e2m1_saturate(y * 2^-X),
+ *          two codes per byte, element 2k in the low nibble (OCP MX v1.0)
+ *
+ * Sources: the RMSNorm + group_size=128 FP8 fusion (page "fused rmsnorm
+ * quant fp8 work", Motivation); the ((fp8, scale), residual) and
+ * ((bf16, fp8, scale), residual) outputs and the keep_bf16 switch (sglang PR
+ * "[AMD] Add fused all-reduce RMSNorm per-group quant for Qwen3.5 FP8",
+ * Motivation and Modifications); the MLA q/kv latent norm and the RMSNorm +
+ * MXFP4 fusion (ATOM PR "Support input_rmsnorm_quant & qknorm_quant fused
+ * for Atom dpsk v2 model", Technical Details). An all-zero group gets scale
+ * 0 (E8M0 byte 0x00) and zero codes that keep the sign of the input.
+ *
+ * Conventions for every compute entry point:
+ *  - Pointers are DEVICE pointers owned by the caller; the library allocates
+ *    nothing and keeps no state between calls. bf16 tensors are passed as
+ *    raw 16-bit storage.
+ *  - Inputs x / residual / q_a / kv_a are row-major with a leading dimension
+ *    (ld_*, in elements, >= the row length); outputs are dense row-major.
+ *  - Requirements checked on the host before anything is launched: non-NULL
+ *    required pointers; H a positive multiple of the group; 16-byte aligned
+ *    bf16 base pointers and leading dimensions that are multiples of 8; 16-
+ *    byte aligned q / y outputs; 4-byte aligned fp32 scales; eps finite and
+ *    >= 0; no output overlapping an input or another output, except that
+ *    out_residual may be exactly residual (in-place update, which needs
+ *    ld_res == H). A failed check returns RMSQ_ERR_INVALID_ARG,
+ *    RMSQ_ERR_MISALIGNED or RMSQ_ERR_UNSUPPORTED and launches nothing.
+ *  - M == 0 returns RMSQ_OK without launching.
+ *  - The work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and the call returns without waiting. A launch failure
+ *    returns RMSQ_ERR_CUDA; rmsq_last_error() then holds the CUDA message.
+ */
+#ifndef RMSQ_H
+#define RMSQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rmsq_status {
+    RMSQ_OK = 0,
+    RMSQ_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size, bad enum, overlap */
+    RMSQ_ERR_MISALIGNED = 2,    /* pointer or leading dimension alignment */
+    RMSQ_ERR_UNSUPPORTED = 3,   /* valid but not implemented (e.g. group != 128 for FP8) */
+    RMSQ_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+    RMSQ_ERR_TIMEOUT = 5        /* a bounded device wait gave up (rmsq_sync_status) */
+} rmsq_status;
+
+typedef enum rmsq_scale_layout {
+    RMSQ_SCALE_ROW_MAJOR = 0,   /* scale[m * (H/128) + g]  ([M, H/128]) */
+    RMSQ_SCALE_COL_MAJOR = 1    /* scale[g * M + m]        ([H/128, M], no padding) */
+} rmsq_scale_layout;
+
+/*
+ * Fused residual add + RMSNorm + 1x128 FP8 (E4M3) quantisation.
+ *
+ *   x            [M, ld_x] bf16, row m at x + m*ld_x
+ *   residual     [M, ld_res] bf16, or NULL for no residual add
+ *   gamma        [H] bf16
+ *   eps          added to mean(r^2)
+ *   group        quantisation group; must be 128
+ *   out_q        [M, H] E4M3 bytes
+ *   out_scale    fp32, [M, H/128] or [H/128, M] per scale_layout
+ *   out_residual [M, H] bf16 = bf16(x + residual); required iff residual
+ *   out_bf16     [M, H] bf16 normalised y, or NULL ("keep_bf16" off)
+ *   stream       cudaStream_t
+ */
+rmsq_status rmsq_add_rmsnorm_quant_group_fp8(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, int32_t group, void *out_q, float *out_scale,
+    int32_t scale_layout, void *out_residual, void *out_bf16, void *stream);
+
+/*
+ * One launch normalising and FP8-quantising the two MLA attention latents
+ * (q_a of width Hq, kv_a of width Hkv) with their own gammas; no residual.
+ * Each latent gets exactly what rmsq_add_rmsnorm_quant_group_fp8 with
+ * residual == NULL would give it.
+ *
+ *   q_a [M, ld_q], kv_a [M, ld_kv] bf16 (kv_a may be a column slice of a
+ *   wider projection output); gamma_q [Hq], gamma_kv [Hkv] bf16;
+ *   out_q_q [M, Hq] and out_kv_q [M, Hkv] E4M3; out_q_scale / out_kv_scale
+ *   fp32 in scale_layout; out_q_bf16 / out_kv_bf16 optional bf16 y.
+ */
+rmsq_status rmsq_qknorm_quant_fp8(
+    const void *q_a, int64_t ld_q, const void *kv_a, int64_t ld_kv, const void *gamma_q,
+    const void *gamma_kv, float eps, int64_t M, int64_t Hq, int64_t Hkv, int32_t group,
+    void *out_q_q, float *out_q_scale, void *out_kv_q, float *out_kv_scale,
+    int32_t scale_layout, void *out_q_bf16, void *out_kv_bf16, void *stream);
+
+/*
+ * Fused residual add + RMSNorm + MXFP4 quantisation (group 32).
+ *
+ *   out_q      [M, H/2] bytes, element 2k in the low nibble of byte k
+ *   out_scale  [M, H/32] E8M0 bytes (X + 127), row-major
+ *   other arguments as for the FP8 call; H must be a multiple of 32.
+ */
+rmsq_status rmsq_add_rmsnorm_quant_mxfp4(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, uint8_t *out_q, uint8_t *out_scale, void *out_residual,
+    void *out_bf16, void *stream);
+
+/* ------------------------------------------------------------ utilities */
+
+/* Static description of a status code. */
+const char *rmsq_status_string(rmsq_status s);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char *rmsq_last_error(void);
+
+/*
+ * Waits for `stream`, then reads and clears the library's device status
+ * word on the current device. Returns RMSQ_ERR_TIMEOUT if a kernel launched
+ * since the last read gave up a bounded wait (its outputs are then
+ * incomplete), RMSQ_ERR_CUDA if the synchronisation failed, else RMSQ_OK.
+ */
+rmsq_status rmsq_sync_status(void *stream);
+
+/* ------------------------------------------------- launch control & tests */
+
+typedef enum rmsq_kernel {
+    RMSQ_KERNEL_AUTO = 0,        /* library's choice */
+    RMSQ_KERNEL_ROWS = 1,        /* one team per row, rows loaded into registers */
+    RMSQ_KERNEL_PERSISTENT = 2   /* grid of resident blocks looping over rows, x / residual
+                                    rows double-buffered in shared memory by bulk copies */
+} rmsq_kernel;
+
+/*
+ * Optional launch control for the _ex entry points (NULL = defaults). Every
+ * choice gives bit-identical outputs for the same vectors-per-thread value;
+ * these exist for tests and tuning.
+ *   kernel          rmsq_kernel
+ *   vpt             16-byte vectors per thread: 0 = auto, else one of
+ *                   1, 2, 3, 4, 6, 7, 8 (must divide H/8 so that the team size
+ *                   H/(8*vpt) is a multiple of the group's vector count and
+ *                   either divides 32 or is a multiple of 32, at most 512)
+ *   rows_per_block  0 = auto
+ *   grid            persistent kernel: number of blocks, 0 = auto
+ *   debug_skip_row  persistent kernel: the copy of this row is never issued,
+ *                   so its wait runs out (test of the bounded wait); -1 = off
+ *   wait_limit_ns   persistent kernel: limit of every wait, 0 = 2 s
+ */
+typedef struct rmsq_launch_opts {
+    int32_t kernel;
+    int32_t vpt;
+    int32_t rows_per_block;
+    int32_t grid;
+    int64_t debug_skip_row;
+    int64_t wait_limit_ns;
+} rmsq_launch_opts;
+
+rmsq_status rmsq_add_rmsnorm_quant_group_fp8_ex(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, int32_t group, void *out_q, float *out_scale,
+    int32_t scale_layout, void *out_residual, void *out_bf16, void *stream,
+    const rmsq_launch_opts *opts);
+
+rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, uint8_t *out_q, uint8_t *out_scale, void *out_residual,
+    void *out_bf16, void *stream, const rmsq_launch_opts *opts);
+
+/*
+ * The device encoders the kernels use, applied elementwise to n fp32 values
+ * (device pointers): E4M3 bytes (round to nearest even, saturating; NaN ->
+ * 0x7F/0xFF), and E2M1 codes, one 4-bit code per output byte. They exist so
+ * that the hardware conversions can be checked against an independent
+ * definition.
+ */
+rmsq_status rmsq_encode_e4m3(const float *in, uint8_t *out, int64_t n, void *stream);
+rmsq_status rmsq_encode_e2m1(const float *in, uint8_t *out, int64_t n, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSQ_H */

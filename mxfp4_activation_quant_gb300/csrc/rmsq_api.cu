@@ -1,0 +1,450 @@
+// C ABI of librmsq (include/rmsq.h): host-side argument checks, choice of
+// kernel and team shape, launch, and status reporting. Nothing here
+// allocates device memory; the only device state is the status word that
+// bounded waits report through.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/rmsq.h"
+#include "rmsq_device.cuh"
+#include "rmsq_internal.h"
+
+namespace rmsq {
+
+// Set by a kernel whose bounded wait ran out; read and cleared by
+// rmsq_sync_status.
+__device__ unsigned int g_status_word;
+
+namespace {
+
+thread_local char g_last_error[512];
+
+rmsq_status fail(rmsq_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+rmsq_status ok()
+{
+    g_last_error[0] = 0;
+    return RMSQ_OK;
+}
+
+struct Range {
+    uintptr_t lo, hi;
+};
+
+Range mat_range(const void *p, int64_t M, int64_t H, int64_t ld, int64_t elem)
+{
+    uintptr_t lo = (uintptr_t)p;
+    return Range{lo, lo + (uintptr_t)(((M - 1) * ld + H) * elem)};
+}
+
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Team shape for a row of nvec 16-byte vectors and groups of gv vectors: the
+// smallest legal team (a multiple of gv dividing 32, or a multiple of 32)
+// that holds the row with vpt vectors per thread. `waste` counts the padded
+// vector slots; padding is always whole groups.
+bool team_ok(int64_t nvec, int vpt, int gv, int &tpr, int64_t &waste)
+{
+    if (!vpt_instantiated(vpt))
+        return false;
+    int64_t need = (nvec + vpt - 1) / vpt;
+    int64_t t;
+    if (need <= 32) {
+        t = gv;
+        while (t < need)
+            t <<= 1;
+    } else {
+        t = (need + 31) / 32 * 32;
+    }
+    if (t > kMaxThreads)
+        return false;
+    tpr = (int)t;
+    waste = t * vpt - nvec;
+    return true;
+}
+
+const int kVptPreference[] = {7, 8, 6, 5, 4, 3, 2, 1};
+
+// Exact shapes first, in preference order; otherwise the least padding.
+int pick_vpt(int64_t nvec, int gv, int forced, int &tpr)
+{
+    int64_t waste;
+    if (forced)
+        return team_ok(nvec, forced, gv, tpr, waste) ? forced : 0;
+    int best = 0, best_tpr = 0;
+    int64_t best_waste = -1;
+    for (int v : kVptPreference) {
+        int t;
+        if (!team_ok(nvec, v, gv, t, waste))
+            continue;
+        if (best_waste < 0 || waste < best_waste) {
+            best = v;
+            best_tpr = t;
+            best_waste = waste;
+        }
+    }
+    tpr = best_tpr;
+    return best;
+}
+
+int default_rows_per_block(int tpr) { return tpr >= 256 ? 1 : 256 / tpr; }
+
+const rmsq_launch_opts kDefaultOpts = {RMSQ_KERNEL_AUTO, 0, 0, 0, -1, 0};
+
+struct Checked {
+    int64_t M, H;
+};
+
+// Checks shared by the single-tensor FP8 and MXFP4 calls.
+rmsq_status check_single(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
+                         const void *gamma, float eps, int64_t M, int64_t H, int64_t group,
+                         const void *out_q, int64_t q_bytes_per_row, const void *out_scale,
+                         int64_t scale_bytes, int64_t scale_align, const void *out_residual,
+                         const void *out_bf16)
+{
+    if (M < 0 || H <= 0)
+        return fail(RMSQ_ERR_INVALID_ARG, "M must be >= 0 and H > 0 (M=%lld, H=%lld)",
+                    (long long)M, (long long)H);
+    if (H % group)
+        return fail(RMSQ_ERR_INVALID_ARG, "H=%lld is not a multiple of the group %lld",
+                    (long long)H, (long long)group);
+    if (H > (int64_t)8 * 8 * kMaxThreads)
+        return fail(RMSQ_ERR_UNSUPPORTED, "H=%lld exceeds the largest row (%d)", (long long)H,
+                    8 * 8 * kMaxThreads);
+    if (!(eps >= 0.0f) || !std::isfinite(eps))
+        return fail(RMSQ_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (M == 0)
+        return RMSQ_OK;
+    if (!x || !gamma || !out_q || !out_scale)
+        return fail(RMSQ_ERR_INVALID_ARG, "x, gamma, out_q and out_scale are required");
+    if ((residual == nullptr) != (out_residual == nullptr))
+        return fail(RMSQ_ERR_INVALID_ARG, "out_residual must be given exactly when residual is");
+    if (ld_x < H || (residual && ld_res < H))
+        return fail(RMSQ_ERR_INVALID_ARG, "leading dimensions must be >= H");
+    if (!aligned(x, 16) || !aligned(gamma, 16) || ld_x % 8 || (residual && (!aligned(residual, 16) || ld_res % 8)))
+        return fail(RMSQ_ERR_MISALIGNED,
+                    "bf16 inputs need 16-byte aligned bases and leading dimensions that are multiples of 8");
+    if (!aligned(out_q, 16) || (out_residual && !aligned(out_residual, 16)) ||
+        (out_bf16 && !aligned(out_bf16, 16)) || !aligned(out_scale, (uintptr_t)scale_align))
+        return fail(RMSQ_ERR_MISALIGNED, "outputs need 16-byte aligned bases (scales: element-aligned)");
+
+    Range rx = mat_range(x, M, H, ld_x, 2);
+    Range rg = mat_range(gamma, 1, H, H, 2);
+    Range rq = mat_range(out_q, M, q_bytes_per_row, q_bytes_per_row, 1);
+    Range rs = mat_range(out_scale, 1, scale_bytes, scale_bytes, 1);
+    Range outs[4] = {rq, rs, {0, 0}, {0, 0}};
+    int nout = 2;
+    if (out_bf16)
+        outs[nout++] = mat_range(out_bf16, M, H, H, 2);
+    Range rres_out = {0, 0};
+    if (out_residual) {
+        rres_out = mat_range(out_residual, M, H, H, 2);
+        outs[nout++] = rres_out;
+    }
+    for (int i = 0; i < nout; ++i) {
+        if (overlaps(outs[i], rx) || overlaps(outs[i], rg))
+            return fail(RMSQ_ERR_INVALID_ARG, "an output overlaps x or gamma");
+        for (int j = i + 1; j < nout; ++j)
+            if (overlaps(outs[i], outs[j]))
+                return fail(RMSQ_ERR_INVALID_ARG, "two outputs overlap");
+    }
+    if (residual) {
+        Range rr = mat_range(residual, M, H, ld_res, 2);
+        bool in_place = out_residual == residual;
+        if (in_place && ld_res != H)
+            return fail(RMSQ_ERR_INVALID_ARG, "in-place residual update needs ld_res == H");
+        for (int i = 0; i < nout; ++i) {
+            if (in_place && outs[i].lo == rres_out.lo && outs[i].hi == rres_out.hi)
+                continue;
+            if (overlaps(outs[i], rr))
+                return fail(RMSQ_ERR_INVALID_ARG, "an output overlaps the residual input");
+        }
+    }
+    return RMSQ_OK;
+}
+
+Seg make_seg(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
+             const void *gamma, float eps, int64_t M, int64_t H, void *out_q, void *out_scale,
+             int32_t layout, void *out_residual, void *out_bf16)
+{
+    Seg s{};
+    s.x = (const uint4 *)x;
+    s.res = (const uint4 *)residual;
+    s.gamma = (const uint4 *)gamma;
+    s.out_res = (uint4 *)out_residual;
+    s.out_bf16 = (uint4 *)out_bf16;
+    s.out_q = (uint8_t *)out_q;
+    s.out_scale = out_scale;
+    s.M = M;
+    s.ldx_v = ld_x / 8;
+    s.ldres_v = residual ? ld_res / 8 : 0;
+    s.H = (int32_t)H;
+    s.layout = layout;
+    s.eps = eps;
+    return s;
+}
+
+rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_t st)
+{
+    const int gv = mx ? 4 : 16;
+    int tpr = 0;
+    int vpt = pick_vpt(s.H / 8, gv, o.vpt, tpr);
+    if (!vpt)
+        return fail(RMSQ_ERR_UNSUPPORTED, "no team shape for H=%d with vpt=%d", s.H, o.vpt);
+    s.tpr = tpr;
+    int kernel = o.kernel == RMSQ_KERNEL_AUTO ? RMSQ_KERNEL_ROWS : o.kernel;
+    if (kernel == RMSQ_KERNEL_ROWS) {
+        int rpb = o.rows_per_block > 0 ? o.rows_per_block : default_rows_per_block(tpr);
+        if ((int64_t)rpb * tpr > kMaxThreads || (tpr > 32 && rpb > 15))
+            return fail(RMSQ_ERR_INVALID_ARG, "rows_per_block=%d too large for %d threads per row",
+                        rpb, tpr);
+        s.rpb = rpb;
+        int64_t blocks = (s.M + rpb - 1) / rpb;
+        if (blocks > 0x7fffffff)
+            return fail(RMSQ_ERR_UNSUPPORTED, "M too large");
+        s.blocks = (int32_t)blocks;
+        LaunchParams p{};
+        p.seg[0] = s;
+        p.nseg = 1;
+        cudaError_t e = mx ? launch_rows_mx(vpt, p, (int)blocks, rpb * tpr, st)
+                           : launch_rows_fp8(vpt, p, (int)blocks, rpb * tpr, st);
+        if (e != cudaSuccess)
+            return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+        return ok();
+    }
+    return fail(RMSQ_ERR_UNSUPPORTED, "kernel %d is not available", o.kernel);
+}
+
+// ------------------------------------------------------- encoder kernels
+
+__global__ void encode_e4m3_kernel(const float *in, uint8_t *out, int64_t n)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = (uint8_t)(e4m3x2(in[i], 0.0f) & 0xffu);
+}
+
+__global__ void encode_e2m1_kernel(const float *in, uint8_t *out, int64_t n)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = (uint8_t)(e2m1x2(in[i], 0.0f) & 0xfu);
+}
+
+}  // namespace
+}  // namespace rmsq
+
+using namespace rmsq;
+
+extern "C" {
+
+const char *rmsq_status_string(rmsq_status s)
+{
+    switch (s) {
+    case RMSQ_OK: return "ok";
+    case RMSQ_ERR_INVALID_ARG: return "invalid argument";
+    case RMSQ_ERR_MISALIGNED: return "misaligned pointer or leading dimension";
+    case RMSQ_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case RMSQ_ERR_CUDA: return "CUDA error";
+    case RMSQ_ERR_TIMEOUT: return "a bounded device wait timed out";
+    }
+    return "unknown status";
+}
+
+const char *rmsq_last_error(void) { return g_last_error; }
+
+rmsq_status rmsq_add_rmsnorm_quant_group_fp8_ex(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, int32_t group, void *out_q, float *out_scale,
+    int32_t scale_layout, void *out_residual, void *out_bf16, void *stream,
+    const rmsq_launch_opts *opts)
+{
+    if (group != 128)
+        return fail(group > 0 ? RMSQ_ERR_UNSUPPORTED : RMSQ_ERR_INVALID_ARG,
+                    "FP8 group must be 128 (got %d)", group);
+    if (scale_layout != RMSQ_SCALE_ROW_MAJOR && scale_layout != RMSQ_SCALE_COL_MAJOR)
+        return fail(RMSQ_ERR_INVALID_ARG, "unknown scale layout %d", scale_layout);
+    rmsq_status st = check_single(x, ld_x, residual, ld_res, gamma, eps, M, H, group, out_q, H,
+                                  out_scale, (H / group) * M * 4, 4, out_residual, out_bf16);
+    if (st != RMSQ_OK || M == 0)
+        return st == RMSQ_OK ? ok() : st;
+    Seg s = make_seg(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q, out_scale, scale_layout,
+                     out_residual, out_bf16);
+    return launch_single(s, false, opts ? *opts : kDefaultOpts, (cudaStream_t)stream);
+}
+
+rmsq_status rmsq_add_rmsnorm_quant_group_fp8(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, int32_t group, void *out_q, float *out_scale,
+    int32_t scale_layout, void *out_residual, void *out_bf16, void *stream)
+{
+    return rmsq_add_rmsnorm_quant_group_fp8_ex(x, ld_x, residual, ld_res, gamma, eps, M, H, group,
+                                               out_q, out_scale, scale_layout, out_residual,
+                                               out_bf16, stream, nullptr);
+}
+
+rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, uint8_t *out_q, uint8_t *out_scale, void *out_residual,
+    void *out_bf16, void *stream, const rmsq_launch_opts *opts)
+{
+    rmsq_status st = check_single(x, ld_x, residual, ld_res, gamma, eps, M, H, 32, out_q, H / 2,
+                                  out_scale, (H / 32) * M, 1, out_residual, out_bf16);
+    if (st != RMSQ_OK || M == 0)
+        return st == RMSQ_OK ? ok() : st;
+    Seg s = make_seg(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q, out_scale, 0,
+                     out_residual, out_bf16);
+    return launch_single(s, true, opts ? *opts : kDefaultOpts, (cudaStream_t)stream);
+}
+
+rmsq_status rmsq_add_rmsnorm_quant_mxfp4(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, uint8_t *out_q, uint8_t *out_scale, void *out_residual,
+    void *out_bf16, void *stream)
+{
+    return rmsq_add_rmsnorm_quant_mxfp4_ex(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q,
+                                           out_scale, out_residual, out_bf16, stream, nullptr);
+}
+
+rmsq_status rmsq_qknorm_quant_fp8(
+    const void *q_a, int64_t ld_q, const void *kv_a, int64_t ld_kv, const void *gamma_q,
+    const void *gamma_kv, float eps, int64_t M, int64_t Hq, int64_t Hkv, int32_t group,
+    void *out_q_q, float *out_q_scale, void *out_kv_q, float *out_kv_scale,
+    int32_t scale_layout, void *out_q_bf16, void *out_kv_bf16, void *stream)
+{
+    if (group != 128)
+        return fail(group > 0 ? RMSQ_ERR_UNSUPPORTED : RMSQ_ERR_INVALID_ARG,
+                    "FP8 group must be 128 (got %d)", group);
+    if (scale_layout != RMSQ_SCALE_ROW_MAJOR && scale_layout != RMSQ_SCALE_COL_MAJOR)
+        return fail(RMSQ_ERR_INVALID_ARG, "unknown scale layout %d", scale_layout);
+    rmsq_status st = check_single(q_a, ld_q, nullptr, 0, gamma_q, eps, M, Hq, group, out_q_q, Hq,
+                                  out_q_scale, (Hq / group) * M * 4, 4, nullptr, out_q_bf16);
+    if (st != RMSQ_OK)
+        return st;
+    st = check_single(kv_a, ld_kv, nullptr, 0, gamma_kv, eps, M, Hkv, group, out_kv_q, Hkv,
+                      out_kv_scale, (Hkv / group) * M * 4, 4, nullptr, out_kv_bf16);
+    if (st != RMSQ_OK)
+        return st;
+    if (M == 0)
+        return ok();
+    // the two latents' outputs must not overlap each other or the other's inputs
+    Range a[4] = {mat_range(out_q_q, M, Hq, Hq, 1), mat_range(out_q_scale, 1, (Hq / 128) * M * 4, 0, 1),
+                  {0, 0}, {0, 0}};
+    Range b[4] = {mat_range(out_kv_q, M, Hkv, Hkv, 1),
+                  mat_range(out_kv_scale, 1, (Hkv / 128) * M * 4, 0, 1), {0, 0}, {0, 0}};
+    int na = 2, nb = 2;
+    if (out_q_bf16)
+        a[na++] = mat_range(out_q_bf16, M, Hq, Hq, 2);
+    if (out_kv_bf16)
+        b[nb++] = mat_range(out_kv_bf16, M, Hkv, Hkv, 2);
+    Range in_q = mat_range(q_a, M, Hq, ld_q, 2), in_kv = mat_range(kv_a, M, Hkv, ld_kv, 2);
+    Range g_q = mat_range(gamma_q, 1, Hq, Hq, 2), g_kv = mat_range(gamma_kv, 1, Hkv, Hkv, 2);
+    for (int i = 0; i < na; ++i) {
+        if (overlaps(a[i], in_kv) || overlaps(a[i], g_kv))
+            return fail(RMSQ_ERR_INVALID_ARG, "a q_a output overlaps a kv_a input");
+        for (int j = 0; j < nb; ++j)
+            if (overlaps(a[i], b[j]))
+                return fail(RMSQ_ERR_INVALID_ARG, "q_a and kv_a outputs overlap");
+    }
+    for (int j = 0; j < nb; ++j)
+        if (overlaps(b[j], in_q) || overlaps(b[j], g_q))
+            return fail(RMSQ_ERR_INVALID_ARG, "a kv_a output overlaps a q_a input");
+
+    Seg sq = make_seg(q_a, ld_q, nullptr, 0, gamma_q, eps, M, Hq, out_q_q, out_q_scale,
+                      scale_layout, nullptr, out_q_bf16);
+    Seg sk = make_seg(kv_a, ld_kv, nullptr, 0, gamma_kv, eps, M, Hkv, out_kv_q, out_kv_scale,
+                      scale_layout, nullptr, out_kv_bf16);
+    // one vectors-per-thread value serves both latents: least padding first
+    int vpt = 0, tq = 0, tk = 0;
+    int64_t best_waste = -1;
+    for (int v : kVptPreference) {
+        int a, b;
+        int64_t wa, wb;
+        if (team_ok(Hq / 8, v, 16, a, wa) && team_ok(Hkv / 8, v, 16, b, wb) &&
+            (best_waste < 0 || wa + wb < best_waste)) {
+            vpt = v;
+            tq = a;
+            tk = b;
+            best_waste = wa + wb;
+        }
+    }
+    if (!vpt)
+        return fail(RMSQ_ERR_UNSUPPORTED, "no common team shape for Hq=%lld, Hkv=%lld",
+                    (long long)Hq, (long long)Hkv);
+    int threads = default_rows_per_block(tq) * tq;
+    int tk_threads = default_rows_per_block(tk) * tk;
+    if (tk_threads > threads)
+        threads = tk_threads;
+    sq.tpr = tq;
+    sk.tpr = tk;
+    sq.rpb = threads / tq;
+    sk.rpb = threads / tk;
+    if ((tq > 32 && sq.rpb > 15) || (tk > 32 && sk.rpb > 15))
+        return fail(RMSQ_ERR_UNSUPPORTED, "team shape needs too many named barriers");
+    int64_t bq = (M + sq.rpb - 1) / sq.rpb, bk = (M + sk.rpb - 1) / sk.rpb;
+    if (bq + bk > 0x7fffffff)
+        return fail(RMSQ_ERR_UNSUPPORTED, "M too large");
+    sq.blocks = (int32_t)bq;
+    sk.blocks = (int32_t)bk;
+    LaunchParams p{};
+    p.seg[0] = sq;
+    p.seg[1] = sk;
+    p.nseg = 2;
+    cudaError_t e = launch_rows_fp8(vpt, p, (int)(bq + bk), threads, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+rmsq_status rmsq_sync_status(void *stream)
+{
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return fail(RMSQ_ERR_CUDA, "synchronize failed: %s", cudaGetErrorString(e));
+    unsigned int word = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof word);
+    if (e == cudaSuccess && word)
+        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
+    if (e != cudaSuccess)
+        return fail(RMSQ_ERR_CUDA, "status word access failed: %s", cudaGetErrorString(e));
+    if (word)
+        return fail(RMSQ_ERR_TIMEOUT, "a bounded wait gave up (status 0x%x)", word);
+    return ok();
+}
+
+rmsq_status rmsq_encode_e4m3(const float *in, uint8_t *out, int64_t n, void *stream)
+{
+    if (n < 0 || (n && (!in || !out)))
+        return fail(RMSQ_ERR_INVALID_ARG, "bad encoder arguments");
+    if (n == 0)
+        return ok();
+    int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    encode_e4m3_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(in, out, n);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ok() : fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+}
+
+rmsq_status rmsq_encode_e2m1(const float *in, uint8_t *out, int64_t n, void *stream)
+{
+    if (n < 0 || (n && (!in || !out)))
+        return fail(RMSQ_ERR_INVALID_ARG, "bad encoder arguments");
+    if (n == 0)
+        return ok();
+    int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    encode_e2m1_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(in, out, n);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ok() : fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Host/device descriptors shared by the C-ABI layer and the kernel units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rmsq {
+
+// One tensor (a "segment") handled by a launch. A launch covers one segment,
+// or two for the MLA q_a / kv_a latent pair. Pointers to bf16 rows are given
+// as 16-byte vectors of 8 bf16 values; leading dimensions are in vectors.
+struct Seg {
+    const uint4 *x;        // [M, ldx_v] bf16 rows
+    const uint4 *res;      // nullable: [M, ldres_v] bf16 residual rows
+    const uint4 *gamma;    // [H] bf16
+    uint4 *out_res;        // [M, H] bf16 (required iff res)
+    uint4 *out_bf16;       // nullable: [M, H] bf16 normalised y
+    uint8_t *out_q;        // FP8: [M, H] e4m3; MXFP4: [M, H/2] packed e2m1
+    void *out_scale;       // FP8: fp32 [M, H/128] or [H/128, M]; MXFP4: e8m0 [M, H/32]
+    int64_t M;
+    int64_t ldx_v, ldres_v;
+    int32_t H;
+    int32_t tpr;           // threads per row (a "team")
+    int32_t rpb;           // rows (teams) per block
+    int32_t blocks;        // blocks of the row kernel that belong to this segment
+    int32_t layout;        // 0 row-major scales, 1 column-major
+    float eps;
+};
+
+struct LaunchParams {
+    Seg seg[2];
+    int32_t nseg;
+};
+
+// Persistent bulk-copy kernel: one segment, one row per team, rows strided
+// by the grid, x / residual rows staged through shared memory.
+struct BulkParams {
+    Seg s;
+    int64_t debug_skip_row;   // -1 normally; a row whose copy is never issued
+    int64_t wait_limit_ns;    // bound on every mbarrier wait
+    unsigned int *status;     // device status word (set on a timed-out wait)
+};
+
+constexpr int kMaxThreads = 512;
+
+// Launchers (one switch over the vectors-per-thread instantiations each).
+cudaError_t launch_rows_fp8(int vpt, const LaunchParams &p, int grid, int threads, cudaStream_t st);
+cudaError_t launch_rows_mx(int vpt, const LaunchParams &p, int grid, int threads, cudaStream_t st);
+cudaError_t launch_bulk_fp8(int vpt, const BulkParams &p, int grid, int threads, size_t smem,
+                            cudaStream_t st);
+cudaError_t launch_bulk_mx(int vpt, const BulkParams &p, int grid, int threads, size_t smem,
+                           cudaStream_t st);
+bool vpt_instantiated(int vpt);
+
+}  // namespace rmsq

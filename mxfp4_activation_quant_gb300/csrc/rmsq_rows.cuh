@@ -1,0 +1,230 @@
+// Per-row body of the fused (add +) RMSNorm + group quant, shared by the
+// register-resident row kernel and the persistent bulk-copy kernel.
+//
+// Layout of work: a row of H bf16 values is split into H/8 16-byte vectors;
+// a team of `tpr` threads owns a row and thread t holds vectors
+// k*tpr + t (k < VPT), so every load and store of a warp is a contiguous,
+// coalesced span. tpr is a multiple of the group's vector count (16 for
+// 1x128 FP8, 4 for MXFP4's 32), so a quant group is held by 16 (or 4)
+// consecutive lanes at the same k and its amax is a 4- (or 2-) step xor
+// shuffle. tpr is either a divisor of 32 (several rows per warp) or a
+// multiple of 32 (rows spanning warps, combined through shared memory with a
+// per-team named barrier). When tpr * VPT exceeds H/8 the team is padded:
+// the vectors past the row end are whole groups (both counts are multiples
+// of the group's vector count), read as zero and never stored.
+//
+// What a row computes (page "fused rmsnorm quant fp8 work", Motivation;
+// sglang PR "[AMD] Add fused all-reduce RMSNorm per-group quant for Qwen3.5
+// FP8", Modifications; ATOM PR "Support input_rmsnorm_quant & qknorm_quant
+// fused for Atom dpsk v2 model", Technical Details):
+//   r = bf16(x + residual)                     -> residual output
+//   inv = f32(1 / sqrt(sum(r^2) / H + eps))
+//   y = bf16((r * inv) * gamma)                -> optional bf16 output
+//   FP8:   scale = amax_128(|y|) / 448, q = e4m3_satfinite(y / scale)
+//   MXFP4: X = clamp(floor(log2 amax_32) - 2, -127, 127), byte X + 127,
+//          q = e2m1_satfinite(y * 2^-X), two per byte, even element low.
+#pragma once
+
+#include "rmsq_device.cuh"
+#include "rmsq_internal.h"
+
+namespace rmsq {
+
+struct RedSmem {
+    float2 part[2][32];   // per-warp double-float partials, two parity sets
+    double dpart[32];     // per-warp fp64 partials for the wide-range path
+};
+
+__device__ __forceinline__ unsigned team_lane_mask(int tpr, int lane)
+{
+    if (tpr >= 32)
+        return 0xffffffffu;
+    unsigned m = (1u << tpr) - 1u;
+    return m << (lane & ~(tpr - 1));
+}
+
+// Barrier over the `tpr` threads of one team (tpr a multiple of 32):
+// named barrier 1 + team; barrier 0 stays with __syncthreads.
+__device__ __forceinline__ void team_bar(int team, int tpr)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(team + 1), "r"(tpr) : "memory");
+}
+
+// bf16 magnitude bits -> the MX shared exponent X (unbiased), clamped to
+// [-127, 127]; zero gives -127. floor(log2) is read from the exponent field,
+// or from the leading mantissa bit for bf16 subnormals (m * 2^-133).
+__device__ __forceinline__ int mx_exponent_from_bits(uint32_t a)
+{
+    if (a == 0)
+        return -127;
+    int E = (int)(a >> 7);
+    int fl = E ? E - 127 : (31 - __clz((int)(a & 0x7fu))) - 133;
+    return min(127, max(-127, fl - 2));
+}
+
+// Team-wide fp64 sum of squares and fp64 finalisation, for rows whose sum
+// lies outside the fp32 range in which the double-float path is exact.
+template <int VPT>
+__device__ __forceinline__ float inv_rms_fp64_path(const uint4 (&r)[VPT], int H, float eps, int tpr,
+                                                   int team, RedSmem &red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned tmask = team_lane_mask(tpr, lane);
+    double acc = 0.0;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const uint32_t w[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            double a = (double)bf_lo(w[j]), b = (double)bf_hi(w[j]);
+            acc = __fma_rn(a, a, acc);
+            acc = __fma_rn(b, b, acc);
+        }
+    }
+    const int wlim = tpr < 32 ? tpr : 32;
+    for (int off = 1; off < wlim; off <<= 1)
+        acc += __shfl_xor_sync(tmask, acc, off);
+    if (tpr > 32) {
+        const int nw = tpr >> 5, w0 = team * nw;
+        if (lane == 0)
+            red.dpart[warp] = acc;
+        team_bar(team, tpr);
+        acc = red.dpart[w0];
+        for (int i = 1; i < nw; ++i)
+            acc += red.dpart[w0 + i];
+        team_bar(team, tpr);
+    }
+    return (float)(1.0 / sqrt(acc / (double)H + (double)eps));
+}
+
+// Everything after the row is loaded: r holds the thread's VPT vectors of
+// bf16 r (residual already added and written back by the caller). gamma is
+// read from shared memory (GAMMA_SHARED) or through the read-only cache.
+template <int VPT, bool MX, bool GAMMA_SHARED>
+__device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int team, int parity,
+                                           RedSmem &red, const uint4 (&r)[VPT],
+                                           const uint4 *gamma_src)
+{
+    constexpr int GV = MX ? 4 : 16;   // 16-byte vectors per quant group
+    const int tpr = s.tpr;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned tmask = team_lane_mask(tpr, lane);
+    const int nvec = s.H >> 3;
+
+    // ---- sum of squares: exact squares, double-float accumulation
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        acc_square(bf_lo(r[k].x), hi, lo);
+        acc_square(bf_hi(r[k].x), hi, lo);
+        acc_square(bf_lo(r[k].y), hi, lo);
+        acc_square(bf_hi(r[k].y), hi, lo);
+        acc_square(bf_lo(r[k].z), hi, lo);
+        acc_square(bf_hi(r[k].z), hi, lo);
+        acc_square(bf_lo(r[k].w), hi, lo);
+        acc_square(bf_hi(r[k].w), hi, lo);
+    }
+    DF S{hi, lo};
+    const int wlim = tpr < 32 ? tpr : 32;
+    for (int off = 1; off < wlim; off <<= 1)
+        S = df_add(S, shfl_xor_df(S, off, tmask));   // identical in every lane
+    if (tpr > 32) {
+        const int nw = tpr >> 5, w0 = team * nw;
+        if (lane == 0)
+            red.part[parity][warp] = make_float2(S.hi, S.lo);
+        team_bar(team, tpr);
+        float2 p0 = red.part[parity][w0];
+        S = DF{p0.x, p0.y};
+        for (int i = 1; i < nw; ++i) {
+            float2 pi = red.part[parity][w0 + i];
+            S = df_add(S, DF{pi.x, pi.y});
+        }
+    }
+    float inv;
+    if (!inv_rms_df(S, s.H, s.eps, inv))     // team-uniform branch
+        inv = inv_rms_fp64_path<VPT>(r, s.H, s.eps, tpr, team, red);
+
+    // ---- normalise: y = bf16((r * inv) * gamma)
+    uint4 y[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int vk = k * tpr + t;
+        const uint4 g = vk >= nvec ? make_uint4(0, 0, 0, 0)
+                        : GAMMA_SHARED ? gamma_src[vk] : ld_keep(gamma_src + vk);
+        const uint32_t rw[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+        uint32_t yw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float a = __fmul_rn(__fmul_rn(bf_lo(rw[j]), inv), bf_lo(gw[j]));
+            float b = __fmul_rn(__fmul_rn(bf_hi(rw[j]), inv), bf_hi(gw[j]));
+            yw[j] = pack_bf16x2(a, b);
+        }
+        y[k] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+    }
+    if (s.out_bf16) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+            if (k * tpr + t < nvec)
+                s.out_bf16[row * nvec + k * tpr + t] = y[k];
+    }
+
+    // ---- group amax over GV lanes (two vectors packed per shuffle)
+    uint32_t am[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+        am[k] = amax_bits_bf16x8(y[k]);
+#pragma unroll
+    for (int k = 0; k < VPT; k += 2) {
+        uint32_t v = am[k] | ((k + 1 < VPT) ? (am[k + 1] << 16) : 0u);
+#pragma unroll
+        for (int off = 1; off < GV; off <<= 1)
+            v = max_u16x2(v, __shfl_xor_sync(tmask, v, off));
+        am[k] = v & 0xffffu;
+        if (k + 1 < VPT)
+            am[k + 1] = v >> 16;
+    }
+
+    // ---- quantise and store
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = k * tpr + t;   // vector index in the row
+        if (v >= nvec)
+            continue;                // padding of the team shape (whole groups)
+        const uint32_t yw[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
+        if constexpr (!MX) {
+            const float amax = __uint_as_float(am[k] << 16);
+            const float scale = __fdiv_rn(amax, 448.0f);
+            const float d = am[k] ? scale : 1.0f;   // all-zero group: codes of +-0
+            if ((t & 15) == 0) {
+                const int64_t g = v >> 4, G = s.H >> 7;   // v is a multiple of 16 here
+                float *sc = (float *)s.out_scale;
+                if (s.layout == 0)
+                    sc[row * G + g] = scale;
+                else
+                    sc[g * s.M + row] = scale;
+            }
+            uint32_t c[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                c[j] = e4m3x2(__fdiv_rn(bf_lo(yw[j]), d), __fdiv_rn(bf_hi(yw[j]), d));
+            uint2 q = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+            *reinterpret_cast<uint2 *>(s.out_q + row * (int64_t)s.H + (int64_t)v * 8) = q;
+        } else {
+            const int X = mx_exponent_from_bits(am[k]);
+            const float mult = __uint_as_float((uint32_t)(127 - X) << 23);   // 2^-X
+            if ((t & 3) == 0) {
+                uint8_t *sc = (uint8_t *)s.out_scale;
+                sc[row * (int64_t)(s.H >> 5) + (v >> 2)] = (uint8_t)(X + 127);
+            }
+            uint32_t c[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                c[j] = e2m1x2(__fmul_rn(bf_lo(yw[j]), mult), __fmul_rn(bf_hi(yw[j]), mult));
+            uint32_t q = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+            *reinterpret_cast<uint32_t *>(s.out_q + row * (int64_t)(s.H >> 1) + (int64_t)v * 4) = q;
+        }
+    }
+}
+
+}  // namespace rmsq

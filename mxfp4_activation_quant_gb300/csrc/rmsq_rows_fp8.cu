@@ -1,0 +1,16 @@
+// Row-kernel instantiations for the 1x128 FP8 E4M3 quantiser.
+#include "rmsq_rowkernel.cuh"
+
+namespace rmsq {
+
+cudaError_t launch_rows_fp8(int vpt, const LaunchParams &p, int grid, int threads, cudaStream_t st)
+{
+    return launch_rows_impl<false>(vpt, p, grid, threads, st);
+}
+
+bool vpt_instantiated(int vpt)
+{
+    return vpt >= 1 && vpt <= 8;
+}
+
+}  // namespace rmsq

@@ -1,0 +1,217 @@
+"""Python binding of librmsq (include/rmsq.h): argument marshalling only.
+
+torch supplies device memory and the current stream; every step of the
+computation runs in the library's CUDA kernels. The shared library must have
+been built (``python -m mxfp4_activation_quant_gb300.build``); without it
+every call raises -- there is no other implementation to fall back to.
+
+Return values follow the tuple forms of sglang PR "[AMD] Add fused
+all-reduce RMSNorm per-group quant for Qwen3.5 FP8" (Modifications):
+``((q, scale), residual)`` or, with ``keep_bf16``, ``((y, q, scale), residual)``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "librmsq.so")
+
+RMSQ_OK = 0
+STATUS_NAMES = {0: "RMSQ_OK", 1: "RMSQ_ERR_INVALID_ARG", 2: "RMSQ_ERR_MISALIGNED",
+                3: "RMSQ_ERR_UNSUPPORTED", 4: "RMSQ_ERR_CUDA", 5: "RMSQ_ERR_TIMEOUT"}
+KERNEL_AUTO, KERNEL_ROWS, KERNEL_PERSISTENT = 0, 1, 2
+SCALE_ROW_MAJOR, SCALE_COL_MAJOR = 0, 1
+
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_f = ctypes.c_float
+
+
+class LaunchOpts(ctypes.Structure):
+    """Mirror of ``rmsq_launch_opts``."""
+    _fields_ = [("kernel", _i32), ("vpt", _i32), ("rows_per_block", _i32), ("grid", _i32),
+                ("debug_skip_row", _i64), ("wait_limit_ns", _i64)]
+
+    def __init__(self, kernel=KERNEL_AUTO, vpt=0, rows_per_block=0, grid=0, debug_skip_row=-1,
+                 wait_limit_ns=0):
+        super().__init__(kernel, vpt, rows_per_block, grid, debug_skip_row, wait_limit_ns)
+
+
+class RmsqError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+_SIGNATURES = {
+    "rmsq_add_rmsnorm_quant_group_fp8": [_p, _i64, _p, _i64, _p, _f, _i64, _i64, _i32, _p, _p, _i32, _p, _p, _p],
+    "rmsq_add_rmsnorm_quant_group_fp8_ex": [_p, _i64, _p, _i64, _p, _f, _i64, _i64, _i32, _p, _p, _i32, _p, _p, _p, _p],
+    "rmsq_qknorm_quant_fp8": [_p, _i64, _p, _i64, _p, _p, _f, _i64, _i64, _i64, _i32, _p, _p, _p, _p, _i32, _p, _p, _p],
+    "rmsq_add_rmsnorm_quant_mxfp4": [_p, _i64, _p, _i64, _p, _f, _i64, _i64, _p, _p, _p, _p, _p],
+    "rmsq_add_rmsnorm_quant_mxfp4_ex": [_p, _i64, _p, _i64, _p, _f, _i64, _i64, _p, _p, _p, _p, _p, _p],
+    "rmsq_sync_status": [_p],
+    "rmsq_encode_e4m3": [_p, _p, _i64, _p],
+    "rmsq_encode_e2m1": [_p, _p, _i64, _p],
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded librmsq; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"librmsq is not built ({LIB_PATH} missing); run "
+                               "`python -m mxfp4_activation_quant_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.rmsq_status_string.argtypes = [ctypes.c_int]
+        L.rmsq_status_string.restype = ctypes.c_char_p
+        L.rmsq_last_error.argtypes = []
+        L.rmsq_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != RMSQ_OK:
+        raise RmsqError(status, lib().rmsq_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _rows_view(t: torch.Tensor, name: str) -> int:
+    """Checks a bf16 CUDA matrix with unit inner stride; returns its leading dimension."""
+    if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D bf16 CUDA tensor")
+    if t.stride(1) != 1 and t.shape[1] > 1:
+        raise ValueError(f"{name} must have contiguous rows")
+    return t.stride(0)
+
+
+def _layout(scale_layout) -> int:
+    return {"row": SCALE_ROW_MAJOR, "col": SCALE_COL_MAJOR,
+            SCALE_ROW_MAJOR: SCALE_ROW_MAJOR, SCALE_COL_MAJOR: SCALE_COL_MAJOR}[scale_layout]
+
+
+def add_rmsnorm_quant_fp8(x: torch.Tensor, gamma: torch.Tensor, residual: torch.Tensor | None = None,
+                          eps: float = 1e-6, group: int = 128, scale_layout="row",
+                          keep_bf16: bool = False, out_residual: torch.Tensor | None = None,
+                          opts: LaunchOpts | None = None):
+    """Residual add + RMSNorm + 1x128 FP8 quant.
+
+    Returns ``((q, scale), residual_out)``, or ``((y, q, scale), residual_out)``
+    when ``keep_bf16``; ``residual_out`` is None without a residual. Pass
+    ``out_residual=residual`` for the in-place residual update.
+    """
+    ldx = _rows_view(x, "x")
+    M, H = x.shape
+    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    dev = x.device
+    layout = _layout(scale_layout)
+    q = torch.empty((M, H), dtype=torch.float8_e4m3fn, device=dev)
+    G = H // group if group > 0 else 0
+    scale = torch.empty((M, G) if layout == SCALE_ROW_MAJOR else (G, M), dtype=torch.float32, device=dev)
+    res_out = None
+    if residual is not None:
+        res_out = out_residual if out_residual is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H, group, _ptr(q), _ptr(scale),
+            layout, _ptr(res_out), _ptr(y), _stream(dev))
+    if opts is None:
+        _check(lib().rmsq_add_rmsnorm_quant_group_fp8(*args))
+    else:
+        _check(lib().rmsq_add_rmsnorm_quant_group_fp8_ex(*args, ctypes.byref(opts)))
+    return ((y, q, scale) if keep_bf16 else (q, scale)), res_out
+
+
+def qknorm_quant_fp8(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Tensor,
+                     gamma_kv: torch.Tensor, eps: float = 1e-6, group: int = 128,
+                     scale_layout="row", keep_bf16: bool = False):
+    """One launch for the MLA q_a / kv_a latents. Returns ``(q_tuple, kv_tuple)``,
+    each ``(q, scale)`` or ``(y, q, scale)``."""
+    ldq = _rows_view(q_a, "q_a")
+    ldk = _rows_view(kv_a, "kv_a")
+    M, Hq = q_a.shape
+    Mk, Hkv = kv_a.shape
+    if Mk != M:
+        raise ValueError("q_a and kv_a must have the same number of rows")
+    dev = q_a.device
+    layout = _layout(scale_layout)
+
+    def outs(H):
+        q = torch.empty((M, H), dtype=torch.float8_e4m3fn, device=dev)
+        G = H // group if group > 0 else 0
+        s = torch.empty((M, G) if layout == SCALE_ROW_MAJOR else (G, M), dtype=torch.float32, device=dev)
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
+        return q, s, y
+
+    qq, qs, qy = outs(Hq)
+    kq, ks, ky = outs(Hkv)
+    _check(lib().rmsq_qknorm_quant_fp8(_ptr(q_a), ldq, _ptr(kv_a), ldk, _ptr(gamma_q), _ptr(gamma_kv),
+                                       eps, M, Hq, Hkv, group, _ptr(qq), _ptr(qs), _ptr(kq), _ptr(ks),
+                                       layout, _ptr(qy), _ptr(ky), _stream(dev)))
+    if keep_bf16:
+        return (qy, qq, qs), (ky, kq, ks)
+    return (qq, qs), (kq, ks)
+
+
+def add_rmsnorm_quant_mxfp4(x: torch.Tensor, gamma: torch.Tensor, residual: torch.Tensor | None = None,
+                            eps: float = 1e-6, keep_bf16: bool = False,
+                            out_residual: torch.Tensor | None = None, opts: LaunchOpts | None = None):
+    """Residual add + RMSNorm + MXFP4 quant: q [M, H/2] uint8 (element 2k in
+    the low nibble), E8M0 scales [M, H/32] uint8. Same tuple forms as the FP8 call."""
+    ldx = _rows_view(x, "x")
+    M, H = x.shape
+    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    dev = x.device
+    q = torch.empty((M, H // 2), dtype=torch.uint8, device=dev)
+    scale = torch.empty((M, H // 32), dtype=torch.uint8, device=dev)
+    res_out = None
+    if residual is not None:
+        res_out = out_residual if out_residual is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H, _ptr(q), _ptr(scale),
+            _ptr(res_out), _ptr(y), _stream(dev))
+    if opts is None:
+        _check(lib().rmsq_add_rmsnorm_quant_mxfp4(*args))
+    else:
+        _check(lib().rmsq_add_rmsnorm_quant_mxfp4_ex(*args, ctypes.byref(opts)))
+    return ((y, q, scale) if keep_bf16 else (q, scale)), res_out
+
+
+def sync_status(device=None) -> int:
+    """Synchronises the current stream and returns the library status word's verdict."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    return lib().rmsq_sync_status(_stream(dev))
+
+
+def encode_e4m3(v: torch.Tensor) -> torch.Tensor:
+    """The kernels' E4M3 conversion applied elementwise (fp32 CUDA tensor -> uint8)."""
+    v = v.contiguous()
+    out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    _check(lib().rmsq_encode_e4m3(_ptr(v), _ptr(out), v.numel(), _stream(v.device)))
+    return out
+
+
+def encode_e2m1(v: torch.Tensor) -> torch.Tensor:
+    """The kernels' E2M1 conversion applied elementwise (one code per byte)."""
+    v = v.contiguous()
+    out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    _check(lib().rmsq_encode_e2m1(_ptr(v), _ptr(out), v.numel(), _stream(v.device)))
+    return out

@@ -1,0 +1,124 @@
+"""Host-side checks of the C ABI: the library loads, exports every function the
+header declares, and rejects bad arguments before launching anything (these
+calls never reach the GPU, so they run on machines without one)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mxfp4_activation_quant_gb300 import build as lib_build
+from mxfp4_activation_quant_gb300 import rmsq
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "rmsq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    lib_build.build()
+    return rmsq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rmsq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    fns = declared_functions()
+    for name in ("rmsq_add_rmsnorm_quant_group_fp8", "rmsq_qknorm_quant_fp8",
+                 "rmsq_add_rmsnorm_quant_mxfp4"):
+        assert name in fns
+
+
+def test_every_declared_symbol_is_exported(L):
+    missing = [f for f in declared_functions() if not hasattr(L, f)]
+    assert not missing, missing
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert L.rmsq_status_string(s)
+    assert L.rmsq_status_string(99) == b"unknown status"
+
+
+# Fake, well-aligned device addresses: every call below must be rejected by
+# the host checks, so nothing is ever dereferenced or launched.
+BASE = 1 << 40
+X, RES, G, Q, S, RO, Y = (BASE + i * (1 << 32) for i in range(7))
+
+
+def fp8(L, **kw):
+    a = dict(x=X, ldx=256, res=RES, ldr=256, gamma=G, eps=1e-6, M=4, H=256, group=128, q=Q, scale=S,
+             layout=0, res_out=RO, y=Y)
+    a.update(kw)
+    return L.rmsq_add_rmsnorm_quant_group_fp8(a["x"], a["ldx"], a["res"], a["ldr"], a["gamma"], a["eps"],
+                                              a["M"], a["H"], a["group"], a["q"], a["scale"], a["layout"],
+                                              a["res_out"], a["y"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), 1),
+    (dict(gamma=None), 1),
+    (dict(H=200), 1),                      # not a multiple of 128
+    (dict(group=64), 3),                   # FP8 groups other than 128 are not implemented
+    (dict(group=0), 1),
+    (dict(layout=7), 1),
+    (dict(eps=-1.0), 1),
+    (dict(eps=float("nan")), 1),
+    (dict(M=-1), 1),
+    (dict(H=0), 1),
+    (dict(res_out=None), 1),               # residual without its output
+    (dict(res=None), 1),                   # output without a residual
+    (dict(x=X + 2), 2),                    # misaligned base
+    (dict(ldx=260), 2),                    # leading dimension not a multiple of 8
+    (dict(ldx=128), 1),                    # leading dimension < H
+    (dict(q=X + 64), 1),                   # output overlaps x
+    (dict(y=Q + 512), 1),                  # two outputs overlap
+    (dict(res_out=RES, ldr=264), 1),       # in-place residual needs ld_res == H
+    (dict(H=1 << 20), 3),                  # row longer than the kernels handle
+])
+def test_fp8_rejects_bad_arguments(L, kw, status):
+    assert fp8(L, **kw) == status
+    assert L.rmsq_last_error()
+
+
+def test_m_zero_is_a_no_op(L):
+    assert fp8(L, M=0) == 0
+    assert L.rmsq_add_rmsnorm_quant_mxfp4(X, 256, RES, 256, G, 1e-6, 0, 256, Q, S, RO, Y, None) == 0
+
+
+def test_mxfp4_rejects_bad_arguments(L):
+    call = L.rmsq_add_rmsnorm_quant_mxfp4
+    assert call(X, 256, RES, 256, G, 1e-6, 4, 48, Q, S, RO, Y, None) == 1         # H % 32
+    assert call(X, 256, RES, 256, None, 1e-6, 4, 256, Q, S, RO, Y, None) == 1     # no gamma
+    assert call(X + 8, 256, RES, 256, G, 1e-6, 4, 256, Q, S, RO, Y, None) == 2    # misaligned
+
+
+def test_qknorm_rejects_bad_arguments(L):
+    call = L.rmsq_qknorm_quant_fp8
+    args = [X, 1536, RES, 512, G, G + 4096, 1e-6, 8, 1536, 512, 128, Q, S, RO, Y, 0, None, None, None]
+    bad = list(args)
+    bad[9] = 500                           # Hkv not a multiple of 128
+    assert call(*bad) == 1
+    bad = list(args)
+    bad[13] = Q + 128                      # kv codes overlap q codes
+    assert call(*bad) == 1
+    bad = list(args)
+    bad[10] = 32
+    assert call(*bad) == 3
+
+
+def test_launch_opts_layout_matches_header():
+    # int32 kernel, vpt, rows_per_block, grid; int64 debug_skip_row, wait_limit_ns
+    assert ctypes.sizeof(rmsq.LaunchOpts) == 32
+    assert rmsq.LaunchOpts.debug_skip_row.offset == 16
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(rmsq, "_lib", None)
+    monkeypatch.setattr(rmsq, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        rmsq.lib()

@@ -1,0 +1,317 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Every test here needs a GPU. Inputs are the seeded workloads of
+mxfp4_activation_quant_gb300.synth; the rules are those of tests/parity.py.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_activation_quant_gb300 import rmsq, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.fail("these tests need a CUDA GPU")
+
+
+def _gpu(d):
+    return {k: v.to(DEV) for k, v in d.items()}
+
+
+def run_fp8(d, w_eps, layout="row", keep=False, residual=True, opts=None):
+    g = _gpu(d)
+    out, res_out = rmsq.add_rmsnorm_quant_fp8(g["x"], g["gamma"], g.get("residual") if residual else None,
+                                              eps=w_eps, scale_layout=layout, keep_bf16=keep, opts=opts)
+    torch.cuda.synchronize()
+    got = {"q": out[-2], "scale": out[-1], "residual_out": res_out, "y": out[0] if keep else None}
+    return got
+
+
+def ref_fp8(O, d, eps, layout="row", residual=True):
+    return O.add_rmsnorm_quant_fp8(d["x"], d.get("residual") if residual else None, d["gamma"], eps,
+                                   layout=layout)
+
+
+def run_mx(d, eps, keep=False, residual=True, opts=None):
+    g = _gpu(d)
+    out, res_out = rmsq.add_rmsnorm_quant_mxfp4(g["x"], g["gamma"], g.get("residual") if residual else None,
+                                                eps=eps, keep_bf16=keep, opts=opts)
+    torch.cuda.synchronize()
+    return {"q": out[-2], "scale": out[-1], "residual_out": res_out, "y": out[0] if keep else None}
+
+
+# ------------------------------------------------------------- workloads
+
+@pytest.mark.parametrize("name,M", [("tiny", None), ("decode", None), ("prefill", 300),
+                                    ("prefill", 37), ("mxfp4", 129)])
+def test_workload_rows(oracle_mod, name, M):
+    w = synth.WORKLOADS[name]
+    d = synth.make_inputs(w, M=M)
+    if w.kind == "fp8":
+        got = run_fp8(d, w.eps, layout=w.scale_layout, keep=w.keep_bf16)
+        ref = ref_fp8(oracle_mod, d, w.eps, layout=w.scale_layout)
+        st = parity.compare_fp8(got, ref, w.scale_layout, what=name)
+    else:
+        got = run_mx(d, w.eps, keep=True)
+        ref = oracle_mod.add_rmsnorm_quant_mxfp4(d["x"], d["residual"], d["gamma"], w.eps)
+        st = parity.compare_mx(got, ref, what=name)
+    print(name, M, st)
+
+
+def test_qknorm_workload(oracle_mod):
+    w = synth.WORKLOADS["qknorm"]
+    d = synth.make_inputs(w, M=301)
+    g = _gpu(d)
+    (qy, qq, qs), (ky, kq, ks) = rmsq.qknorm_quant_fp8(g["q_a"], g["kv_a"], g["gamma_q"], g["gamma_kv"],
+                                                       eps=w.eps, keep_bf16=True)
+    torch.cuda.synchronize()
+    ref = oracle_mod.qknorm_quant_fp8(d["q_a"], d["kv_a"], d["gamma_q"], d["gamma_kv"], w.eps)
+    parity.compare_fp8({"q": qq, "scale": qs, "y": qy}, ref["q"], what="q_a")
+    parity.compare_fp8({"q": kq, "scale": ks, "y": ky}, ref["kv"], what="kv_a")
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "qknorm", "mxfp4"])
+def test_full_size_workloads(oracle_mod, name):
+    """Full-size workloads, every row compared, default launch configuration."""
+    w = synth.WORKLOADS[name]
+    d = synth.make_inputs(w)
+    if w.kind == "qknorm":
+        g = _gpu(d)
+        (qq, qs), (kq, ks) = rmsq.qknorm_quant_fp8(g["q_a"], g["kv_a"], g["gamma_q"], g["gamma_kv"], eps=w.eps)
+        torch.cuda.synchronize()
+        ref = oracle_mod.qknorm_quant_fp8(d["q_a"], d["kv_a"], d["gamma_q"], d["gamma_kv"], w.eps)
+        st = [parity.compare_fp8({"q": qq, "scale": qs}, ref["q"], what="q_a"),
+              parity.compare_fp8({"q": kq, "scale": ks}, ref["kv"], what="kv_a")]
+    elif w.kind == "fp8":
+        got = run_fp8(d, w.eps, layout=w.scale_layout, keep=w.keep_bf16)
+        st = parity.compare_fp8(got, ref_fp8(oracle_mod, d, w.eps, w.scale_layout), w.scale_layout, what=name)
+    else:
+        got = run_mx(d, w.eps)
+        ref = oracle_mod.add_rmsnorm_quant_mxfp4(d["x"], d["residual"], d["gamma"], w.eps)
+        st = parity.compare_mx(got, ref, what=name)
+    print(name, st)
+
+
+# ------------------------------------------------------ hand-worked rows
+
+def _golden_rows():
+    p = os.path.join(os.path.dirname(__file__), "golden", "handworked_rows.json")
+    return json.load(open(p))["rows"]
+
+
+def _vec(spec, H):
+    v = np.full(H, spec["fill"], dtype=np.float64)
+    for i, val in spec["set"]:
+        v[i] = val
+    return torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("row", _golden_rows(), ids=lambda r: r["name"])
+def test_handworked_rows_on_gpu(row):
+    H = row["H"]
+    x = _vec(row["x"], H)[None, :].to(DEV)
+    res = None if row["residual"] is None else _vec(row["residual"], H)[None, :].to(DEV)
+    gamma = _vec(row["gamma"], H).to(DEV)
+    exp = row["expect"]
+    if row["kind"] == "fp8":
+        (y, q, s), _ = rmsq.add_rmsnorm_quant_fp8(x, gamma, res, eps=row["eps"], keep_bf16=True)
+        torch.cuda.synchronize()
+        want_q = np.full(H, exp["q"]["fill"], dtype=np.uint8)
+        for i, c in exp["q"]["set"]:
+            want_q[i] = c
+        np.testing.assert_array_equal(parity.u8(q)[0], want_q)
+        if "y" in exp:
+            np.testing.assert_array_equal(y[0].float().cpu().numpy(), _vec(exp["y"], H).float().numpy())
+    else:
+        (y, q, s), _ = rmsq.add_rmsnorm_quant_mxfp4(x, gamma, res, eps=row["eps"], keep_bf16=True)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(parity.u8(s)[0], np.array(exp["mx_scale"], dtype=np.uint8))
+        codes = np.full(H, exp["codes"]["fill"], dtype=np.uint8)
+        for i, c in exp["codes"]["set"]:
+            codes[i] = c
+        np.testing.assert_array_equal(parity.u8(q)[0], codes[0::2] | (codes[1::2] << 4))
+
+
+# -------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("H", [128, 256, 384, 512, 640, 1024, 1536, 2048, 3072, 4096, 7168, 8192, 16384])
+def test_shapes_fp8(oracle_mod, H):
+    M = 19                                          # ragged against every rows-per-block
+    d = {"x": synth.random_bf16(10 + H, (M, H)), "residual": synth.random_bf16(20 + H, (M, H), var=4.0,
+                                                                               tensor="residual"),
+         "gamma": synth.gaussian_bf16(30 + H, "gamma", (H,), mean=1.0, var=0.1)}
+    got = run_fp8(d, 1e-6, keep=True)
+    parity.compare_fp8(got, ref_fp8(oracle_mod, d, 1e-6), what=f"H={H}")
+
+
+@pytest.mark.parametrize("H", [32, 64, 96, 128, 160, 256, 512, 1024, 7168])
+def test_shapes_mxfp4(oracle_mod, H):
+    M = 23
+    d = {"x": synth.student_t3_bf16(40 + H, "x", (M, H)),
+         "residual": synth.random_bf16(50 + H, (M, H), tensor="residual"),
+         "gamma": synth.gaussian_bf16(60 + H, "gamma", (H,), mean=1.0, var=0.1)}
+    got = run_mx(d, 1e-6, keep=True)
+    ref = oracle_mod.add_rmsnorm_quant_mxfp4(d["x"], d["residual"], d["gamma"], 1e-6)
+    parity.compare_mx(got, ref, what=f"H={H}")
+
+
+@pytest.mark.parametrize("vpt", [1, 2, 4, 7])
+def test_team_shapes_agree(oracle_mod, vpt):
+    """Every vectors-per-thread choice for H=7168 meets the bar; outside
+    boundary rows they are bit-identical to the oracle and so to each other."""
+    w = synth.WORKLOADS["prefill"]
+    d = synth.make_inputs(w, M=64)
+    if 7168 // 8 // vpt > 512:
+        pytest.skip("team larger than a block")
+    got = run_fp8(d, w.eps, keep=True, opts=rmsq.LaunchOpts(kernel=rmsq.KERNEL_ROWS, vpt=vpt))
+    parity.compare_fp8(got, ref_fp8(oracle_mod, d, w.eps), what=f"vpt={vpt}")
+
+
+@pytest.mark.parametrize("rpb", [1, 2, 3])
+def test_rows_per_block(oracle_mod, rpb):
+    w = synth.WORKLOADS["prefill"]
+    d = synth.make_inputs(w, M=41)
+    got = run_fp8(d, w.eps, opts=rmsq.LaunchOpts(kernel=rmsq.KERNEL_ROWS, rows_per_block=rpb))
+    parity.compare_fp8(got, ref_fp8(oracle_mod, d, w.eps), what=f"rpb={rpb}")
+
+
+def test_no_residual_and_column_major(oracle_mod):
+    w = synth.WORKLOADS["decode"]
+    d = synth.make_inputs(w, M=33)
+    got = run_fp8(d, w.eps, layout="col", residual=False, keep=True)
+    assert got["residual_out"] is None
+    parity.compare_fp8(got, ref_fp8(oracle_mod, d, w.eps, layout="col", residual=False), "col", what="nores")
+
+
+def test_single_row_and_in_place_residual(oracle_mod):
+    w = synth.WORKLOADS["decode"]
+    d = synth.make_inputs(w, M=1)
+    g = _gpu(d)
+    res = g["residual"].clone()
+    (q, s), r = rmsq.add_rmsnorm_quant_fp8(g["x"], g["gamma"], res, eps=w.eps, out_residual=res)
+    torch.cuda.synchronize()
+    assert r.data_ptr() == res.data_ptr()
+    parity.compare_fp8({"q": q, "scale": s, "residual_out": res}, ref_fp8(oracle_mod, d, w.eps), what="inplace")
+
+
+def test_strided_rows(oracle_mod):
+    """kv_a as a column slice of a wider projection output (leading dim > H)."""
+    wide = synth.random_bf16(77, (40, 576 + 64))
+    d = {"x": wide[:, :512], "gamma": synth.gaussian_bf16(78, "gamma", (512,), mean=1.0, var=0.1)}
+    g = {"x": wide.to(DEV)[:, :512], "gamma": d["gamma"].to(DEV)}
+    (q, s), _ = rmsq.add_rmsnorm_quant_fp8(g["x"], g["gamma"], None, eps=1e-6)
+    torch.cuda.synchronize()
+    ref = oracle_mod.add_rmsnorm_quant_fp8(parity.u16(d["x"].contiguous()), None, d["gamma"], 1e-6)
+    parity.compare_fp8({"q": q, "scale": s}, ref, what="strided")
+
+
+def test_zero_and_extreme_rows(oracle_mod):
+    """All-zero rows; huge and tiny magnitudes (the wide-range fp64 path);
+    bf16 subnormals (no flush to zero anywhere)."""
+    H = 1024
+    rng = np.random.default_rng(0)
+    base = rng.standard_normal((6, H)).astype(np.float32)
+    rows = np.stack([np.zeros(H, np.float32), base[1] * 1e30, base[2] * 1e-30,
+                     base[3] * np.float32(2.0 ** -130), base[4] * 3e38 / 8, base[5]])
+    x = torch.from_numpy(rows).to(torch.bfloat16)
+    gamma = synth.gaussian_bf16(5, "gamma", (H,), mean=1.0, var=0.1)
+    for eps in (1e-6, 0.0):
+        # with eps = 0 a zero row has no finite inv_rms, and a subnormal row's
+        # inv_rms overflows fp32 (inf/inf codes are NaN): keep those to eps > 0
+        xx = x if eps > 0 else x[[1, 2, 4, 5]]
+        got = run_fp8({"x": xx, "gamma": gamma}, eps, residual=False, keep=True)
+        ref = oracle_mod.add_rmsnorm_quant_fp8(xx, None, gamma, eps)
+        parity.compare_fp8(got, ref, what=f"extreme eps={eps}")
+        gm = run_mx({"x": xx, "gamma": gamma}, eps, residual=False, keep=True)
+        parity.compare_mx(gm, oracle_mod.add_rmsnorm_quant_mxfp4(xx, None, gamma, eps), what=f"extreme mx eps={eps}")
+
+
+def test_add_edge_pairs(oracle_mod):
+    """Residual pairs at bf16 ties, wide exponent gaps, cancellation, subnormals."""
+    H = 2048
+    rng = np.random.default_rng(1)
+    a = rng.standard_normal((4, H)).astype(np.float32)
+    b = (rng.standard_normal((4, H)) * np.exp2(rng.integers(-40, 40, (4, H)))).astype(np.float32)
+    b[0] = -a[0]
+    b[1] = a[1] * np.float32(2.0 ** -8)
+    a[2, ::2] = np.float32(2.0 ** -128)
+    b[2, ::2] = np.float32(2.0 ** -131)
+    x = torch.from_numpy(a).to(torch.bfloat16)
+    res = torch.from_numpy(b).to(torch.bfloat16)
+    gamma = torch.ones(H, dtype=torch.bfloat16)
+    got = run_fp8({"x": x, "residual": res, "gamma": gamma}, 1e-6)
+    ref = oracle_mod.add_rmsnorm_quant_fp8(x, res, gamma, 1e-6)
+    np.testing.assert_array_equal(parity.u16(got["residual_out"]), ref["residual_out"])
+
+
+def test_guard_bands_untouched(oracle_mod):
+    """Outputs carved from larger buffers: bytes around them keep their canary."""
+    w = synth.WORKLOADS["prefill"]
+    M, H = 29, 7168
+    d = _gpu(synth.make_inputs(w, M=M))
+    pad = 4096
+    qbuf = torch.full((M * H + 2 * pad,), 0xA5, dtype=torch.uint8, device=DEV)
+    sbuf = torch.full((M * 56 + 2 * pad,), -7.0, dtype=torch.float32, device=DEV)
+    rbuf = torch.full((M * H + 2 * pad,), 3.0, dtype=torch.bfloat16, device=DEV)
+    ybuf = torch.full((M * H + 2 * pad,), 5.0, dtype=torch.bfloat16, device=DEV)
+    st = rmsq.lib().rmsq_add_rmsnorm_quant_group_fp8(
+        d["x"].data_ptr(), H, d["residual"].data_ptr(), H, d["gamma"].data_ptr(), 1e-6, M, H, 128,
+        qbuf.data_ptr() + pad, sbuf.data_ptr() + pad * 4, 0, rbuf.data_ptr() + pad * 2,
+        ybuf.data_ptr() + pad * 2, torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    for buf, val, n in ((qbuf, 0xA5, M * H), (sbuf, -7.0, M * 56), (rbuf, 3.0, M * H), (ybuf, 5.0, M * H)):
+        assert torch.all(buf[:pad] == val) and torch.all(buf[pad + n:] == val)
+
+
+def test_misaligned_tensor_is_rejected():
+    x = torch.zeros(4 * 256 + 1, dtype=torch.bfloat16, device=DEV)[1:].view(4, 256)
+    gamma = torch.ones(256, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(rmsq.RmsqError, match="MISALIGNED"):
+        rmsq.add_rmsnorm_quant_fp8(x, gamma)
+
+
+# --------------------------------------------------------------- encoders
+
+def _probe(values):
+    base = np.concatenate([values, (values[:-1] + values[1:]) / 2]).astype(np.float32)
+    near = [base]
+    up, dn = base, base
+    for _ in range(3):
+        up = np.nextafter(up, np.float32(np.inf))
+        dn = np.nextafter(dn, np.float32(0))
+        near += [up, dn]
+    rng = np.random.default_rng(42)
+    rand = rng.integers(0, 0x7F800000, 4_000_000, dtype=np.uint32).view(np.float32)
+    mags = np.exp2(rng.uniform(-20, 12, 2_000_000)).astype(np.float32)
+    special = np.array([0.0, 1e-45, 1e-40, 1.1754942e-38, 1e30, 3.4e38, np.inf], dtype=np.float32)
+    v = np.concatenate(near + [rand, mags, special])
+    return np.concatenate([v, -v])
+
+
+def test_device_e4m3_encoder_matches_oracle(oracle_mod):
+    table = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    v = _probe(table[:0x7F].astype(np.float64))
+    got = rmsq.encode_e4m3(torch.from_numpy(v).to(DEV)).cpu().numpy()
+    np.testing.assert_array_equal(got, oracle_mod.e4m3_encode(v))
+    nan = rmsq.encode_e4m3(torch.tensor([float("nan")], device=DEV)).cpu().numpy()
+    assert (nan[0] & 0x7F) == 0x7F
+
+
+def test_device_e2m1_encoder_matches_oracle(oracle_mod):
+    v = _probe(np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]))
+    got = rmsq.encode_e2m1(torch.from_numpy(v).to(DEV)).cpu().numpy()
+    np.testing.assert_array_equal(got, oracle_mod.e2m1_encode(v))
