@@ -102,10 +102,6 @@ int default_rows_per_block(int tpr) { return tpr >= 256 ? 1 : 256 / tpr; }
 
 const rmsq_launch_opts kDefaultOpts = {RMSQ_KERNEL_AUTO, 0, 0, 0, -1, 0};
 
-struct Checked {
-    int64_t M, H;
-};
-
 // Checks shared by the single-tensor FP8 and MXFP4 calls.
 rmsq_status check_single(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
                          const void *gamma, float eps, int64_t M, int64_t H, int64_t group,
@@ -195,6 +191,21 @@ Seg make_seg(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
     return s;
 }
 
+// Device address of the status word, looked up once per device.
+unsigned int *status_word_ptr(int dev)
+{
+    static unsigned int *ptrs[128];
+    if (dev < 0 || dev >= 128)
+        return nullptr;
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess)
+            return nullptr;
+        ptrs[dev] = (unsigned int *)p;
+    }
+    return ptrs[dev];
+}
+
 rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_t st)
 {
     const int gv = mx ? 4 : 16;
@@ -223,7 +234,46 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
             return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
         return ok();
     }
-    return fail(RMSQ_ERR_UNSUPPORTED, "kernel %d is not available", o.kernel);
+    if (kernel == RMSQ_KERNEL_PERSISTENT) {
+        if (tpr < 32)
+            return fail(RMSQ_ERR_UNSUPPORTED, "the persistent kernel needs rows of >= 32 threads");
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        int sms = 0, smem_max = 0;
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess)
+            return fail(RMSQ_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+        size_t smem = bulk_smem(s.H, s.res != nullptr);
+        if (smem + sizeof(float2) * 64 + 256 > (size_t)smem_max)
+            return fail(RMSQ_ERR_UNSUPPORTED, "H=%d needs %zu bytes of shared memory", s.H, smem);
+        int64_t grid = o.grid;
+        if (grid <= 0) {
+            int per_sm = bulk_occupancy(mx, vpt, tpr, smem);
+            if (per_sm <= 0)
+                return fail(RMSQ_ERR_UNSUPPORTED, "persistent kernel does not fit on an SM");
+            grid = (int64_t)per_sm * sms;
+        }
+        if (grid > s.M)
+            grid = s.M;
+        unsigned int *status = status_word_ptr(dev);
+        if (!status)
+            return fail(RMSQ_ERR_CUDA, "status word address unavailable");
+        s.rpb = 1;
+        BulkParams bp{};
+        bp.s = s;
+        bp.debug_skip_row = o.debug_skip_row;
+        bp.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
+        bp.status = status;
+        e = mx ? launch_bulk_mx(vpt, bp, (int)grid, tpr, smem, st)
+               : launch_bulk_fp8(vpt, bp, (int)grid, tpr, smem, st);
+        if (e != cudaSuccess)
+            return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+        return ok();
+    }
+    return fail(RMSQ_ERR_INVALID_ARG, "unknown kernel %d", o.kernel);
 }
 
 // ------------------------------------------------------- encoder kernels

@@ -1,0 +1,26 @@
+// Persistent bulk-copy kernel instantiations (FP8 1x128 and MXFP4 1x32).
+#include "rmsq_bulk.cuh"
+
+namespace rmsq {
+
+cudaError_t launch_bulk_fp8(int vpt, const BulkParams &p, int grid, int threads, size_t smem,
+                            cudaStream_t st)
+{
+    return launch_bulk_impl<false>(vpt, p, grid, threads, smem, st);
+}
+
+cudaError_t launch_bulk_mx(int vpt, const BulkParams &p, int grid, int threads, size_t smem,
+                           cudaStream_t st)
+{
+    return launch_bulk_impl<true>(vpt, p, grid, threads, smem, st);
+}
+
+int bulk_occupancy(bool mx, int vpt, int threads, size_t smem)
+{
+    return mx ? bulk_blocks_per_sm<true>(vpt, threads, smem)
+              : bulk_blocks_per_sm<false>(vpt, threads, smem);
+}
+
+size_t bulk_smem(int H, bool has_res) { return bulk_smem_bytes(H, has_res); }
+
+}  // namespace rmsq

@@ -50,6 +50,8 @@ cudaError_t launch_bulk_fp8(int vpt, const BulkParams &p, int grid, int threads,
                             cudaStream_t st);
 cudaError_t launch_bulk_mx(int vpt, const BulkParams &p, int grid, int threads, size_t smem,
                            cudaStream_t st);
+int bulk_occupancy(bool mx, int vpt, int threads, size_t smem);
+size_t bulk_smem(int H, bool has_res);
 bool vpt_instantiated(int vpt);
 
 }  // namespace rmsq

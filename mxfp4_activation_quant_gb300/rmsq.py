@@ -140,6 +140,51 @@ def add_rmsnorm_quant_fp8(x: torch.Tensor, gamma: torch.Tensor, residual: torch.
     return ((y, q, scale) if keep_bf16 else (q, scale)), res_out
 
 
+def add_rmsnorm_quant_fp8_into(x, gamma, residual, q, scale, res_out=None, y=None, eps: float = 1e-6,
+                               group: int = 128, scale_layout="row", opts: LaunchOpts | None = None,
+                               stream: int | None = None) -> None:
+    """As add_rmsnorm_quant_fp8, writing into caller-allocated outputs (no allocation)."""
+    ldx = _rows_view(x, "x")
+    M, H = x.shape
+    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    st = _stream(x.device) if stream is None else stream
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H, group, _ptr(q), _ptr(scale),
+            _layout(scale_layout), _ptr(res_out), _ptr(y), st)
+    if opts is None:
+        _check(lib().rmsq_add_rmsnorm_quant_group_fp8(*args))
+    else:
+        _check(lib().rmsq_add_rmsnorm_quant_group_fp8_ex(*args, ctypes.byref(opts)))
+
+
+def add_rmsnorm_quant_mxfp4_into(x, gamma, residual, q, scale, res_out=None, y=None, eps: float = 1e-6,
+                                 opts: LaunchOpts | None = None, stream: int | None = None) -> None:
+    """As add_rmsnorm_quant_mxfp4, writing into caller-allocated outputs."""
+    ldx = _rows_view(x, "x")
+    M, H = x.shape
+    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    st = _stream(x.device) if stream is None else stream
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H, _ptr(q), _ptr(scale),
+            _ptr(res_out), _ptr(y), st)
+    if opts is None:
+        _check(lib().rmsq_add_rmsnorm_quant_mxfp4(*args))
+    else:
+        _check(lib().rmsq_add_rmsnorm_quant_mxfp4_ex(*args, ctypes.byref(opts)))
+
+
+def qknorm_quant_fp8_into(q_a, kv_a, gamma_q, gamma_kv, qq, qs, kq, ks, qy=None, ky=None,
+                          eps: float = 1e-6, group: int = 128, scale_layout="row",
+                          stream: int | None = None) -> None:
+    """As qknorm_quant_fp8, writing into caller-allocated outputs."""
+    ldq = _rows_view(q_a, "q_a")
+    ldk = _rows_view(kv_a, "kv_a")
+    M, Hq = q_a.shape
+    Hkv = kv_a.shape[1]
+    st = _stream(q_a.device) if stream is None else stream
+    _check(lib().rmsq_qknorm_quant_fp8(_ptr(q_a), ldq, _ptr(kv_a), ldk, _ptr(gamma_q), _ptr(gamma_kv), eps,
+                                       M, Hq, Hkv, group, _ptr(qq), _ptr(qs), _ptr(kq), _ptr(ks),
+                                       _layout(scale_layout), _ptr(qy), _ptr(ky), st))
+
+
 def qknorm_quant_fp8(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Tensor,
                      gamma_kv: torch.Tensor, eps: float = 1e-6, group: int = 128,
                      scale_layout="row", keep_bf16: bool = False):

@@ -224,8 +224,9 @@ def test_zero_and_extreme_rows(oracle_mod):
     H = 1024
     rng = np.random.default_rng(0)
     base = rng.standard_normal((6, H)).astype(np.float32)
-    rows = np.stack([np.zeros(H, np.float32), base[1] * 1e30, base[2] * 1e-30,
-                     base[3] * np.float32(2.0 ** -130), base[4] * 3e38 / 8, base[5]])
+    rows = np.stack([np.zeros(H, np.float32), base[1] * np.float32(1e30), base[2] * np.float32(1e-30),
+                     base[3] * np.float32(2.0 ** -130), base[4] * np.float32(3e38 / 8), base[5]])
+    assert np.all(np.isfinite(rows))
     x = torch.from_numpy(rows).to(torch.bfloat16)
     gamma = synth.gaussian_bf16(5, "gamma", (H,), mean=1.0, var=0.1)
     for eps in (1e-6, 0.0):
@@ -315,3 +316,61 @@ def test_device_e2m1_encoder_matches_oracle(oracle_mod):
     v = _probe(np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]))
     got = rmsq.encode_e2m1(torch.from_numpy(v).to(DEV)).cpu().numpy()
     np.testing.assert_array_equal(got, oracle_mod.e2m1_encode(v))
+
+
+# ------------------------------------------------- persistent bulk-copy kernel
+
+PERSIST = rmsq.KERNEL_PERSISTENT
+
+
+@pytest.mark.parametrize("name,M,grid", [("prefill", 1000, 0), ("prefill", 333, 7), ("decode", None, 0),
+                                         ("mxfp4", 517, 0), ("prefill", 5, 0)])
+def test_persistent_kernel_matches_oracle_and_rows_kernel(oracle_mod, name, M, grid):
+    """Ragged row counts against the grid; grid 7 makes every block loop many times."""
+    w = synth.WORKLOADS[name]
+    d = synth.make_inputs(w, M=M)
+    for vpt in (7, 4):
+        po = rmsq.LaunchOpts(kernel=PERSIST, vpt=vpt, grid=grid)
+        ro = rmsq.LaunchOpts(kernel=rmsq.KERNEL_ROWS, vpt=vpt)
+        if w.kind == "fp8":
+            a = run_fp8(d, w.eps, layout=w.scale_layout, keep=True, opts=po)
+            b = run_fp8(d, w.eps, layout=w.scale_layout, keep=True, opts=ro)
+            parity.compare_fp8(a, ref_fp8(oracle_mod, d, w.eps, w.scale_layout), w.scale_layout,
+                               what=f"persistent {name} vpt={vpt}")
+        else:
+            a = run_mx(d, w.eps, keep=True, opts=po)
+            b = run_mx(d, w.eps, keep=True, opts=ro)
+            parity.compare_mx(a, oracle_mod.add_rmsnorm_quant_mxfp4(d["x"], d["residual"], d["gamma"], w.eps),
+                              what=f"persistent {name} vpt={vpt}")
+        for k in ("q", "scale", "y", "residual_out"):
+            assert torch.equal(a[k].view(torch.uint8) if a[k].dtype == torch.float8_e4m3fn else a[k],
+                               b[k].view(torch.uint8) if b[k].dtype == torch.float8_e4m3fn else b[k]), k
+    assert rmsq.sync_status() == 0
+
+
+def test_persistent_kernel_without_residual(oracle_mod):
+    w = synth.WORKLOADS["prefill"]
+    d = synth.make_inputs(w, M=200)
+    got = run_fp8(d, w.eps, residual=False, keep=True, opts=rmsq.LaunchOpts(kernel=PERSIST, grid=16))
+    parity.compare_fp8(got, ref_fp8(oracle_mod, d, w.eps, residual=False), what="persistent no residual")
+
+
+def test_persistent_wait_times_out_cleanly(oracle_mod):
+    """A row whose copy is never issued: its block's bounded wait gives up
+    after 1 ms, the status reads RMSQ_ERR_TIMEOUT, the other blocks' rows are
+    intact and the context stays usable."""
+    w = synth.WORKLOADS["prefill"]
+    M = 64
+    d = synth.make_inputs(w, M=M)
+    opts = rmsq.LaunchOpts(kernel=PERSIST, grid=8, debug_skip_row=10, wait_limit_ns=1_000_000)
+    got = run_fp8(d, w.eps, opts=opts)
+    assert rmsq.sync_status() == 5                     # RMSQ_ERR_TIMEOUT
+    assert rmsq.sync_status() == 0                     # the word was cleared
+    ref = ref_fp8(oracle_mod, d, w.eps)
+    done = np.array([r % 8 != 10 % 8 for r in range(M)])   # block 2 stopped at row 10
+    done |= np.array([r < 10 for r in range(M)])
+    np.testing.assert_array_equal(parity.u8(got["q"])[done], ref["q"][done])
+    # the context is still healthy: a normal call afterwards is exact
+    again = run_fp8(d, w.eps)
+    parity.compare_fp8(again, ref, what="after timeout")
+    assert rmsq.sync_status() == 0
