@@ -183,6 +183,17 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
 rmsq_status rmsq_encode_e4m3(const float *in, uint8_t *out, int64_t n, void *stream);
 rmsq_status rmsq_encode_e2m1(const float *in, uint8_t *out, int64_t n, void *stream);
 
+/*
+ * Exhaustive self-check of the FP8 quantiser's division: for every positive
+ * finite bf16 amax and every bf16 y with |y| <= amax (both signs), the E4M3
+ * code the kernels produce for y / (amax/448) is compared with the code of
+ * IEEE fp32 division, and the kernels' scale amax/448 with the IEEE
+ * quotient. `counts` is a caller-zeroed device array of four unsigned
+ * 64-bit counters, incremented by: code mismatches, fp32 quotient mismatches,
+ * (amax, y) pairs checked, scale mismatches. Enqueued on `stream`.
+ */
+rmsq_status rmsq_check_group_division(unsigned long long *counts, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

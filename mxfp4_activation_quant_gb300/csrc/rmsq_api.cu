@@ -188,6 +188,7 @@ Seg make_seg(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
     s.H = (int32_t)H;
     s.layout = layout;
     s.eps = eps;
+    s.inv_h = (float)(1.0 / (double)H);
     return s;
 }
 

@@ -25,6 +25,7 @@ struct Seg {
     int32_t blocks;        // blocks of the row kernel that belong to this segment
     int32_t layout;        // 0 row-major scales, 1 column-major
     float eps;
+    float inv_h;           // fp32 rounding of 1/H
 };
 
 struct LaunchParams {

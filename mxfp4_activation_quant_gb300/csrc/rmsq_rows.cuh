@@ -100,6 +100,7 @@ __device__ __forceinline__ float inv_rms_fp64_path(const uint4 (&r)[VPT], int H,
 // Everything after the row is loaded: r holds the thread's VPT vectors of
 // bf16 r (residual already added and written back by the caller). gamma is
 // read from shared memory (GAMMA_SHARED) or through the read-only cache.
+// Elementwise arithmetic runs on packed fp32 pairs.
 template <int VPT, bool MX, bool GAMMA_SHARED>
 __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int team, int parity,
                                            RedSmem &red, const uint4 (&r)[VPT],
@@ -111,20 +112,16 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
     const unsigned tmask = team_lane_mask(tpr, lane);
     const int nvec = s.H >> 3;
 
-    // ---- sum of squares: exact squares, double-float accumulation
-    float hi = 0.0f, lo = 0.0f;
+    // ---- sum of squares: exact squares, two packed double-float accumulators
+    float2 hi = f2(0.0f), lo = f2(0.0f);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-        acc_square(bf_lo(r[k].x), hi, lo);
-        acc_square(bf_hi(r[k].x), hi, lo);
-        acc_square(bf_lo(r[k].y), hi, lo);
-        acc_square(bf_hi(r[k].y), hi, lo);
-        acc_square(bf_lo(r[k].z), hi, lo);
-        acc_square(bf_hi(r[k].z), hi, lo);
-        acc_square(bf_lo(r[k].w), hi, lo);
-        acc_square(bf_hi(r[k].w), hi, lo);
+        acc_square2(unpack_bf16x2(r[k].x), hi, lo);
+        acc_square2(unpack_bf16x2(r[k].y), hi, lo);
+        acc_square2(unpack_bf16x2(r[k].z), hi, lo);
+        acc_square2(unpack_bf16x2(r[k].w), hi, lo);
     }
-    DF S{hi, lo};
+    DF S = df_add(DF{hi.x, lo.x}, DF{hi.y, lo.y});
     const int wlim = tpr < 32 ? tpr : 32;
     for (int off = 1; off < wlim; off <<= 1)
         S = df_add(S, shfl_xor_df(S, off, tmask));   // identical in every lane
@@ -141,8 +138,9 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         }
     }
     float inv;
-    if (!inv_rms_df(S, s.H, s.eps, inv))     // team-uniform branch
+    if (!inv_rms_df(S, s.H, s.inv_h, s.eps, inv))     // team-uniform branch
         inv = inv_rms_fp64_path<VPT>(r, s.H, s.eps, tpr, team, red);
+    const float2 inv2 = f2(inv);
 
     // ---- normalise: y = bf16((r * inv) * gamma)
     uint4 y[VPT];
@@ -156,9 +154,8 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         uint32_t yw[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float a = __fmul_rn(__fmul_rn(bf_lo(rw[j]), inv), bf_lo(gw[j]));
-            float b = __fmul_rn(__fmul_rn(bf_hi(rw[j]), inv), bf_hi(gw[j]));
-            yw[j] = pack_bf16x2(a, b);
+            const float2 v = mul2(mul2(unpack_bf16x2(rw[j]), inv2), unpack_bf16x2(gw[j]));
+            yw[j] = pack_bf16x2(v.x, v.y);
         }
         y[k] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
     }
@@ -194,7 +191,7 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         const uint32_t yw[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
         if constexpr (!MX) {
             const float amax = __uint_as_float(am[k] << 16);
-            const float scale = __fdiv_rn(amax, 448.0f);
+            const float scale = div448(amax);
             const float d = am[k] ? scale : 1.0f;   // all-zero group: codes of +-0
             if ((t & 15) == 0) {
                 const int64_t g = v >> 4, G = s.H >> 7;   // v is a multiple of 16 here
@@ -204,23 +201,34 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
                 else
                     sc[g * s.M + row] = scale;
             }
+            const GroupDivisor gd = make_group_divisor(d);
             uint32_t c[4];
+            if (gd.fast) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                c[j] = e4m3x2(__fdiv_rn(bf_lo(yw[j]), d), __fdiv_rn(bf_hi(yw[j]), d));
+                for (int j = 0; j < 4; ++j) {
+                    const float2 qv = div_fast2(unpack_bf16x2(yw[j]), gd);
+                    c[j] = e4m3x2(qv.x, qv.y);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    c[j] = e4m3x2(__fdiv_rn(bf_lo(yw[j]), d), __fdiv_rn(bf_hi(yw[j]), d));
+            }
             uint2 q = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
             *reinterpret_cast<uint2 *>(s.out_q + row * (int64_t)s.H + (int64_t)v * 8) = q;
         } else {
             const int X = mx_exponent_from_bits(am[k]);
-            const float mult = __uint_as_float((uint32_t)(127 - X) << 23);   // 2^-X
+            const float2 mult = f2(__uint_as_float((uint32_t)(127 - X) << 23));   // 2^-X
             if ((t & 3) == 0) {
                 uint8_t *sc = (uint8_t *)s.out_scale;
                 sc[row * (int64_t)(s.H >> 5) + (v >> 2)] = (uint8_t)(X + 127);
             }
             uint32_t c[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                c[j] = e2m1x2(__fmul_rn(bf_lo(yw[j]), mult), __fmul_rn(bf_hi(yw[j]), mult));
+            for (int j = 0; j < 4; ++j) {
+                const float2 qv = mul2(unpack_bf16x2(yw[j]), mult);
+                c[j] = e2m1x2(qv.x, qv.y);
+            }
             uint32_t q = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
             *reinterpret_cast<uint32_t *>(s.out_q + row * (int64_t)(s.H >> 1) + (int64_t)v * 4) = q;
         }

@@ -59,6 +59,7 @@ _SIGNATURES = {
     "rmsq_sync_status": [_p],
     "rmsq_encode_e4m3": [_p, _p, _i64, _p],
     "rmsq_encode_e2m1": [_p, _p, _i64, _p],
+    "rmsq_check_group_division": [_p, _p],
 }
 
 
@@ -260,3 +261,12 @@ def encode_e2m1(v: torch.Tensor) -> torch.Tensor:
     out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
     _check(lib().rmsq_encode_e2m1(_ptr(v), _ptr(out), v.numel(), _stream(v.device)))
     return out
+
+
+def check_group_division(device=None) -> dict:
+    """Runs the library's exhaustive division self-check; returns its counters."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    counts = torch.zeros(4, dtype=torch.int64, device=dev)
+    _check(lib().rmsq_check_group_division(_ptr(counts), _stream(dev)))
+    c = counts.cpu().tolist()
+    return {"code_mismatches": c[0], "quotient_mismatches": c[1], "pairs": c[2], "scale_mismatches": c[3]}

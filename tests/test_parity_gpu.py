@@ -374,3 +374,13 @@ def test_persistent_wait_times_out_cleanly(oracle_mod):
     again = run_fp8(d, w.eps)
     parity.compare_fp8(again, ref, what="after timeout")
     assert rmsq.sync_status() == 0
+
+
+def test_group_division_is_exact_over_the_whole_domain():
+    """The FP8 quantiser's per-group reciprocal + FMA-correction division gives
+    the same E4M3 code as IEEE division for every (amax, y) pair it can see."""
+    c = rmsq.check_group_division()
+    assert c["pairs"] == sum(2 * (a + 1) for a in range(1, 0x7F80)), c
+    assert c["code_mismatches"] == 0, c
+    assert c["scale_mismatches"] == 0, c
+    print(c)
