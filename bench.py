@@ -307,12 +307,68 @@ def other_workloads(dev, stream) -> dict:
     return out
 
 
+def rank_workload(w, rank: int):
+    """Each rank draws its own batch of the same workload (seed + 1000 * rank)."""
+    from mxfp4_activation_quant_gb300 import synth
+    return synth.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank})
+
+
+def make_step(name: str, dev, rank: int, rows: int, opts):
+    """Inputs (CPU copies kept for the end-to-end leg), outputs and the step
+    function of one workload; returns (step, bytes, rows, io) where io lists
+    (device tensor, host tensor) pairs for the copies of the e2e leg."""
+    import torch
+    from mxfp4_activation_quant_gb300 import rmsq, synth
+
+    w = synth.WORKLOADS[name]
+    if rows:
+        w = synth.Workload(**{**w.__dict__, "M": rows})
+    wr = rank_workload(w, rank)
+    d_cpu = synth.make_inputs(wr)
+    d = {k: v.to(dev) for k, v in d_cpu.items()}
+    M = w.M
+    if w.kind == "qknorm":
+        outs = {"qq": torch.empty((M, w.Hq), dtype=torch.uint8, device=dev),
+                "qs": torch.empty((M, w.Hq // 128), dtype=torch.float32, device=dev),
+                "kq": torch.empty((M, w.Hkv), dtype=torch.uint8, device=dev),
+                "ks": torch.empty((M, w.Hkv // 128), dtype=torch.float32, device=dev)}
+
+        def step():
+            rmsq.qknorm_quant_fp8_into(d["q_a"], d["kv_a"], d["gamma_q"], d["gamma_kv"], outs["qq"], outs["qs"],
+                                       outs["kq"], outs["ks"], eps=w.eps)
+        nbytes = qk_bytes(M, w.Hq, w.Hkv)
+    elif w.kind == "mxfp4":
+        outs = {"q": torch.empty((M, w.H // 2), dtype=torch.uint8, device=dev),
+                "s": torch.empty((M, w.H // 32), dtype=torch.uint8, device=dev),
+                "r": torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)}
+
+        def step():
+            rmsq.add_rmsnorm_quant_mxfp4_into(d["x"], d["gamma"], d["residual"], outs["q"], outs["s"], outs["r"],
+                                              None, eps=w.eps, opts=opts)
+        nbytes = mx_bytes(M, w.H)
+    else:
+        col = w.scale_layout == "col"
+        outs = {"q": torch.empty((M, w.H), dtype=torch.uint8, device=dev),
+                "s": torch.empty(((w.H // 128, M) if col else (M, w.H // 128)), dtype=torch.float32, device=dev),
+                "r": torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)}
+        if w.keep_bf16:
+            outs["y"] = torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)
+
+        def step():
+            rmsq.add_rmsnorm_quant_fp8_into(d["x"], d["gamma"], d["residual"], outs["q"], outs["s"], outs["r"],
+                                            outs.get("y"), eps=w.eps, scale_layout=w.scale_layout, opts=opts)
+        nbytes = algorithmic_bytes(M, w.H, True, w.keep_bf16)
+    io_in = [(d[k], d_cpu[k].pin_memory()) for k in d]
+    io_out = [(v, torch.empty(v.shape, dtype=v.dtype).pin_memory()) for v in outs.values()]
+    return step, nbytes, M, io_in, io_out, w, d_cpu
+
+
 def run_ours(args) -> None:
     import torch
     import torch.distributed as dist
 
     from mxfp4_activation_quant_gb300 import build as lib_build
-    from mxfp4_activation_quant_gb300 import rmsq, synth
+    from mxfp4_activation_quant_gb300 import rmsq
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -324,26 +380,10 @@ def run_ours(args) -> None:
     lib_build.build()
     rmsq.lib()
 
-    w = synth.WORKLOADS[WORKLOAD]
-    if args.rows:                                    # smaller case for profiler captures only
-        w = synth.Workload(**{**w.__dict__, "M": args.rows})
-    M, H = w.M, w.H
-    # each rank its own batch: the prefill seed shifted by the rank
-    wr = synth.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank})
-    d_cpu = synth.make_inputs(wr)
-    x, res, gamma = (d_cpu[k].to(dev) for k in ("x", "residual", "gamma"))
-    q = torch.empty((M, H), dtype=torch.float8_e4m3fn, device=dev)
-    scale = torch.empty((M, H // 128), dtype=torch.float32, device=dev)
-    res_out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
-    y = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.current_stream(dev)
     kernel = {"auto": rmsq.KERNEL_AUTO, "rows": rmsq.KERNEL_ROWS, "persistent": rmsq.KERNEL_PERSISTENT}[args.kernel]
     opts = rmsq.LaunchOpts(kernel=kernel) if kernel != rmsq.KERNEL_AUTO else None
-
-    def step():
-        rmsq.add_rmsnorm_quant_fp8_into(x, gamma, res, q, scale, res_out, y, eps=w.eps, opts=opts)
-
-    bytes_step = algorithmic_bytes(M, H)
+    step, bytes_step, M, io_in, io_out, w, d_cpu = make_step(args.workload, dev, rank, args.rows, opts)
+    stream = torch.cuda.current_stream(dev)
     peak, peak_kind = measured_peaks()
     sampler = ClockSampler(gpu_id_for(dev)) if rank == 0 else None
     time.sleep(0.25 if sampler else 0)
@@ -356,62 +396,49 @@ def run_ours(args) -> None:
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_ms = max_over_ranks(total_ms, world, dev)
     value = world * bytes_step * args.steps / (max_ms * 1e-3) / 1e9
     launch_ms = statistics.mean(each_ms)
     achieved = bytes_step / (launch_ms * 1e-3) / 1e9
 
     # end to end through the public API: pinned host buffers, copies inside the timed region
-    x_h, r_h, g_h = (d_cpu[k].pin_memory() for k in ("x", "residual", "gamma"))
-    q_h = torch.empty(q.shape, dtype=torch.uint8).pin_memory()
-    s_h = torch.empty(scale.shape, dtype=torch.float32).pin_memory()
-    ro_h = torch.empty(res_out.shape, dtype=torch.bfloat16).pin_memory()
-    y_h = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
-
     def e2e_step():
-        x.copy_(x_h, non_blocking=True)
-        res.copy_(r_h, non_blocking=True)
-        gamma.copy_(g_h, non_blocking=True)
-        rmsq.add_rmsnorm_quant_fp8_into(x, gamma, res, q, scale, res_out, y, eps=w.eps, opts=opts)
-        q_h.copy_(q.view(torch.uint8), non_blocking=True)
-        s_h.copy_(scale, non_blocking=True)
-        ro_h.copy_(res_out, non_blocking=True)
-        y_h.copy_(y, non_blocking=True)
+        for dv, hv in io_in:
+            dv.copy_(hv, non_blocking=True)
+        step()
+        for dv, hv in io_out:
+            hv.copy_(dv, non_blocking=True)
 
-    e2e_steps = max(3, min(20, args.steps))
     e2e_value = None
     if not args.no_e2e:
+        e2e_steps = max(3, min(20, args.steps))
         for _ in range(2):
             e2e_step()
         if world > 1:
             dist.barrier()
         e2e_ms, _ = time_launches(e2e_step, e2e_steps, stream)
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_value = round(world * bytes_step * e2e_steps / (float(t.item()) * 1e-3) / 1e9, 1)
-    h2d = sum(v.numel() * v.element_size() for v in (x_h, r_h, g_h))
-    d2h = sum(v.numel() * v.element_size() for v in (q_h, s_h, ro_h, y_h))
+        e2e_value = round(world * bytes_step * e2e_steps / (max_over_ranks(e2e_ms, world, dev) * 1e-3) / 1e9, 1)
+    h2d = sum(hv.numel() * hv.element_size() for _, hv in io_in)
+    d2h = sum(hv.numel() * hv.element_size() for _, hv in io_out)
 
-    extra = other_workloads(dev, stream) if (rank == 0 and not args.no_extra) else None
-    cpu = cpu_baseline(d_cpu, w) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    headline = args.workload == WORKLOAD and not args.rows
+    extra = other_workloads(dev, stream) if (rank == 0 and headline and not args.no_extra) else None
+    cpu = cpu_baseline(d_cpu, w) if (rank == 0 and world == 1 and headline and not args.no_cpu) else None
     if world > 1:
         dist.barrier()
     if rank == 0:
-        kernel_name = "rmsq_rows_kernel" if kernel in (rmsq.KERNEL_AUTO, rmsq.KERNEL_ROWS) else "rmsq_bulk_kernel"
+        kernel_name = f"{args.workload}:{'bulk' if kernel == rmsq.KERNEL_PERSISTENT else 'rows'}"
         traffic = recorded_traffic(kernel_name)
         line = {
-            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "metric": METRIC if headline else f"HBM GB/s & rows/s, {args.workload} workload",
+            "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": f"prefill input RMSNorm: M={M} H={H} bf16, residual add, "
-                                   "FP8 E4M3 1x128 groups, fp32 scales [M,56], keep_bf16 y",
+            "config": {"workload": WORKLOAD_TEXT[w.kind if w.kind != "fp8" else args.workload].format(M=M),
                        "global_rows": M * world, "parallelism": f"rows sharded, {world} independent batch(es)",
-                       "l2": "inputs (470 MB) larger than L2 (129 MB); no flush needed",
+                       "l2": ("inputs larger than L2 (129 MB); no flush needed" if bytes_step > 400e6 else
+                              "inputs smaller than L2: back-to-back steps are partly L2-resident"),
                        "kernel": args.kernel, "bytes_per_step": bytes_step},
             "rows_per_s": round(world * M * args.steps / (max_ms * 1e-3), 1),
             "pct_of_peak": round(100 * value / world / peak, 2),
@@ -430,6 +457,26 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
 
 
+WORKLOAD_TEXT = {
+    "prefill": "prefill input RMSNorm: M={M} H=7168 bf16, residual add, FP8 E4M3 1x128 groups, "
+               "fp32 scales [M,56], keep_bf16 y",
+    "decode": "decode input RMSNorm: M={M} H=7168 bf16, residual add, FP8 E4M3 1x128, column-major scales",
+    "qknorm": "MLA latents: q_a [M,1536] + kv_a [M,512], no residual, FP8 E4M3 1x128, one launch",
+    "mxfp4": "input RMSNorm M={M} H=7168, residual add, MXFP4 (E8M0 per 32, E2M1 packed)",
+}
+
+
+def max_over_ranks(ms: float, world: int, dev) -> float:
+    """The slowest rank's time (all ranks call this)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -437,6 +484,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--kernel", choices=["auto", "rows", "persistent"], default="auto")
+    ap.add_argument("--workload", choices=["prefill", "decode", "qknorm", "mxfp4"], default=WORKLOAD,
+                    help="the timed step (the headline line is prefill)")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / qknorm / MXFP4 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")

@@ -188,9 +188,10 @@ rmsq_status rmsq_encode_e2m1(const float *in, uint8_t *out, int64_t n, void *str
  * finite bf16 amax and every bf16 y with |y| <= amax (both signs), the E4M3
  * code the kernels produce for y / (amax/448) is compared with the code of
  * IEEE fp32 division, and the kernels' scale amax/448 with the IEEE
- * quotient. `counts` is a caller-zeroed device array of four unsigned
+ * quotient. `counts` is a caller-zeroed device array of five unsigned
  * 64-bit counters, incremented by: code mismatches, fp32 quotient mismatches,
- * (amax, y) pairs checked, scale mismatches. Enqueued on `stream`.
+ * (amax, y) pairs checked, scale mismatches, quotient mismatches whose IEEE
+ * quotient is a normal fp32 number. Enqueued on `stream`.
  */
 rmsq_status rmsq_check_group_division(unsigned long long *counts, void *stream);
 

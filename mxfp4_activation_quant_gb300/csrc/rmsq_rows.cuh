@@ -206,7 +206,7 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
             if (gd.fast) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float2 qv = div_fast2(unpack_bf16x2(yw[j]), gd);
+                    const float2 qv = div_fast_neg2(unpack_bf16x2(yw[j] ^ 0x80008000u), gd);
                     c[j] = e4m3x2(qv.x, qv.y);
                 }
             } else {

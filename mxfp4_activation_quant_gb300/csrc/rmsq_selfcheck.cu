@@ -17,19 +17,21 @@ __global__ void check_group_division_kernel(unsigned long long *counts)
     const GroupDivisor g = make_group_divisor(d);
     if (threadIdx.x == 0 && __float_as_uint(d) != __float_as_uint(__fdiv_rn(amax, 448.0f)))
         atomicAdd(&counts[3], 1ull);
-    unsigned long long code_bad = 0, quot_bad = 0, n = 0;
+    unsigned long long code_bad = 0, quot_bad = 0, norm_bad = 0, n = 0;
     for (uint32_t b = threadIdx.x; b <= a; b += blockDim.x) {
         for (uint32_t sgn = 0; sgn < 2; ++sgn) {
             const float y = __uint_as_float((b | (sgn << 15)) << 16);
             const float ref = __fdiv_rn(y, d);
-            float got = __fdiv_rn(y, d);
+            float got = ref;
             if (g.fast) {
-                const float2 pair = div_fast2(make_float2(y, -y), g);   // the packed form the kernels use
+                // the packed form the kernels use, on -y in both lanes
+                const float2 pair = div_fast_neg2(make_float2(-y, -y), g);
                 got = pair.x;
-                quot_bad += __float_as_uint(pair.y) != __float_as_uint(__fdiv_rn(-y, d));
             }
             code_bad += (e4m3x2(got, 0.0f) & 0xffu) != (e4m3x2(ref, 0.0f) & 0xffu);
-            quot_bad += __float_as_uint(got) != __float_as_uint(ref);
+            const bool qb = __float_as_uint(got) != __float_as_uint(ref);
+            quot_bad += qb;
+            norm_bad += qb && fabsf(ref) >= 0x1p-126f;
             ++n;
         }
     }
@@ -37,11 +39,13 @@ __global__ void check_group_division_kernel(unsigned long long *counts)
         code_bad += __shfl_xor_sync(0xffffffffu, code_bad, off);
         quot_bad += __shfl_xor_sync(0xffffffffu, quot_bad, off);
         n += __shfl_xor_sync(0xffffffffu, n, off);
+        norm_bad += __shfl_xor_sync(0xffffffffu, norm_bad, off);
     }
     if ((threadIdx.x & 31) == 0) {
         atomicAdd(&counts[0], code_bad);
         atomicAdd(&counts[1], quot_bad);
         atomicAdd(&counts[2], n);
+        atomicAdd(&counts[4], norm_bad);
     }
 }
 

@@ -266,7 +266,8 @@ def encode_e2m1(v: torch.Tensor) -> torch.Tensor:
 def check_group_division(device=None) -> dict:
     """Runs the library's exhaustive division self-check; returns its counters."""
     dev = torch.device("cuda") if device is None else torch.device(device)
-    counts = torch.zeros(4, dtype=torch.int64, device=dev)
+    counts = torch.zeros(5, dtype=torch.int64, device=dev)
     _check(lib().rmsq_check_group_division(_ptr(counts), _stream(dev)))
     c = counts.cpu().tolist()
-    return {"code_mismatches": c[0], "quotient_mismatches": c[1], "pairs": c[2], "scale_mismatches": c[3]}
+    return {"code_mismatches": c[0], "quotient_mismatches": c[1], "pairs": c[2], "scale_mismatches": c[3],
+            "normal_quotient_mismatches": c[4]}
