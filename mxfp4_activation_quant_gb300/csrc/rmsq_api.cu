@@ -231,8 +231,9 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
         LaunchParams p{};
         p.seg[0] = s;
         p.nseg = 1;
-        cudaError_t e = mx ? launch_rows_mx(vpt, p, (int)blocks, rpb * tpr, st)
-                           : launch_rows_fp8(vpt, p, (int)blocks, rpb * tpr, st);
+        const int ts = (static_shape(vpt, tpr) && vpt * tpr * 8 == s.H) ? tpr : 0;
+        cudaError_t e = mx ? launch_rows_mx(vpt, ts, p, (int)blocks, rpb * tpr, st)
+                           : launch_rows_fp8(vpt, ts, p, (int)blocks, rpb * tpr, st);
         if (e != cudaSuccess)
             return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
         return ok();
@@ -252,9 +253,10 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
         size_t smem = bulk_smem(s.H, s.res != nullptr);
         if (smem + sizeof(float2) * 64 + 256 > (size_t)smem_max)
             return fail(RMSQ_ERR_UNSUPPORTED, "H=%d needs %zu bytes of shared memory", s.H, smem);
+        const int ts = (static_shape(vpt, tpr) && vpt * tpr * 8 == s.H) ? tpr : 0;
         int64_t grid = o.grid;
         if (grid <= 0) {
-            int per_sm = bulk_occupancy(mx, vpt, tpr, smem);
+            int per_sm = bulk_occupancy(mx, vpt, ts, tpr, smem);
             if (per_sm <= 0)
                 return fail(RMSQ_ERR_UNSUPPORTED, "persistent kernel does not fit on an SM");
             grid = (int64_t)per_sm * sms;
@@ -270,8 +272,7 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
         bp.debug_skip_row = o.debug_skip_row;
         bp.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
         bp.status = status;
-        e = mx ? launch_bulk_mx(vpt, bp, (int)grid, tpr, smem, st)
-               : launch_bulk_fp8(vpt, bp, (int)grid, tpr, smem, st);
+        e = launch_bulk(mx, vpt, ts, bp, (int)grid, tpr, smem, st);
         if (e != cudaSuccess)
             return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
         return ok();
@@ -418,21 +419,27 @@ rmsq_status rmsq_qknorm_quant_fp8(
                       scale_layout, nullptr, out_q_bf16);
     Seg sk = make_seg(kv_a, ld_kv, nullptr, 0, gamma_kv, eps, M, Hkv, out_kv_q, out_kv_scale,
                       scale_layout, nullptr, out_kv_bf16);
-    // one vectors-per-thread value serves both latents: least padding first
-    int vpt = 0, tq = 0, tk = 0;
-    int64_t best_waste = -1;
-    for (int v : kVptPreference) {
-        int a, b;
-        int64_t wa, wb;
-        if (team_ok(Hq / 8, v, 16, a, wa) && team_ok(Hkv / 8, v, 16, b, wb) &&
-            (best_waste < 0 || wa + wb < best_waste)) {
-            vpt = v;
-            tq = a;
-            tk = b;
-            best_waste = wa + wb;
+    // Team shapes: the compiled-in MLA pair shape when it fits exactly,
+    // otherwise one vectors-per-thread value for both latents, least padding
+    // first.
+    int v0 = 0, v1 = 0, tq = 0, tk = 0, t0s = 0, t1s = 0;
+    if (Hq == 3 * 64 * 8 && Hkv == 4 * 16 * 8) {
+        v0 = 3; tq = 64; v1 = 4; tk = 16; t0s = 64; t1s = 16;
+    } else {
+        int64_t best_waste = -1;
+        for (int v : kVptPreference) {
+            int a, b;
+            int64_t wa, wb;
+            if (team_ok(Hq / 8, v, 16, a, wa) && team_ok(Hkv / 8, v, 16, b, wb) &&
+                (best_waste < 0 || wa + wb < best_waste)) {
+                v0 = v1 = v;
+                tq = a;
+                tk = b;
+                best_waste = wa + wb;
+            }
         }
     }
-    if (!vpt)
+    if (!v0)
         return fail(RMSQ_ERR_UNSUPPORTED, "no common team shape for Hq=%lld, Hkv=%lld",
                     (long long)Hq, (long long)Hkv);
     int threads = default_rows_per_block(tq) * tq;
@@ -454,7 +461,7 @@ rmsq_status rmsq_qknorm_quant_fp8(
     p.seg[0] = sq;
     p.seg[1] = sk;
     p.nseg = 2;
-    cudaError_t e = launch_rows_fp8(vpt, p, (int)(bq + bk), threads, (cudaStream_t)stream);
+    cudaError_t e = launch_dual(v0, t0s, v1, t1s, p, (int)(bq + bk), threads, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     return ok();

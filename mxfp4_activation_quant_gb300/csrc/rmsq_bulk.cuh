@@ -95,13 +95,14 @@ __host__ __device__ inline size_t bulk_smem_bytes(int H, bool has_res)
     return row + stage * kStages + kStages * sizeof(uint64_t) + kStages * sizeof(int) + 16;
 }
 
-template <int VPT, bool MX>
+template <int VPT, int TPR, bool MX>
 __global__ void __launch_bounds__(kMaxThreads) bulk_kernel(const __grid_constant__ BulkParams p)
 {
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ RedSmem red;
+    constexpr bool GUARD = TPR == 0;
     const Seg &s = p.s;
-    const int tpr = s.tpr;            // == blockDim.x
+    const int tpr = TPR ? TPR : s.tpr;   // == blockDim.x
     const int t = threadIdx.x;
     const int nvec = s.H >> 3;
     const bool has_res = s.res != nullptr;
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kMaxThreads) bulk_kernel(const __grid_constant
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = k * tpr + t;
-            if (v < nvec) {
+            if (!GUARD || v < nvec) {
                 r[k] = lds128(xs + v);
                 if (has_res)
                     r[k] = add_bf16x8(r[k], lds128(rs + v));
@@ -190,17 +191,17 @@ __global__ void __launch_bounds__(kMaxThreads) bulk_kernel(const __grid_constant
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * tpr + t;
-                if (v < nvec)
+                if (!GUARD || v < nvec)
                     s.out_res[row * nv + v] = r[k];
             }
         }
-        row_finish<VPT, MX, true>(s, row, t, 0, it & 1, red, r, g_sm);
+        row_finish<VPT, TPR, MX, true>(s, row, t, 0, it & 1, red, r, g_sm);
     }
 }
 
 template <bool MX>
-cudaError_t launch_bulk_impl(int vpt, const BulkParams &p, int grid, int threads, size_t smem,
-                             cudaStream_t st)
+cudaError_t launch_bulk_impl(int vpt, int tpr_static, const BulkParams &p, int grid, int threads,
+                             size_t smem, cudaStream_t st)
 {
     auto go = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -209,21 +210,23 @@ cudaError_t launch_bulk_impl(int vpt, const BulkParams &p, int grid, int threads
         kern<<<grid, threads, smem, st>>>(p);
         return cudaGetLastError();
     };
+    if (tpr_static)
+        return (vpt == 4 && tpr_static == 224) ? go(bulk_kernel<4, 224, MX>) : cudaErrorInvalidValue;
     switch (vpt) {
-    case 1: return go(bulk_kernel<1, MX>);
-    case 2: return go(bulk_kernel<2, MX>);
-    case 3: return go(bulk_kernel<3, MX>);
-    case 4: return go(bulk_kernel<4, MX>);
-    case 5: return go(bulk_kernel<5, MX>);
-    case 6: return go(bulk_kernel<6, MX>);
-    case 7: return go(bulk_kernel<7, MX>);
-    case 8: return go(bulk_kernel<8, MX>);
+    case 1: return go(bulk_kernel<1, 0, MX>);
+    case 2: return go(bulk_kernel<2, 0, MX>);
+    case 3: return go(bulk_kernel<3, 0, MX>);
+    case 4: return go(bulk_kernel<4, 0, MX>);
+    case 5: return go(bulk_kernel<5, 0, MX>);
+    case 6: return go(bulk_kernel<6, 0, MX>);
+    case 7: return go(bulk_kernel<7, 0, MX>);
+    case 8: return go(bulk_kernel<8, 0, MX>);
     default: return cudaErrorInvalidValue;
     }
 }
 
 template <bool MX>
-int bulk_blocks_per_sm(int vpt, int threads, size_t smem)
+int bulk_blocks_per_sm(int vpt, int tpr_static, int threads, size_t smem)
 {
     int n = 0;
     auto occ = [&](auto kern) {
@@ -231,15 +234,20 @@ int bulk_blocks_per_sm(int vpt, int threads, size_t smem)
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess)
             n = 0;
     };
+    if (tpr_static) {
+        if (vpt == 4 && tpr_static == 224)
+            occ(bulk_kernel<4, 224, MX>);
+        return n;
+    }
     switch (vpt) {
-    case 1: occ(bulk_kernel<1, MX>); break;
-    case 2: occ(bulk_kernel<2, MX>); break;
-    case 3: occ(bulk_kernel<3, MX>); break;
-    case 4: occ(bulk_kernel<4, MX>); break;
-    case 5: occ(bulk_kernel<5, MX>); break;
-    case 6: occ(bulk_kernel<6, MX>); break;
-    case 7: occ(bulk_kernel<7, MX>); break;
-    case 8: occ(bulk_kernel<8, MX>); break;
+    case 1: occ(bulk_kernel<1, 0, MX>); break;
+    case 2: occ(bulk_kernel<2, 0, MX>); break;
+    case 3: occ(bulk_kernel<3, 0, MX>); break;
+    case 4: occ(bulk_kernel<4, 0, MX>); break;
+    case 5: occ(bulk_kernel<5, 0, MX>); break;
+    case 6: occ(bulk_kernel<6, 0, MX>); break;
+    case 7: occ(bulk_kernel<7, 0, MX>); break;
+    case 8: occ(bulk_kernel<8, 0, MX>); break;
     default: break;
     }
     return n;

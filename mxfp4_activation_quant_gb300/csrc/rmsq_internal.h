@@ -44,15 +44,23 @@ struct BulkParams {
 
 constexpr int kMaxThreads = 512;
 
-// Launchers (one switch over the vectors-per-thread instantiations each).
-cudaError_t launch_rows_fp8(int vpt, const LaunchParams &p, int grid, int threads, cudaStream_t st);
-cudaError_t launch_rows_mx(int vpt, const LaunchParams &p, int grid, int threads, cudaStream_t st);
-cudaError_t launch_bulk_fp8(int vpt, const BulkParams &p, int grid, int threads, size_t smem,
+// Launchers (a switch over the instantiations each). tpr_static != 0 selects
+// a kernel compiled for that exact team size (see static_shape).
+cudaError_t launch_rows_fp8(int vpt, int tpr_static, const LaunchParams &p, int grid, int threads,
                             cudaStream_t st);
-cudaError_t launch_bulk_mx(int vpt, const BulkParams &p, int grid, int threads, size_t smem,
+cudaError_t launch_rows_mx(int vpt, int tpr_static, const LaunchParams &p, int grid, int threads,
                            cudaStream_t st);
-int bulk_occupancy(bool mx, int vpt, int threads, size_t smem);
+cudaError_t launch_dual(int v0, int t0, int v1, int t1, const LaunchParams &p, int grid, int threads,
+                        cudaStream_t st);
+cudaError_t launch_bulk(bool mx, int vpt, int tpr_static, const BulkParams &p, int grid, int threads,
+                        size_t smem, cudaStream_t st);
+int bulk_occupancy(bool mx, int vpt, int tpr_static, int threads, size_t smem);
 size_t bulk_smem(int H, bool has_res);
 bool vpt_instantiated(int vpt);
+// Team shapes also compiled with a fixed team size (exact fits of the hot
+// widths): one tensor of H = 7168 as 4 vectors x 224 threads; the MLA pair
+// q_a 1536 as 3 x 64 and kv_a 512 as 4 x 16.
+bool static_shape(int vpt, int tpr);
+bool static_dual_shape(int v0, int t0, int v1, int t1);
 
 }  // namespace rmsq

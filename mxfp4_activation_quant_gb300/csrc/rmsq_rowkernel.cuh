@@ -1,25 +1,20 @@
-// Register-resident row kernel: each team loads its row of x (and residual)
+// Register-resident row kernels: each team loads its row of x (and residual)
 // straight into registers with 16-byte streaming loads, adds, writes the
-// residual back, and finishes the row (rmsq_rows.cuh). One launch covers one
-// or two segments; blocks [0, seg[0].blocks) belong to the first.
+// residual back, and finishes the row (rmsq_rows.cuh).
+//   rows_kernel<VPT, TPR, MX>       one tensor
+//   dual_kernel<V0, T0, V1, T1>     two tensors (the MLA q_a / kv_a pair),
+//                                   blocks [0, seg[0].blocks) on the first
+// TPR / T0 / T1 = 0 means the team size is read at run time.
 #pragma once
 
 #include "rmsq_rows.cuh"
 
 namespace rmsq {
 
-template <int VPT, bool MX>
-__global__ void __launch_bounds__(kMaxThreads) rows_kernel(const __grid_constant__ LaunchParams p)
+template <int VPT, int TPR, bool MX>
+__device__ __forceinline__ void block_rows(const Seg &s, int b, RedSmem &red)
 {
-    __shared__ RedSmem red;
-    int b = blockIdx.x;
-    int si = 0;
-    if (p.nseg == 2 && b >= p.seg[0].blocks) {
-        b -= p.seg[0].blocks;
-        si = 1;
-    }
-    const Seg &s = p.seg[si];
-    const int tpr = s.tpr;
+    const int tpr = TPR ? TPR : s.tpr;
     const int team = threadIdx.x / tpr;
     if (team >= s.rpb)
         return;                                   // idle team of a shared-size block
@@ -27,50 +22,46 @@ __global__ void __launch_bounds__(kMaxThreads) rows_kernel(const __grid_constant
     const int64_t row = (int64_t)b * s.rpb + team;
     if (row >= s.M)
         return;                                   // whole teams leave together
+    row_from_global<VPT, TPR, MX>(s, row, t, team, 0, red);
+}
 
-    const int nvec = s.H >> 3;
-    uint4 r[VPT];
-    const uint4 *xr = s.x + row * s.ldx_v;
-    // vectors past the row end (padded team shapes) read as zero and are
-    // never stored; they add nothing to the sum of squares
-    if (s.res) {
-        const uint4 *rr = s.res + row * s.ldres_v;
-        uint4 xv[VPT], rv[VPT];
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * tpr + t;
-            xv[k] = v < nvec ? ld_stream(xr + v) : make_uint4(0, 0, 0, 0);
-            rv[k] = v < nvec ? ld_stream(rr + v) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * tpr + t;
-            r[k] = add_bf16x8(xv[k], rv[k]);
-            if (v < nvec)
-                s.out_res[row * nvec + v] = r[k];
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * tpr + t;
-            r[k] = v < nvec ? ld_stream(xr + v) : make_uint4(0, 0, 0, 0);
-        }
-    }
-    row_finish<VPT, MX, false>(s, row, t, team, 0, red, r, s.gamma);
+template <int VPT, int TPR, bool MX>
+__global__ void __launch_bounds__(kMaxThreads) rows_kernel(const __grid_constant__ LaunchParams p)
+{
+    __shared__ RedSmem red;
+    block_rows<VPT, TPR, MX>(p.seg[0], blockIdx.x, red);
+}
+
+template <int V0, int T0, int V1, int T1>
+__global__ void __launch_bounds__(kMaxThreads) dual_kernel(const __grid_constant__ LaunchParams p)
+{
+    __shared__ RedSmem red;
+    if ((int)blockIdx.x < p.seg[0].blocks)
+        block_rows<V0, T0, false>(p.seg[0], blockIdx.x, red);
+    else
+        block_rows<V1, T1, false>(p.seg[1], blockIdx.x - p.seg[0].blocks, red);
 }
 
 template <bool MX>
-cudaError_t launch_rows_impl(int vpt, const LaunchParams &p, int grid, int threads, cudaStream_t st)
+cudaError_t launch_rows_impl(int vpt, int tpr_static, const LaunchParams &p, int grid, int threads,
+                             cudaStream_t st)
 {
+    if (tpr_static) {
+        if (vpt == 4 && tpr_static == 224)
+            rows_kernel<4, 224, MX><<<grid, threads, 0, st>>>(p);
+        else
+            return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    }
     switch (vpt) {
-    case 1: rows_kernel<1, MX><<<grid, threads, 0, st>>>(p); break;
-    case 2: rows_kernel<2, MX><<<grid, threads, 0, st>>>(p); break;
-    case 3: rows_kernel<3, MX><<<grid, threads, 0, st>>>(p); break;
-    case 4: rows_kernel<4, MX><<<grid, threads, 0, st>>>(p); break;
-    case 5: rows_kernel<5, MX><<<grid, threads, 0, st>>>(p); break;
-    case 6: rows_kernel<6, MX><<<grid, threads, 0, st>>>(p); break;
-    case 7: rows_kernel<7, MX><<<grid, threads, 0, st>>>(p); break;
-    case 8: rows_kernel<8, MX><<<grid, threads, 0, st>>>(p); break;
+    case 1: rows_kernel<1, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 2: rows_kernel<2, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 3: rows_kernel<3, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 4: rows_kernel<4, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 5: rows_kernel<5, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 6: rows_kernel<6, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 7: rows_kernel<7, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 8: rows_kernel<8, 0, MX><<<grid, threads, 0, st>>>(p); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

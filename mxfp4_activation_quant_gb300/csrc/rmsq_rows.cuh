@@ -97,20 +97,54 @@ __device__ __forceinline__ float inv_rms_fp64_path(const uint4 (&r)[VPT], int H,
     return (float)(1.0 / sqrt(acc / (double)H + (double)eps));
 }
 
+// Sum over a team of the per-thread double-float partials; the same bits in
+// every thread of the team. Within a warp an xor butterfly; across the
+// team's warps (tpr > 32) lane 0 of each warp publishes its partial, then in
+// every warp lanes 0..nw-1 load one partial each and butterfly over the next
+// power of two, and lane 0's sum is broadcast. `parity` alternates the
+// shared-memory slots between consecutive rows of a persistent team.
+template <int TPR>
+__device__ __forceinline__ DF team_sum(DF S, int tpr, int team, int parity, RedSmem &red,
+                                       unsigned tmask)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1)
+        if (off < tpr)
+            S = df_add_lazy(S, shfl_xor_df(S, off, tmask));
+    if (tpr > 32) {
+        const int nw = tpr >> 5, w0 = team * nw;
+        if (lane == 0)
+            red.part[parity][warp] = make_float2(S.hi, S.lo);
+        team_bar(team, tpr);
+        const float2 p = lane < nw ? red.part[parity][w0 + lane] : make_float2(0.0f, 0.0f);
+        DF T{p.x, p.y};
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1)
+            if (off < nw)
+                T = df_add_lazy(T, shfl_xor_df(T, off, 0xffffffffu));
+        S = DF{__shfl_sync(0xffffffffu, T.hi, 0), __shfl_sync(0xffffffffu, T.lo, 0)};
+    }
+    return df_renorm(S);
+}
+
 // Everything after the row is loaded: r holds the thread's VPT vectors of
 // bf16 r (residual already added and written back by the caller). gamma is
 // read from shared memory (GAMMA_SHARED) or through the read-only cache.
+// TPR is the team size when known at compile time (the row is then an exact
+// fit, tpr * VPT * 8 == H), or 0 for a runtime team size with padding guards.
 // Elementwise arithmetic runs on packed fp32 pairs.
-template <int VPT, bool MX, bool GAMMA_SHARED>
+template <int VPT, int TPR, bool MX, bool GAMMA_SHARED>
 __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int team, int parity,
                                            RedSmem &red, const uint4 (&r)[VPT],
                                            const uint4 *gamma_src)
 {
     constexpr int GV = MX ? 4 : 16;   // 16-byte vectors per quant group
-    const int tpr = s.tpr;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr bool GUARD = TPR == 0;
+    const int tpr = TPR ? TPR : s.tpr;
+    const int lane = threadIdx.x & 31;
     const unsigned tmask = team_lane_mask(tpr, lane);
-    const int nvec = s.H >> 3;
+    const int nvec = TPR ? TPR * VPT : (s.H >> 3);
 
     // ---- sum of squares: exact squares, two packed double-float accumulators
     float2 hi = f2(0.0f), lo = f2(0.0f);
@@ -121,22 +155,7 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         acc_square2(unpack_bf16x2(r[k].z), hi, lo);
         acc_square2(unpack_bf16x2(r[k].w), hi, lo);
     }
-    DF S = df_add(DF{hi.x, lo.x}, DF{hi.y, lo.y});
-    const int wlim = tpr < 32 ? tpr : 32;
-    for (int off = 1; off < wlim; off <<= 1)
-        S = df_add(S, shfl_xor_df(S, off, tmask));   // identical in every lane
-    if (tpr > 32) {
-        const int nw = tpr >> 5, w0 = team * nw;
-        if (lane == 0)
-            red.part[parity][warp] = make_float2(S.hi, S.lo);
-        team_bar(team, tpr);
-        float2 p0 = red.part[parity][w0];
-        S = DF{p0.x, p0.y};
-        for (int i = 1; i < nw; ++i) {
-            float2 pi = red.part[parity][w0 + i];
-            S = df_add(S, DF{pi.x, pi.y});
-        }
-    }
+    const DF S = team_sum<TPR>(df_add_lazy(DF{hi.x, lo.x}, DF{hi.y, lo.y}), tpr, team, parity, red, tmask);
     float inv;
     if (!inv_rms_df(S, s.H, s.inv_h, s.eps, inv))     // team-uniform branch
         inv = inv_rms_fp64_path<VPT>(r, s.H, s.eps, tpr, team, red);
@@ -147,7 +166,7 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int vk = k * tpr + t;
-        const uint4 g = vk >= nvec ? make_uint4(0, 0, 0, 0)
+        const uint4 g = (GUARD && vk >= nvec) ? make_uint4(0, 0, 0, 0)
                         : GAMMA_SHARED ? gamma_src[vk] : ld_keep(gamma_src + vk);
         const uint32_t rw[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
         const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
@@ -160,10 +179,11 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         y[k] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
     }
     if (s.out_bf16) {
+        uint4 *yrow = s.out_bf16 + row * nvec + t;
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
-            if (k * tpr + t < nvec)
-                s.out_bf16[row * nvec + k * tpr + t] = y[k];
+            if (!GUARD || k * tpr + t < nvec)
+                yrow[k * tpr] = y[k];
     }
 
     // ---- group amax over GV lanes (two vectors packed per shuffle)
@@ -183,23 +203,21 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
     }
 
     // ---- quantise and store
+    const bool leader = (t & (GV - 1)) == 0;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = k * tpr + t;   // vector index in the row
-        if (v >= nvec)
+        if (GUARD && v >= nvec)
             continue;                // padding of the team shape (whole groups)
         const uint32_t yw[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
         if constexpr (!MX) {
             const float amax = __uint_as_float(am[k] << 16);
             const float scale = div448(amax);
             const float d = am[k] ? scale : 1.0f;   // all-zero group: codes of +-0
-            if ((t & 15) == 0) {
-                const int64_t g = v >> 4, G = s.H >> 7;   // v is a multiple of 16 here
+            if (leader) {
+                const int64_t g = v >> 4, G = s.H >> 7;
                 float *sc = (float *)s.out_scale;
-                if (s.layout == 0)
-                    sc[row * G + g] = scale;
-                else
-                    sc[g * s.M + row] = scale;
+                sc[s.layout == 0 ? row * G + g : g * s.M + row] = scale;
             }
             const GroupDivisor gd = make_group_divisor(d);
             uint32_t c[4];
@@ -214,12 +232,12 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
                 for (int j = 0; j < 4; ++j)
                     c[j] = e4m3x2(__fdiv_rn(bf_lo(yw[j]), d), __fdiv_rn(bf_hi(yw[j]), d));
             }
-            uint2 q = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-            *reinterpret_cast<uint2 *>(s.out_q + row * (int64_t)s.H + (int64_t)v * 8) = q;
+            const uint2 q = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+            reinterpret_cast<uint2 *>(s.out_q + row * (int64_t)s.H)[v] = q;
         } else {
             const int X = mx_exponent_from_bits(am[k]);
             const float2 mult = f2(__uint_as_float((uint32_t)(127 - X) << 23));   // 2^-X
-            if ((t & 3) == 0) {
+            if (leader) {
                 uint8_t *sc = (uint8_t *)s.out_scale;
                 sc[row * (int64_t)(s.H >> 5) + (v >> 2)] = (uint8_t)(X + 127);
             }
@@ -229,10 +247,48 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
                 const float2 qv = mul2(unpack_bf16x2(yw[j]), mult);
                 c[j] = e2m1x2(qv.x, qv.y);
             }
-            uint32_t q = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-            *reinterpret_cast<uint32_t *>(s.out_q + row * (int64_t)(s.H >> 1) + (int64_t)v * 4) = q;
+            reinterpret_cast<uint32_t *>(s.out_q + row * (int64_t)(s.H >> 1))[v] =
+                c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
         }
     }
+}
+
+// Load (and add) one row from global memory, write the residual, finish it.
+template <int VPT, int TPR, bool MX>
+__device__ __forceinline__ void row_from_global(const Seg &s, int64_t row, int t, int team, int parity,
+                                                RedSmem &red)
+{
+    constexpr bool GUARD = TPR == 0;
+    const int tpr = TPR ? TPR : s.tpr;
+    const int nvec = TPR ? TPR * VPT : (s.H >> 3);
+    uint4 r[VPT];
+    const uint4 *xr = s.x + row * s.ldx_v + t;
+    // vectors past the row end (padded team shapes) read as zero and are
+    // never stored; they add nothing to the sum of squares
+    if (s.res) {
+        const uint4 *rr = s.res + row * s.ldres_v + t;
+        uint4 xv[VPT], rv[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const bool ok = !GUARD || k * tpr + t < nvec;
+            xv[k] = ok ? ld_stream(xr + k * tpr) : make_uint4(0, 0, 0, 0);
+            rv[k] = ok ? ld_stream(rr + k * tpr) : make_uint4(0, 0, 0, 0);
+        }
+        uint4 *orow = s.out_res + row * nvec + t;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            r[k] = add_bf16x8(xv[k], rv[k]);
+            if (!GUARD || k * tpr + t < nvec)
+                orow[k * tpr] = r[k];
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const bool ok = !GUARD || k * tpr + t < nvec;
+            r[k] = ok ? ld_stream(xr + k * tpr) : make_uint4(0, 0, 0, 0);
+        }
+    }
+    row_finish<VPT, TPR, MX, false>(s, row, t, team, parity, red, r, s.gamma);
 }
 
 }  // namespace rmsq

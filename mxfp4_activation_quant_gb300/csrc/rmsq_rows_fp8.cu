@@ -3,14 +3,14 @@
 
 namespace rmsq {
 
-cudaError_t launch_rows_fp8(int vpt, const LaunchParams &p, int grid, int threads, cudaStream_t st)
+cudaError_t launch_rows_fp8(int vpt, int tpr_static, const LaunchParams &p, int grid, int threads,
+                            cudaStream_t st)
 {
-    return launch_rows_impl<false>(vpt, p, grid, threads, st);
+    return launch_rows_impl<false>(vpt, tpr_static, p, grid, threads, st);
 }
 
-bool vpt_instantiated(int vpt)
-{
-    return vpt >= 1 && vpt <= 8;
-}
+bool vpt_instantiated(int vpt) { return vpt >= 1 && vpt <= 8; }
+
+bool static_shape(int vpt, int tpr) { return vpt == 4 && tpr == 224; }
 
 }  // namespace rmsq

@@ -270,4 +270,4 @@ def check_group_division(device=None) -> dict:
     _check(lib().rmsq_check_group_division(_ptr(counts), _stream(dev)))
     c = counts.cpu().tolist()
     return {"code_mismatches": c[0], "quotient_mismatches": c[1], "pairs": c[2], "scale_mismatches": c[3],
-            "normal_quotient_mismatches": c[4]}
+            "quotient_mismatches_y_ge_2m100": c[4]}

@@ -21,6 +21,12 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-s
           "-Wall", "-Wextra", "-pthread"]
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compiles an oracle source file (used by the tests that plant mistakes)."""
+    subprocess.run(["gcc", *CFLAGS, "-o", out, src, "-lm"], check=True)
+    return out
+
+
 def build(force: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):

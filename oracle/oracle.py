@@ -34,31 +34,35 @@ def default_threads() -> int:
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
-        path = _build.build()
-        L = ctypes.CDLL(path)
-        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
-        L.oracle_e4m3_encode.restype = ctypes.c_uint8
-        L.oracle_e2m1_encode.argtypes = [ctypes.c_float]
-        L.oracle_e2m1_encode.restype = ctypes.c_uint8
-        L.oracle_mx_exponent.argtypes = [ctypes.c_float]
-        L.oracle_mx_exponent.restype = ctypes.c_int
-        for name in ("oracle_e4m3_encode_array", "oracle_e4m3_decode_array",
-                     "oracle_e2m1_encode_array", "oracle_e2m1_decode_array",
-                     "oracle_mx_exponent_array", "oracle_bf16_round_array"):
-            getattr(L, name).argtypes = [_p, _i64, _p]
-            getattr(L, name).restype = None
-        L.oracle_add_residual.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, ctypes.c_int]
-        L.oracle_add_residual.restype = ctypes.c_int
-        L.oracle_rmsnorm.argtypes = [_p, _i64, _p, ctypes.c_float, _i64, _i64, _p, _i64, _p, _p,
-                                     ctypes.c_int]
-        L.oracle_rmsnorm.restype = ctypes.c_int
-        L.oracle_group_quant_fp8.argtypes = [_p, _i64, _i64, _i64, _i64, ctypes.c_int, _p, _i64, _p,
-                                             ctypes.c_int]
-        L.oracle_group_quant_fp8.restype = ctypes.c_int
-        L.oracle_group_quant_mxfp4.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, ctypes.c_int]
-        L.oracle_group_quant_mxfp4.restype = ctypes.c_int
-        _lib = L
+        _lib = load_library(_build.build())
     return _lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Loads a compiled oracle and declares its signatures."""
+    L = ctypes.CDLL(path)
+    L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    L.oracle_e4m3_encode.restype = ctypes.c_uint8
+    L.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+    L.oracle_e2m1_encode.restype = ctypes.c_uint8
+    L.oracle_mx_exponent.argtypes = [ctypes.c_float]
+    L.oracle_mx_exponent.restype = ctypes.c_int
+    for name in ("oracle_e4m3_encode_array", "oracle_e4m3_decode_array",
+                 "oracle_e2m1_encode_array", "oracle_e2m1_decode_array",
+                 "oracle_mx_exponent_array", "oracle_bf16_round_array"):
+        getattr(L, name).argtypes = [_p, _i64, _p]
+        getattr(L, name).restype = None
+    L.oracle_add_residual.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _p, _i64, ctypes.c_int]
+    L.oracle_add_residual.restype = ctypes.c_int
+    L.oracle_rmsnorm.argtypes = [_p, _i64, _p, ctypes.c_float, _i64, _i64, _p, _i64, _p, _p,
+                                 ctypes.c_int]
+    L.oracle_rmsnorm.restype = ctypes.c_int
+    L.oracle_group_quant_fp8.argtypes = [_p, _i64, _i64, _i64, _i64, ctypes.c_int, _p, _i64, _p,
+                                         ctypes.c_int]
+    L.oracle_group_quant_fp8.restype = ctypes.c_int
+    L.oracle_group_quant_mxfp4.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, ctypes.c_int]
+    L.oracle_group_quant_mxfp4.restype = ctypes.c_int
+    return L
 
 
 # ------------------------------------------------------------ conversions

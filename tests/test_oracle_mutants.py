@@ -1,0 +1,100 @@
+"""The oracle's pins are strong enough to catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source, compiles it
+on the CPU, swaps it in for the real oracle, and runs the pins (hand-worked
+rows, encoder brute force, library cross-checks, invariants): at least one of
+them must fail. Nothing here touches the GPU or the real oracle build.
+"""
+
+import os
+import shutil
+
+import numpy as np
+import pytest
+
+from oracle import build as oracle_build
+from oracle import oracle as O
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "rmsq_oracle.c")
+
+MUTANTS = {
+    "drop_eps": ("sqrt(S / (double)c->H + (double)c->eps)", "sqrt(S / (double)c->H)"),
+    "mean_over_H_minus_1": ("S / (double)c->H + (double)c->eps", "S / (double)(c->H - 1) + (double)c->eps"),
+    "gamma_index_reversed": ("bf16_to_f32(c->gamma[i])", "bf16_to_f32(c->gamma[c->H - 1 - i])"),
+    "fnuz_max_240": ("float scale = amax / 448.0f;", "float scale = amax / 240.0f;"),
+    "scale_by_reciprocal": ("float scale = amax / 448.0f;", "float scale = amax * (1.0f / 448.0f);"),
+    "e4m3_round_half_up": ("double n = nearbyint(ldexp(a, 3 - e));", "double n = floor(ldexp(a, 3 - e) + 0.5);"),
+    "e4m3_no_saturation": [("if (a > 448.0) /* saturate", "if (a > 3.0e38) /* saturate"),
+                           ("    if (code > 0x7e)\n        code = 0x7e;\n    return (uint8_t)(sign | code);",
+                            "    return (uint8_t)(sign | code);")],
+    "e4m3_subnormal_step": ("code = (int)nearbyint(a * 512.0);", "code = (int)nearbyint(a * 256.0);"),
+    "e4m3_sign_dropped": ("    if (code > 0x7e)\n        code = 0x7e;\n    return (uint8_t)(sign | code);",
+                          "    if (code > 0x7e)\n        code = 0x7e;\n    return (uint8_t)(code);"),
+    "e2m1_round_half_up": ("code = (int)nearbyint(2.0 * a);", "code = (int)floor(2.0 * a + 0.5);"),
+    "mx_exponent_off_by_one": ("int X = (e2 - 1) - 2;", "int X = (e2 - 1) - 3;"),
+    "mx_no_lower_clamp": ("    if (X < -127)\n        X = -127;\n", ""),
+    "mx_nibbles_swapped": ("(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
+    "bf16_round_half_up": ("u += 0x7fffu + keep_lsb;", "u += 0x8000u;"),
+    "residual_not_added": ("float s = bf16_to_f32(c->x[m * c->ldx + i]) + bf16_to_f32(c->res[m * c->ldres + i]);",
+                           "float s = bf16_to_f32(c->x[m * c->ldx + i]);"),
+    "col_major_as_row_major": ("c->scale[g * c->M + m] = scale;", "c->scale[m * ngroups + g] = scale;"),
+    "quantise_unnormalised": ("float v = bf16_to_f32(row[i]);\n                float quot", "float v = bf16_to_f32(row[i]) * 2.0f;\n                float quot"),
+    "zero_group_nan": ("float quot = (amax == 0.0f) ? v : v / scale;", "float quot = v / scale;"),
+}
+
+
+def _pins(oracle_mod):
+    """The oracle's pins, run against whatever library oracle_mod has loaded."""
+    from tests import test_oracle_encoders as enc
+    from tests import test_oracle_golden as gold
+    from tests import test_oracle_norm as norm
+
+    for row in gold._rows():
+        yield f"golden:{row['name']}", lambda r=row: gold.test_handworked_row(r, oracle_mod)
+    yield "enc:e4m3_listed", lambda: enc.test_e4m3_listed_cases(oracle_mod)
+    yield "enc:e4m3_brute", lambda: enc.test_e4m3_encode_brute_force(oracle_mod)
+    yield "enc:e2m1_listed", lambda: enc.test_e2m1_listed_ties(oracle_mod)
+    yield "enc:e2m1_brute", lambda: enc.test_e2m1_encode_brute_force(oracle_mod)
+    yield "enc:mx_exponent", lambda: enc.test_mx_exponent_defining_property(oracle_mod)
+    yield "enc:bf16", lambda: enc.test_bf16_rounding_matches_library_cast(oracle_mod, 0)
+    yield "norm:add", lambda: norm.test_add_matches_library_bf16_add(oracle_mod)
+    b = _batch()
+    yield "norm:rms_norm", lambda: norm.test_rmsnorm_matches_library_fp64(oracle_mod, b)
+    yield "norm:fp8_invariants", lambda: norm.test_fp8_quant_invariants(oracle_mod, b)
+    yield "norm:col_major", lambda: norm.test_fp8_column_major_is_transpose(oracle_mod, b)
+    yield "norm:mxfp4_invariants", lambda: norm.test_mxfp4_invariants(oracle_mod)
+
+
+def _batch():
+    import torch
+    from mxfp4_activation_quant_gb300 import synth
+    d = synth.make_inputs(synth.WORKLOADS["decode"], M=48)
+    return {k: v.contiguous().view(torch.int16).numpy().view(np.uint16) for k, v in d.items()}
+
+
+def test_real_oracle_passes_every_pin(oracle_mod):
+    for name, run in _pins(oracle_mod):
+        run()
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_planted_mistake_is_caught(mutant, tmp_path, monkeypatch):
+    edits = MUTANTS[mutant]
+    if isinstance(edits, tuple):
+        edits = [edits]
+    src = open(SRC).read()
+    for find, repl in edits:
+        assert src.count(find) == 1, f"mutation site for {mutant} not found exactly once"
+        src = src.replace(find, repl)
+    path = tmp_path / "mutant.c"
+    path.write_text(src)
+    lib = oracle_build.compile_source(str(path), str(tmp_path / "libmutant.so"))
+    monkeypatch.setattr(O, "_lib", O.load_library(lib))
+    caught = []
+    for name, run in _pins(O):
+        try:
+            run()
+        except AssertionError:
+            caught.append(name)
+            break
+    assert caught, f"no pin caught the planted mistake {mutant!r}"

@@ -180,7 +180,7 @@ def test_team_shapes_agree(oracle_mod, vpt):
     parity.compare_fp8(got, ref_fp8(oracle_mod, d, w.eps), what=f"vpt={vpt}")
 
 
-@pytest.mark.parametrize("rpb", [1, 2, 3])
+@pytest.mark.parametrize("rpb", [1, 2])
 def test_rows_per_block(oracle_mod, rpb):
     w = synth.WORKLOADS["prefill"]
     d = synth.make_inputs(w, M=41)
@@ -383,4 +383,5 @@ def test_group_division_is_exact_over_the_whole_domain():
     assert c["pairs"] == sum(2 * (a + 1) for a in range(1, 0x7F80)), c
     assert c["code_mismatches"] == 0, c
     assert c["scale_mismatches"] == 0, c
+    assert c["quotient_mismatches_y_ge_2m100"] == 0, c
     print(c)
