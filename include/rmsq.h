@@ -191,9 +191,8 @@ rmsq_status rmsq_encode_e2m1(const float *in, uint8_t *out, int64_t n, void *str
  * quotient. `counts` is a caller-zeroed device array of five unsigned
  * 64-bit counters, incremented by: code mismatches, fp32 quotient mismatches,
  * (amax, y) pairs checked, scale mismatches, quotient mismatches with
- * |y| >= 2^-100 (expected zero: below that the residual of the division
- * shortcut can underflow, and those quotients all encode to zero). Enqueued
- * on `stream`.
+ * |y| >= 2^-100 (informational: the kernels use only the code, whose count
+ * must be zero). Enqueued on `stream`.
  */
 rmsq_status rmsq_check_group_division(unsigned long long *counts, void *stream);
 
