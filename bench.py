@@ -16,7 +16,9 @@ device time of K back-to-back launches with inputs resident in HBM; under
 torchrun each rank runs its own batch (weak scaling) and the time is the max
 over ranks. ``e2e`` is the same metric measured through the public API with
 pinned host buffers, the host->device copy of x / residual / gamma and the
-device->host copy of every output inside the timed region. ``roofline``
+device->host copy of every output inside the timed region; the rows are cut
+into chunks whose copies and calls are pipelined over three streams (rows are
+independent, so this is exact). ``roofline``
 relates the kernel's achieved GB/s to the measured HBM copy peak.
 ``--impl reference`` times the CPU oracle (test infrastructure, plain C)
 on the host cores on bounded samples of the same workload.
@@ -314,9 +316,13 @@ def rank_workload(w, rank: int):
 
 
 def make_step(name: str, dev, rank: int, rows: int, opts):
-    """Inputs (CPU copies kept for the end-to-end leg), outputs and the step
-    function of one workload; returns (step, bytes, rows, io) where io lists
-    (device tensor, host tensor) pairs for the copies of the e2e leg."""
+    """Inputs, outputs and a launcher of one workload.
+
+    Returns (run, nbytes, M, inputs, outputs, w, d_cpu, chunkable): ``run(r0,
+    r1, stream)`` calls the library on rows [r0, r1) on ``stream``; inputs and
+    outputs are (device tensor, pinned host tensor, row-indexed) triples for
+    the end-to-end leg; ``chunkable`` says whether every per-row tensor is
+    row-major (so a row range is a contiguous slice)."""
     import torch
     from mxfp4_activation_quant_gb300 import rmsq, synth
 
@@ -327,40 +333,92 @@ def make_step(name: str, dev, rank: int, rows: int, opts):
     d_cpu = synth.make_inputs(wr)
     d = {k: v.to(dev) for k, v in d_cpu.items()}
     M = w.M
+    chunkable = True
     if w.kind == "qknorm":
         outs = {"qq": torch.empty((M, w.Hq), dtype=torch.uint8, device=dev),
                 "qs": torch.empty((M, w.Hq // 128), dtype=torch.float32, device=dev),
                 "kq": torch.empty((M, w.Hkv), dtype=torch.uint8, device=dev),
                 "ks": torch.empty((M, w.Hkv // 128), dtype=torch.float32, device=dev)}
 
-        def step():
-            rmsq.qknorm_quant_fp8_into(d["q_a"], d["kv_a"], d["gamma_q"], d["gamma_kv"], outs["qq"], outs["qs"],
-                                       outs["kq"], outs["ks"], eps=w.eps)
+        def run(r0, r1, st):
+            o = {k: v[r0:r1] for k, v in outs.items()}
+            rmsq.qknorm_quant_fp8_into(d["q_a"][r0:r1], d["kv_a"][r0:r1], d["gamma_q"], d["gamma_kv"],
+                                       o["qq"], o["qs"], o["kq"], o["ks"], eps=w.eps, stream=st)
         nbytes = qk_bytes(M, w.Hq, w.Hkv)
     elif w.kind == "mxfp4":
         outs = {"q": torch.empty((M, w.H // 2), dtype=torch.uint8, device=dev),
                 "s": torch.empty((M, w.H // 32), dtype=torch.uint8, device=dev),
                 "r": torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)}
 
-        def step():
-            rmsq.add_rmsnorm_quant_mxfp4_into(d["x"], d["gamma"], d["residual"], outs["q"], outs["s"], outs["r"],
-                                              None, eps=w.eps, opts=opts)
+        def run(r0, r1, st):
+            rmsq.add_rmsnorm_quant_mxfp4_into(d["x"][r0:r1], d["gamma"], d["residual"][r0:r1], outs["q"][r0:r1],
+                                              outs["s"][r0:r1], outs["r"][r0:r1], None, eps=w.eps, opts=opts,
+                                              stream=st)
         nbytes = mx_bytes(M, w.H)
     else:
         col = w.scale_layout == "col"
+        chunkable = not col
         outs = {"q": torch.empty((M, w.H), dtype=torch.uint8, device=dev),
                 "s": torch.empty(((w.H // 128, M) if col else (M, w.H // 128)), dtype=torch.float32, device=dev),
                 "r": torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)}
         if w.keep_bf16:
             outs["y"] = torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)
 
-        def step():
-            rmsq.add_rmsnorm_quant_fp8_into(d["x"], d["gamma"], d["residual"], outs["q"], outs["s"], outs["r"],
-                                            outs.get("y"), eps=w.eps, scale_layout=w.scale_layout, opts=opts)
+        def run(r0, r1, st):
+            sc = outs["s"] if col else outs["s"][r0:r1]
+            y = outs["y"][r0:r1] if "y" in outs else None
+            rmsq.add_rmsnorm_quant_fp8_into(d["x"][r0:r1], d["gamma"], d["residual"][r0:r1], outs["q"][r0:r1],
+                                            sc, outs["r"][r0:r1], y, eps=w.eps, scale_layout=w.scale_layout,
+                                            opts=opts, stream=st)
         nbytes = algorithmic_bytes(M, w.H, True, w.keep_bf16)
-    io_in = [(d[k], d_cpu[k].pin_memory()) for k in d]
-    io_out = [(v, torch.empty(v.shape, dtype=v.dtype).pin_memory()) for v in outs.values()]
-    return step, nbytes, M, io_in, io_out, w, d_cpu
+    inputs = [(d[k], d_cpu[k].pin_memory(), d[k].dim() == 2) for k in d]
+    outputs = [(v, torch.empty(v.shape, dtype=v.dtype).pin_memory(), not (col_scales(w) and k == "s"))
+               for k, v in outs.items()]
+    return run, nbytes, M, inputs, outputs, w, d_cpu, chunkable
+
+
+def col_scales(w) -> bool:
+    return w.kind == "fp8" and w.scale_layout == "col"
+
+
+def make_e2e_step(run, M: int, inputs, outputs, chunks: int, dev):
+    """One end-to-end step: host->device copies, the library call and the
+    device->host copies for row chunks spread over three streams, so that
+    copies in both directions overlap the kernels of other chunks."""
+    import torch
+    streams = [torch.cuda.current_stream(dev)] + [torch.cuda.Stream(dev) for _ in range(2)]
+    bounds = [(M * i // chunks, M * (i + 1) // chunks) for i in range(chunks)]
+
+    def step():
+        s0 = streams[0]
+        start = torch.cuda.Event()
+        for dv, hv, per_row in inputs:
+            if not per_row:
+                with torch.cuda.stream(s0):
+                    dv.copy_(hv, non_blocking=True)
+        start.record(s0)
+        for s in streams[1:]:
+            s.wait_event(start)
+        for c, (r0, r1) in enumerate(bounds):
+            s = streams[c % len(streams)]
+            with torch.cuda.stream(s):
+                for dv, hv, per_row in inputs:
+                    if per_row:
+                        dv[r0:r1].copy_(hv[r0:r1], non_blocking=True)
+                run(r0, r1, s.cuda_stream)
+                for dv, hv, per_row in outputs:
+                    if per_row:
+                        hv[r0:r1].copy_(dv[r0:r1], non_blocking=True)
+        for dv, hv, per_row in outputs:
+            if not per_row:
+                with torch.cuda.stream(streams[(len(bounds) - 1) % len(streams)]):
+                    hv.copy_(dv, non_blocking=True)
+        for s in streams[1:]:
+            e = torch.cuda.Event()
+            e.record(s)
+            s0.wait_event(e)
+
+    return step
 
 
 def run_ours(args) -> None:
@@ -382,8 +440,12 @@ def run_ours(args) -> None:
 
     kernel = {"auto": rmsq.KERNEL_AUTO, "rows": rmsq.KERNEL_ROWS, "persistent": rmsq.KERNEL_PERSISTENT}[args.kernel]
     opts = rmsq.LaunchOpts(kernel=kernel) if kernel != rmsq.KERNEL_AUTO else None
-    step, bytes_step, M, io_in, io_out, w, d_cpu = make_step(args.workload, dev, rank, args.rows, opts)
+    run, bytes_step, M, io_in, io_out, w, d_cpu, chunkable = make_step(args.workload, dev, rank, args.rows, opts)
     stream = torch.cuda.current_stream(dev)
+
+    def step():
+        run(0, M, stream.cuda_stream)
+
     peak, peak_kind = measured_peaks()
     sampler = ClockSampler(gpu_id_for(dev)) if rank == 0 else None
     time.sleep(0.25 if sampler else 0)
@@ -401,14 +463,10 @@ def run_ours(args) -> None:
     launch_ms = statistics.mean(each_ms)
     achieved = bytes_step / (launch_ms * 1e-3) / 1e9
 
-    # end to end through the public API: pinned host buffers, copies inside the timed region
-    def e2e_step():
-        for dv, hv in io_in:
-            dv.copy_(hv, non_blocking=True)
-        step()
-        for dv, hv in io_out:
-            hv.copy_(dv, non_blocking=True)
-
+    # end to end through the public API: pinned host buffers, copies inside the
+    # timed region, row chunks pipelined over three streams
+    chunks = args.e2e_chunks if chunkable else 1
+    e2e_step = make_e2e_step(run, M, io_in, io_out, chunks, dev)
     e2e_value = None
     if not args.no_e2e:
         e2e_steps = max(3, min(20, args.steps))
@@ -418,8 +476,8 @@ def run_ours(args) -> None:
             dist.barrier()
         e2e_ms, _ = time_launches(e2e_step, e2e_steps, stream)
         e2e_value = round(world * bytes_step * e2e_steps / (max_over_ranks(e2e_ms, world, dev) * 1e-3) / 1e9, 1)
-    h2d = sum(hv.numel() * hv.element_size() for _, hv in io_in)
-    d2h = sum(hv.numel() * hv.element_size() for _, hv in io_out)
+    h2d = sum(hv.numel() * hv.element_size() for _, hv, _ in io_in)
+    d2h = sum(hv.numel() * hv.element_size() for _, hv, _ in io_out)
 
     headline = args.workload == WORKLOAD and not args.rows
     extra = other_workloads(dev, stream) if (rank == 0 and headline and not args.no_extra) else None
@@ -446,7 +504,7 @@ def run_ours(args) -> None:
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} HBM copy"},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "row_chunks": chunks, "streams": 3},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -489,6 +547,7 @@ def main() -> None:
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / qknorm / MXFP4 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    ap.add_argument("--e2e-chunks", type=int, default=8, help="row chunks pipelined in the e2e leg")
     ap.add_argument("--rows", type=int, default=0,
                     help="rows of the batch (profiler captures only; the benchmark is M=16384)")
     args = ap.parse_args()
