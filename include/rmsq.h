@@ -61,8 +61,12 @@ typedef enum rmsq_status {
 } rmsq_status;
 
 typedef enum rmsq_scale_layout {
-    RMSQ_SCALE_ROW_MAJOR = 0,   /* scale[m * (H/128) + g]  ([M, H/128]) */
-    RMSQ_SCALE_COL_MAJOR = 1    /* scale[g * M + m]        ([H/128, M], no padding) */
+    RMSQ_SCALE_ROW_MAJOR = 0,     /* scale[m * (H/128) + g]  ([M, H/128]) */
+    RMSQ_SCALE_COL_MAJOR = 1,     /* scale[g * M + m]        ([H/128, M], no padding) */
+    RMSQ_SCALE_COL_MAJOR_PAD4 = 2 /* scale[g * Mp + m], Mp = M rounded up to a multiple of 4, so
+                                     every column starts on 16 bytes (a blockwise-FP8 GEMM's TMA
+                                     load); out_scale must be 16-byte aligned; the padding
+                                     entries are not written */
 } rmsq_scale_layout;
 
 /*
@@ -111,6 +115,38 @@ rmsq_status rmsq_qknorm_quant_fp8(
 rmsq_status rmsq_add_rmsnorm_quant_mxfp4(
     const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
     float eps, int64_t M, int64_t H, uint8_t *out_q, uint8_t *out_scale, void *out_residual,
+    void *out_bf16, void *stream);
+
+/*
+ * The MLA latent pair in one launch, MXFP4 flavour (the pages' "FP4 qknorm"):
+ * each latent gets exactly what rmsq_add_rmsnorm_quant_mxfp4 with
+ * residual == NULL would give it. Hq and Hkv are multiples of 32.
+ *
+ *   out_q_q [M, Hq/2], out_kv_q [M, Hkv/2] packed E2M1 bytes;
+ *   out_q_scale [M, Hq/32], out_kv_scale [M, Hkv/32] E8M0 bytes (row-major);
+ *   out_q_bf16 / out_kv_bf16 optional bf16 y.
+ */
+rmsq_status rmsq_qknorm_quant_mxfp4(
+    const void *q_a, int64_t ld_q, const void *kv_a, int64_t ld_kv, const void *gamma_q,
+    const void *gamma_kv, float eps, int64_t M, int64_t Hq, int64_t Hkv, uint8_t *out_q_q,
+    uint8_t *out_q_scale, uint8_t *out_kv_q, uint8_t *out_kv_scale, void *out_q_bf16,
+    void *out_kv_bf16, void *stream);
+
+/*
+ * As rmsq_add_rmsnorm_quant_mxfp4, with the E8M0 scales written directly in
+ * the layout Blackwell's block-scaled MMA reads its scale factors from
+ * (the GB300 counterpart of the pages' GEMM-specific "preshuffle" scale
+ * layouts): the [M, H/32] scale matrix is cut into tiles of 128 rows x 4
+ * groups, 512 bytes each, stored row-tile major (ceil(H/128) tiles per row
+ * tile); inside a tile, row r and group c are at byte
+ * (r % 32) * 16 + (r / 32) * 4 + c. Scale (m, g) is therefore at
+ *   ((m / 128) * ceil(H/128) + g / 4) * 512 + (m % 32) * 16 + ((m % 128) / 32) * 4 + g % 4.
+ * out_scale_tiles holds ceil(M/128) * ceil(H/128) * 512 bytes, 16-byte aligned;
+ * entries for rows >= M or groups >= H/32 (tile padding) are not written.
+ */
+rmsq_status rmsq_add_rmsnorm_quant_mxfp4_mma_scales(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, uint8_t *out_q, uint8_t *out_scale_tiles, void *out_residual,
     void *out_bf16, void *stream);
 
 /* ------------------------------------------------------------ utilities */

@@ -189,6 +189,7 @@ Seg make_seg(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
     s.ldres_v = residual ? ld_res / 8 : 0;
     s.H = (int32_t)H;
     s.layout = layout;
+    s.scale_ld = M;
     s.eps = eps;
     s.inv_h = (float)(1.0 / (double)H);
     return s;
@@ -296,6 +297,121 @@ __global__ void encode_e2m1_kernel(const float *in, uint8_t *out, int64_t n)
         out[i] = (uint8_t)(e2m1x2(in[i], 0.0f) & 0xfu);
 }
 
+// The MLA latent pair, FP8 (group 128, fp32 scales) or MXFP4 (group 32, E8M0
+// bytes, q packed two per byte).
+rmsq_status qknorm_common(bool mx, const void *q_a, int64_t ld_q, const void *kv_a, int64_t ld_kv,
+                          const void *gamma_q, const void *gamma_kv, float eps, int64_t M, int64_t Hq,
+                          int64_t Hkv, int32_t group, void *out_q_q, void *out_q_scale, void *out_kv_q,
+                          void *out_kv_scale, int32_t scale_layout, void *out_q_bf16, void *out_kv_bf16,
+                          void *stream)
+{
+    const int64_t qb = mx ? 2 : 1;                      // elements per code byte
+    const int64_t sb = mx ? 1 : 4;                      // bytes per scale
+    rmsq_status st = check_single(q_a, ld_q, nullptr, 0, gamma_q, eps, M, Hq, group, out_q_q, Hq / qb,
+                                  out_q_scale, (Hq / group) * M * sb, sb, nullptr, out_q_bf16);
+    if (st != RMSQ_OK)
+        return st;
+    st = check_single(kv_a, ld_kv, nullptr, 0, gamma_kv, eps, M, Hkv, group, out_kv_q, Hkv / qb,
+                      out_kv_scale, (Hkv / group) * M * sb, sb, nullptr, out_kv_bf16);
+    if (st != RMSQ_OK)
+        return st;
+    if (M == 0)
+        return ok();
+    // the two latents' outputs must not overlap each other or the other's inputs
+    Range a[4] = {mat_range(out_q_q, M, Hq / qb, Hq / qb, 1),
+                  mat_range(out_q_scale, 1, (Hq / group) * M * sb, 0, 1), {0, 0}, {0, 0}};
+    Range b[4] = {mat_range(out_kv_q, M, Hkv / qb, Hkv / qb, 1),
+                  mat_range(out_kv_scale, 1, (Hkv / group) * M * sb, 0, 1), {0, 0}, {0, 0}};
+    int na = 2, nb = 2;
+    if (out_q_bf16)
+        a[na++] = mat_range(out_q_bf16, M, Hq, Hq, 2);
+    if (out_kv_bf16)
+        b[nb++] = mat_range(out_kv_bf16, M, Hkv, Hkv, 2);
+    Range in_q = mat_range(q_a, M, Hq, ld_q, 2), in_kv = mat_range(kv_a, M, Hkv, ld_kv, 2);
+    Range g_q = mat_range(gamma_q, 1, Hq, Hq, 2), g_kv = mat_range(gamma_kv, 1, Hkv, Hkv, 2);
+    for (int i = 0; i < na; ++i) {
+        if (overlaps(a[i], in_kv) || overlaps(a[i], g_kv))
+            return fail(RMSQ_ERR_INVALID_ARG, "a q_a output overlaps a kv_a input");
+        for (int j = 0; j < nb; ++j)
+            if (overlaps(a[i], b[j]))
+                return fail(RMSQ_ERR_INVALID_ARG, "q_a and kv_a outputs overlap");
+    }
+    for (int j = 0; j < nb; ++j)
+        if (overlaps(b[j], in_q) || overlaps(b[j], g_q))
+            return fail(RMSQ_ERR_INVALID_ARG, "a kv_a output overlaps a q_a input");
+
+    Seg sq = make_seg(q_a, ld_q, nullptr, 0, gamma_q, eps, M, Hq, out_q_q, out_q_scale,
+                      scale_layout, nullptr, out_q_bf16);
+    Seg sk = make_seg(kv_a, ld_kv, nullptr, 0, gamma_kv, eps, M, Hkv, out_kv_q, out_kv_scale,
+                      scale_layout, nullptr, out_kv_bf16);
+    // Team shapes: the compiled-in MLA pair shape when it fits exactly,
+    // otherwise one vectors-per-thread value for both latents, least padding
+    // first.
+    int v0 = 0, v1 = 0, tq = 0, tk = 0, t0s = 0, t1s = 0;
+    const int gv = mx ? 4 : 16;
+    if (Hq == 3 * 64 * 8 && Hkv == 4 * 16 * 8) {
+        v0 = 3; tq = 64; v1 = 4; tk = 16; t0s = 64; t1s = 16;
+    } else {
+        int64_t best_waste = -1;
+        for (int v : kVptPreference) {
+            int a, b;
+            int64_t wa, wb;
+            if (team_ok(Hq / 8, v, gv, a, wa) && team_ok(Hkv / 8, v, gv, b, wb) &&
+                (best_waste < 0 || wa + wb < best_waste)) {
+                v0 = v1 = v;
+                tq = a;
+                tk = b;
+                best_waste = wa + wb;
+            }
+        }
+    }
+    if (!v0)
+        return fail(RMSQ_ERR_UNSUPPORTED, "no common team shape for Hq=%lld, Hkv=%lld",
+                    (long long)Hq, (long long)Hkv);
+    int threads = default_rows_per_block(tq) * tq;
+    int tk_threads = default_rows_per_block(tk) * tk;
+    if (tk_threads > threads)
+        threads = tk_threads;
+    sq.tpr = tq;
+    sk.tpr = tk;
+    sq.rpb = threads / tq;
+    sk.rpb = threads / tk;
+    if ((tq > 32 && sq.rpb > 15) || (tk > 32 && sk.rpb > 15))
+        return fail(RMSQ_ERR_UNSUPPORTED, "team shape needs too many named barriers");
+    int64_t bq = (M + sq.rpb - 1) / sq.rpb, bk = (M + sk.rpb - 1) / sk.rpb;
+    if (bq + bk > 0x7fffffff)
+        return fail(RMSQ_ERR_UNSUPPORTED, "M too large");
+    sq.blocks = (int32_t)bq;
+    sk.blocks = (int32_t)bk;
+    LaunchParams p{};
+    p.seg[0] = sq;
+    p.seg[1] = sk;
+    p.nseg = 2;
+    cudaError_t e = launch_dual(mx, v0, t0s, v1, t1s, p, (int)(bq + bk), threads, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+// MXFP4 single tensor, scales row-major (layout 0) or in the block-scaled MMA
+// tile layout (layout 1: ceil(M/128) x ceil(H/128) tiles of 512 bytes).
+rmsq_status mxfp4_common(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
+                         const void *gamma, float eps, int64_t M, int64_t H, uint8_t *out_q,
+                         uint8_t *out_scale, int layout, void *out_residual, void *out_bf16, void *stream,
+                         const rmsq_launch_opts *opts)
+{
+    const int64_t ktiles = (H / 32 + 3) / 4;
+    const int64_t sbytes = layout == 0 ? (H / 32) * M : (M + 127) / 128 * ktiles * 512;
+    rmsq_status st = check_single(x, ld_x, residual, ld_res, gamma, eps, M, H, 32, out_q, H / 2,
+                                  out_scale, sbytes, layout == 0 ? 1 : 16, out_residual, out_bf16);
+    if (st != RMSQ_OK || M == 0)
+        return st == RMSQ_OK ? ok() : st;
+    Seg s = make_seg(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q, out_scale, layout,
+                     out_residual, out_bf16);
+    s.scale_ld = ktiles;
+    return launch_single(s, true, opts ? *opts : kDefaultOpts, (cudaStream_t)stream);
+}
+
 }  // namespace
 }  // namespace rmsq
 
@@ -327,14 +443,19 @@ rmsq_status rmsq_add_rmsnorm_quant_group_fp8_ex(
     if (group != 128)
         return fail(group > 0 ? RMSQ_ERR_UNSUPPORTED : RMSQ_ERR_INVALID_ARG,
                     "FP8 group must be 128 (got %d)", group);
-    if (scale_layout != RMSQ_SCALE_ROW_MAJOR && scale_layout != RMSQ_SCALE_COL_MAJOR)
+    if (scale_layout != RMSQ_SCALE_ROW_MAJOR && scale_layout != RMSQ_SCALE_COL_MAJOR &&
+        scale_layout != RMSQ_SCALE_COL_MAJOR_PAD4)
         return fail(RMSQ_ERR_INVALID_ARG, "unknown scale layout %d", scale_layout);
+    const int64_t sld = scale_layout == RMSQ_SCALE_COL_MAJOR_PAD4 ? (M + 3) / 4 * 4 : M;
     rmsq_status st = check_single(x, ld_x, residual, ld_res, gamma, eps, M, H, group, out_q, H,
-                                  out_scale, (H / group) * M * 4, 4, out_residual, out_bf16);
+                                  out_scale, (H / group) * sld * 4,
+                                  scale_layout == RMSQ_SCALE_COL_MAJOR_PAD4 ? 16 : 4, out_residual,
+                                  out_bf16);
     if (st != RMSQ_OK || M == 0)
         return st == RMSQ_OK ? ok() : st;
-    Seg s = make_seg(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q, out_scale, scale_layout,
-                     out_residual, out_bf16);
+    Seg s = make_seg(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q, out_scale,
+                     scale_layout == RMSQ_SCALE_ROW_MAJOR ? 0 : 1, out_residual, out_bf16);
+    s.scale_ld = sld;
     return launch_single(s, false, opts ? *opts : kDefaultOpts, (cudaStream_t)stream);
 }
 
@@ -353,13 +474,17 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
     float eps, int64_t M, int64_t H, uint8_t *out_q, uint8_t *out_scale, void *out_residual,
     void *out_bf16, void *stream, const rmsq_launch_opts *opts)
 {
-    rmsq_status st = check_single(x, ld_x, residual, ld_res, gamma, eps, M, H, 32, out_q, H / 2,
-                                  out_scale, (H / 32) * M, 1, out_residual, out_bf16);
-    if (st != RMSQ_OK || M == 0)
-        return st == RMSQ_OK ? ok() : st;
-    Seg s = make_seg(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q, out_scale, 0,
-                     out_residual, out_bf16);
-    return launch_single(s, true, opts ? *opts : kDefaultOpts, (cudaStream_t)stream);
+    return mxfp4_common(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q, out_scale, 0, out_residual,
+                        out_bf16, stream, opts);
+}
+
+rmsq_status rmsq_add_rmsnorm_quant_mxfp4_mma_scales(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, uint8_t *out_q, uint8_t *out_scale_tiles, void *out_residual,
+    void *out_bf16, void *stream)
+{
+    return mxfp4_common(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q, out_scale_tiles, 1,
+                        out_residual, out_bf16, stream, nullptr);
 }
 
 rmsq_status rmsq_add_rmsnorm_quant_mxfp4(
@@ -382,89 +507,20 @@ rmsq_status rmsq_qknorm_quant_fp8(
                     "FP8 group must be 128 (got %d)", group);
     if (scale_layout != RMSQ_SCALE_ROW_MAJOR && scale_layout != RMSQ_SCALE_COL_MAJOR)
         return fail(RMSQ_ERR_INVALID_ARG, "unknown scale layout %d", scale_layout);
-    rmsq_status st = check_single(q_a, ld_q, nullptr, 0, gamma_q, eps, M, Hq, group, out_q_q, Hq,
-                                  out_q_scale, (Hq / group) * M * 4, 4, nullptr, out_q_bf16);
-    if (st != RMSQ_OK)
-        return st;
-    st = check_single(kv_a, ld_kv, nullptr, 0, gamma_kv, eps, M, Hkv, group, out_kv_q, Hkv,
-                      out_kv_scale, (Hkv / group) * M * 4, 4, nullptr, out_kv_bf16);
-    if (st != RMSQ_OK)
-        return st;
-    if (M == 0)
-        return ok();
-    // the two latents' outputs must not overlap each other or the other's inputs
-    Range a[4] = {mat_range(out_q_q, M, Hq, Hq, 1), mat_range(out_q_scale, 1, (Hq / 128) * M * 4, 0, 1),
-                  {0, 0}, {0, 0}};
-    Range b[4] = {mat_range(out_kv_q, M, Hkv, Hkv, 1),
-                  mat_range(out_kv_scale, 1, (Hkv / 128) * M * 4, 0, 1), {0, 0}, {0, 0}};
-    int na = 2, nb = 2;
-    if (out_q_bf16)
-        a[na++] = mat_range(out_q_bf16, M, Hq, Hq, 2);
-    if (out_kv_bf16)
-        b[nb++] = mat_range(out_kv_bf16, M, Hkv, Hkv, 2);
-    Range in_q = mat_range(q_a, M, Hq, ld_q, 2), in_kv = mat_range(kv_a, M, Hkv, ld_kv, 2);
-    Range g_q = mat_range(gamma_q, 1, Hq, Hq, 2), g_kv = mat_range(gamma_kv, 1, Hkv, Hkv, 2);
-    for (int i = 0; i < na; ++i) {
-        if (overlaps(a[i], in_kv) || overlaps(a[i], g_kv))
-            return fail(RMSQ_ERR_INVALID_ARG, "a q_a output overlaps a kv_a input");
-        for (int j = 0; j < nb; ++j)
-            if (overlaps(a[i], b[j]))
-                return fail(RMSQ_ERR_INVALID_ARG, "q_a and kv_a outputs overlap");
-    }
-    for (int j = 0; j < nb; ++j)
-        if (overlaps(b[j], in_q) || overlaps(b[j], g_q))
-            return fail(RMSQ_ERR_INVALID_ARG, "a kv_a output overlaps a q_a input");
+    return qknorm_common(false, q_a, ld_q, kv_a, ld_kv, gamma_q, gamma_kv, eps, M, Hq, Hkv, group,
+                         out_q_q, out_q_scale, out_kv_q, out_kv_scale, scale_layout, out_q_bf16,
+                         out_kv_bf16, stream);
+}
 
-    Seg sq = make_seg(q_a, ld_q, nullptr, 0, gamma_q, eps, M, Hq, out_q_q, out_q_scale,
-                      scale_layout, nullptr, out_q_bf16);
-    Seg sk = make_seg(kv_a, ld_kv, nullptr, 0, gamma_kv, eps, M, Hkv, out_kv_q, out_kv_scale,
-                      scale_layout, nullptr, out_kv_bf16);
-    // Team shapes: the compiled-in MLA pair shape when it fits exactly,
-    // otherwise one vectors-per-thread value for both latents, least padding
-    // first.
-    int v0 = 0, v1 = 0, tq = 0, tk = 0, t0s = 0, t1s = 0;
-    if (Hq == 3 * 64 * 8 && Hkv == 4 * 16 * 8) {
-        v0 = 3; tq = 64; v1 = 4; tk = 16; t0s = 64; t1s = 16;
-    } else {
-        int64_t best_waste = -1;
-        for (int v : kVptPreference) {
-            int a, b;
-            int64_t wa, wb;
-            if (team_ok(Hq / 8, v, 16, a, wa) && team_ok(Hkv / 8, v, 16, b, wb) &&
-                (best_waste < 0 || wa + wb < best_waste)) {
-                v0 = v1 = v;
-                tq = a;
-                tk = b;
-                best_waste = wa + wb;
-            }
-        }
-    }
-    if (!v0)
-        return fail(RMSQ_ERR_UNSUPPORTED, "no common team shape for Hq=%lld, Hkv=%lld",
-                    (long long)Hq, (long long)Hkv);
-    int threads = default_rows_per_block(tq) * tq;
-    int tk_threads = default_rows_per_block(tk) * tk;
-    if (tk_threads > threads)
-        threads = tk_threads;
-    sq.tpr = tq;
-    sk.tpr = tk;
-    sq.rpb = threads / tq;
-    sk.rpb = threads / tk;
-    if ((tq > 32 && sq.rpb > 15) || (tk > 32 && sk.rpb > 15))
-        return fail(RMSQ_ERR_UNSUPPORTED, "team shape needs too many named barriers");
-    int64_t bq = (M + sq.rpb - 1) / sq.rpb, bk = (M + sk.rpb - 1) / sk.rpb;
-    if (bq + bk > 0x7fffffff)
-        return fail(RMSQ_ERR_UNSUPPORTED, "M too large");
-    sq.blocks = (int32_t)bq;
-    sk.blocks = (int32_t)bk;
-    LaunchParams p{};
-    p.seg[0] = sq;
-    p.seg[1] = sk;
-    p.nseg = 2;
-    cudaError_t e = launch_dual(v0, t0s, v1, t1s, p, (int)(bq + bk), threads, (cudaStream_t)stream);
-    if (e != cudaSuccess)
-        return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
-    return ok();
+rmsq_status rmsq_qknorm_quant_mxfp4(
+    const void *q_a, int64_t ld_q, const void *kv_a, int64_t ld_kv, const void *gamma_q,
+    const void *gamma_kv, float eps, int64_t M, int64_t Hq, int64_t Hkv, uint8_t *out_q_q,
+    uint8_t *out_q_scale, uint8_t *out_kv_q, uint8_t *out_kv_scale, void *out_q_bf16,
+    void *out_kv_bf16, void *stream)
+{
+    return qknorm_common(true, q_a, ld_q, kv_a, ld_kv, gamma_q, gamma_kv, eps, M, Hq, Hkv, 32,
+                         out_q_q, out_q_scale, out_kv_q, out_kv_scale, RMSQ_SCALE_ROW_MAJOR, out_q_bf16,
+                         out_kv_bf16, stream);
 }
 
 rmsq_status rmsq_sync_status(void *stream)

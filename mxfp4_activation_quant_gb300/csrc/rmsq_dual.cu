@@ -1,4 +1,4 @@
-// Dual-tensor (MLA q_a / kv_a) kernel instantiations, FP8 1x128.
+// Dual-tensor (MLA q_a / kv_a) kernel instantiations, FP8 1x128 and MXFP4.
 #include "rmsq_rowkernel.cuh"
 
 namespace rmsq {
@@ -8,12 +8,13 @@ bool static_dual_shape(int v0, int t0, int v1, int t1)
     return v0 == 3 && t0 == 64 && v1 == 4 && t1 == 16;
 }
 
-cudaError_t launch_dual(int v0, int t0, int v1, int t1, const LaunchParams &p, int grid, int threads,
-                        cudaStream_t st)
+template <bool MX>
+cudaError_t launch_dual_impl(int v0, int t0, int v1, int t1, const LaunchParams &p, int grid, int threads,
+                             cudaStream_t st)
 {
     if (t0 || t1) {
         if (static_dual_shape(v0, t0, v1, t1))
-            dual_kernel<3, 64, 4, 16><<<grid, threads, 0, st>>>(p);
+            dual_kernel<3, 64, 4, 16, MX><<<grid, threads, 0, st>>>(p);
         else
             return cudaErrorInvalidValue;
         return cudaGetLastError();
@@ -21,17 +22,24 @@ cudaError_t launch_dual(int v0, int t0, int v1, int t1, const LaunchParams &p, i
     if (v0 != v1)
         return cudaErrorInvalidValue;
     switch (v0) {
-    case 1: dual_kernel<1, 0, 1, 0><<<grid, threads, 0, st>>>(p); break;
-    case 2: dual_kernel<2, 0, 2, 0><<<grid, threads, 0, st>>>(p); break;
-    case 3: dual_kernel<3, 0, 3, 0><<<grid, threads, 0, st>>>(p); break;
-    case 4: dual_kernel<4, 0, 4, 0><<<grid, threads, 0, st>>>(p); break;
-    case 5: dual_kernel<5, 0, 5, 0><<<grid, threads, 0, st>>>(p); break;
-    case 6: dual_kernel<6, 0, 6, 0><<<grid, threads, 0, st>>>(p); break;
-    case 7: dual_kernel<7, 0, 7, 0><<<grid, threads, 0, st>>>(p); break;
-    case 8: dual_kernel<8, 0, 8, 0><<<grid, threads, 0, st>>>(p); break;
+    case 1: dual_kernel<1, 0, 1, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 2: dual_kernel<2, 0, 2, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 3: dual_kernel<3, 0, 3, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 4: dual_kernel<4, 0, 4, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 5: dual_kernel<5, 0, 5, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 6: dual_kernel<6, 0, 6, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 7: dual_kernel<7, 0, 7, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 8: dual_kernel<8, 0, 8, 0, MX><<<grid, threads, 0, st>>>(p); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_dual(bool mx, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,
+                        int threads, cudaStream_t st)
+{
+    return mx ? launch_dual_impl<true>(v0, t0, v1, t1, p, grid, threads, st)
+              : launch_dual_impl<false>(v0, t0, v1, t1, p, grid, threads, st);
 }
 
 }  // namespace rmsq

@@ -23,7 +23,9 @@ struct Seg {
     int32_t tpr;           // threads per row (a "team")
     int32_t rpb;           // rows (teams) per block
     int32_t blocks;        // blocks of the row kernel that belong to this segment
-    int32_t layout;        // 0 row-major scales, 1 column-major
+    int32_t layout;        // FP8: 0 row-major, 1 column-major (either padded); MXFP4: 0 row-major,
+                           // 1 the 128x4-tile layout of block-scaled MMA scale factors
+    int64_t scale_ld;      // FP8 column-major: leading dimension (>= M); MXFP4 tiled: k-tiles per row tile
     float eps;
     float inv_h;           // fp32 rounding of 1/H
 };
@@ -50,8 +52,8 @@ cudaError_t launch_rows_fp8(int vpt, int tpr_static, const LaunchParams &p, int 
                             cudaStream_t st);
 cudaError_t launch_rows_mx(int vpt, int tpr_static, const LaunchParams &p, int grid, int threads,
                            cudaStream_t st);
-cudaError_t launch_dual(int v0, int t0, int v1, int t1, const LaunchParams &p, int grid, int threads,
-                        cudaStream_t st);
+cudaError_t launch_dual(bool mx, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,
+                        int threads, cudaStream_t st);
 cudaError_t launch_bulk(bool mx, int vpt, int tpr_static, const BulkParams &p, int grid, int threads,
                         size_t smem, cudaStream_t st);
 int bulk_occupancy(bool mx, int vpt, int tpr_static, int threads, size_t smem);

@@ -2,7 +2,7 @@
 // straight into registers with 16-byte streaming loads, adds, writes the
 // residual back, and finishes the row (rmsq_rows.cuh).
 //   rows_kernel<VPT, TPR, MX>       one tensor
-//   dual_kernel<V0, T0, V1, T1>     two tensors (the MLA q_a / kv_a pair),
+//   dual_kernel<V0, T0, V1, T1, MX> two tensors (the MLA q_a / kv_a pair),
 //                                   blocks [0, seg[0].blocks) on the first
 // TPR / T0 / T1 = 0 means the team size is read at run time.
 #pragma once
@@ -32,14 +32,14 @@ __global__ void __launch_bounds__(kMaxThreads) rows_kernel(const __grid_constant
     block_rows<VPT, TPR, MX>(p.seg[0], blockIdx.x, red);
 }
 
-template <int V0, int T0, int V1, int T1>
+template <int V0, int T0, int V1, int T1, bool MX>
 __global__ void __launch_bounds__(kMaxThreads) dual_kernel(const __grid_constant__ LaunchParams p)
 {
     __shared__ RedSmem red;
     if ((int)blockIdx.x < p.seg[0].blocks)
-        block_rows<V0, T0, false>(p.seg[0], blockIdx.x, red);
+        block_rows<V0, T0, MX>(p.seg[0], blockIdx.x, red);
     else
-        block_rows<V1, T1, false>(p.seg[1], blockIdx.x - p.seg[0].blocks, red);
+        block_rows<V1, T1, MX>(p.seg[1], blockIdx.x - p.seg[0].blocks, red);
 }
 
 template <bool MX>

@@ -62,6 +62,18 @@ __device__ __forceinline__ int mx_exponent_from_bits(uint32_t a)
     return min(127, max(-127, fl - 2));
 }
 
+// Byte offset of the E8M0 scale of (row, group g) in the scale-factor layout
+// that Blackwell's block-scaled MMA reads: 128-row x 4-group tiles of 512
+// bytes, tiles ordered row-tile major with `ktiles` tiles per row tile; inside
+// a tile, row r and group c sit at (r % 32) * 16 + (r / 32) * 4 + c, so the
+// four groups of a row are adjacent and rows r, r+32, r+64, r+96 share a
+// 16-byte line.
+__device__ __forceinline__ int64_t mma_scale_offset(int64_t row, int64_t g, int64_t ktiles)
+{
+    const int64_t r = row & 127;
+    return ((row >> 7) * ktiles + (g >> 2)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (g & 3);
+}
+
 // Team-wide fp64 sum of squares and fp64 finalisation, for rows whose sum
 // lies outside the fp32 range in which the double-float path is exact.
 template <int VPT>
@@ -217,7 +229,7 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
             if (leader) {
                 const int64_t g = v >> 4, G = s.H >> 7;
                 float *sc = (float *)s.out_scale;
-                sc[s.layout == 0 ? row * G + g : g * s.M + row] = scale;
+                sc[s.layout == 0 ? row * G + g : g * s.scale_ld + row] = scale;
             }
             const GroupDivisor gd = make_group_divisor(d);
             uint32_t c[4];
@@ -239,7 +251,9 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
             const float2 mult = f2(__uint_as_float((uint32_t)(127 - X) << 23));   // 2^-X
             if (leader) {
                 uint8_t *sc = (uint8_t *)s.out_scale;
-                sc[row * (int64_t)(s.H >> 5) + (v >> 2)] = (uint8_t)(X + 127);
+                const int64_t g = v >> 2;
+                sc[s.layout == 0 ? row * (int64_t)(s.H >> 5) + g : mma_scale_offset(row, g, s.scale_ld)] =
+                    (uint8_t)(X + 127);
             }
             uint32_t c[4];
 #pragma unroll

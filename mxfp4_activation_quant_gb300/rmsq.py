@@ -24,7 +24,7 @@ RMSQ_OK = 0
 STATUS_NAMES = {0: "RMSQ_OK", 1: "RMSQ_ERR_INVALID_ARG", 2: "RMSQ_ERR_MISALIGNED",
                 3: "RMSQ_ERR_UNSUPPORTED", 4: "RMSQ_ERR_CUDA", 5: "RMSQ_ERR_TIMEOUT"}
 KERNEL_AUTO, KERNEL_ROWS, KERNEL_PERSISTENT = 0, 1, 2
-SCALE_ROW_MAJOR, SCALE_COL_MAJOR = 0, 1
+SCALE_ROW_MAJOR, SCALE_COL_MAJOR, SCALE_COL_MAJOR_PAD4 = 0, 1, 2
 
 _p = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -56,6 +56,8 @@ _SIGNATURES = {
     "rmsq_qknorm_quant_fp8": [_p, _i64, _p, _i64, _p, _p, _f, _i64, _i64, _i64, _i32, _p, _p, _p, _p, _i32, _p, _p, _p],
     "rmsq_add_rmsnorm_quant_mxfp4": [_p, _i64, _p, _i64, _p, _f, _i64, _i64, _p, _p, _p, _p, _p],
     "rmsq_add_rmsnorm_quant_mxfp4_ex": [_p, _i64, _p, _i64, _p, _f, _i64, _i64, _p, _p, _p, _p, _p, _p],
+    "rmsq_qknorm_quant_mxfp4": [_p, _i64, _p, _i64, _p, _p, _f, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p],
+    "rmsq_add_rmsnorm_quant_mxfp4_mma_scales": [_p, _i64, _p, _i64, _p, _f, _i64, _i64, _p, _p, _p, _p, _p],
     "rmsq_sync_status": [_p],
     "rmsq_encode_e4m3": [_p, _p, _i64, _p],
     "rmsq_encode_e2m1": [_p, _p, _i64, _p],
@@ -106,8 +108,24 @@ def _rows_view(t: torch.Tensor, name: str) -> int:
 
 
 def _layout(scale_layout) -> int:
-    return {"row": SCALE_ROW_MAJOR, "col": SCALE_COL_MAJOR,
-            SCALE_ROW_MAJOR: SCALE_ROW_MAJOR, SCALE_COL_MAJOR: SCALE_COL_MAJOR}[scale_layout]
+    return {"row": SCALE_ROW_MAJOR, "col": SCALE_COL_MAJOR, "col_pad4": SCALE_COL_MAJOR_PAD4,
+            SCALE_ROW_MAJOR: SCALE_ROW_MAJOR, SCALE_COL_MAJOR: SCALE_COL_MAJOR,
+            SCALE_COL_MAJOR_PAD4: SCALE_COL_MAJOR_PAD4}[scale_layout]
+
+
+def scale_shape(M: int, H: int, group: int, layout: int) -> tuple:
+    """Shape of the fp32 scale tensor for a layout (column-major padded: [H/G, M rounded up to 4])."""
+    G = H // group if group > 0 else 0
+    if layout == SCALE_ROW_MAJOR:
+        return (M, G)
+    if layout == SCALE_COL_MAJOR:
+        return (G, M)
+    return (G, (M + 3) // 4 * 4)
+
+
+def mma_scale_bytes(M: int, H: int) -> int:
+    """Bytes of MXFP4 scales in the block-scaled MMA tile layout."""
+    return (M + 127) // 128 * ((H // 32 + 3) // 4) * 512
 
 
 def add_rmsnorm_quant_fp8(x: torch.Tensor, gamma: torch.Tensor, residual: torch.Tensor | None = None,
@@ -126,8 +144,7 @@ def add_rmsnorm_quant_fp8(x: torch.Tensor, gamma: torch.Tensor, residual: torch.
     dev = x.device
     layout = _layout(scale_layout)
     q = torch.empty((M, H), dtype=torch.float8_e4m3fn, device=dev)
-    G = H // group if group > 0 else 0
-    scale = torch.empty((M, G) if layout == SCALE_ROW_MAJOR else (G, M), dtype=torch.float32, device=dev)
+    scale = torch.empty(scale_shape(M, H, group, layout), dtype=torch.float32, device=dev)
     res_out = None
     if residual is not None:
         res_out = out_residual if out_residual is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
@@ -217,6 +234,34 @@ def qknorm_quant_fp8(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Tenso
     return (qq, qs), (kq, ks)
 
 
+def qknorm_quant_mxfp4(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Tensor,
+                       gamma_kv: torch.Tensor, eps: float = 1e-6, keep_bf16: bool = False):
+    """One launch for the MLA latents, MXFP4: ``(q_tuple, kv_tuple)``, each
+    ``(q, scale)`` or ``(y, q, scale)`` with q [M, H/2] uint8 and E8M0 scales [M, H/32]."""
+    ldq = _rows_view(q_a, "q_a")
+    ldk = _rows_view(kv_a, "kv_a")
+    M, Hq = q_a.shape
+    Mk, Hkv = kv_a.shape
+    if Mk != M:
+        raise ValueError("q_a and kv_a must have the same number of rows")
+    dev = q_a.device
+
+    def outs(H):
+        q = torch.empty((M, H // 2), dtype=torch.uint8, device=dev)
+        s = torch.empty((M, H // 32), dtype=torch.uint8, device=dev)
+        y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
+        return q, s, y
+
+    qq, qs, qy = outs(Hq)
+    kq, ks, ky = outs(Hkv)
+    _check(lib().rmsq_qknorm_quant_mxfp4(_ptr(q_a), ldq, _ptr(kv_a), ldk, _ptr(gamma_q), _ptr(gamma_kv), eps,
+                                         M, Hq, Hkv, _ptr(qq), _ptr(qs), _ptr(kq), _ptr(ks), _ptr(qy),
+                                         _ptr(ky), _stream(dev)))
+    if keep_bf16:
+        return (qy, qq, qs), (ky, kq, ks)
+    return (qq, qs), (kq, ks)
+
+
 def add_rmsnorm_quant_mxfp4(x: torch.Tensor, gamma: torch.Tensor, residual: torch.Tensor | None = None,
                             eps: float = 1e-6, keep_bf16: bool = False,
                             out_residual: torch.Tensor | None = None, opts: LaunchOpts | None = None):
@@ -238,6 +283,27 @@ def add_rmsnorm_quant_mxfp4(x: torch.Tensor, gamma: torch.Tensor, residual: torc
         _check(lib().rmsq_add_rmsnorm_quant_mxfp4(*args))
     else:
         _check(lib().rmsq_add_rmsnorm_quant_mxfp4_ex(*args, ctypes.byref(opts)))
+    return ((y, q, scale) if keep_bf16 else (q, scale)), res_out
+
+
+def add_rmsnorm_quant_mxfp4_mma_scales(x: torch.Tensor, gamma: torch.Tensor,
+                                       residual: torch.Tensor | None = None, eps: float = 1e-6,
+                                       keep_bf16: bool = False, scale_out: torch.Tensor | None = None):
+    """MXFP4 with the E8M0 scales in the block-scaled MMA tile layout (a flat
+    uint8 tensor of ``mma_scale_bytes(M, H)``; padding bytes are left as they
+    are in ``scale_out``, zero-filled when it is allocated here)."""
+    ldx = _rows_view(x, "x")
+    M, H = x.shape
+    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    dev = x.device
+    q = torch.empty((M, H // 2), dtype=torch.uint8, device=dev)
+    scale = scale_out if scale_out is not None else torch.zeros(mma_scale_bytes(M, H), dtype=torch.uint8,
+                                                                device=dev)
+    res_out = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if residual is not None else None
+    y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
+    _check(lib().rmsq_add_rmsnorm_quant_mxfp4_mma_scales(_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps,
+                                                         M, H, _ptr(q), _ptr(scale), _ptr(res_out), _ptr(y),
+                                                         _stream(dev)))
     return ((y, q, scale) if keep_bf16 else (q, scale)), res_out
 
 

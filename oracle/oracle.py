@@ -25,6 +25,7 @@ _p = ctypes.c_void_p
 
 SCALE_ROW_MAJOR = 0
 SCALE_COL_MAJOR = 1
+SCALE_COL_MAJOR_PAD4 = 2
 
 
 def default_threads() -> int:
@@ -62,6 +63,8 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_group_quant_fp8.restype = ctypes.c_int
     L.oracle_group_quant_mxfp4.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _i64, ctypes.c_int]
     L.oracle_group_quant_mxfp4.restype = ctypes.c_int
+    L.oracle_mx_scale_tiles.argtypes = [_p, _i64, _i64, _p]
+    L.oracle_mx_scale_tiles.restype = ctypes.c_int
     return L
 
 
@@ -164,8 +167,13 @@ def group_quant_fp8(y, group: int = 128, layout: int = SCALE_ROW_MAJOR,
     if H % group:
         raise ValueError("H must be a multiple of the group size")
     q = np.empty((M, H), dtype=np.uint8)
-    shape = (M, H // group) if layout == SCALE_ROW_MAJOR else (H // group, M)
-    scale = np.empty(shape, dtype=np.float32)
+    if layout == SCALE_ROW_MAJOR:
+        shape = (M, H // group)
+    elif layout == SCALE_COL_MAJOR:
+        shape = (H // group, M)
+    else:
+        shape = (H // group, (M + 3) // 4 * 4)
+    scale = np.full(shape, np.nan, dtype=np.float32)     # padding stays NaN
     py, ldy = _rows(y)
     rc = lib().oracle_group_quant_fp8(py, ldy, M, H, group, layout, q.ctypes.data, H,
                                       scale.ctypes.data, nthreads or default_threads())
@@ -197,7 +205,20 @@ def _layout_code(layout) -> int:
         return SCALE_ROW_MAJOR
     if layout in ("col", SCALE_COL_MAJOR):
         return SCALE_COL_MAJOR
+    if layout in ("col_pad4", SCALE_COL_MAJOR_PAD4):
+        return SCALE_COL_MAJOR_PAD4
     raise ValueError(f"unknown scale layout {layout!r}")
+
+
+def mx_scale_tiles(scale, fill: int = 0) -> np.ndarray:
+    """Row-major [M, G] E8M0 bytes -> the block-scaled MMA tile layout
+    (ceil(M/128) * ceil(G/4) * 512 bytes; padding bytes are ``fill``)."""
+    scale = np.ascontiguousarray(scale, dtype=np.uint8)
+    M, G = scale.shape
+    out = np.full(((M + 127) // 128) * ((G + 3) // 4) * 512, fill, dtype=np.uint8)
+    if lib().oracle_mx_scale_tiles(scale.ctypes.data, M, G, out.ctypes.data):
+        raise ValueError("oracle_mx_scale_tiles rejected its arguments")
+    return out
 
 
 def add_rmsnorm_quant_fp8(x, residual, gamma, eps: float = 1e-6, group: int = 128,
@@ -234,3 +255,10 @@ def add_rmsnorm_quant_mxfp4(x, residual, gamma, eps: float = 1e-6,
     if residual is not None:
         out["residual_out"] = r
     return out
+
+
+def qknorm_quant_mxfp4(q_a, kv_a, gamma_q, gamma_kv, eps: float = 1e-6,
+                       nthreads: int | None = None) -> dict:
+    """Each latent normalised with its own gamma and MXFP4-quantised separately."""
+    return {"q": add_rmsnorm_quant_mxfp4(q_a, None, gamma_q, eps, nthreads),
+            "kv": add_rmsnorm_quant_mxfp4(kv_a, None, gamma_kv, eps, nthreads)}

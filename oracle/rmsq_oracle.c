@@ -321,7 +321,9 @@ int oracle_rmsnorm(const uint16_t *r, int64_t ldr, const uint16_t *gamma, float 
 
 /* ----------------------------------------------- 3a. FP8 group quant */
 
-enum { ORACLE_SCALE_ROW_MAJOR = 0, ORACLE_SCALE_COL_MAJOR = 1 };
+/* Scale layouts: row-major [M, H/G]; column-major [H/G, M]; column-major with
+ * the leading dimension M rounded up to a multiple of 4 (padding untouched). */
+enum { ORACLE_SCALE_ROW_MAJOR = 0, ORACLE_SCALE_COL_MAJOR = 1, ORACLE_SCALE_COL_MAJOR_PAD4 = 2 };
 
 typedef struct {
     const uint16_t *y;
@@ -348,8 +350,10 @@ static void fp8q_rows(void *p, int64_t m0, int64_t m1)
             float scale = amax / 448.0f;
             if (c->layout == ORACLE_SCALE_ROW_MAJOR)
                 c->scale[m * ngroups + g] = scale;
-            else
+            else if (c->layout == ORACLE_SCALE_COL_MAJOR)
                 c->scale[g * c->M + m] = scale;
+            else
+                c->scale[g * ((c->M + 3) / 4 * 4) + m] = scale;
             for (int64_t i = g * c->G; i < (g + 1) * c->G; ++i) {
                 float v = bf16_to_f32(row[i]);
                 float quot = (amax == 0.0f) ? v : v / scale;
@@ -366,7 +370,8 @@ int oracle_group_quant_fp8(const uint16_t *y, int64_t ldy, int64_t M, int64_t H,
 {
     if (!y || !q || !scale || M < 0 || H <= 0 || G <= 0 || H % G != 0)
         return -1;
-    if (layout != ORACLE_SCALE_ROW_MAJOR && layout != ORACLE_SCALE_COL_MAJOR)
+    if (layout != ORACLE_SCALE_ROW_MAJOR && layout != ORACLE_SCALE_COL_MAJOR &&
+        layout != ORACLE_SCALE_COL_MAJOR_PAD4)
         return -1;
     fp8q_ctx c = {y, ldy, M, H, G, layout, q, ldq, scale};
     for_rows(fp8q_rows, &c, M, nthreads);
@@ -418,6 +423,29 @@ int oracle_group_quant_mxfp4(const uint16_t *y, int64_t ldy, int64_t M, int64_t 
         return -1;
     mxq_ctx c = {y, ldy, H, q, ldq, scale, ldscale};
     for_rows(mxq_rows, &c, M, nthreads);
+    return 0;
+}
+
+/* ------------------------------------ MXFP4 scales in MMA tile layout */
+
+/* Re-lays a row-major [M, G] matrix of E8M0 scale bytes into the layout that
+ * Blackwell's block-scaled MMA reads scale factors from (NVIDIA PTX ISA,
+ * tcgen05 block scaling; cuBLAS, "1D block scaling factors layout"): tiles of
+ * 128 rows x 4 groups (512 bytes), stored row-tile major with ceil(G/4)
+ * tiles per row tile; inside a tile, row r and group c at
+ * (r % 32) * 16 + (r / 32) * 4 + c. Padding bytes of partial tiles are left
+ * as they are. */
+int oracle_mx_scale_tiles(const uint8_t *s, int64_t M, int64_t G, uint8_t *out)
+{
+    if (!s || !out || M < 0 || G <= 0)
+        return -1;
+    int64_t ktiles = (G + 3) / 4;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t g = 0; g < G; ++g) {
+            int64_t tile = (m / 128) * ktiles + g / 4;
+            int64_t r = m % 128, c = g % 4;
+            out[tile * 512 + (r % 32) * 16 + (r / 32) * 4 + c] = s[m * G + g];
+        }
     return 0;
 }
 

@@ -39,6 +39,9 @@ MUTANTS = {
                            "float s = bf16_to_f32(c->x[m * c->ldx + i]);"),
     "col_major_as_row_major": ("c->scale[g * c->M + m] = scale;", "c->scale[m * ngroups + g] = scale;"),
     "quantise_unnormalised": ("float v = bf16_to_f32(row[i]);\n                float quot", "float v = bf16_to_f32(row[i]) * 2.0f;\n                float quot"),
+    "mx_tiles_rows_transposed": ("out[tile * 512 + (r % 32) * 16 + (r / 32) * 4 + c]",
+                                 "out[tile * 512 + (r / 32) * 16 + (r % 32) * 4 + c]"),
+    "col_pad4_unpadded": ("c->scale[g * ((c->M + 3) / 4 * 4) + m] = scale;", "c->scale[g * c->M + m] = scale;"),
     "zero_group_nan": ("float quot = (amax == 0.0f) ? v : v / scale;", "float quot = v / scale;"),
 }
 
@@ -63,6 +66,9 @@ def _pins(oracle_mod):
     yield "norm:fp8_invariants", lambda: norm.test_fp8_quant_invariants(oracle_mod, b)
     yield "norm:col_major", lambda: norm.test_fp8_column_major_is_transpose(oracle_mod, b)
     yield "norm:mxfp4_invariants", lambda: norm.test_mxfp4_invariants(oracle_mod)
+    from tests import test_oracle_layouts as lay
+    yield "layout:mx_tiles", lambda: lay.test_mx_scale_tiles_hand_positions(oracle_mod)
+    yield "layout:col_pad4", lambda: lay.test_fp8_padded_column_major(oracle_mod)
 
 
 def _batch():

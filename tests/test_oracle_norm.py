@@ -179,3 +179,13 @@ def test_strided_input_rows(oracle_mod, batch):
     b = oracle_mod.add_rmsnorm_quant_fp8(np.ascontiguousarray(batch["x"][:8]), None, batch["gamma"], 1e-6)
     np.testing.assert_array_equal(a["q"], b["q"])
     np.testing.assert_array_equal(a["y"], b["y"])
+
+
+def test_mxfp4_qknorm_halves_equal_single_calls(oracle_mod):
+    w = synth.WORKLOADS["qknorm"]
+    d = {k: _bits(v) for k, v in synth.make_inputs(w, M=16).items()}
+    both = oracle_mod.qknorm_quant_mxfp4(d["q_a"], d["kv_a"], d["gamma_q"], d["gamma_kv"], 1e-6)
+    one = oracle_mod.add_rmsnorm_quant_mxfp4(d["q_a"], None, d["gamma_q"], 1e-6)
+    for k in ("q", "scale", "y"):
+        np.testing.assert_array_equal(both["q"][k], one[k])
+    assert both["kv"]["q"].shape == (16, 256) and both["kv"]["scale"].shape == (16, 16)

@@ -384,3 +384,60 @@ def test_group_division_is_exact_over_the_whole_domain():
     assert c["code_mismatches"] == 0, c
     assert c["scale_mismatches"] == 0, c
     print(c)
+
+
+@pytest.mark.parametrize("M,Hq,Hkv", [(301, 1536, 512), (8192, 1536, 512), (37, 96, 32), (19, 640, 160)])
+def test_qknorm_mxfp4(oracle_mod, M, Hq, Hkv):
+    """The MXFP4 latent pair in one launch: the compiled-in shape (1536/512) at a
+    ragged and the full row count, and generic shapes."""
+    d = {"q_a": synth.random_bf16(90 + Hq, (M, Hq)),
+         "kv_a": synth.random_bf16(91 + Hkv, (M, Hkv), var=2.0, tensor="kv_a"),
+         "gamma_q": synth.gaussian_bf16(92, "gamma_q", (Hq,), mean=1.0, var=0.1),
+         "gamma_kv": synth.gaussian_bf16(93, "gamma_kv", (Hkv,), mean=1.0, var=0.1)}
+    g = _gpu(d)
+    (qy, qq, qs), (ky, kq, ks) = rmsq.qknorm_quant_mxfp4(g["q_a"], g["kv_a"], g["gamma_q"], g["gamma_kv"],
+                                                         eps=1e-6, keep_bf16=True)
+    torch.cuda.synchronize()
+    ref = oracle_mod.qknorm_quant_mxfp4(d["q_a"], d["kv_a"], d["gamma_q"], d["gamma_kv"], 1e-6)
+    parity.compare_mx({"q": qq, "scale": qs, "y": qy}, ref["q"], what="mx q_a")
+    parity.compare_mx({"q": kq, "scale": ks, "y": ky}, ref["kv"], what="mx kv_a")
+
+
+# ------------------------------------------------------- GEMM-ready scale layouts
+
+@pytest.mark.parametrize("M", [1, 37, 64, 300])
+def test_fp8_padded_column_major_scales(oracle_mod, M):
+    w = synth.WORKLOADS["decode"]
+    d = synth.make_inputs(w, M=M)
+    g = _gpu(d)
+    Mp = (M + 3) // 4 * 4
+    scale = torch.full((56, Mp), -3.0, dtype=torch.float32, device=DEV)     # canary in the padding
+    q = torch.empty((M, 7168), dtype=torch.uint8, device=DEV)
+    ro = torch.empty((M, 7168), dtype=torch.bfloat16, device=DEV)
+    rmsq.add_rmsnorm_quant_fp8_into(g["x"], g["gamma"], g["residual"], q, scale, ro, None, eps=w.eps,
+                                    scale_layout="col_pad4")
+    torch.cuda.synchronize()
+    ref = oracle_mod.add_rmsnorm_quant_fp8(d["x"], d["residual"], d["gamma"], w.eps, layout="col_pad4")
+    parity.compare_fp8({"q": q, "scale": scale[:, :M], "residual_out": ro},
+                       {**ref, "scale": ref["scale"][:, :M]}, "col", what=f"col_pad4 M={M}")
+    assert torch.all(scale[:, M:] == -3.0)
+
+
+@pytest.mark.parametrize("M,H", [(300, 7168), (128, 7168), (5, 96), (8192, 7168)])
+def test_mxfp4_mma_tile_scales(oracle_mod, M, H):
+    d = {"x": synth.student_t3_bf16(70 + M, "x", (M, H)),
+         "residual": synth.random_bf16(71 + M, (M, H), tensor="residual"),
+         "gamma": synth.gaussian_bf16(72, "gamma", (H,), mean=1.0, var=0.1)}
+    g = _gpu(d)
+    nbytes = rmsq.mma_scale_bytes(M, H)
+    canary = torch.full((nbytes,), 0xEE, dtype=torch.uint8, device=DEV)
+    (q, s), ro = rmsq.add_rmsnorm_quant_mxfp4_mma_scales(g["x"], g["gamma"], g["residual"], eps=1e-6,
+                                                          scale_out=canary)
+    torch.cuda.synchronize()
+    ref = oracle_mod.add_rmsnorm_quant_mxfp4(d["x"], d["residual"], d["gamma"], 1e-6)
+    want = oracle_mod.mx_scale_tiles(ref["scale"], fill=0xEE)
+    boundary = ref["margin"] < parity.BOUNDARY
+    if not boundary.any():
+        np.testing.assert_array_equal(parity.u8(s), want)
+    parity.compare_mx({"q": q, "scale": torch.from_numpy(ref["scale"]), "residual_out": ro}, ref,
+                      what=f"mx tiles M={M}")
