@@ -7,7 +7,7 @@
 #include <cstdio>
 #include <cstring>
 
-#include "../../include/rmsq.h"
+#include "rmsq.h"
 #include "rmsq_device.cuh"
 #include "rmsq_internal.h"
 

@@ -3,7 +3,7 @@
 // signs), the E4M3 code of the shortcut quotient is compared with the code of
 // IEEE fp32 division by d = RN(amax / 448), and the shortcut scale itself with
 // IEEE amax / 448. Counts are accumulated in a caller-provided device array.
-#include "../../include/rmsq.h"
+#include "rmsq.h"
 #include "rmsq_device.cuh"
 
 namespace rmsq {
