@@ -441,3 +441,52 @@ def test_mxfp4_mma_tile_scales(oracle_mod, M, H):
         np.testing.assert_array_equal(parity.u8(s), want)
     parity.compare_mx({"q": q, "scale": torch.from_numpy(ref["scale"]), "residual_out": ro}, ref,
                       what=f"mx tiles M={M}")
+
+
+# ---------------------------------------------------------------- maximum sizes
+
+def _sample_rows(M, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, n)]))
+
+
+def test_chunked_prefill_maximum_rows(oracle_mod):
+    """131072 tokens (the largest chunked-prefill size on the pages) x 7168:
+    inputs drawn on the device (torch, fixed seed), 64 sampled rows checked
+    against the oracle, in the default launch configuration."""
+    M, H = 131072, 7168
+    gen = torch.Generator(device=DEV).manual_seed(1234)
+    x = torch.randn((M, H), generator=gen, device=DEV).to(torch.bfloat16)
+    res = (torch.randn((M, H), generator=gen, device=DEV) * 2).to(torch.bfloat16)
+    gamma = (1 + 0.3 * torch.randn((H,), generator=gen, device=DEV)).to(torch.bfloat16)
+    (y, q, s), ro = rmsq.add_rmsnorm_quant_fp8(x, gamma, res, eps=1e-6, keep_bf16=True)
+    torch.cuda.synchronize()
+    rows = torch.from_numpy(_sample_rows(M, 62, 5)).to(DEV)
+    ref = oracle_mod.add_rmsnorm_quant_fp8(x[rows].cpu(), res[rows].cpu(), gamma.cpu(), 1e-6)
+    got = {"q": q[rows], "scale": s[rows], "y": y[rows], "residual_out": ro[rows]}
+    parity.compare_fp8(got, ref, what="M=131072")
+    del x, res, y, q, s, ro
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kind", ["fp8", "mxfp4"])
+def test_widest_row(oracle_mod, kind):
+    """H = 32768, the widest row the kernels take (8 vectors x 512 threads)."""
+    M, H = 9, 32768
+    d = {"x": synth.random_bf16(3, (M, H)), "residual": synth.random_bf16(4, (M, H), tensor="residual"),
+         "gamma": synth.gaussian_bf16(5, "gamma", (H,), mean=1.0, var=0.1)}
+    if kind == "fp8":
+        parity.compare_fp8(run_fp8(d, 1e-6, keep=True), ref_fp8(oracle_mod, d, 1e-6), what="H=32768")
+    else:
+        parity.compare_mx(run_mx(d, 1e-6, keep=True),
+                          oracle_mod.add_rmsnorm_quant_mxfp4(d["x"], d["residual"], d["gamma"], 1e-6),
+                          what="mx H=32768")
+
+
+def test_empty_batch_is_a_no_op():
+    x = torch.empty((0, 7168), dtype=torch.bfloat16, device=DEV)
+    g = torch.ones(7168, dtype=torch.bfloat16, device=DEV)
+    (q, s), r = rmsq.add_rmsnorm_quant_fp8(x, g, x.clone())
+    (mq, ms), _ = rmsq.add_rmsnorm_quant_mxfp4(x, g)
+    torch.cuda.synchronize()
+    assert q.shape == (0, 7168) and s.shape == (0, 56) and mq.shape == (0, 3584)
