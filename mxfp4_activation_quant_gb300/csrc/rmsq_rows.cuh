@@ -32,6 +32,7 @@ namespace rmsq {
 
 struct RedSmem {
     float2 part[2][32];   // per-warp double-float partials, two parity sets
+    float inv[2][16];     // per-team inv_rms (NaN: take the fp64 path), two parity sets
     double dpart[32];     // per-warp fp64 partials for the wide-range path
 };
 
@@ -109,35 +110,49 @@ __device__ __forceinline__ float inv_rms_fp64_path(const uint4 (&r)[VPT], int H,
     return (float)(1.0 / sqrt(acc / (double)H + (double)eps));
 }
 
-// Sum over a team of the per-thread double-float partials; the same bits in
-// every thread of the team. Within a warp an xor butterfly; across the
-// team's warps (tpr > 32) lane 0 of each warp publishes its partial, then in
-// every warp lanes 0..nw-1 load one partial each and butterfly over the next
-// power of two, and lane 0's sum is broadcast. `parity` alternates the
-// shared-memory slots between consecutive rows of a persistent team.
+// inv_rms of a team's row from the per-thread double-float partials of its
+// sum of squares; the same value in every thread of the team. Within a warp
+// an xor butterfly (bit-identical in every lane). For teams wider than a
+// warp, lane 0 of each warp publishes its partial; the team's first warp
+// alone combines them (butterfly over the next power of two) and finalises,
+// and the result is broadcast through shared memory. `parity` alternates
+// the shared slots between consecutive rows of a persistent team. A NaN
+// result means the sum left the double-float range: the caller takes the
+// fp64 path.
 template <int TPR>
-__device__ __forceinline__ DF team_sum(DF S, int tpr, int team, int parity, RedSmem &red,
-                                       unsigned tmask)
+__device__ __forceinline__ float team_inv_rms(DF S, const Seg &s, int tpr, int team, int parity,
+                                              RedSmem &red, unsigned tmask)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1)
         if (off < tpr)
             S = df_add_lazy(S, shfl_xor_df(S, off, tmask));
-    if (tpr > 32) {
-        const int nw = tpr >> 5, w0 = team * nw;
-        if (lane == 0)
-            red.part[parity][warp] = make_float2(S.hi, S.lo);
-        team_bar(team, tpr);
+    float inv;
+    if (tpr <= 32) {
+        if (!inv_rms_df(df_renorm(S), s.H, s.inv_h, s.eps, inv))
+            inv = __int_as_float(0x7fffffff);
+        return inv;
+    }
+    const int nw = tpr >> 5, w0 = team * nw;
+    if (lane == 0)
+        red.part[parity][warp] = make_float2(S.hi, S.lo);
+    team_bar(team, tpr);
+    if (warp == w0) {
         const float2 p = lane < nw ? red.part[parity][w0 + lane] : make_float2(0.0f, 0.0f);
         DF T{p.x, p.y};
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1)
             if (off < nw)
                 T = df_add_lazy(T, shfl_xor_df(T, off, 0xffffffffu));
-        S = DF{__shfl_sync(0xffffffffu, T.hi, 0), __shfl_sync(0xffffffffu, T.lo, 0)};
+        if (lane == 0) {
+            if (!inv_rms_df(df_renorm(T), s.H, s.inv_h, s.eps, inv))
+                inv = __int_as_float(0x7fffffff);
+            red.inv[parity][team] = inv;
+        }
     }
-    return df_renorm(S);
+    team_bar(team, tpr);
+    return red.inv[parity][team];
 }
 
 // Everything after the row is loaded: r holds the thread's VPT vectors of
@@ -167,9 +182,9 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         acc_square2(unpack_bf16x2(r[k].z), hi, lo);
         acc_square2(unpack_bf16x2(r[k].w), hi, lo);
     }
-    const DF S = team_sum<TPR>(df_add_lazy(DF{hi.x, lo.x}, DF{hi.y, lo.y}), tpr, team, parity, red, tmask);
-    float inv;
-    if (!inv_rms_df(S, s.H, s.inv_h, s.eps, inv))     // team-uniform branch
+    float inv = team_inv_rms<TPR>(df_add_lazy(DF{hi.x, lo.x}, DF{hi.y, lo.y}), s, tpr, team, parity, red,
+                                  tmask);
+    if (inv != inv)                                   // team-uniform: NaN asks for the fp64 path
         inv = inv_rms_fp64_path<VPT>(r, s.H, s.eps, tpr, team, red);
     const float2 inv2 = f2(inv);
 
