@@ -254,7 +254,7 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
         size_t smem = bulk_smem(s.H, s.res != nullptr);
         if (smem + sizeof(float2) * 64 + 256 > (size_t)smem_max)
             return fail(RMSQ_ERR_UNSUPPORTED, "H=%d needs %zu bytes of shared memory", s.H, smem);
-        const int ts = (static_shape(vpt, tpr) && vpt * tpr * 8 == s.H) ? tpr : 0;
+        const int ts = (vpt == 4 && tpr == 224 && s.H == 7168) ? tpr : 0;
         int64_t grid = o.grid;
         if (grid <= 0) {
             int per_sm = bulk_occupancy(mx, vpt, ts, tpr, smem);

@@ -59,9 +59,10 @@ cudaError_t launch_bulk(bool mx, int vpt, int tpr_static, const BulkParams &p, i
 int bulk_occupancy(bool mx, int vpt, int tpr_static, int threads, size_t smem);
 size_t bulk_smem(int H, bool has_res);
 bool vpt_instantiated(int vpt);
-// Team shapes also compiled with a fixed team size (exact fits of the hot
-// widths): one tensor of H = 7168 as 4 vectors x 224 threads; the MLA pair
-// q_a 1536 as 3 x 64 and kv_a 512 as 4 x 16.
+// Team shapes also compiled with a fixed team size (exact fits of common
+// widths, listed in rmsq_rowkernel.cuh; H = 7168 is 4 vectors x 224 threads);
+// the MLA pair q_a 1536 as 3 x 64 and kv_a 512 as 4 x 16. The persistent
+// kernel has a fixed-size instantiation for 4 x 224 only.
 bool static_shape(int vpt, int tpr);
 bool static_dual_shape(int v0, int t0, int v1, int t1);
 

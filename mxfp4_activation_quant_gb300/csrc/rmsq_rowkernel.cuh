@@ -42,16 +42,30 @@ __global__ void __launch_bounds__(kMaxThreads) dual_kernel(const __grid_constant
         block_rows<V1, T1, MX>(p.seg[1], blockIdx.x - p.seg[0].blocks, red);
 }
 
+// Team shapes compiled with a fixed team size: exact fits of common hidden
+// sizes (vectors per thread x threads x 8 = H).
+#define RMSQ_STATIC_SHAPES(X) \
+    X(4, 224) /* H = 7168 */  \
+    X(4, 256) /* H = 8192 */  \
+    X(4, 160) /* H = 5120 */  \
+    X(4, 128) /* H = 4096 */  \
+    X(4, 64)  /* H = 2048 */  \
+    X(3, 64)  /* H = 1536 */  \
+    X(4, 16)  /* H = 512  */
+
 template <bool MX>
 cudaError_t launch_rows_impl(int vpt, int tpr_static, const LaunchParams &p, int grid, int threads,
                              cudaStream_t st)
 {
     if (tpr_static) {
-        if (vpt == 4 && tpr_static == 224)
-            rows_kernel<4, 224, MX><<<grid, threads, 0, st>>>(p);
-        else
-            return cudaErrorInvalidValue;
-        return cudaGetLastError();
+#define RMSQ_LAUNCH_STATIC(V, T)                                    \
+        if (vpt == V && tpr_static == T) {                          \
+            rows_kernel<V, T, MX><<<grid, threads, 0, st>>>(p);     \
+            return cudaGetLastError();                              \
+        }
+        RMSQ_STATIC_SHAPES(RMSQ_LAUNCH_STATIC)
+#undef RMSQ_LAUNCH_STATIC
+        return cudaErrorInvalidValue;
     }
     switch (vpt) {
     case 1: rows_kernel<1, 0, MX><<<grid, threads, 0, st>>>(p); break;

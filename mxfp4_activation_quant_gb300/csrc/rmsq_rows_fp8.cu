@@ -11,6 +11,14 @@ cudaError_t launch_rows_fp8(int vpt, int tpr_static, const LaunchParams &p, int 
 
 bool vpt_instantiated(int vpt) { return vpt >= 1 && vpt <= 8; }
 
-bool static_shape(int vpt, int tpr) { return vpt == 4 && tpr == 224; }
+bool static_shape(int vpt, int tpr)
+{
+#define RMSQ_IS_STATIC(V, T) \
+    if (vpt == V && tpr == T) \
+        return true;
+    RMSQ_STATIC_SHAPES(RMSQ_IS_STATIC)
+#undef RMSQ_IS_STATIC
+    return false;
+}
 
 }  // namespace rmsq

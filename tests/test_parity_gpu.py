@@ -147,7 +147,7 @@ def test_handworked_rows_on_gpu(row):
 
 # -------------------------------------------------------------- edge cases
 
-@pytest.mark.parametrize("H", [128, 256, 384, 512, 640, 1024, 1536, 2048, 3072, 4096, 7168, 8192, 16384])
+@pytest.mark.parametrize("H", [128, 256, 384, 512, 640, 1024, 1536, 2048, 3072, 4096, 5120, 7168, 8192, 16384])
 def test_shapes_fp8(oracle_mod, H):
     M = 19                                          # ragged against every rows-per-block
     d = {"x": synth.random_bf16(10 + H, (M, H)), "residual": synth.random_bf16(20 + H, (M, H), var=4.0,
@@ -157,7 +157,7 @@ def test_shapes_fp8(oracle_mod, H):
     parity.compare_fp8(got, ref_fp8(oracle_mod, d, 1e-6), what=f"H={H}")
 
 
-@pytest.mark.parametrize("H", [32, 64, 96, 128, 160, 256, 512, 1024, 7168])
+@pytest.mark.parametrize("H", [32, 64, 96, 128, 160, 256, 512, 1024, 1536, 2048, 4096, 5120, 7168, 8192])
 def test_shapes_mxfp4(oracle_mod, H):
     M = 23
     d = {"x": synth.student_t3_bf16(40 + H, "x", (M, H)),
