@@ -247,19 +247,17 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
                 sc[s.layout == 0 ? row * G + g : g * s.scale_ld + row] = scale;
             }
             const GroupDivisor gd = make_group_divisor(d);
-            uint32_t c[4];
+            float2 qv[4];
             if (gd.fast) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 qv = div_fast_neg2(unpack_bf16x2(yw[j] ^ 0x80008000u), gd);
-                    c[j] = e4m3x2(qv.x, qv.y);
-                }
+                for (int j = 0; j < 4; ++j)
+                    qv[j] = div_fast_neg2(unpack_bf16x2(yw[j] ^ 0x80008000u), gd);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    c[j] = e4m3x2(__fdiv_rn(bf_lo(yw[j]), d), __fdiv_rn(bf_hi(yw[j]), d));
+                    qv[j] = make_float2(__fdiv_rn(bf_lo(yw[j]), d), __fdiv_rn(bf_hi(yw[j]), d));
             }
-            const uint2 q = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+            const uint2 q = make_uint2(e4m3x4(qv[0], qv[1]), e4m3x4(qv[2], qv[3]));
             reinterpret_cast<uint2 *>(s.out_q + row * (int64_t)s.H)[v] = q;
         } else {
             const int X = mx_exponent_from_bits(am[k]);
@@ -270,14 +268,9 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
                 sc[s.layout == 0 ? row * (int64_t)(s.H >> 5) + g : mma_scale_offset(row, g, s.scale_ld)] =
                     (uint8_t)(X + 127);
             }
-            uint32_t c[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 qv = mul2(unpack_bf16x2(yw[j]), mult);
-                c[j] = e2m1x2(qv.x, qv.y);
-            }
             reinterpret_cast<uint32_t *>(s.out_q + row * (int64_t)(s.H >> 1))[v] =
-                c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+                e2m1x8(mul2(unpack_bf16x2(yw[0]), mult), mul2(unpack_bf16x2(yw[1]), mult),
+                       mul2(unpack_bf16x2(yw[2]), mult), mul2(unpack_bf16x2(yw[3]), mult));
         }
     }
 }

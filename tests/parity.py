@@ -58,9 +58,19 @@ def unpack_e2m1(q: np.ndarray) -> np.ndarray:
     return out
 
 
+def _boundary_rows(ref: dict, what: str) -> np.ndarray:
+    """Rows the oracle flags as within 2^-40 of an fp32 rounding boundary of
+    inv_rms. Such rows are rare (about 2^-16 of random rows); a comparison
+    that would exempt more than a few is refused, so that a broken margin
+    cannot weaken the checks."""
+    boundary = ref["margin"] < BOUNDARY
+    assert boundary.sum() <= max(2, len(boundary) // 1000), f"{what}: {boundary.sum()} boundary rows"
+    return boundary
+
+
 def compare_fp8(got: dict, ref: dict, scale_layout: str = "row", what: str = "") -> dict:
     """got/ref: dicts with q (codes [M,H]), scale, optional y, residual_out (bf16 bits)."""
-    boundary = ref["margin"] < BOUNDARY
+    boundary = _boundary_rows(ref, what)
     stats = {"rows": int(len(boundary)), "boundary_rows": int(boundary.sum())}
     ok_rows = ~boundary
     if "residual_out" in ref:
@@ -90,7 +100,7 @@ def compare_fp8(got: dict, ref: dict, scale_layout: str = "row", what: str = "")
 
 
 def compare_mx(got: dict, ref: dict, what: str = "") -> dict:
-    boundary = ref["margin"] < BOUNDARY
+    boundary = _boundary_rows(ref, what)
     stats = {"rows": int(len(boundary)), "boundary_rows": int(boundary.sum())}
     ok_rows = ~boundary
     if "residual_out" in ref:

@@ -189,3 +189,19 @@ def test_mxfp4_qknorm_halves_equal_single_calls(oracle_mod):
     for k in ("q", "scale", "y"):
         np.testing.assert_array_equal(both["q"][k], one[k])
     assert both["kv"]["q"].shape == (16, 256) and both["kv"]["scale"].shape == (16, 16)
+
+
+def test_margin_is_the_distance_to_the_fp32_rounding_boundary(oracle_mod, batch):
+    """The per-row margin (which decides the rows where parity may differ by
+    one bf16 step) equals the relative distance of numpy's fp64 inv_rms from
+    the nearest point where its fp32 rounding changes."""
+    r = oracle_mod.add_residual(batch["x"], batch["residual"])
+    _, inv, margin = oracle_mod.rmsnorm(r, batch["gamma"], 1e-6)
+    t = 1.0 / np.sqrt(np.mean(_f(r).astype(np.float64) ** 2, axis=1) + np.float64(np.float32(1e-6)))
+    f = t.astype(np.float32)
+    up = np.nextafter(f, np.float32(np.inf)).astype(np.float64)
+    dn = np.nextafter(f, np.float32(0)).astype(np.float64)
+    want = np.minimum(np.abs(t - (f + up) / 2), np.abs(t - (f + dn) / 2)) / t
+    # the oracle's S and numpy's mean differ in the last bits only
+    np.testing.assert_allclose(margin, want, rtol=0, atol=2.0 ** -50)
+    assert margin.max() < 2.0 ** -23 and np.median(margin) > 2.0 ** -30
