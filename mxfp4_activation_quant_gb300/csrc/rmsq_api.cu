@@ -195,6 +195,22 @@ Seg make_seg(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
     return s;
 }
 
+// Number of SMs of the current device (0 if the query fails).
+int sm_count()
+{
+    static int cached[128];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
+        return 0;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
 // Device address of the status word, looked up once per device.
 unsigned int *status_word_ptr(int dev)
 {
@@ -225,6 +241,11 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
             return fail(RMSQ_ERR_INVALID_ARG, "rows_per_block=%d too large for %d threads per row",
                         rpb, tpr);
         s.rpb = rpb;
+        // L2 prefetch about three resident blocks per SM ahead (measured on
+        // GB300: 300-600 rows ahead helps the MXFP4 row kernel by ~3 % and is
+        // neutral for FP8; twice as far hurts both); only for long batches.
+        const int64_t ahead = (int64_t)3 * sm_count() * rpb;
+        s.prefetch_rows = (ahead > 0 && s.M > 4 * ahead) ? ahead : 0;
         int64_t blocks = (s.M + rpb - 1) / rpb;
         if (blocks > 0x7fffffff)
             return fail(RMSQ_ERR_UNSUPPORTED, "M too large");

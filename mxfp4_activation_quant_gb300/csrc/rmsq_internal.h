@@ -28,6 +28,7 @@ struct Seg {
     int64_t scale_ld;      // FP8 column-major: leading dimension (>= M); MXFP4 tiled: k-tiles per row tile
     float eps;
     float inv_h;           // fp32 rounding of 1/H
+    int64_t prefetch_rows; // row kernel: rows ahead whose x / residual are prefetched into L2 (0 = off)
 };
 
 struct LaunchParams {

@@ -22,6 +22,21 @@ __device__ __forceinline__ void block_rows(const Seg &s, int b, RedSmem &red)
     const int64_t row = (int64_t)b * s.rpb + team;
     if (row >= s.M)
         return;                                   // whole teams leave together
+    if (s.prefetch_rows && t == 0) {
+        // Keep HBM busy while the resident blocks are in their reduction and
+        // quantise phases: pull the x / residual rows of a later block into L2
+        // with one 1-D bulk prefetch each.
+        const int64_t pr = row + s.prefetch_rows;
+        if (pr < s.M) {
+            const uint32_t bytes = (uint32_t)s.H * 2;
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s.x + pr * s.ldx_v), "r"(bytes)
+                         : "memory");
+            if (s.res)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s.res + pr * s.ldres_v),
+                             "r"(bytes)
+                             : "memory");
+        }
+    }
     row_from_global<VPT, TPR, MX>(s, row, t, team, 0, red);
 }
 
