@@ -175,14 +175,18 @@ typedef enum rmsq_kernel {
 } rmsq_kernel;
 
 /*
- * Optional launch control for the _ex entry points (NULL = defaults). Every
- * choice gives bit-identical outputs for the same vectors-per-thread value;
- * these exist for tests and tuning.
+ * Optional launch control for the _ex entry points (NULL = defaults). Kernels
+ * and rows-per-block choices with the same team shape give bit-identical
+ * outputs; different team shapes sum the squares in a different order and
+ * can differ only in rows whose inv_rms is within ~2^-44 of an fp32 rounding
+ * boundary. These exist for tests and tuning.
  *   kernel          rmsq_kernel
- *   vpt             16-byte vectors per thread: 0 = auto, else one of
- *                   1, 2, 3, 4, 6, 7, 8 (must divide H/8 so that the team size
- *                   H/(8*vpt) is a multiple of the group's vector count and
- *                   either divides 32 or is a multiple of 32, at most 512)
+ *   vpt             16-byte vectors (8 bf16) per thread, 1..8; 0 = auto. The
+ *                   team (threads per row) is the smallest size that holds
+ *                   H/8 vectors at vpt each and is either a power-of-two
+ *                   multiple of the group's vector count up to 32 or a
+ *                   multiple of 32, at most 512; vectors past the row end
+ *                   are idle (whole groups).
  *   rows_per_block  0 = auto
  *   grid            persistent kernel: number of blocks, 0 = auto
  *   debug_skip_row  persistent kernel: the copy of this row is never issued,
