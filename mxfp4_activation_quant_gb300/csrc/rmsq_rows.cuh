@@ -251,7 +251,7 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
             if (gd.fast) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    qv[j] = div_fast_neg2(unpack_bf16x2(yw[j] ^ 0x80008000u), gd);
+                    qv[j] = div_fast_neg2(unpack_neg_bf16x2(yw[j]), gd);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)

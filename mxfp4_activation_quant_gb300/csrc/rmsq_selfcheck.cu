@@ -22,13 +22,17 @@ __global__ void check_group_division_kernel(unsigned long long *counts)
         for (uint32_t sgn = 0; sgn < 2; ++sgn) {
             const float y = __uint_as_float((b | (sgn << 15)) << 16);
             const float ref = __fdiv_rn(y, d);
-            float got = ref;
+            float got = ref, got_hi = ref;
             if (g.fast) {
-                // the packed form the kernels use, on -y in both lanes
-                const float2 pair = div_fast_neg2(make_float2(-y, -y), g);
+                // the packed form the kernels use: y in both halves of a bf16
+                // pair, so both lanes' unpacking paths are exercised
+                const uint32_t w = b | (sgn << 15);
+                const float2 pair = div_fast_neg2(unpack_neg_bf16x2(w | (w << 16)), g);
                 got = pair.x;
+                got_hi = pair.y;
             }
-            code_bad += (e4m3x2(got, 0.0f) & 0xffu) != (e4m3x2(ref, 0.0f) & 0xffu);
+            code_bad += (e4m3x2(got, 0.0f) & 0xffu) != (e4m3x2(ref, 0.0f) & 0xffu) ||
+                        (e4m3x2(got_hi, 0.0f) & 0xffu) != (e4m3x2(ref, 0.0f) & 0xffu);
             const bool qb = __float_as_uint(got) != __float_as_uint(ref);
             quot_bad += qb;
             norm_bad += qb && fabsf(y) >= 0x1p-100f;
