@@ -217,20 +217,27 @@ def time_launches(fn, steps: int, stream) -> tuple[float, list[float]]:
 
 def time_graph(fn, steps: int, stream) -> float:
     """Total ms of `steps` calls captured into one CUDA graph and replayed (the
-    host-side cost of each call is paid once, at capture)."""
+    host-side cost of each call is paid once, at capture). `fn` must launch on
+    `stream`, a non-default stream: capture happens there."""
     import torch
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
+    with torch.cuda.graph(g, stream=stream):
         for _ in range(steps):
             fn()
-    g.replay()
-    torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    g.replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        g.replay()
+        torch.cuda.synchronize()
+        start.record(stream)
+        g.replay()
+        end.record(stream)
     torch.cuda.synchronize()
-    return start.elapsed_time(end)
+    ms = start.elapsed_time(end)
+    # a kernel node costs ~0.5 us of replay; far less per step means the calls
+    # launched outside the capture and the graph is empty
+    if not ms * 1e3 / steps > 0.1:
+        raise RuntimeError("the captured graph ran no work: the calls did not launch on the capture stream")
+    return ms
 
 
 def other_workloads(dev, stream) -> dict:
@@ -475,7 +482,10 @@ def run_ours(args) -> None:
     # small workloads are shorter than one host-side call: replay them from a graph
     use_graph = args.graph == "on" or (args.graph == "auto" and args.workload in ("decode", "qknorm"))
     if use_graph:
-        total_ms = time_graph(step, args.steps, stream)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        total_ms = time_graph(lambda: run(0, M, side.cuda_stream), args.steps, side)
+        stream.wait_stream(side)
         each_ms = [total_ms / args.steps]
     else:
         total_ms, each_ms = time_launches(step, args.steps, stream)

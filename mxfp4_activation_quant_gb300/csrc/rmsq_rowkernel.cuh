@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kMaxThreads) rows_kernel(const __grid_constant
 }
 
 template <int V0, int T0, int V1, int T1, bool MX>
-__global__ void __launch_bounds__(kMaxThreads) dual_kernel(const __grid_constant__ LaunchParams p)
+__global__ void __launch_bounds__(kMaxThreads, 2) dual_kernel(const __grid_constant__ LaunchParams p)
 {
     __shared__ RedSmem red;
     if ((int)blockIdx.x < p.seg[0].blocks)
