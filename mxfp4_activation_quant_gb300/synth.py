@@ -52,6 +52,7 @@ TENSOR_IDS = {
     "x": 1, "residual": 2, "gamma": 3, "outlier": 4,
     "q_a": 5, "kv_a": 6, "gamma_q": 7, "gamma_kv": 8,
     "chi1": 9, "chi2": 10, "chi3": 11,
+    "w_codes": 12, "w_scales": 13,
 }
 
 
@@ -133,6 +134,24 @@ def hidden_with_outliers_bf16(seed: int, shape, scale: float = 20.0) -> torch.Te
     v = normals(seed, "x", M * H).reshape(M, H)
     v[:, outlier_channels(seed, H)] *= scale
     return to_bf16(v, shape)
+
+
+def mxfp4_weights(seed: int, N: int, K: int, scale_lo: int = 118, scale_hi: int = 122):
+    """Synthetic MXFP4 weights of a linear layer [N, K]: packed codes
+    (uint8 [N, K/2], every nibble uniform over the 16 E2M1 codes: byte j of
+    the stream is word j // 8's byte j % 8) and E8M0 scale bytes (uint8
+    [N, K/32], uniform in [scale_lo, scale_hi), i.e. 2^-9 .. 2^-6 by default,
+    the size of trained weights' block scales). The values are drawn, not
+    quantised from anything: the GEMM consumes codes and scales as given."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    nb = N * K // 2
+    w = words(stream_key(seed, "w_codes"), 0, (nb + 7) // 8)
+    codes = w.astype("<u8").view(np.uint8)[:nb].reshape(N, K // 2).copy()
+    ns = N * K // 32
+    sw = words(stream_key(seed, "w_scales"), 0, ns)
+    scales = (scale_lo + (sw % np.uint64(scale_hi - scale_lo))).astype(np.uint8).reshape(N, K // 32)
+    return torch.from_numpy(codes), torch.from_numpy(scales)
 
 
 @dataclass

@@ -65,6 +65,8 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_group_quant_mxfp4.restype = ctypes.c_int
     L.oracle_mx_scale_tiles.argtypes = [_p, _i64, _i64, _p]
     L.oracle_mx_scale_tiles.restype = ctypes.c_int
+    L.oracle_mxfp4_gemm.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _p, _p, ctypes.c_int]
+    L.oracle_mxfp4_gemm.restype = ctypes.c_int
     return L
 
 
@@ -262,3 +264,37 @@ def qknorm_quant_mxfp4(q_a, kv_a, gamma_q, gamma_kv, eps: float = 1e-6,
     """Each latent normalised with its own gamma and MXFP4-quantised separately."""
     return {"q": add_rmsnorm_quant_mxfp4(q_a, None, gamma_q, eps, nthreads),
             "kv": add_rmsnorm_quant_mxfp4(kv_a, None, gamma_kv, eps, nthreads)}
+
+
+# ------------------------------------------------------- consumer GEMM
+
+def mxfp4_gemm(a_q, a_scale, b_q, b_scale, nthreads: int | None = None) -> dict:
+    """D = A B^T on MXFP4 operands: a_q [M, K/2], a_scale [M, K/32], b_q
+    [N, K/2], b_scale [N, K/32] (packed codes and row-major E8M0 bytes).
+    Returns {"d64": exact fp64 [M,N], "abs": sum |term| [M,N], "d": bf16 bits
+    [M,N] = bf16(f32(d64))}."""
+    a_q, a_scale = np.ascontiguousarray(a_q, np.uint8), np.ascontiguousarray(a_scale, np.uint8)
+    b_q, b_scale = np.ascontiguousarray(b_q, np.uint8), np.ascontiguousarray(b_scale, np.uint8)
+    M, K = a_q.shape[0], a_q.shape[1] * 2
+    N = b_q.shape[0]
+    if b_q.shape != (N, K // 2) or a_scale.shape != (M, K // 32) or b_scale.shape != (N, K // 32):
+        raise ValueError("operand shapes do not agree")
+    d64 = np.empty((M, N), dtype=np.float64)
+    mag = np.empty((M, N), dtype=np.float64)
+    d = np.empty((M, N), dtype=np.uint16)
+    rc = lib().oracle_mxfp4_gemm(a_q.ctypes.data, a_scale.ctypes.data, b_q.ctypes.data,
+                                 b_scale.ctypes.data, M, N, K, d64.ctypes.data, mag.ctypes.data,
+                                 d.ctypes.data, nthreads or default_threads())
+    if rc:
+        raise ValueError("oracle_mxfp4_gemm rejected its arguments")
+    return {"d64": d64, "abs": mag, "d": d}
+
+
+def a16wfp4_gemm(a_bf16, b_q, b_scale, nthreads: int | None = None) -> dict:
+    """The "prequant" placement: the bf16 activation is MXFP4-quantised (the
+    same group quant as step 3b) and then multiplied; returns mxfp4_gemm's
+    dict plus the activation codes and scales."""
+    q, s = group_quant_mxfp4(a_bf16, nthreads)
+    out = mxfp4_gemm(q, s, b_q, b_scale, nthreads)
+    out["a_q"], out["a_scale"] = q, s
+    return out

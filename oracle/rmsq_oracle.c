@@ -37,6 +37,9 @@
  *             -127, 127), scale byte = X + 127 (E8M0), elements
  *             e2m1_rne_sat(y_i * 2^-X), two per byte, even element in the low
  *             nibble (OCP Microscaling Formats v1.0, MXFP4).
+ *   4. consumer GEMM: D = A B^T on MXFP4 operands (activation A from 3b,
+ *             weights B), fp64 exact sum, fp32 accumulator reading, bf16
+ *             output; see the GEMM section below for its citation.
  *   qknorm:   steps 2 and 3a applied separately to the MLA q_a and kv_a
  *             latents with their own gammas and no residual (page "fused
  *             rmsnorm quant fp8 work", Modifications, "DeepseekV2AttentionMLA
@@ -446,6 +449,85 @@ int oracle_mx_scale_tiles(const uint8_t *s, int64_t M, int64_t G, uint8_t *out)
             int64_t r = m % 128, c = g % 4;
             out[tile * 512 + (r % 32) * 16 + (r / 32) * 4 + c] = s[m * G + g];
         }
+    return 0;
+}
+
+/* ------------------------------------- 4. consumer GEMM on MXFP4 data */
+
+/* The GEMM that consumes the quantised activations: the MLA / MoE
+ * projections of the DeepSeek models run as "A16W-FP4" GEMMs whose
+ * activation operand is quantised to MXFP4 either by the fused norm + quant
+ * kernel before the GEMM or in the GEMM itself ("prequant"; ATOM PR
+ * "Triton fusion/GEMM optimizations for DS FP4 and FP8": the required AITER
+ * PR list, "Triton A16WFP4 GEMM prequant", and the environment-variable
+ * notes that pick one placement or the other by concurrency).
+ *
+ * Both operands are MXFP4 along K (OCP Microscaling Formats v1.0: blocks of
+ * 32 E2M1 elements sharing one E8M0 scale 2^(byte - 127)); a [M, K/2] and
+ * b [N, K/2] are row-major packed codes (even element in the low nibble),
+ * sa [M, K/32] and sb [N, K/32] row-major scale bytes. The result is
+ *   D[m][n] = sum_k dec(a[m][k]) 2^(sa[m][k/32]-127) dec(b[n][k]) 2^(sb[n][k/32]-127),
+ * i.e. a times b transposed, both "K-major" as the weights of a linear layer
+ * are stored. Every term is exact in fp64 (E2M1 values have two significant
+ * bits); the sum is Neumaier-compensated, so d64 is the exact sum rounded
+ * once to fp64 unless the terms span more than ~100 binades. Reading adopted
+ * where the pages give no precision: an fp32 accumulator, so the bf16 output
+ * is bf16_rne(f32(d64)). abs64 receives sum_k |term| (the scale of the
+ * accumulation error any fp32 summation order can make). d64, abs64 and
+ * dbf16 may each be NULL. */
+typedef struct {
+    const uint8_t *a, *sa, *b, *sb;
+    int64_t N, K;
+    double *d64, *abs64;
+    uint16_t *dbf16;
+} gemm_ctx;
+
+static double mx_element(const uint8_t *q, const uint8_t *s, int64_t k)
+{
+    uint8_t byte = q[k / 2];
+    uint8_t code = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+    return ldexp((double)oracle_e2m1_decode(code), (int)s[k / 32] - 127);
+}
+
+static void gemm_rows(void *p, int64_t m0, int64_t m1)
+{
+    gemm_ctx *c = (gemm_ctx *)p;
+    const int64_t K = c->K;
+    for (int64_t m = m0; m < m1; ++m) {
+        const uint8_t *arow = c->a + m * (K / 2), *asc = c->sa + m * (K / 32);
+        for (int64_t n = 0; n < c->N; ++n) {
+            const uint8_t *brow = c->b + n * (K / 2), *bsc = c->sb + n * (K / 32);
+            double sum = 0.0, comp = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double term = mx_element(arow, asc, k) * mx_element(brow, bsc, k);
+                double t = sum + term;
+                if (fabs(sum) >= fabs(term))
+                    comp += (sum - t) + term;
+                else
+                    comp += (term - t) + sum;
+                sum = t;
+                mag += fabs(term);
+            }
+            double d = sum + comp;
+            int64_t o = m * c->N + n;
+            if (c->d64)
+                c->d64[o] = d;
+            if (c->abs64)
+                c->abs64[o] = mag;
+            if (c->dbf16)
+                c->dbf16[o] = f32_to_bf16_rne((float)d);
+        }
+    }
+}
+
+int oracle_mxfp4_gemm(const uint8_t *a, const uint8_t *sa, const uint8_t *b, const uint8_t *sb,
+                      int64_t M, int64_t N, int64_t K, double *d64, double *abs64, uint16_t *dbf16,
+                      int nthreads)
+{
+    if (!a || !sa || !b || !sb || M < 0 || N < 0 || K <= 0 || K % 32 != 0)
+        return -1;
+    gemm_ctx c = {a, sa, b, sb, N, K, d64, abs64, dbf16};
+    for_rows(gemm_rows, &c, M, nthreads);
     return 0;
 }
 

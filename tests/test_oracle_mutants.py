@@ -42,6 +42,14 @@ MUTANTS = {
     "mx_tiles_rows_transposed": ("out[tile * 512 + (r % 32) * 16 + (r / 32) * 4 + c]",
                                  "out[tile * 512 + (r / 32) * 16 + (r % 32) * 4 + c]"),
     "col_pad4_unpadded": ("c->scale[g * ((c->M + 3) / 4 * 4) + m] = scale;", "c->scale[g * c->M + m] = scale;"),
+    # swapping the nibble order of BOTH operands leaves every sum unchanged;
+    # a mismatch between the two is the mistake that matters
+    "gemm_a_nibbles_swapped": ("mx_element(arow, asc, k)", "mx_element(arow, asc, k ^ 1)"),
+    "gemm_scale_bias_128": ("(int)s[k / 32] - 127", "(int)s[k / 32] - 128"),
+    "gemm_b_scales_by_a_row": ("*bsc = c->sb + n * (K / 32)", "*bsc = c->sb + m * (K / 32)"),
+    "gemm_plain_running_sum": ("double d = sum + comp;", "double d = sum;"),
+    "gemm_output_truncated": ("c->dbf16[o] = f32_to_bf16_rne((float)d);",
+                              "c->dbf16[o] = (uint16_t)(*(uint32_t *)&(float){(float)d} >> 16);"),
     "zero_group_nan": ("float quot = (amax == 0.0f) ? v : v / scale;", "float quot = v / scale;"),
 }
 
@@ -69,6 +77,13 @@ def _pins(oracle_mod):
     from tests import test_oracle_layouts as lay
     yield "layout:mx_tiles", lambda: lay.test_mx_scale_tiles_hand_positions(oracle_mod)
     yield "layout:col_pad4", lambda: lay.test_fp8_padded_column_major(oracle_mod)
+    from tests import test_oracle_gemm as gemm
+    yield "gemm:hand", lambda: gemm.test_hand_worked_product(oracle_mod)
+    yield "gemm:one_hot", lambda: gemm.test_one_hot_weights_extract_the_activation(oracle_mod)
+    yield "gemm:transpose", lambda: gemm.test_swapping_operands_transposes(oracle_mod)
+    yield "gemm:numpy_fp64", lambda: gemm.test_exact_fp64_matrix_product(oracle_mod)
+    yield "gemm:scale_group", lambda: gemm.test_scale_byte_scales_its_group_only(oracle_mod)
+    yield "gemm:cancellation", lambda: gemm.test_cancellation_keeps_small_terms(oracle_mod)
 
 
 def _batch():

@@ -38,3 +38,16 @@ def test_workload_shapes_and_distributions():
     assert 1.3 < q["kv_a"].float().std().item() < 1.5
     t = synth.make_inputs(synth.WORKLOADS["mxfp4"], M=16)["x"].float()
     assert t.abs().max().item() > 8           # heavy tail
+
+
+def test_mxfp4_weights_are_seeded_and_in_range():
+    q1, s1 = synth.mxfp4_weights(7, 40, 256)
+    q2, s2 = synth.mxfp4_weights(7, 40, 256)
+    assert q1.shape == (40, 128) and s1.shape == (40, 8)
+    assert torch.equal(q1, q2) and torch.equal(s1, s2)
+    assert not torch.equal(q1, synth.mxfp4_weights(8, 40, 256)[0])
+    s = s1.numpy()
+    assert s.min() >= 118 and s.max() < 122
+    nib = np.concatenate([(q1.numpy() & 0xF).ravel(), (q1.numpy() >> 4).ravel()])
+    counts = np.bincount(nib, minlength=16)
+    assert counts.min() > 0.7 * nib.size / 16 and counts.max() < 1.3 * nib.size / 16
