@@ -149,6 +149,67 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_mma_scales(
     float eps, int64_t M, int64_t H, uint8_t *out_q, uint8_t *out_scale_tiles, void *out_residual,
     void *out_bf16, void *stream);
 
+/*
+ * Residual add + RMSNorm alone: r and y as above, no quantisation. This is
+ * the norm of the unfused placement in which the quant moves into the
+ * consumer GEMM (ATOM PR "Triton fusion/GEMM optimizations for DS FP4 and
+ * FP8": "AR_RMS + Quant_GEMM" at concurrency 4, with the "Triton A16WFP4
+ * GEMM prequant" kernel); y goes to rmsq_a16wfp4_gemm. out_bf16 is required;
+ * H must be a multiple of 32. Same conventions and checks as the fused calls.
+ */
+rmsq_status rmsq_add_rmsnorm(
+    const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
+    float eps, int64_t M, int64_t H, void *out_residual, void *out_bf16, void *stream);
+
+/* ------------------------------------------------------- consumer GEMM */
+
+/*
+ * The GEMM that consumes the quantised activation, on the block-scaled
+ * tensor cores (tcgen05.mma kind::mxf4), in the two placements the ATOM PR
+ * "Triton fusion/GEMM optimizations for DS FP4 and FP8" chooses between by
+ * concurrency (its environment-variable notes and the AITER PR list:
+ * "Triton A16WFP4 GEMM prequant"):
+ *
+ *   D[M, N] = A[M, K] * B[N, K]^T,   D bf16 (fp32 accumulation, rounded to
+ *                                    nearest even once), row-major, ld_d
+ *
+ * A and B are MXFP4 along K: E2M1 codes two per byte (element 2k in the low
+ * nibble; [rows, K/2] row-major with a leading dimension in BYTES) and one
+ * E8M0 scale per 32 elements, given in the MMA tile layout of
+ * rmsq_add_rmsnorm_quant_mxfp4_mma_scales (ceil(rows/128) * K/128 tiles of
+ * 512 bytes; rmsq_mx_scale_tiles converts a row-major scale matrix). B is
+ * the weight of a linear layer, [out_features, in_features].
+ *
+ * rmsq_mxfp4_gemm takes A quantised (the fused norm + quant placement);
+ * rmsq_a16wfp4_gemm takes A in bf16 ([M, K], ld_a in elements) and
+ * quantises it inside the GEMM with exactly the rule of
+ * rmsq_add_rmsnorm_quant_mxfp4 (the prequant placement), so both give
+ * bit-identical D for the same activation.
+ *
+ * Requirements (checked on the host; nothing is launched on failure):
+ * K a positive multiple of 256 and N a multiple of 8 (RMSQ_ERR_UNSUPPORTED
+ * otherwise); 16-byte aligned a_q / a / b_q / scale tiles / d; ld_a, ld_b
+ * multiples of 16 bytes (bf16 ld_a: multiple of 8 elements) and at least a
+ * row; ld_d a multiple of 8 elements, >= N; d must not overlap an input.
+ * M == 0 or N == 0 returns RMSQ_OK. Tiles of D with rows >= M or columns >=
+ * N are not written.
+ */
+rmsq_status rmsq_mxfp4_gemm(
+    const void *a_q, int64_t ld_a, const void *a_scale_tiles, const void *b_q, int64_t ld_b,
+    const void *b_scale_tiles, void *d, int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream);
+
+rmsq_status rmsq_a16wfp4_gemm(
+    const void *a, int64_t ld_a, const void *b_q, int64_t ld_b, const void *b_scale_tiles, void *d,
+    int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * Row-major [R, G] E8M0 scale bytes (leading dimension ld) -> the MMA tile
+ * layout above: out receives ceil(R/128) * ceil(G/4) * 512 bytes, padding
+ * (rows >= R, groups >= G) set to `fill`. For preparing weight scales.
+ */
+rmsq_status rmsq_mx_scale_tiles(const uint8_t *scale, int64_t ld, int64_t R, int64_t G, uint8_t *out,
+                                uint8_t fill, void *stream);
+
 /* ------------------------------------------------------------ utilities */
 
 /* Static description of a status code. */
@@ -212,6 +273,28 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
     const void *x, int64_t ld_x, const void *residual, int64_t ld_res, const void *gamma,
     float eps, int64_t M, int64_t H, uint8_t *out_q, uint8_t *out_scale, void *out_residual,
     void *out_bf16, void *stream, const rmsq_launch_opts *opts);
+
+/*
+ * Optional control of the GEMM launch (NULL = defaults), for tests and
+ * tuning; results do not depend on it.
+ *   bn             rows of B per CTA tile: 64, 128 or 256; 0 = auto (the
+ *                  largest that still gives at least one tile per SM)
+ *   wait_limit_ns  limit of every wait inside the kernel, 0 = 2 s
+ */
+typedef struct rmsq_gemm_opts {
+    int32_t bn;
+    int32_t reserved;
+    int64_t wait_limit_ns;
+} rmsq_gemm_opts;
+
+rmsq_status rmsq_mxfp4_gemm_ex(
+    const void *a_q, int64_t ld_a, const void *a_scale_tiles, const void *b_q, int64_t ld_b,
+    const void *b_scale_tiles, void *d, int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream,
+    const rmsq_gemm_opts *opts);
+
+rmsq_status rmsq_a16wfp4_gemm_ex(
+    const void *a, int64_t ld_a, const void *b_q, int64_t ld_b, const void *b_scale_tiles, void *d,
+    int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream, const rmsq_gemm_opts *opts);
 
 /*
  * The device encoders the kernels use, applied elementwise to n fp32 values

@@ -1,0 +1,584 @@
+// Block-scaled MXFP4 GEMM on the 5th-generation tensor cores (tcgen05): the
+// consumer of the fused norm + MXFP4 quant,
+//     D[M, N] (bf16) = A[M, K] B[N, K]^T,
+// A and B in MXFP4 along K (E2M1 codes two per byte, one E8M0 scale per 32
+// elements; OCP Microscaling Formats v1.0). It serves the comparison of the
+// two places the activation quant can sit (ATOM PR "Triton fusion/GEMM
+// optimizations for DS FP4 and FP8": fused RMSNorm + quant ahead of the GEMM
+// above concurrency 4, the quant inside an A16W-FP4 GEMM, "prequant", at
+// concurrency 4):
+//   * A already quantised -- codes [M, K/2] and scales in the MMA tile layout,
+//     as rmsq_add_rmsnorm_quant_mxfp4_mma_scales writes them -- loaded by TMA;
+//   * A in bf16 (prequant): four warps quantise every 128 x 256 stage of A into
+//     shared memory with the fused kernel's own group-32 rule.
+//
+// One CTA computes a 128 x BN tile (BN = 64, 128 or 256): the MMA's M = 128
+// rows of A, N = BN rows of B. K advances in stages of 256 elements = 128
+// bytes per row, one 128-byte swizzle span, i.e. four MMAs of K = 64.
+// Warp roles (256 threads): warp 0 lane 0 issues the TMA and bulk loads;
+// warp 1 owns the tensor memory and its lane 0 issues tcgen05.cp (scale
+// factors, shared -> tensor memory) and tcgen05.mma; warps 4-7 quantise A
+// (prequant) and then run the epilogue (tcgen05.ld -> bf16 -> global).
+// Every mbarrier wait is bounded; a wait that runs out sets the status word,
+// makes the other roles stop, drains what is in flight and frees the tensor
+// memory before the CTA exits.
+//
+// Layouts (measured on GB300 with a self-checking probe before this kernel
+// was written, and pinned by the parity tests):
+//   * operands in shared memory: K-major rows of 128 bytes, 8-row / 1024-byte
+//     atoms with the 128-byte swizzle (16-byte chunk c of row r stored at
+//     chunk c ^ (r % 8)); the descriptor's start address moves 32 bytes per
+//     MMA (K = 64 E2M1 elements), stride between 8-row groups 1024 bytes;
+//   * scale factors in tensor memory, per 128-element K chunk: A in 4
+//     columns, B in 4 columns per 128 rows of B. Row m of A reads lane m,
+//     column m / 32, bytes sf_id and sf_id + 1 (its two 32-element groups of
+//     the MMA's K = 64); row n of B reads lane n % 32, column n / 32. That is
+//     the 512-byte tile of 128 rows x 4 groups at (r % 32) * 16 + (r / 32) * 4
+//     + g copied by tcgen05.cp .32x128b.warpx4 (rows r % 32 -> lanes, the
+//     same data in all four lane quarters).
+#include <cuda.h>
+#include <cstdio>
+
+#include "rmsq.h"
+#include "rmsq_device.cuh"
+#include "rmsq_internal.h"
+
+namespace rmsq {
+namespace {
+
+constexpr int kBM = 128;          // MMA M: rows of A per tile
+constexpr int kStageBytes = 128;  // bytes of one operand row per stage (256 E2M1)
+constexpr int kStageK = 256;      // K elements per stage
+constexpr int kGemmThreads = 256;
+
+constexpr int pow2_at_least(int v)
+{
+    int p = 32;
+    while (p < v)
+        p <<= 1;
+    return p;
+}
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int kABytes = kBM * kStageBytes;
+    static constexpr int kBBytes = BN * kStageBytes;
+    static constexpr int kSfbAtoms = BN >= 128 ? BN / 128 : 1;   // 128-row scale tiles of B per stage chunk
+    static constexpr int kSfaBytes = 2 * 512;                    // two 128-element K chunks
+    static constexpr int kSfbBytes = kSfbAtoms * 2 * 512;
+    static constexpr int kSfCols = 8 + 8 * kSfbAtoms;            // scale-factor TMEM columns per stage
+    static constexpr int kTmemCols = pow2_at_least(BN + kStages * kSfCols);
+    static constexpr int kOffB = kABytes;
+    static constexpr int kAB = kABytes + kBBytes;
+    static constexpr int kOffSfa = kStages * kAB;
+    static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
+    static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
+    static constexpr int kBarBytes = (2 * kStages + 2) * 8 + 16;
+    static constexpr size_t kSmem = 1024 + kOffBar + kBarBytes;
+    static_assert(kTmemCols <= 512, "tensor memory");
+    static_assert(kSmem <= 232448, "shared memory");
+};
+
+struct GemmParams {
+    const uint8_t *a_scale;     // MMA tile layout, ceil(M/128) x K/128 tiles of 512 bytes
+    const uint8_t *b_scale;     // same for B
+    const uint4 *a_bf16;        // prequant: bf16 rows, 16-byte vectors
+    int64_t lda_v;              // prequant: leading dimension in vectors
+    uint16_t *d;                // bf16 [M, ldd]
+    int64_t ldd;
+    int64_t M, N;
+    int32_t k_stages;           // K / 256
+    int32_t b_row_tiles;        // ceil(N / 128): 128-row scale tiles that exist for B
+    int64_t wait_limit_ns;
+    unsigned int *status;
+};
+
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t gtimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity. Returns false
+// (after raising the CTA's abort flag and the status word) if it ran out, or
+// if another role of the CTA already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          const GemmParams &p)
+{
+    if (mbar_test(bar, parity))
+        return true;
+    const uint64_t t0 = gtimer();
+    for (;;) {
+        if (mbar_test(bar, parity))
+            return true;
+        if (*abort)
+            return false;
+        if (gtimer() - t0 > (uint64_t)p.wait_limit_ns) {
+            *abort = 1;
+            atomicOr(p.status, 2u);
+            return false;
+        }
+    }
+}
+
+// The same wait taken by lane 0 for the whole warp (warp-uniform result, so
+// that the .sync.aligned tensor-memory instructions after it see all lanes).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          const GemmParams &p)
+{
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0)
+        ok = mbar_wait(bar, parity, abort, p) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Descriptor of a 32-row x 16-byte scale tile (no swizzle, 8-row core
+// matrices 128 bytes apart) for tcgen05.cp.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor of kind::mxf4 (E2M1 x E2M1, UE8M0 scales, fp32
+// accumulator, both operands K-major, M = 128).
+__host__ __device__ constexpr uint32_t idesc_mxf4(int n, int sf_id)
+{
+    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(kBM >> 4) << 24) |
+           ((uint32_t)sf_id << 29) | ((uint32_t)sf_id << 4);
+}
+
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void cp_sf(uint32_t taddr, uint64_t desc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 32 columns of fp32 from tensor memory.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------- prequant (A in bf16)
+
+// One group of 32 bf16 values -> 16 bytes of E2M1 codes and the E8M0 byte,
+// with the fused kernel's arithmetic: X from the group's largest magnitude,
+// elements times 2^-X (exact), saturating round-to-nearest-even E2M1.
+__device__ __forceinline__ uint4 quant_group32(const uint4 (&v)[4], uint32_t &scale_byte)
+{
+    const uint32_t am = max(max(amax_bits_bf16x8(v[0]), amax_bits_bf16x8(v[1])),
+                            max(amax_bits_bf16x8(v[2]), amax_bits_bf16x8(v[3])));
+    const int X = mx_exponent_from_bits(am);
+    scale_byte = (uint32_t)(X + 127);
+    const float2 mult = f2(__uint_as_float((uint32_t)(127 - X) << 23));   // 2^-X
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = e2m1x8(mul2(unpack_bf16x2(v[i].x), mult), mul2(unpack_bf16x2(v[i].y), mult),
+                      mul2(unpack_bf16x2(v[i].z), mult), mul2(unpack_bf16x2(v[i].w), mult));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Quantise this thread's row (r = 0..127) of one stage: 256 bf16 values from
+// global memory -> 128 swizzled code bytes in sA and 8 scale bytes in the two
+// 512-byte scale tiles at sSfa.
+__device__ __forceinline__ void prequant_row(const GemmParams &p, int64_t m, int r, int stage_k,
+                                             uint8_t *sA, uint8_t *sSfa)
+{
+    const uint4 *src = p.a_bf16 + m * p.lda_v + (int64_t)stage_k * (kStageK / 8);
+    uint32_t sc[8];
+    uint4 cur[4], nxt[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        cur[i] = __ldg(src + i);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        if (g + 1 < 8) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                nxt[i] = __ldg(src + (g + 1) * 4 + i);
+        }
+        const uint4 codes = quant_group32(cur, sc[g]);
+        // group g is 16-byte chunk g of the row, swizzled within its 8-row atom
+        *reinterpret_cast<uint4 *>(sA + r * kStageBytes + ((g ^ (r & 7)) << 4)) = codes;
+        if (g + 1 < 8) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                cur[i] = nxt[i];
+        }
+    }
+    // scale tile j holds groups 4j..4j+3 of row r at (r % 32) * 16 + (r / 32) * 4
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        *reinterpret_cast<uint32_t *>(sSfa + j * 512 + (r & 31) * 16 + (r >> 5) * 4) =
+            sc[4 * j] | (sc[4 * j + 1] << 8) | (sc[4 * j + 2] << 16) | (sc[4 * j + 3] << 24);
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int BN, bool PREQUANT>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    mxfp4_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
+                      const __grid_constant__ CUtensorMap map_b)
+{
+    using C = GemmCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = (uint64_t *)(smem + C::kOffBar);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *accum = empty + C::kStages;
+    uint64_t *drain = accum + 1;
+    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
+    volatile int *abort = (volatile int *)(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tile = blockIdx.x, m_tile = blockIdx.y;
+    const int64_t m0 = (int64_t)m_tile * kBM, n0 = (int64_t)n_tile * BN;
+    const int KS = p.k_stages;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(full + s)),
+                         "r"(PREQUANT ? 1 + 128 : 1));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(empty + s)));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(accum)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(drain)));
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                     "r"(C::kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_sf = tmem + BN;   // scale-factor columns follow the accumulator
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- loads
+        if (lane == 0) {
+            const uint32_t b_tx = C::kBBytes;
+            const int bt0 = (int)(n0 >> 7);                       // first 128-row scale tile of B
+            int issued = 0;
+            for (int ks = 0; ks < KS; ++ks) {
+                const int s = ks % C::kStages;
+                const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
+                if (!mbar_wait(saddr(empty + s), ph ^ 1u, abort, p))
+                    break;
+                int atoms = 0;
+                for (int t = 0; t < C::kSfbAtoms; ++t)
+                    atoms += (bt0 + t < p.b_row_tiles);
+                const uint32_t tx = b_tx + atoms * 1024u + (PREQUANT ? 0u : (uint32_t)(C::kABytes + C::kSfaBytes));
+                const uint32_t fb = saddr(full + s);
+                mbar_arrive_tx(fb, tx);
+                uint8_t *stage = smem + s * C::kAB;
+                if (!PREQUANT) {
+                    tma_2d(saddr(stage), &map_a, ks * kStageBytes, (int)m0, fb);
+                    bulk_g2s(saddr(smem + C::kOffSfa + s * C::kSfaBytes),
+                             p.a_scale + ((int64_t)m_tile * (2 * KS) + 2 * ks) * 512, 1024, fb);
+                }
+                tma_2d(saddr(stage + C::kOffB), &map_b, ks * kStageBytes, (int)n0, fb);
+                for (int t = 0; t < C::kSfbAtoms; ++t)
+                    if (bt0 + t < p.b_row_tiles)
+                        bulk_g2s(saddr(smem + C::kOffSfb + s * C::kSfbBytes + t * 1024),
+                                 p.b_scale + ((int64_t)(bt0 + t) * (2 * KS) + 2 * ks) * 512, 1024, fb);
+                issued = ks + 1;
+            }
+            if (*abort) {
+                // let the copies already issued land before the CTA goes away
+                // (one deadline for all of them)
+                const uint64_t t0 = gtimer();
+                for (int ks = (issued > C::kStages ? issued - C::kStages : 0); ks < issued; ++ks) {
+                    const uint32_t fb = saddr(full + ks % C::kStages);
+                    const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
+                    while (!mbar_test(fb, ph) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            // a 64-row B tile sits in the lower or upper half of its 128-row scale tile
+            const uint32_t sfb_row_col = (BN == 64) ? (uint32_t)(((n0 >> 6) & 1) * 2) : 0u;
+            bool any = false;
+            for (int ks = 0; ks < KS; ++ks) {
+                const int s = ks % C::kStages;
+                const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
+                if (!mbar_wait(saddr(full + s), ph, abort, p))
+                    break;
+                tc_fence_after();
+                const uint32_t sfa_col = tmem_sf + s * C::kSfCols;
+                const uint32_t sfb_col = sfa_col + 8;
+                const uint32_t sfa_smem = saddr(smem + C::kOffSfa + s * C::kSfaBytes);
+                const uint32_t sfb_smem = saddr(smem + C::kOffSfb + s * C::kSfbBytes);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    cp_sf(sfa_col + 4 * j, desc_sf(sfa_smem + j * 512));
+#pragma unroll
+                    for (int t = 0; t < C::kSfbAtoms; ++t)
+                        cp_sf(sfb_col + 4 * C::kSfbAtoms * j + 4 * t, desc_sf(sfb_smem + t * 1024 + j * 512));
+                }
+                const uint32_t a_smem = saddr(smem + s * C::kAB), b_smem = a_smem + C::kOffB;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int j = k >> 1;
+                    mma_mxf4(tmem, desc_sw128(a_smem + 32 * k), desc_sw128(b_smem + 32 * k),
+                             idesc_mxf4(BN, (k & 1) * 2), sfa_col + 4 * j,
+                             sfb_col + 4 * C::kSfbAtoms * j + sfb_row_col, (ks | k) != 0);
+                }
+                mma_commit(saddr(empty + s));
+                any = true;
+            }
+            if (!*abort) {
+                mma_commit(saddr(accum));
+            } else if (any) {
+                // drain the tensor core before the tensor memory is freed
+                mma_commit(saddr(drain));
+                const uint64_t t0 = gtimer();
+                while (!mbar_test(saddr(drain), 0) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        const int q = warp - 4;              // lane quarter of tensor memory this warp may access
+        const int r = q * 32 + lane;         // row of the tile
+        const int64_t m = m0 + r;
+        if (PREQUANT) {
+            // ------------------------------------------- quantise A stages
+            for (int ks = 0; ks < KS; ++ks) {
+                const int s = ks % C::kStages;
+                const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
+                if (!warp_wait(saddr(empty + s), ph ^ 1u, abort, p))
+                    break;
+                if (m < p.M)
+                    prequant_row(p, m, r, ks, smem + s * C::kAB, smem + C::kOffSfa + s * C::kSfaBytes);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(saddr(full + s));
+            }
+        }
+        // ------------------------------------------------------- epilogue
+        if (warp_wait(saddr(accum), 0, abort, p)) {
+            tc_fence_after();
+            const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+            uint16_t *drow = p.d + m * p.ldd + n0;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t acc[32];
+                tmem_ld32(trow + c0, acc);
+                if (m < p.M) {
+                    const int64_t valid = p.N - (n0 + c0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        if (valid >= 8 * (v + 1)) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(acc[8 * v + 0]), __uint_as_float(acc[8 * v + 1]));
+                            o.y = pack_bf16x2(__uint_as_float(acc[8 * v + 2]), __uint_as_float(acc[8 * v + 3]));
+                            o.z = pack_bf16x2(__uint_as_float(acc[8 * v + 4]), __uint_as_float(acc[8 * v + 5]));
+                            o.w = pack_bf16x2(__uint_as_float(acc[8 * v + 6]), __uint_as_float(acc[8 * v + 7]));
+                            *reinterpret_cast<uint4 *>(drow + c0 + 8 * v) = o;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
+    }
+}
+
+// ----------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)f;
+    }
+    return fn;
+}
+
+// 2-D map over `rows` rows of `row_bytes` code bytes (leading dimension
+// `ld` bytes), boxes of 128 bytes x box_rows rows, 128-byte swizzle; rows
+// past the end read as zero codes.
+bool make_code_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row_bytes, int64_t ld, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld};
+    cuuint32_t box[2] = {(cuuint32_t)kStageBytes, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool PRE>
+cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int m_tiles,
+                          int n_tiles, cudaStream_t st)
+{
+    using C = GemmCfg<BN>;
+    static bool attr[128];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 128)
+        return cudaErrorInvalidDevice;
+    if (!attr[dev]) {
+        e = cudaFuncSetAttribute(mxfp4_gemm_kernel<BN, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::kSmem);
+        if (e != cudaSuccess)
+            return e;
+        attr[dev] = true;
+    }
+    mxfp4_gemm_kernel<BN, PRE><<<dim3(n_tiles, m_tiles), kGemmThreads, C::kSmem, st>>>(p, ma, mb);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
+{
+    GemmParams p{};
+    p.a_scale = (const uint8_t *)g.a_scale;
+    p.b_scale = (const uint8_t *)g.b_scale;
+    p.a_bf16 = (const uint4 *)g.a_bf16;
+    p.lda_v = g.a_bf16 ? g.lda / 8 : 0;
+    p.d = (uint16_t *)g.d;
+    p.ldd = g.ldd;
+    p.M = g.M;
+    p.N = g.N;
+    p.k_stages = (int32_t)(g.K / kStageK);
+    p.b_row_tiles = (int32_t)((g.N + 127) / 128);
+    p.wait_limit_ns = g.wait_limit_ns;
+    p.status = g.status;
+    CUtensorMap ma, mb;
+    if (!make_code_map(&mb, g.b_q, g.N, g.K / 2, g.ldb, g.bn))
+        return cudaErrorInvalidValue;
+    if (g.a_bf16) {
+        ma = mb;   // unused by the prequant kernel
+    } else if (!make_code_map(&ma, g.a_q, g.M, g.K / 2, g.lda, kBM)) {
+        return cudaErrorInvalidValue;
+    }
+    const int m_tiles = (int)((g.M + kBM - 1) / kBM), n_tiles = (int)((g.N + g.bn - 1) / g.bn);
+    const bool pre = g.a_bf16 != nullptr;
+    switch (g.bn) {
+    case 64: return pre ? launch_gemm_t<64, true>(p, ma, mb, m_tiles, n_tiles, st)
+                        : launch_gemm_t<64, false>(p, ma, mb, m_tiles, n_tiles, st);
+    case 128: return pre ? launch_gemm_t<128, true>(p, ma, mb, m_tiles, n_tiles, st)
+                         : launch_gemm_t<128, false>(p, ma, mb, m_tiles, n_tiles, st);
+    case 256: return pre ? launch_gemm_t<256, true>(p, ma, mb, m_tiles, n_tiles, st)
+                         : launch_gemm_t<256, false>(p, ma, mb, m_tiles, n_tiles, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+bool tensor_map_encoder_available() { return encode_fn() != nullptr; }
+
+}  // namespace rmsq

@@ -45,6 +45,25 @@ struct BulkParams {
     unsigned int *status;     // device status word (set on a timed-out wait)
 };
 
+// One MXFP4 GEMM launch: D[M, N] bf16 = A B^T (see rmsq_gemm.cu). A is
+// either MXFP4 codes + tiled scales (a_q, a_scale; lda in bytes) or bf16
+// (a_bf16; lda in elements, quantised in the kernel's prologue).
+struct GemmLaunch {
+    const void *a_q, *a_scale, *a_bf16;
+    int64_t lda;
+    const void *b_q, *b_scale;
+    int64_t ldb;               // bytes
+    void *d;
+    int64_t ldd;               // elements
+    int64_t M, N, K;
+    int bn;                    // 64, 128 or 256
+    int64_t wait_limit_ns;
+    unsigned int *status;
+};
+
+cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st);
+bool tensor_map_encoder_available();
+
 constexpr int kMaxThreads = 512;
 
 // Launchers (a switch over the instantiations each). tpr_static != 0 selects

@@ -51,18 +51,6 @@ __device__ __forceinline__ void team_bar(int team, int tpr)
     asm volatile("bar.sync %0, %1;" ::"r"(team + 1), "r"(tpr) : "memory");
 }
 
-// bf16 magnitude bits -> the MX shared exponent X (unbiased), clamped to
-// [-127, 127]; zero gives -127. floor(log2) is read from the exponent field,
-// or from the leading mantissa bit for bf16 subnormals (m * 2^-133).
-__device__ __forceinline__ int mx_exponent_from_bits(uint32_t a)
-{
-    if (a == 0)
-        return -127;
-    int E = (int)(a >> 7);
-    int fl = E ? E - 127 : (31 - __clz((int)(a & 0x7fu))) - 133;
-    return min(127, max(-127, fl - 2));
-}
-
 // Byte offset of the E8M0 scale of (row, group g) in the scale-factor layout
 // that Blackwell's block-scaled MMA reads: 128-row x 4-group tiles of 512
 // bytes, tiles ordered row-tile major with `ktiles` tiles per row tile; inside
@@ -212,6 +200,8 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
             if (!GUARD || k * tpr + t < nvec)
                 yrow[k * tpr] = y[k];
     }
+    if (!s.out_q)   // norm only (rmsq_add_rmsnorm)
+        return;
 
     // ---- group amax over GV lanes (two vectors packed per shuffle)
     uint32_t am[VPT];

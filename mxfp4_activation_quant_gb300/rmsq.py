@@ -42,6 +42,14 @@ class LaunchOpts(ctypes.Structure):
         super().__init__(kernel, vpt, rows_per_block, grid, debug_skip_row, wait_limit_ns)
 
 
+class GemmOpts(ctypes.Structure):
+    """Mirror of ``rmsq_gemm_opts``."""
+    _fields_ = [("bn", _i32), ("reserved", _i32), ("wait_limit_ns", _i64)]
+
+    def __init__(self, bn=0, wait_limit_ns=0):
+        super().__init__(bn, 0, wait_limit_ns)
+
+
 class RmsqError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
@@ -58,6 +66,12 @@ _SIGNATURES = {
     "rmsq_add_rmsnorm_quant_mxfp4_ex": [_p, _i64, _p, _i64, _p, _f, _i64, _i64, _p, _p, _p, _p, _p, _p],
     "rmsq_qknorm_quant_mxfp4": [_p, _i64, _p, _i64, _p, _p, _f, _i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p],
     "rmsq_add_rmsnorm_quant_mxfp4_mma_scales": [_p, _i64, _p, _i64, _p, _f, _i64, _i64, _p, _p, _p, _p, _p],
+    "rmsq_add_rmsnorm": [_p, _i64, _p, _i64, _p, _f, _i64, _i64, _p, _p, _p],
+    "rmsq_mxfp4_gemm": [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
+    "rmsq_mxfp4_gemm_ex": [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _p],
+    "rmsq_a16wfp4_gemm": [_p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
+    "rmsq_a16wfp4_gemm_ex": [_p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _p],
+    "rmsq_mx_scale_tiles": [_p, _i64, _i64, _i64, _p, ctypes.c_uint8, _p],
     "rmsq_sync_status": [_p],
     "rmsq_encode_e4m3": [_p, _p, _i64, _p],
     "rmsq_encode_e2m1": [_p, _p, _i64, _p],
@@ -305,6 +319,91 @@ def add_rmsnorm_quant_mxfp4_mma_scales(x: torch.Tensor, gamma: torch.Tensor,
                                                          M, H, _ptr(q), _ptr(scale), _ptr(res_out), _ptr(y),
                                                          _stream(dev)))
     return ((y, q, scale) if keep_bf16 else (q, scale)), res_out
+
+
+def add_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, residual: torch.Tensor | None = None,
+                eps: float = 1e-6, out: torch.Tensor | None = None, out_residual: torch.Tensor | None = None,
+                stream: int | None = None):
+    """Residual add + RMSNorm without quantisation: returns ``(y, residual_out)``
+    (``residual_out`` None without a residual). H must be a multiple of 32."""
+    ldx = _rows_view(x, "x")
+    M, H = x.shape
+    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    dev = x.device
+    y = out if out is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    res_out = None
+    if residual is not None:
+        res_out = out_residual if out_residual is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    st = _stream(dev) if stream is None else stream
+    _check(lib().rmsq_add_rmsnorm(_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H, _ptr(res_out),
+                                  _ptr(y), st))
+    return y, res_out
+
+
+def mx_scale_tiles(scale: torch.Tensor, fill: int = 0, stream: int | None = None) -> torch.Tensor:
+    """Row-major [R, G] E8M0 bytes (uint8 CUDA) -> the block-scaled MMA tile
+    layout (flat uint8, ceil(R/128) * ceil(G/4) * 512 bytes, padding = fill)."""
+    if not scale.is_cuda or scale.dtype != torch.uint8 or scale.dim() != 2 or scale.stride(1) != 1:
+        raise ValueError("scale must be a 2-D uint8 CUDA tensor with contiguous rows")
+    R, G = scale.shape
+    out = torch.empty((R + 127) // 128 * ((G + 3) // 4) * 512, dtype=torch.uint8, device=scale.device)
+    st = _stream(scale.device) if stream is None else stream
+    _check(lib().rmsq_mx_scale_tiles(_ptr(scale), scale.stride(0), R, G, _ptr(out), fill, st))
+    return out
+
+
+def _codes_view(t: torch.Tensor, name: str) -> int:
+    if not t.is_cuda or t.dtype != torch.uint8 or t.dim() != 2 or (t.stride(1) != 1 and t.shape[1] > 1):
+        raise ValueError(f"{name} must be a 2-D uint8 CUDA tensor with contiguous rows")
+    return t.stride(0)
+
+
+def _gemm_out(M, N, dev, out):
+    if out is None:
+        return torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if out.dtype != torch.bfloat16 or out.dim() != 2 or out.shape[0] != M or out.shape[1] != N or out.stride(1) != 1:
+        raise ValueError("out must be a [M, N] bf16 tensor with contiguous rows")
+    return out
+
+
+def mxfp4_gemm(a_q: torch.Tensor, a_scale_tiles: torch.Tensor, b_q: torch.Tensor, b_scale_tiles: torch.Tensor,
+               out: torch.Tensor | None = None, opts: GemmOpts | None = None, stream: int | None = None):
+    """D = A B^T (bf16 [M, N]) on the block-scaled tensor cores, A and B MXFP4:
+    codes [rows, K/2] uint8, scales in the MMA tile layout (flat uint8)."""
+    lda, ldb = _codes_view(a_q, "a_q"), _codes_view(b_q, "b_q")
+    M, K = a_q.shape[0], a_q.shape[1] * 2
+    N = b_q.shape[0]
+    if b_q.shape[1] * 2 != K:
+        raise ValueError("A and B have different K")
+    d = _gemm_out(M, N, a_q.device, out)
+    st = _stream(a_q.device) if stream is None else stream
+    args = (_ptr(a_q), lda, _ptr(a_scale_tiles), _ptr(b_q), ldb, _ptr(b_scale_tiles), _ptr(d), d.stride(0),
+            M, N, K, st)
+    if opts is None:
+        _check(lib().rmsq_mxfp4_gemm(*args))
+    else:
+        _check(lib().rmsq_mxfp4_gemm_ex(*args, ctypes.byref(opts)))
+    return d
+
+
+def a16wfp4_gemm(a: torch.Tensor, b_q: torch.Tensor, b_scale_tiles: torch.Tensor,
+                 out: torch.Tensor | None = None, opts: GemmOpts | None = None, stream: int | None = None):
+    """The prequant placement: A bf16 [M, K] is MXFP4-quantised inside the
+    GEMM (same rule as add_rmsnorm_quant_mxfp4), then D = A B^T (bf16 [M, N])."""
+    lda = _rows_view(a, "a")
+    ldb = _codes_view(b_q, "b_q")
+    M, K = a.shape
+    N = b_q.shape[0]
+    if b_q.shape[1] * 2 != K:
+        raise ValueError("A and B have different K")
+    d = _gemm_out(M, N, a.device, out)
+    st = _stream(a.device) if stream is None else stream
+    args = (_ptr(a), lda, _ptr(b_q), ldb, _ptr(b_scale_tiles), _ptr(d), d.stride(0), M, N, K, st)
+    if opts is None:
+        _check(lib().rmsq_a16wfp4_gemm(*args))
+    else:
+        _check(lib().rmsq_a16wfp4_gemm_ex(*args, ctypes.byref(opts)))
+    return d
 
 
 def sync_status(device=None) -> int:

@@ -119,3 +119,27 @@ def compare_mx(got: dict, ref: dict, what: str = "") -> dict:
     assert np.array_equal(gs[ok_rows], rs[ok_rows]), f"{what}: E8M0 scales differ outside boundary rows"
     assert np.all(np.abs(gs.astype(np.int32) - rs.astype(np.int32)) <= 1), f"{what}: E8M0 off by > 1"
     return stats
+
+
+def compare_gemm(got, ref: dict, K: int, what: str = "") -> dict:
+    """GEMM output (bf16 [M, N]) against the oracle's exact sum.
+
+    Bound per element: the tensor core adds K/64 MMA results into an fp32
+    accumulator, each rounding at most 2^-24 of the magnitude sum of the terms
+    so far, so the accumulation error is at most (K/64) * 2^-24 * sum|term|
+    (taken here with a factor-2 margin, plus two roundings); the bf16 output
+    rounding adds at most 2^-8 of the value. Also reports the fraction of
+    outputs bit-equal to the oracle's bf16(f32(exact sum)), which is near one
+    for data without heavy cancellation."""
+    g = u16(got)
+    d = (g.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    d64, mag = ref["d64"], ref["abs"]
+    acc = (K / 64 + 2) * 2.0 ** -23 * mag
+    bound = acc * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(d64) + 2.0 ** -133
+    err = np.abs(d - d64)
+    assert np.all(np.isfinite(d)), f"{what}: non-finite outputs"
+    bad = err > bound
+    assert not bad.any(), f"{what}: {bad.sum()} outputs beyond the bound, worst excess {np.max(err / bound):.3g}"
+    exact = float(np.mean(g == ref["d"]))
+    return {"outputs": int(g.size), "bit_equal_fraction": exact,
+            "max_err_over_bound": float(np.max(err / bound, initial=0.0))}

@@ -122,3 +122,67 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(rmsq, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="not built"):
         rmsq.lib()
+
+
+def test_gemm_opts_layout_matches_header():
+    assert ctypes.sizeof(rmsq.GemmOpts) == 16
+    assert rmsq.GemmOpts.wait_limit_ns.offset == 8
+
+
+A_Q, A_S, B_Q, B_S, D = (BASE + i * (1 << 32) for i in range(5))
+
+
+def gemm(L, pre=False, **kw):
+    a = dict(a=A_Q, lda=2048 if pre else 512, a_s=A_S, b=B_Q, ldb=512, b_s=B_S, d=D, ldd=256,
+             M=64, N=256, K=1024)
+    a.update(kw)
+    if pre:
+        return L.rmsq_a16wfp4_gemm(a["a"], a["lda"], a["b"], a["ldb"], a["b_s"], a["d"], a["ldd"],
+                                   a["M"], a["N"], a["K"], None)
+    return L.rmsq_mxfp4_gemm(a["a"], a["lda"], a["a_s"], a["b"], a["ldb"], a["b_s"], a["d"], a["ldd"],
+                             a["M"], a["N"], a["K"], None)
+
+
+@pytest.mark.parametrize("pre", [False, True])
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=1000), 3),                     # K not a multiple of 256
+    (dict(K=0), 1),
+    (dict(N=260), 3),                      # N not a multiple of 8
+    (dict(M=-1), 1),
+    (dict(b=None), 1),
+    (dict(b_s=None), 1),
+    (dict(d=None), 1),
+    (dict(ldb=256), 1),                    # B rows are K/2 = 512 bytes
+    (dict(ldd=128), 1),                    # ld_d < N
+    (dict(b=B_Q + 8), 2),                  # misaligned
+    (dict(ldd=260), 2),                    # ld_d not a multiple of 8
+    (dict(d=B_Q + 1024), 1),               # D overlaps B
+])
+def test_gemm_rejects_bad_arguments(L, pre, kw, status):
+    assert gemm(L, pre, **kw) == status
+    assert L.rmsq_last_error()
+
+
+def test_gemm_specific_checks(L):
+    assert gemm(L, False, a_s=None) == 1                     # quantised A needs its scales
+    assert gemm(L, False, lda=256) == 1                      # A rows are K/2 bytes
+    assert gemm(L, True, lda=1000) == 1                      # bf16 A rows are K elements
+    assert gemm(L, True, lda=1028) == 2                      # bf16 leading dimension % 8
+    assert gemm(L, False, M=0) == 0 and gemm(L, True, N=0) == 0
+    opts = rmsq.GemmOpts(bn=96)
+    assert L.rmsq_mxfp4_gemm_ex(A_Q, 512, A_S, B_Q, 512, B_S, D, 256, 64, 256, 1024, None,
+                                ctypes.byref(opts)) == 1
+
+
+def test_norm_only_and_tiles_reject_bad_arguments(L):
+    call = L.rmsq_add_rmsnorm
+    assert call(X, 256, RES, 256, G, 1e-6, 4, 256, RO, None, None) == 1    # out_bf16 required
+    assert call(X, 256, RES, 256, G, 1e-6, 4, 48, RO, Y, None) == 1        # H % 32
+    assert call(X, 256, None, 0, G, 1e-6, 4, 256, RO, Y, None) == 1        # residual output without input
+    assert call(X, 256, RES, 256, G, 1e-6, 4, 256, RO, X + 64, None) == 1  # y overlaps x
+    assert call(X, 256, RES, 256, G, 1e-6, 0, 256, RO, Y, None) == 0
+    tiles = L.rmsq_mx_scale_tiles
+    assert tiles(A_S, 4, 10, 8, B_S, 0, None) == 1                         # ld < G
+    assert tiles(None, 8, 10, 8, B_S, 0, None) == 1
+    assert tiles(A_S, 8, 1000, 8, A_S + 512, 0, None) == 1                 # out overlaps the input
+    assert tiles(A_S, 8, 0, 8, B_S, 0, None) == 0

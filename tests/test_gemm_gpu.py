@@ -1,0 +1,166 @@
+"""Parity of the block-scaled MXFP4 consumer GEMM (both placements of the
+activation quant) with the CPU oracle, through the C ABI.
+
+The operands are seeded synthetic MXFP4 data; the comparison rule is
+tests/parity.py's compare_gemm (a bound derived from fp32 accumulation and
+the bf16 output rounding). The two placements -- quant fused into the norm,
+quant in the GEMM's prologue -- must give bit-identical outputs."""
+
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_activation_quant_gb300 import rmsq, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.fail("these tests need a CUDA GPU")
+
+
+def operands(seed, M, N, K):
+    """A (activation-like scale bytes 124..130) and B (weights) as MXFP4."""
+    a_q, a_s = synth.mxfp4_weights(seed, M, K, scale_lo=124, scale_hi=131)
+    b_q, b_s = synth.mxfp4_weights(seed + 1000, N, K)
+    return a_q, a_s, b_q, b_s
+
+
+def gpu_gemm(a_q, a_s, b_q, b_s, bn=0):
+    ga, gb = a_q.to(DEV), b_q.to(DEV)
+    ta, tb = rmsq.mx_scale_tiles(a_s.to(DEV)), rmsq.mx_scale_tiles(b_s.to(DEV))
+    d = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=bn) if bn else None)
+    torch.cuda.synchronize()
+    return d
+
+
+def test_scale_tiles_match_oracle(oracle_mod):
+    for R, G, fill in [(300, 56, 0), (128, 8, 7), (5, 3, 255), (1, 224, 0)]:
+        s = torch.randint(0, 256, (R, G), dtype=torch.uint8, generator=torch.Generator().manual_seed(R + G))
+        got = rmsq.mx_scale_tiles(s.to(DEV), fill=fill).cpu().numpy()
+        assert np.array_equal(got, oracle_mod.mx_scale_tiles(s.numpy(), fill=fill)), (R, G)
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("M,N,K", [(200, 328, 512), (128, 256, 256), (4, 520, 2048), (129, 64, 1536)])
+def test_mxfp4_gemm_matches_oracle(oracle_mod, bn, M, N, K):
+    a_q, a_s, b_q, b_s = operands(M * 7 + N, M, N, K)
+    d = gpu_gemm(a_q, a_s, b_q, b_s, bn)
+    ref = oracle_mod.mxfp4_gemm(a_q.numpy(), a_s.numpy(), b_q.numpy(), b_s.numpy())
+    st = parity.compare_gemm(d, ref, K, what=f"bn={bn} {M}x{N}x{K}")
+    assert st["bit_equal_fraction"] > 0.95, st
+    assert rmsq.sync_status() == 0
+    print(bn, M, N, K, st)
+
+
+def test_tile_choices_agree_bitwise():
+    """Tiles of 64, 128 and 256 B rows run the same MMAs in the same K order."""
+    a_q, a_s, b_q, b_s = operands(5, 256, 512, 1024)
+    outs = [gpu_gemm(a_q, a_s, b_q, b_s, bn) for bn in (64, 128, 256, 0)]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_long_k_wraps_the_stage_ring(oracle_mod):
+    """K = 7168 is 28 stages: every ring slot is reused several times."""
+    M, N, K = 130, 136, 7168
+    a_q, a_s, b_q, b_s = operands(9, M, N, K)
+    for bn in (64, 256):
+        d = gpu_gemm(a_q, a_s, b_q, b_s, bn)
+        ref = oracle_mod.mxfp4_gemm(a_q.numpy(), a_s.numpy(), b_q.numpy(), b_s.numpy())
+        print(bn, parity.compare_gemm(d, ref, K, what=f"long K bn={bn}"))
+
+
+def test_degenerate_operands():
+    M, N, K = 130, 264, 512
+    z = torch.zeros((M, K // 2), dtype=torch.uint8)
+    s_hi = torch.full((M, K // 32), 254, dtype=torch.uint8)       # 2^127 scales on zero codes
+    b_q, b_s = synth.mxfp4_weights(3, N, K)
+    d = gpu_gemm(z, s_hi, b_q, b_s)
+    assert torch.count_nonzero(d.float()).item() == 0             # exact zeros, no NaN / Inf
+    s_lo = torch.zeros((M, K // 32), dtype=torch.uint8)           # 2^-127: products underflow to 0
+    a_q, _ = synth.mxfp4_weights(4, M, K)
+    d = gpu_gemm(a_q, s_lo, b_q, b_s)
+    assert torch.isfinite(d.float()).all()
+    empty = torch.empty((0, K // 2), dtype=torch.uint8, device=DEV)
+    out = rmsq.mxfp4_gemm(empty, torch.zeros(512, dtype=torch.uint8, device=DEV), b_q.to(DEV),
+                          rmsq.mx_scale_tiles(b_s.to(DEV)))
+    assert out.shape == (0, N)
+
+
+def test_output_guard_band():
+    """The GEMM writes exactly D[:M, :N]: canary bytes around a strided D stay."""
+    M, N, K = 70, 136, 512
+    a_q, a_s, b_q, b_s = operands(11, M, N, K)
+    big = torch.full((M + 2, N + 24), -7.0, dtype=torch.bfloat16, device=DEV)
+    d = big[1:M + 1, 8:N + 8]
+    rmsq.mxfp4_gemm(a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV)), b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV)),
+                    out=d)
+    torch.cuda.synchronize()
+    ref = gpu_gemm(a_q, a_s, b_q, b_s)
+    assert torch.equal(d, ref)
+    mask = torch.ones_like(big, dtype=torch.bool)
+    mask[1:M + 1, 8:N + 8] = False
+    assert (big[mask] == -7.0).all()
+
+
+def _pipeline_inputs(M, K, seed):
+    w = synth.Workload("gemm_in", "mxfp4", M=M, H=K, seed=seed, group=32, x_dist="student_t3")
+    return {k: v.to(DEV) for k, v in synth.make_inputs(w).items()}, synth.make_inputs(w)
+
+
+@pytest.mark.parametrize("M", [4, 64, 300])
+def test_placements_agree_and_match_oracle(oracle_mod, M):
+    """norm + MXFP4 quant fused, then the GEMM == norm alone, then the GEMM
+    with the quant in its prologue; both against the oracle's composition."""
+    K, N = 7168, 2112
+    g, d_cpu = _pipeline_inputs(M, K, 21)
+    b_q, b_s = synth.mxfp4_weights(22, N, K)
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    (a_q, a_tiles), r1 = rmsq.add_rmsnorm_quant_mxfp4_mma_scales(g["x"], g["gamma"], g["residual"])
+    fused = rmsq.mxfp4_gemm(a_q, a_tiles, gb, tb)
+    y, r2 = rmsq.add_rmsnorm(g["x"], g["gamma"], g["residual"])
+    pre = rmsq.a16wfp4_gemm(y, gb, tb)
+    torch.cuda.synchronize()
+    assert torch.equal(r1, r2)
+    assert torch.equal(fused, pre), "the two placements differ"
+    ref_q = oracle_mod.add_rmsnorm_quant_mxfp4(d_cpu["x"], d_cpu["residual"], d_cpu["gamma"])
+    boundary = ref_q["margin"] < parity.BOUNDARY
+    assert np.array_equal(parity.u16(y)[~boundary], ref_q["y"][~boundary])
+    ref = oracle_mod.mxfp4_gemm(ref_q["q"], ref_q["scale"], b_q.numpy(), b_s.numpy())
+    st = parity.compare_gemm(fused[~torch.from_numpy(boundary).to(DEV)],
+                             {k: v[~boundary] for k, v in ref.items()}, K, what=f"pipeline M={M}")
+    assert rmsq.sync_status() == 0
+    print(M, st)
+
+
+def test_full_size_sampled(oracle_mod):
+    """The benchmarked shape (M=8192 tokens, N=2112, K=7168): the placements
+    agree on every output; sampled rows (rows are independent) against the
+    oracle's composition computed from the same input rows."""
+    M, K, N = 8192, 7168, 2112
+    g, d_cpu = _pipeline_inputs(M, K, 31)
+    b_q, b_s = synth.mxfp4_weights(32, N, K)
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    (a_q, a_tiles), _ = rmsq.add_rmsnorm_quant_mxfp4_mma_scales(g["x"], g["gamma"], g["residual"])
+    fused = rmsq.mxfp4_gemm(a_q, a_tiles, gb, tb)
+    y, _ = rmsq.add_rmsnorm(g["x"], g["gamma"], g["residual"])
+    pre = rmsq.a16wfp4_gemm(y, gb, tb)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, pre)
+    rows = [0, 1, 127, 128, 4095, 5000, 8190, 8191]
+    sub = {k: (v[rows] if v.dim() == 2 else v) for k, v in d_cpu.items()}
+    ref_q = oracle_mod.add_rmsnorm_quant_mxfp4(sub["x"], sub["residual"], sub["gamma"])
+    keep = ref_q["margin"] >= parity.BOUNDARY
+    ref = oracle_mod.mxfp4_gemm(ref_q["q"], ref_q["scale"], b_q.numpy(), b_s.numpy())
+    got = fused[torch.tensor(rows, device=DEV)][torch.from_numpy(keep).to(DEV)]
+    st = parity.compare_gemm(got, {k: v[keep] for k, v in ref.items()}, K, what="full size")
+    assert rmsq.sync_status() == 0
+    print(st)
