@@ -90,6 +90,7 @@ struct GemmParams {
     int64_t M, N;
     int32_t k_stages;           // K / 256
     int32_t b_row_tiles;        // ceil(N / 128): 128-row scale tiles that exist for B
+    int32_t a_box_rows;         // rows of A per TMA box: 128, or M rounded up to 8 when M < 128
     int64_t wait_limit_ns;
     unsigned int *status;
 };
@@ -121,21 +122,29 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
 // Bounded wait for the phase of `bar` with the given parity. Returns false
 // (after raising the CTA's abort flag and the status word) if it ran out, or
 // if another role of the CTA already aborted.
+// The clock and the abort flag are looked at only every 64 polls: reading
+// %globaltimer on every poll made the waiting thread notice a completed
+// phase hundreds of nanoseconds late (measured on GB300).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           const GemmParams &p)
 {
     if (mbar_test(bar, parity))
         return true;
-    const uint64_t t0 = gtimer();
-    for (;;) {
+    uint64_t t0 = 0;
+    for (uint32_t n = 1;; ++n) {
         if (mbar_test(bar, parity))
             return true;
-        if (*abort)
-            return false;
-        if (gtimer() - t0 > (uint64_t)p.wait_limit_ns) {
-            *abort = 1;
-            atomicOr(p.status, 2u);
-            return false;
+        if ((n & 63) == 0) {
+            if (*abort)
+                return false;
+            const uint64_t t = gtimer();
+            if (!t0) {
+                t0 = t;
+            } else if (t - t0 > (uint64_t)p.wait_limit_ns) {
+                *abort = 1;
+                atomicOr(p.status, 2u);
+                return false;
+            }
         }
     }
 }
@@ -149,6 +158,18 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     if ((threadIdx.x & 31) == 0)
         ok = mbar_wait(bar, parity, abort, p) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// One lane of the (fully active) warp, chosen by the hardware.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes)
@@ -315,6 +336,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int64_t m0 = (int64_t)m_tile * kBM, n0 = (int64_t)n_tile * BN;
     const int KS = p.k_stages;
 
+    if (threadIdx.x == 32) {
+        // bring both tensor maps into the descriptor cache before the first copy
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_b) : "memory");
+        if (!PREQUANT)
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_a) : "memory");
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(full + s)),
@@ -340,19 +367,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------- loads
-        if (lane == 0) {
-            const uint32_t b_tx = C::kBBytes;
-            const int bt0 = (int)(n0 >> 7);                       // first 128-row scale tile of B
-            int issued = 0;
-            for (int ks = 0; ks < KS; ++ks) {
-                const int s = ks % C::kStages;
-                const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
-                if (!mbar_wait(saddr(empty + s), ph ^ 1u, abort, p))
-                    break;
-                int atoms = 0;
-                for (int t = 0; t < C::kSfbAtoms; ++t)
-                    atoms += (bt0 + t < p.b_row_tiles);
-                const uint32_t tx = b_tx + atoms * 1024u + (PREQUANT ? 0u : (uint32_t)(C::kABytes + C::kSfaBytes));
+        // The whole warp runs the loop (its values stay warp-uniform) and one
+        // elected lane issues the copies.
+        const uint32_t b_tx = C::kBBytes;
+        const int bt0 = (int)(n0 >> 7);                           // first 128-row scale tile of B
+        int atoms = 0;
+        for (int t = 0; t < C::kSfbAtoms; ++t)
+            atoms += (bt0 + t < p.b_row_tiles);
+        const uint32_t tx = b_tx + atoms * 1024u +
+                            (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kStageBytes + C::kSfaBytes));
+        int issued = 0;
+        for (int ks = 0; ks < KS; ++ks) {
+            const int s = ks % C::kStages;
+            const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
+            if (!warp_wait(saddr(empty + s), ph ^ 1u, abort, p))
+                break;
+            if (elect_one()) {
                 const uint32_t fb = saddr(full + s);
                 mbar_arrive_tx(fb, tx);
                 uint8_t *stage = smem + s * C::kAB;
@@ -366,37 +396,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (bt0 + t < p.b_row_tiles)
                         bulk_g2s(saddr(smem + C::kOffSfb + s * C::kSfbBytes + t * 1024),
                                  p.b_scale + ((int64_t)(bt0 + t) * (2 * KS) + 2 * ks) * 512, 1024, fb);
-                issued = ks + 1;
             }
-            if (*abort) {
-                // let the copies already issued land before the CTA goes away
-                // (one deadline for all of them)
-                const uint64_t t0 = gtimer();
-                for (int ks = (issued > C::kStages ? issued - C::kStages : 0); ks < issued; ++ks) {
-                    const uint32_t fb = saddr(full + ks % C::kStages);
-                    const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
-                    while (!mbar_test(fb, ph) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
-                    }
+            __syncwarp();
+            issued = ks + 1;
+        }
+        if (*abort && lane == 0) {
+            // let the copies already issued land before the CTA goes away
+            // (one deadline for all of them)
+            const uint64_t t0 = gtimer();
+            for (int ks = (issued > C::kStages ? issued - C::kStages : 0); ks < issued; ++ks) {
+                const uint32_t fb = saddr(full + ks % C::kStages);
+                const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
+                while (!mbar_test(fb, ph) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
-        if (lane == 0) {
-            // a 64-row B tile sits in the lower or upper half of its 128-row scale tile
-            const uint32_t sfb_row_col = (BN == 64) ? (uint32_t)(((n0 >> 6) & 1) * 2) : 0u;
-            bool any = false;
-            for (int ks = 0; ks < KS; ++ks) {
-                const int s = ks % C::kStages;
-                const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
-                if (!mbar_wait(saddr(full + s), ph, abort, p))
-                    break;
-                tc_fence_after();
-                const uint32_t sfa_col = tmem_sf + s * C::kSfCols;
-                const uint32_t sfb_col = sfa_col + 8;
-                const uint32_t sfa_smem = saddr(smem + C::kOffSfa + s * C::kSfaBytes);
-                const uint32_t sfb_smem = saddr(smem + C::kOffSfb + s * C::kSfbBytes);
+        // warp-uniform loop, one elected lane issues the tensor-core work
+        // a 64-row B tile sits in the lower or upper half of its 128-row scale tile
+        const uint32_t sfb_row_col = (BN == 64) ? (uint32_t)(((n0 >> 6) & 1) * 2) : 0u;
+        bool any = false;
+        for (int ks = 0; ks < KS; ++ks) {
+            const int s = ks % C::kStages;
+            const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
+            if (!warp_wait(saddr(full + s), ph, abort, p))
+                break;
+            tc_fence_after();
+            const uint32_t sfa_col = tmem_sf + s * C::kSfCols;
+            const uint32_t sfb_col = sfa_col + 8;
+            const uint32_t sfa_smem = saddr(smem + C::kOffSfa + s * C::kSfaBytes);
+            const uint32_t sfb_smem = saddr(smem + C::kOffSfb + s * C::kSfbBytes);
+            const uint32_t a_smem = saddr(smem + s * C::kAB), b_smem = a_smem + C::kOffB;
+            if (elect_one()) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     cp_sf(sfa_col + 4 * j, desc_sf(sfa_smem + j * 512));
@@ -404,7 +437,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int t = 0; t < C::kSfbAtoms; ++t)
                         cp_sf(sfb_col + 4 * C::kSfbAtoms * j + 4 * t, desc_sf(sfb_smem + t * 1024 + j * 512));
                 }
-                const uint32_t a_smem = saddr(smem + s * C::kAB), b_smem = a_smem + C::kOffB;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int j = k >> 1;
@@ -413,8 +445,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                              sfb_col + 4 * C::kSfbAtoms * j + sfb_row_col, (ks | k) != 0);
                 }
                 mma_commit(saddr(empty + s));
-                any = true;
             }
+            __syncwarp();
+            any = true;
+        }
+        if (elect_one()) {
             if (!*abort) {
                 mma_commit(saddr(accum));
             } else if (any) {
@@ -556,6 +591,10 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
     p.N = g.N;
     p.k_stages = (int32_t)(g.K / kStageK);
     p.b_row_tiles = (int32_t)((g.N + 127) / 128);
+    // Rows of the A tile past M are never stored, so with fewer than 128
+    // rows only those (rounded up to a swizzle atom of 8) are loaded; the
+    // rest of the tile keeps whatever it held and feeds only discarded rows.
+    p.a_box_rows = g.M >= kBM ? kBM : (int32_t)((g.M + 7) / 8 * 8);
     p.wait_limit_ns = g.wait_limit_ns;
     p.status = g.status;
     CUtensorMap ma, mb;
@@ -563,7 +602,7 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
         return cudaErrorInvalidValue;
     if (g.a_bf16) {
         ma = mb;   // unused by the prequant kernel
-    } else if (!make_code_map(&ma, g.a_q, g.M, g.K / 2, g.lda, kBM)) {
+    } else if (!make_code_map(&ma, g.a_q, g.M, g.K / 2, g.lda, p.a_box_rows)) {
         return cudaErrorInvalidValue;
     }
     const int m_tiles = (int)((g.M + kBM - 1) / kBM), n_tiles = (int)((g.N + g.bn - 1) / g.bn);
