@@ -278,12 +278,20 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
  * Optional control of the GEMM launch (NULL = defaults), for tests and
  * tuning; results do not depend on it.
  *   bn             rows of B per CTA tile: 64, 128 or 256; 0 = auto (the
- *                  largest that still gives at least one tile per SM)
+ *                  largest that still gives at least one tile per SM, else 64)
+ *   ksplit         CTAs, launched as one thread-block cluster, that split K
+ *                  for each tile and add their fp32 partial sums through
+ *                  distributed shared memory (rank order, so deterministic):
+ *                  1..8 and at most K/256; 0 = auto (enough to give every SM
+ *                  a CTA when there are fewer tiles than SMs). Splitting K
+ *                  changes the order of the fp32 additions, so results can
+ *                  differ between ksplit values in the last bits (both
+ *                  placements agree bit for bit at equal ksplit and bn).
  *   wait_limit_ns  limit of every wait inside the kernel, 0 = 2 s
  */
 typedef struct rmsq_gemm_opts {
     int32_t bn;
-    int32_t reserved;
+    int32_t ksplit;
     int64_t wait_limit_ns;
 } rmsq_gemm_opts;
 

@@ -466,6 +466,8 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
         return fail(RMSQ_ERR_INVALID_ARG, "need M >= 0, N >= 0, K > 0");
     if (o.bn != 0 && o.bn != 64 && o.bn != 128 && o.bn != 256)
         return fail(RMSQ_ERR_INVALID_ARG, "bn must be 0, 64, 128 or 256 (got %d)", o.bn);
+    if (o.ksplit < 0 || o.ksplit > 8)
+        return fail(RMSQ_ERR_INVALID_ARG, "ksplit must be 0..8 (got %d)", o.ksplit);
     if (o.wait_limit_ns < 0)
         return fail(RMSQ_ERR_INVALID_ARG, "wait_limit_ns must be >= 0");
     if (K % 256)
@@ -504,9 +506,12 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     unsigned int *status = status_word_ptr(dev);
     if (!status)
         return fail(RMSQ_ERR_CUDA, "status word address unavailable");
+    // Tiles: the widest B tile that still gives every SM a tile; with fewer
+    // tiles than SMs, narrow 64-row B tiles and K split over a cluster of up
+    // to 8 CTAs (each at least one K stage) fill the GPU.
+    const int sms = sm_count();
     int bn = o.bn;
     if (!bn) {
-        const int sms = sm_count();
         bn = 64;
         for (int c : {256, 128})
             if (m_tiles * ((N + c - 1) / c) >= sms) {
@@ -514,6 +519,18 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
                 break;
             }
     }
+    const int64_t tiles = m_tiles * ((N + bn - 1) / bn);
+    int ksplit = o.ksplit;
+    if (!ksplit) {
+        int64_t k = tiles >= sms ? 1 : sms / tiles;
+        if (k > 8)
+            k = 8;
+        if (k > K / 256)
+            k = K / 256;
+        ksplit = (int)(k < 1 ? 1 : k);
+    }
+    if (ksplit > K / 256)
+        return fail(RMSQ_ERR_INVALID_ARG, "ksplit=%d exceeds the %lld K stages", ksplit, (long long)(K / 256));
     GemmLaunch g{};
     if (prequant) {
         g.a_bf16 = a;
@@ -531,6 +548,7 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     g.N = N;
     g.K = K;
     g.bn = bn;
+    g.ksplit = ksplit;
     g.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
     g.status = status;
     cudaError_t e = launch_mxfp4_gemm(g, (cudaStream_t)stream);

@@ -91,6 +91,7 @@ struct GemmParams {
     int32_t k_stages;           // K / 256
     int32_t b_row_tiles;        // ceil(N / 128): 128-row scale tiles that exist for B
     int32_t a_box_rows;         // rows of A per TMA box: 128, or M rounded up to 8 when M < 128
+    int32_t ksplit;             // CTAs of a cluster that split K (1 = no split)
     int64_t wait_limit_ns;
     unsigned int *status;
 };
@@ -261,57 +262,140 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 
 // ---------------------------------------------------- prequant (A in bf16)
 
-// One group of 32 bf16 values -> 16 bytes of E2M1 codes and the E8M0 byte,
-// with the fused kernel's arithmetic: X from the group's largest magnitude,
-// elements times 2^-X (exact), saturating round-to-nearest-even E2M1.
-__device__ __forceinline__ uint4 quant_group32(const uint4 (&v)[4], uint32_t &scale_byte)
+// The 128 threads of warps 4-7 quantise the valid rows R of the A tile for
+// each of this CTA's K stages. Item i = t + 128 j of a stage is 16-byte vector
+// (i % 32) of row (i / 32): warp w takes rows w, w + 4, ..., a row's 32 lanes
+// read its 512 contiguous bytes, and the 4 lanes of a 32-element group find
+// the group's amax with two shuffles. The arithmetic is the fused kernel's:
+// X from the group's largest magnitude, elements times 2^-X (exact),
+// saturating round-to-nearest-even E2M1.
+//
+// A thread's items (NI per stage) run through its stages in order, in chunks
+// of up to 8: the next chunk's loads are issued before the current chunk is
+// processed (so with few rows, loads run several stages ahead), the waits
+// for the chunk's stage slots come before it and the arrivals after it, and
+// the chunk's items go through each step together without branches, which
+// lets their load -> shuffle -> convert chains overlap. A chunk spans at
+// most STAGES - 1 stages, so it never waits for a slot that only its own
+// arrivals could free.
+template <int STAGES, int AB, int OFF_SFA>
+__device__ __forceinline__ bool prequant_loop(const GemmParams &p, int64_t m0, int R, int ks0, int KL,
+                                              uint8_t *smem, uint64_t *full, uint64_t *empty, volatile int *abort)
 {
-    const uint32_t am = max(max(amax_bits_bf16x8(v[0]), amax_bits_bf16x8(v[1])),
-                            max(amax_bits_bf16x8(v[2]), amax_bits_bf16x8(v[3])));
-    const int X = mx_exponent_from_bits(am);
-    scale_byte = (uint32_t)(X + 127);
-    const float2 mult = f2(__uint_as_float((uint32_t)(127 - X) << 23));   // 2^-X
-    uint32_t w[4];
+    const int t = threadIdx.x - 128;
+    const int w = t >> 5, vec = t & 31, g = vec >> 2;
+    const int NI = (R + 3) >> 2;                       // items per thread per stage
+    const int total = KL * NI;
+    const int ch = min(8, (STAGES - 2) * NI + 1);      // items per chunk
+    const uint4 *base = p.a_bf16 + m0 * p.lda_v + vec;
+    uint4 cur[8], nxt[8];
+
+    auto load_chunk = [&](int c0, uint4 (&v)[8]) {
+        int i = c0 / NI, j = c0 - i * NI;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        w[i] = e2m1x8(mul2(unpack_bf16x2(v[i].x), mult), mul2(unpack_bf16x2(v[i].y), mult),
-                      mul2(unpack_bf16x2(v[i].z), mult), mul2(unpack_bf16x2(v[i].w), mult));
-    return make_uint4(w[0], w[1], w[2], w[3]);
+        for (int u = 0; u < 8; ++u) {
+            const int row = w + 4 * j;
+            const bool ok = u < ch && c0 + u < total && row < R;
+            v[u] = ok ? __ldg(base + row * p.lda_v + (int64_t)(ks0 + i) * (kStageK / 8)) : make_uint4(0, 0, 0, 0);
+            if (++j == NI) {
+                j = 0;
+                ++i;
+            }
+        }
+    };
+
+    load_chunk(0, cur);
+    for (int c0 = 0; c0 < total; c0 += ch) {
+        if (c0 + ch < total)
+            load_chunk(c0 + ch, nxt);
+        const int ic = c0 / NI, jc = c0 - ic * NI;
+        // slots of the stages this chunk starts
+        {
+            int i = ic, j = jc;
+            for (int u = 0; u < ch && c0 + u < total; ++u) {
+                if (j == 0 && !warp_wait(saddr(empty + i % STAGES), ((uint32_t)(i / STAGES) & 1u) ^ 1u, abort, p))
+                    return false;
+                if (++j == NI) {
+                    j = 0;
+                    ++i;
+                }
+            }
+        }
+        // the chunk's items, step by step
+        uint32_t am[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            am[u] = amax_bits_bf16x8(cur[u]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            am[u] = max(am[u], __shfl_xor_sync(0xffffffffu, am[u], 1));
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            am[u] = max(am[u], __shfl_xor_sync(0xffffffffu, am[u], 2));
+        {
+            int i = ic, j = jc;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int row = w + 4 * j;
+                const int s = i % STAGES;
+                const bool ok = u < ch && c0 + u < total && row < R;
+                const int X = mx_exponent_from_bits(am[u]);
+                const float2 mult = f2(__uint_as_float((uint32_t)(127 - X) << 23));   // 2^-X
+                const uint4 v = cur[u];
+                const uint32_t codes =
+                    e2m1x8(mul2(unpack_bf16x2(v.x), mult), mul2(unpack_bf16x2(v.y), mult),
+                           mul2(unpack_bf16x2(v.z), mult), mul2(unpack_bf16x2(v.w), mult));
+                if (ok) {
+                    *reinterpret_cast<uint32_t *>(smem + s * AB + row * kStageBytes + ((g ^ (row & 7)) << 4) +
+                                                  (vec & 3) * 4) = codes;
+                    if ((vec & 3) == 0)        // scale tile g/4: (row % 32) * 16 + (row / 32) * 4 + g % 4
+                        smem[OFF_SFA + s * 1024 + (g >> 2) * 512 + (row & 31) * 16 + (row >> 5) * 4 + (g & 3)] =
+                            (uint8_t)(X + 127);
+                }
+                if (++j == NI) {
+                    j = 0;
+                    ++i;
+                }
+            }
+        }
+        // stages this chunk completes
+        {
+            int i = ic, j = jc;
+            for (int u = 0; u < ch && c0 + u < total; ++u) {
+                if (j == NI - 1) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive(saddr(full + i % STAGES));
+                }
+                if (++j == NI) {
+                    j = 0;
+                    ++i;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            cur[u] = nxt[u];
+    }
+    return true;
 }
 
-// Quantise this thread's row (r = 0..127) of one stage: 256 bf16 values from
-// global memory -> 128 swizzled code bytes in sA and 8 scale bytes in the two
-// 512-byte scale tiles at sSfa.
-__device__ __forceinline__ void prequant_row(const GemmParams &p, int64_t m, int r, int stage_k,
-                                             uint8_t *sA, uint8_t *sSfa)
+// ------------------------------------------------------- cluster (split K)
+
+__device__ __forceinline__ void cluster_sync()
 {
-    const uint4 *src = p.a_bf16 + m * p.lda_v + (int64_t)stage_k * (kStageK / 8);
-    uint32_t sc[8];
-    uint4 cur[4], nxt[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        cur[i] = __ldg(src + i);
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-        if (g + 1 < 8) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                nxt[i] = __ldg(src + (g + 1) * 4 + i);
-        }
-        const uint4 codes = quant_group32(cur, sc[g]);
-        // group g is 16-byte chunk g of the row, swizzled within its 8-row atom
-        *reinterpret_cast<uint4 *>(sA + r * kStageBytes + ((g ^ (r & 7)) << 4)) = codes;
-        if (g + 1 < 8) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                cur[i] = nxt[i];
-        }
-    }
-    // scale tile j holds groups 4j..4j+3 of row r at (r % 32) * 16 + (r / 32) * 4
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-        *reinterpret_cast<uint32_t *>(sSfa + j * 512 + (r & 31) * 16 + (r >> 5) * 4) =
-            sc[4 * j] | (sc[4 * j + 1] << 8) | (sc[4 * j + 2] << 16) | (sc[4 * j + 3] << 24);
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ float4 ld_peer_f4(const float *local, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr(local)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -334,7 +418,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tile = blockIdx.x, m_tile = blockIdx.y;
     const int64_t m0 = (int64_t)m_tile * kBM, n0 = (int64_t)n_tile * BN;
+    // this CTA's stages of K: all of them, or its share when a cluster splits K
     const int KS = p.k_stages;
+    const int kz = (int)blockIdx.z;
+    const int ks0 = (int)((int64_t)KS * kz / p.ksplit), KL = (int)((int64_t)KS * (kz + 1) / p.ksplit) - ks0;
+    const int R = (int)min((int64_t)kBM, p.M - m0);    // rows of the tile that exist
 
     if (threadIdx.x == 32) {
         // bring both tensor maps into the descriptor cache before the first copy
@@ -377,9 +465,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t tx = b_tx + atoms * 1024u +
                             (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kStageBytes + C::kSfaBytes));
         int issued = 0;
-        for (int ks = 0; ks < KS; ++ks) {
-            const int s = ks % C::kStages;
-            const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
+        for (int i = 0; i < KL; ++i) {
+            const int ks = ks0 + i, s = i % C::kStages;
+            const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
             if (!warp_wait(saddr(empty + s), ph ^ 1u, abort, p))
                 break;
             if (elect_one()) {
@@ -398,15 +486,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                  p.b_scale + ((int64_t)(bt0 + t) * (2 * KS) + 2 * ks) * 512, 1024, fb);
             }
             __syncwarp();
-            issued = ks + 1;
+            issued = i + 1;
         }
         if (*abort && lane == 0) {
             // let the copies already issued land before the CTA goes away
             // (one deadline for all of them)
             const uint64_t t0 = gtimer();
-            for (int ks = (issued > C::kStages ? issued - C::kStages : 0); ks < issued; ++ks) {
-                const uint32_t fb = saddr(full + ks % C::kStages);
-                const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
+            for (int i = (issued > C::kStages ? issued - C::kStages : 0); i < issued; ++i) {
+                const uint32_t fb = saddr(full + i % C::kStages);
+                const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
                 while (!mbar_test(fb, ph) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
                 }
             }
@@ -418,9 +506,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // a 64-row B tile sits in the lower or upper half of its 128-row scale tile
         const uint32_t sfb_row_col = (BN == 64) ? (uint32_t)(((n0 >> 6) & 1) * 2) : 0u;
         bool any = false;
-        for (int ks = 0; ks < KS; ++ks) {
-            const int s = ks % C::kStages;
-            const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
+        for (int i = 0; i < KL; ++i) {
+            const int s = i % C::kStages;
+            const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
             if (!warp_wait(saddr(full + s), ph, abort, p))
                 break;
             tc_fence_after();
@@ -442,7 +530,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int j = k >> 1;
                     mma_mxf4(tmem, desc_sw128(a_smem + 32 * k), desc_sw128(b_smem + 32 * k),
                              idesc_mxf4(BN, (k & 1) * 2), sfa_col + 4 * j,
-                             sfb_col + 4 * C::kSfbAtoms * j + sfb_row_col, (ks | k) != 0);
+                             sfb_col + 4 * C::kSfbAtoms * j + sfb_row_col, (i | k) != 0);
                 }
                 mma_commit(saddr(empty + s));
             }
@@ -465,44 +553,74 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int q = warp - 4;              // lane quarter of tensor memory this warp may access
         const int r = q * 32 + lane;         // row of the tile
         const int64_t m = m0 + r;
-        if (PREQUANT) {
-            // ------------------------------------------- quantise A stages
-            for (int ks = 0; ks < KS; ++ks) {
-                const int s = ks % C::kStages;
-                const uint32_t ph = (uint32_t)(ks / C::kStages) & 1u;
-                if (!warp_wait(saddr(empty + s), ph ^ 1u, abort, p))
-                    break;
-                if (m < p.M)
-                    prequant_row(p, m, r, ks, smem + s * C::kAB, smem + C::kOffSfa + s * C::kSfaBytes);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(saddr(full + s));
-            }
-        }
+        bool ok = true;
+        if (PREQUANT)
+            ok = prequant_loop<C::kStages, C::kAB, C::kOffSfa>(p, m0, R, ks0, KL, smem, full, empty, abort);
         // ------------------------------------------------------- epilogue
-        if (warp_wait(saddr(accum), 0, abort, p)) {
+        if (ok && warp_wait(saddr(accum), 0, abort, p)) {
             tc_fence_after();
             const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
             uint16_t *drow = p.d + m * p.ldd + n0;
+            // split K: this CTA's partial sums go to its shared memory (the
+            // operand ring is free now), padded rows against bank conflicts
+            float *red = (float *)smem + r * (BN + 4);
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t acc[32];
                 tmem_ld32(trow + c0, acc);
-                if (m < p.M) {
-                    const int64_t valid = p.N - (n0 + c0);
+                if (r >= R)
+                    continue;
+                if (p.ksplit > 1) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        if (valid >= 8 * (v + 1)) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(acc[8 * v + 0]), __uint_as_float(acc[8 * v + 1]));
-                            o.y = pack_bf16x2(__uint_as_float(acc[8 * v + 2]), __uint_as_float(acc[8 * v + 3]));
-                            o.z = pack_bf16x2(__uint_as_float(acc[8 * v + 4]), __uint_as_float(acc[8 * v + 5]));
-                            o.w = pack_bf16x2(__uint_as_float(acc[8 * v + 6]), __uint_as_float(acc[8 * v + 7]));
-                            *reinterpret_cast<uint4 *>(drow + c0 + 8 * v) = o;
-                        }
+                    for (int v = 0; v < 8; ++v)
+                        *reinterpret_cast<float4 *>(red + c0 + 4 * v) =
+                            make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
+                                        __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3]));
+                    continue;
+                }
+                const int64_t valid = p.N - (n0 + c0);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    if (valid >= 8 * (v + 1)) {
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(acc[8 * v + 0]), __uint_as_float(acc[8 * v + 1]));
+                        o.y = pack_bf16x2(__uint_as_float(acc[8 * v + 2]), __uint_as_float(acc[8 * v + 3]));
+                        o.z = pack_bf16x2(__uint_as_float(acc[8 * v + 4]), __uint_as_float(acc[8 * v + 5]));
+                        o.w = pack_bf16x2(__uint_as_float(acc[8 * v + 6]), __uint_as_float(acc[8 * v + 7]));
+                        *reinterpret_cast<uint4 *>(drow + c0 + 8 * v) = o;
                     }
                 }
             }
         }
+    }
+
+    if (p.ksplit > 1) {
+        // ------------------------------------------- split-K reduction
+        // Every CTA of the cluster reaches both barriers, whatever happened
+        // before (an aborted CTA contributes garbage and has set the status
+        // word), so no CTA waits on one that left. CTA z sums a contiguous
+        // share of the tile's (row, 4-column) units over the cluster's
+        // partials in rank order 0, 1, ... (deterministic), then rounds to bf16.
+        cluster_sync();
+        const int units = R * (BN / 4);
+        const int u0 = (int)((int64_t)units * kz / p.ksplit), u1 = (int)((int64_t)units * (kz + 1) / p.ksplit);
+        for (int u = u0 + (int)threadIdx.x; u < u1; u += kGemmThreads) {
+            const int row = u / (BN / 4), c = (u - row * (BN / 4)) * 4;
+            if (n0 + c >= p.N)
+                continue;
+            const float *src = (const float *)smem + row * (BN + 4) + c;
+            float4 acc = ld_peer_f4(src, 0);
+            for (int z = 1; z < p.ksplit; ++z) {
+                const float4 v = ld_peer_f4(src, (uint32_t)z);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            *reinterpret_cast<uint2 *>(p.d + (m0 + row) * p.ldd + n0 + c) =
+                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        }
+        cluster_sync();
     }
 
     // ------------------------------------------------------------ teardown
@@ -572,8 +690,25 @@ cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUte
             return e;
         attr[dev] = true;
     }
-    mxfp4_gemm_kernel<BN, PRE><<<dim3(n_tiles, m_tiles), kGemmThreads, C::kSmem, st>>>(p, ma, mb);
-    return cudaGetLastError();
+    if (p.ksplit == 1) {
+        mxfp4_gemm_kernel<BN, PRE><<<dim3(n_tiles, m_tiles, 1), kGemmThreads, C::kSmem, st>>>(p, ma, mb);
+        return cudaGetLastError();
+    }
+    // the CTAs that split one tile's K form a cluster (they exchange partial
+    // sums through distributed shared memory)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_tiles, m_tiles, p.ksplit);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute cl[1];
+    cl[0].id = cudaLaunchAttributeClusterDimension;
+    cl[0].val.clusterDim.x = 1;
+    cl[0].val.clusterDim.y = 1;
+    cl[0].val.clusterDim.z = (unsigned)p.ksplit;
+    cfg.attrs = cl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<BN, PRE>, p, ma, mb);
 }
 
 }  // namespace
@@ -595,6 +730,9 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
     // rows only those (rounded up to a swizzle atom of 8) are loaded; the
     // rest of the tile keeps whatever it held and feeds only discarded rows.
     p.a_box_rows = g.M >= kBM ? kBM : (int32_t)((g.M + 7) / 8 * 8);
+    p.ksplit = g.ksplit;
+    if (p.ksplit < 1 || p.ksplit > 8 || p.ksplit > p.k_stages)
+        return cudaErrorInvalidValue;
     p.wait_limit_ns = g.wait_limit_ns;
     p.status = g.status;
     CUtensorMap ma, mb;

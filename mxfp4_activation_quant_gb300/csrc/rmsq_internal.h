@@ -57,6 +57,7 @@ struct GemmLaunch {
     int64_t ldd;               // elements
     int64_t M, N, K;
     int bn;                    // 64, 128 or 256
+    int ksplit;                // 1..8 CTAs (a cluster) per tile splitting K
     int64_t wait_limit_ns;
     unsigned int *status;
 };

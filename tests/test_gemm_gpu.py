@@ -33,10 +33,11 @@ def operands(seed, M, N, K):
     return a_q, a_s, b_q, b_s
 
 
-def gpu_gemm(a_q, a_s, b_q, b_s, bn=0):
+def gpu_gemm(a_q, a_s, b_q, b_s, bn=0, ksplit=0):
     ga, gb = a_q.to(DEV), b_q.to(DEV)
     ta, tb = rmsq.mx_scale_tiles(a_s.to(DEV)), rmsq.mx_scale_tiles(b_s.to(DEV))
-    d = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=bn) if bn else None)
+    opts = rmsq.GemmOpts(bn=bn, ksplit=ksplit) if (bn or ksplit) else None
+    d = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=opts)
     torch.cuda.synchronize()
     return d
 
@@ -60,10 +61,27 @@ def test_mxfp4_gemm_matches_oracle(oracle_mod, bn, M, N, K):
     print(bn, M, N, K, st)
 
 
+@pytest.mark.parametrize("ksplit", [2, 3, 8])
+@pytest.mark.parametrize("bn", [64, 256])
+def test_split_k_matches_oracle(oracle_mod, bn, ksplit):
+    """K split over a cluster of CTAs, partial sums added through distributed
+    shared memory: same bound, and no output outside D."""
+    M, N, K = 70, 328, 2560
+    a_q, a_s, b_q, b_s = operands(17 + ksplit, M, N, K)
+    d = gpu_gemm(a_q, a_s, b_q, b_s, bn, ksplit)
+    ref = oracle_mod.mxfp4_gemm(a_q.numpy(), a_s.numpy(), b_q.numpy(), b_s.numpy())
+    st = parity.compare_gemm(d, ref, K, what=f"bn={bn} ksplit={ksplit}")
+    assert st["bit_equal_fraction"] > 0.95, st
+    again = gpu_gemm(a_q, a_s, b_q, b_s, bn, ksplit)
+    assert torch.equal(d, again), "split-K result is not deterministic"
+    assert rmsq.sync_status() == 0
+    print(bn, ksplit, st)
+
+
 def test_tile_choices_agree_bitwise():
     """Tiles of 64, 128 and 256 B rows run the same MMAs in the same K order."""
     a_q, a_s, b_q, b_s = operands(5, 256, 512, 1024)
-    outs = [gpu_gemm(a_q, a_s, b_q, b_s, bn) for bn in (64, 128, 256, 0)]
+    outs = [gpu_gemm(a_q, a_s, b_q, b_s, bn, 1) for bn in (64, 128, 256)]
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
 
@@ -116,7 +134,7 @@ def _pipeline_inputs(M, K, seed):
     return {k: v.to(DEV) for k, v in synth.make_inputs(w).items()}, synth.make_inputs(w)
 
 
-@pytest.mark.parametrize("M", [4, 64, 300])
+@pytest.mark.parametrize("M", [4, 64, 300, 1100])
 def test_placements_agree_and_match_oracle(oracle_mod, M):
     """norm + MXFP4 quant fused, then the GEMM == norm alone, then the GEMM
     with the quant in its prologue; both against the oracle's composition."""
