@@ -71,13 +71,37 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_digest() -> str:
+# Dense FP4 (E2M1) tensor rate over dense bf16 on GB300, from the nominal
+# figures (13.5 and 2.25 PFLOP/s); the measured bf16 GEMM rate times this is
+# the FP4 roofline.
+FP4_OVER_BF16 = 6.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def measured_fp4_peak() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            bf16 = float(json.load(fh)["bf16_tflops"])
+        return bf16 * FP4_OVER_BF16, "measured bf16 burst x nominal fp4/bf16 ratio 6"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS * FP4_OVER_BF16, "fallback bf16 x nominal fp4/bf16 ratio 6"
+
+
+GEMM_SOURCES = ("rmsq_gemm.cu", "rmsq_device.cuh", "rmsq_internal.h")
+
+
+def kernel_source_digest(kind: str = "rows") -> str:
+    """Hash of the sources a kernel family is built from: the GEMM's own
+    files for "gemm", everything but the GEMM for the norm + quant kernels."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mxfp4_activation_quant_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+        if not f.endswith((".cu", ".cuh", ".h")):
+            continue
+        if (kind == "gemm" and f not in GEMM_SOURCES) or (kind == "rows" and f == GEMM_SOURCES[0]):
+            continue
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -90,7 +114,8 @@ def recorded_traffic(kernel_name: str) -> float | None:
     except (OSError, ValueError):
         return None
     ent = rec.get(kernel_name)
-    if not ent or ent.get("kernel_source_digest") != kernel_source_digest():
+    kind = "gemm" if kernel_name.startswith("consumer") else "rows"
+    if not ent or ent.get("kernel_source_digest") != kernel_source_digest(kind):
         return None
     return float(ent["dram_bytes_per_launch"])
 
@@ -331,6 +356,79 @@ def other_workloads(dev, stream) -> dict:
     total, each = time_launches(mx, 50, stream)
     us = statistics.mean(each) * 1e3
     out["mxfp4_m8192"] = {"us_per_call": round(us, 2), "GBps": round(mx_bytes(M, H) / us / 1e3, 1)}
+    out["quant_placement"] = consumer_placements(dev)
+    return out
+
+
+# The consumer of the input RMSNorm in the DeepSeek-V3 MLA block: the fused
+# q_a + kv_a (+ rope) projection, 7168 -> 1536 + 576 = 2112 outputs.
+CONSUMER_N, CONSUMER_K = 2112, 7168
+
+
+def consumer_setup(dev, M: int):
+    """Inputs and outputs of the two placements of the MXFP4 activation quant
+    for M tokens: step functions (taking a stream handle) for the fused path,
+    the prequant path and the GEMM alone."""
+    import torch
+    from mxfp4_activation_quant_gb300 import rmsq, synth
+    K, N = CONSUMER_K, CONSUMER_N
+    w = synth.Workload("consumer", "mxfp4", M=M, H=K, seed=41, group=32, x_dist="student_t3")
+    d = {k: v.to(dev) for k, v in synth.make_inputs(w).items()}
+    b_q, b_s = synth.mxfp4_weights(42, N, K)
+    gb, tb = b_q.to(dev), rmsq.mx_scale_tiles(b_s.to(dev))
+    q = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    st = torch.zeros(rmsq.mma_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    ro = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+    def quant(s):
+        rmsq.add_rmsnorm_quant_mxfp4_mma_scales_into(d["x"], d["gamma"], d["residual"], q, st, ro, stream=s)
+
+    def gemm(s):
+        rmsq.mxfp4_gemm(q, st, gb, tb, out=D, stream=s)
+
+    def norm(s):
+        rmsq.add_rmsnorm(d["x"], d["gamma"], d["residual"], out=y, out_residual=ro, stream=s)
+
+    def pre(s):
+        rmsq.a16wfp4_gemm(y, gb, tb, out=D, stream=s)
+
+    return {"fused": lambda s: (quant(s), gemm(s)), "prequant": lambda s: (norm(s), pre(s)),
+            "quant": quant, "gemm": gemm, "norm": norm, "prequant_gemm": pre}
+
+
+def time_on_side_stream(dev, fn, reps: int) -> float:
+    """Microseconds per call of fn(stream_handle), replayed from a CUDA graph of
+    `reps` calls on a side stream (launch-free, as a serving step would run)."""
+    import torch
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn(side.cuda_stream)
+    torch.cuda.synchronize()
+    return time_graph(lambda: fn(side.cuda_stream), reps, side) * 1e3 / reps
+
+
+def consumer_placements(dev, Ms=(4, 64, 8192)) -> dict:
+    """Fused norm + MXFP4 quant followed by the block-scaled GEMM, against the
+    norm alone followed by the GEMM that quantises its bf16 input itself
+    ("prequant"): microseconds per step for each token count, and the GEMM's
+    own time and tensor throughput."""
+    from mxfp4_activation_quant_gb300 import rmsq
+    out = {"shape": f"tokens x 7168 (residual add + RMSNorm) -> MXFP4 -> x [{CONSUMER_N}, {CONSUMER_K}]^T "
+                    "MXFP4 weights, bf16 out",
+           "timing": "CUDA graph replay, inputs partly L2-resident across calls"}
+    for M in Ms:
+        f = consumer_setup(dev, M)
+        reps = 20 if M >= 4096 else 100
+        r = {k: round(time_on_side_stream(dev, fn, reps), 2) for k, fn in f.items()}
+        r["gemm_tflops"] = round(2.0 * M * CONSUMER_N * CONSUMER_K / r["gemm"] / 1e6, 1)
+        r["faster"] = "fused" if r["fused"] <= r["prequant"] else "prequant"
+        out[f"M{M}"] = r
+        if rmsq.sync_status(dev) != 0:
+            raise RuntimeError("a GEMM kernel reported a timed-out wait")
     return out
 
 
@@ -550,6 +648,89 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
 
 
+def run_consumer(args) -> None:
+    """--workload consumer: the block-scaled MXFP4 GEMM that consumes the fused
+    quant's output, timed alone at M=8192 tokens (tensor roofline), with both
+    placements of the quant reported beside it."""
+    import torch
+
+    from mxfp4_activation_quant_gb300 import build as lib_build
+    from mxfp4_activation_quant_gb300 import rmsq, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib_build.build()
+    M, N, K = args.rows or 8192, CONSUMER_N, CONSUMER_K
+    f = consumer_setup(dev, M)
+    stream = torch.cuda.current_stream(dev)
+    f["quant"](stream.cuda_stream)
+    step = lambda: f["gemm"](stream.cuda_stream)
+    sampler = ClockSampler(gpu_id_for(dev))
+    time.sleep(0.25)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    total_ms, each = time_launches(step, args.steps, stream)
+    clocks = sampler.stop()
+    if rmsq.sync_status(dev) != 0:
+        raise RuntimeError("the GEMM reported a timed-out wait")
+    flops = 2.0 * M * N * K
+    value = flops * args.steps / (total_ms * 1e-3) / 1e12
+    achieved = flops / (statistics.mean(each) * 1e-3) / 1e12
+    peak, peak_kind = measured_fp4_peak()
+    # end to end: A codes + scale tiles in from pinned host memory, D out
+    a_q = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+    a_t = torch.empty(rmsq.mma_scale_bytes(M, K), dtype=torch.uint8, device=dev)
+    (q, t), _ = rmsq.add_rmsnorm_quant_mxfp4_mma_scales(*[synth.make_inputs(synth.Workload(
+        "consumer", "mxfp4", M=M, H=K, seed=41, group=32, x_dist="student_t3"))[k].to(dev)
+        for k in ("x", "gamma", "residual")])
+    hq, ht = q.cpu().pin_memory(), t.cpu().pin_memory()
+    b_q, b_s = synth.mxfp4_weights(42, N, K)
+    gb, tb = b_q.to(dev), rmsq.mx_scale_tiles(b_s.to(dev))
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    hD = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+
+    def e2e():
+        a_q.copy_(hq, non_blocking=True)
+        a_t.copy_(ht, non_blocking=True)
+        rmsq.mxfp4_gemm(a_q, a_t, gb, tb, out=D)
+        hD.copy_(D, non_blocking=True)
+    for _ in range(2):
+        e2e()
+    e2e_steps = max(3, min(20, args.steps))
+    e2e_ms, _ = time_launches(e2e, e2e_steps, stream)
+    cpu = None
+    if not args.no_cpu:
+        from oracle import oracle
+        rows = 8
+        s_q, s_s = synth.mxfp4_weights(43, rows, K, 124, 131)     # activation-like MXFP4 rows
+        t0 = time.perf_counter()
+        oracle.mxfp4_gemm(s_q.numpy(), s_s.numpy(), b_q.numpy(), b_s.numpy())
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(2.0 * rows * N * K / dt / 1e12, 6), "unit": "TFLOP/s",
+               "cores": oracle.default_threads(), "kind": "oracle",
+               "sample": f"{rows} of the {M} token rows x all {N} outputs (exact fp64 sums)"}
+    line = {
+        "metric": "block-scaled MXFP4 GEMM TFLOP/s (consumer of the fused quant)", "value": round(value, 1),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
+        "config": {"workload": f"D[{M},{N}] = A[{M},{K}] B[{N},{K}]^T, A and B MXFP4 (E2M1, E8M0 per 32), "
+                               "bf16 out; A from the fused norm + quant", "M": M, "N": N, "K": K,
+                   "l2": "operands (37 MB) L2-resident across back-to-back calls",
+                   "timing": "K back-to-back calls"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic("consumer:gemm"), "peak_kind": peak_kind},
+        "e2e": {"value": round(flops * e2e_steps / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": hq.numel() + ht.numel(), "d2h_bytes_per_step": hD.numel() * 2},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "quant_placement": None if args.no_extra else consumer_placements(dev),
+    }
+    print(json.dumps(line))
+
+
 WORKLOAD_TEXT = {
     "prefill": "prefill input RMSNorm: M={M} H=7168 bf16, residual add, FP8 E4M3 1x128 groups, "
                "fp32 scales [M,56], keep_bf16 y",
@@ -577,8 +758,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--kernel", choices=["auto", "rows", "persistent"], default="auto")
-    ap.add_argument("--workload", choices=["prefill", "decode", "qknorm", "mxfp4"], default=WORKLOAD,
-                    help="the timed step (the headline line is prefill)")
+    ap.add_argument("--workload", choices=["prefill", "decode", "qknorm", "mxfp4", "consumer"], default=WORKLOAD,
+                    help="the timed step (the headline line is prefill; consumer: the MXFP4 GEMM)")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / qknorm / MXFP4 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
@@ -592,6 +773,8 @@ def main() -> None:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "consumer":
+        run_consumer(args)
     else:
         run_ours(args)
 

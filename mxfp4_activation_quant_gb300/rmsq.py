@@ -406,6 +406,17 @@ def a16wfp4_gemm(a: torch.Tensor, b_q: torch.Tensor, b_scale_tiles: torch.Tensor
     return d
 
 
+def add_rmsnorm_quant_mxfp4_mma_scales_into(x, gamma, residual, q, scale_tiles, res_out=None, y=None,
+                                            eps: float = 1e-6, stream: int | None = None) -> None:
+    """As add_rmsnorm_quant_mxfp4_mma_scales, writing into caller-allocated outputs."""
+    ldx = _rows_view(x, "x")
+    M, H = x.shape
+    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    st = _stream(x.device) if stream is None else stream
+    _check(lib().rmsq_add_rmsnorm_quant_mxfp4_mma_scales(_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H,
+                                                         _ptr(q), _ptr(scale_tiles), _ptr(res_out), _ptr(y), st))
+
+
 def sync_status(device=None) -> int:
     """Synchronises the current stream and returns the library status word's verdict."""
     dev = torch.device("cuda") if device is None else torch.device(device)
