@@ -277,8 +277,10 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
 /*
  * Optional control of the GEMM launch (NULL = defaults), for tests and
  * tuning; results do not depend on it.
- *   bn             rows of B per CTA tile: 64, 128 or 256; 0 = auto (the
- *                  largest that still gives at least one tile per SM, else 64)
+ *   bn             rows of B per CTA tile: 64, 128 or 256; 0 = auto (256 for
+ *                  the prequant GEMM, which quantises A once per B tile; for
+ *                  the plain GEMM 256 once that gives half the SMs a tile,
+ *                  else 128 with two or more 128-row tiles of A, else 64)
  *   ksplit         CTAs, launched as one thread-block cluster, that split K
  *                  for each tile and add their fp32 partial sums through
  *                  distributed shared memory (rank order, so deterministic):

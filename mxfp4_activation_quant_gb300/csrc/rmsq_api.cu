@@ -506,18 +506,19 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     unsigned int *status = status_word_ptr(dev);
     if (!status)
         return fail(RMSQ_ERR_CUDA, "status word address unavailable");
-    // Tiles: the widest B tile that still gives every SM a tile; with fewer
-    // tiles than SMs, narrow 64-row B tiles and K split over a cluster of up
-    // to 8 CTAs (each at least one K stage) fill the GPU.
+    // Tile width, from measurements on GB300 (N = 2112, K = 7168): the
+    // prequant kernel quantises A once per B tile, so it always takes the
+    // widest tile; the plain GEMM takes 256-row B tiles once they give at
+    // least half the SMs a tile, 128 from two row tiles of A on, and 64 for a
+    // single row tile (decode). With fewer tiles than SMs, K is split over a
+    // cluster of up to 8 CTAs (each at least one K stage).
     const int sms = sm_count();
     int bn = o.bn;
     if (!bn) {
-        bn = 64;
-        for (int c : {256, 128})
-            if (m_tiles * ((N + c - 1) / c) >= sms) {
-                bn = c;
-                break;
-            }
+        if (prequant || m_tiles * ((N + 255) / 256) * 2 >= sms)
+            bn = 256;
+        else
+            bn = m_tiles >= 2 ? 128 : 64;
     }
     const int64_t tiles = m_tiles * ((N + bn - 1) / bn);
     int ksplit = o.ksplit;

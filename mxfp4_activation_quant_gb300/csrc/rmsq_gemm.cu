@@ -15,10 +15,11 @@
 // One CTA computes a 128 x BN tile (BN = 64, 128 or 256): the MMA's M = 128
 // rows of A, N = BN rows of B. K advances in stages of 256 elements = 128
 // bytes per row, one 128-byte swizzle span, i.e. four MMAs of K = 64.
-// Warp roles (256 threads): warp 0 lane 0 issues the TMA and bulk loads;
-// warp 1 owns the tensor memory and its lane 0 issues tcgen05.cp (scale
-// factors, shared -> tensor memory) and tcgen05.mma; warps 4-7 quantise A
-// (prequant) and then run the epilogue (tcgen05.ld -> bf16 -> global).
+// Warp roles (256 threads): warp 0 issues the TMA and bulk loads; warp 1
+// owns the tensor memory and issues tcgen05.cp (scale factors, shared ->
+// tensor memory) and tcgen05.mma (one elected lane each); warps 4-7 run the
+// epilogue (tcgen05.ld -> bf16 -> global). The prequant kernel has 384
+// threads: warps 4-11 quantise A and then share the epilogue.
 // Every mbarrier wait is bounded; a wait that runs out sets the status word,
 // makes the other roles stop, drains what is in flight and frees the tensor
 // memory before the CTA exits.
@@ -49,7 +50,10 @@ namespace {
 constexpr int kBM = 128;          // MMA M: rows of A per tile
 constexpr int kStageBytes = 128;  // bytes of one operand row per stage (256 E2M1)
 constexpr int kStageK = 256;      // K elements per stage
-constexpr int kGemmThreads = 256;
+// 8 warps; the prequant kernel has 4 more, so that 8 warps quantise A
+template <bool PREQUANT>
+constexpr int gemm_threads() { return PREQUANT ? 384 : 256; }
+constexpr int kQuantThreads = 256;   // warps 4-11 of the prequant kernel
 
 constexpr int pow2_at_least(int v)
 {
@@ -262,9 +266,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 
 // ---------------------------------------------------- prequant (A in bf16)
 
-// The 128 threads of warps 4-7 quantise the valid rows R of the A tile for
-// each of this CTA's K stages. Item i = t + 128 j of a stage is 16-byte vector
-// (i % 32) of row (i / 32): warp w takes rows w, w + 4, ..., a row's 32 lanes
+// The 256 threads of warps 4-11 quantise the valid rows R of the A tile for
+// each of this CTA's K stages. Item i = t + 256 j of a stage is 16-byte vector
+// (i % 32) of row (i / 32): warp w takes rows w, w + 8, ..., a row's 32 lanes
 // read its 512 contiguous bytes, and the 4 lanes of a 32-element group find
 // the group's amax with two shuffles. The arithmetic is the fused kernel's:
 // X from the group's largest magnitude, elements times 2^-X (exact),
@@ -282,9 +286,9 @@ template <int STAGES, int AB, int OFF_SFA>
 __device__ __forceinline__ bool prequant_loop(const GemmParams &p, int64_t m0, int R, int ks0, int KL,
                                               uint8_t *smem, uint64_t *full, uint64_t *empty, volatile int *abort)
 {
-    const int t = threadIdx.x - 128;
+    const int t = threadIdx.x - 128;          // 0 .. kQuantThreads - 1
     const int w = t >> 5, vec = t & 31, g = vec >> 2;
-    const int NI = (R + 3) >> 2;                       // items per thread per stage
+    const int NI = (R + 7) >> 3;                       // items per thread per stage
     const int total = KL * NI;
     const int ch = min(8, (STAGES - 2) * NI + 1);      // items per chunk
     const uint4 *base = p.a_bf16 + m0 * p.lda_v + vec;
@@ -294,7 +298,7 @@ __device__ __forceinline__ bool prequant_loop(const GemmParams &p, int64_t m0, i
         int i = c0 / NI, j = c0 - i * NI;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int row = w + 4 * j;
+            const int row = w + 8 * j;
             const bool ok = u < ch && c0 + u < total && row < R;
             v[u] = ok ? __ldg(base + row * p.lda_v + (int64_t)(ks0 + i) * (kStageK / 8)) : make_uint4(0, 0, 0, 0);
             if (++j == NI) {
@@ -336,7 +340,7 @@ __device__ __forceinline__ bool prequant_loop(const GemmParams &p, int64_t m0, i
             int i = ic, j = jc;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int row = w + 4 * j;
+                const int row = w + 8 * j;
                 const int s = i % STAGES;
                 const bool ok = u < ch && c0 + u < total && row < R;
                 const int X = mx_exponent_from_bits(am[u]);
@@ -401,7 +405,7 @@ __device__ __forceinline__ float4 ld_peer_f4(const float *local, uint32_t rank)
 // ------------------------------------------------------------------ kernel
 
 template <int BN, bool PREQUANT>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     mxfp4_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                       const __grid_constant__ CUtensorMap map_b)
 {
@@ -433,7 +437,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(full + s)),
-                         "r"(PREQUANT ? 1 + 128 : 1));
+                         "r"(PREQUANT ? 1 + kQuantThreads : 1));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(empty + s)));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(accum)));
@@ -550,8 +554,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         __syncwarp();
     } else if (warp >= 4) {
-        const int q = warp - 4;              // lane quarter of tensor memory this warp may access
+        const int q = warp & 3;              // lane quarter of tensor memory this warp may access
         const int r = q * 32 + lane;         // row of the tile
+        // prequant: warps 4-7 and 8-11 share the epilogue by column halves
+        const int c_lo = (PREQUANT && warp >= 8) ? BN / 2 : 0;
+        const int c_hi = (PREQUANT && warp < 8) ? BN / 2 : BN;
         const int64_t m = m0 + r;
         bool ok = true;
         if (PREQUANT)
@@ -565,7 +572,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // operand ring is free now), padded rows against bank conflicts
             float *red = (float *)smem + r * (BN + 4);
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
                 uint32_t acc[32];
                 tmem_ld32(trow + c0, acc);
                 if (r >= R)
@@ -604,7 +611,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         cluster_sync();
         const int units = R * (BN / 4);
         const int u0 = (int)((int64_t)units * kz / p.ksplit), u1 = (int)((int64_t)units * (kz + 1) / p.ksplit);
-        for (int u = u0 + (int)threadIdx.x; u < u1; u += kGemmThreads) {
+        for (int u = u0 + (int)threadIdx.x; u < u1; u += (int)blockDim.x) {
             const int row = u / (BN / 4), c = (u - row * (BN / 4)) * 4;
             if (n0 + c >= p.N)
                 continue;
@@ -691,14 +698,14 @@ cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUte
         attr[dev] = true;
     }
     if (p.ksplit == 1) {
-        mxfp4_gemm_kernel<BN, PRE><<<dim3(n_tiles, m_tiles, 1), kGemmThreads, C::kSmem, st>>>(p, ma, mb);
+        mxfp4_gemm_kernel<BN, PRE><<<dim3(n_tiles, m_tiles, 1), gemm_threads<PRE>(), C::kSmem, st>>>(p, ma, mb);
         return cudaGetLastError();
     }
     // the CTAs that split one tile's K form a cluster (they exchange partial
     // sums through distributed shared memory)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_tiles, m_tiles, p.ksplit);
-    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.blockDim = dim3(gemm_threads<PRE>(), 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute cl[1];

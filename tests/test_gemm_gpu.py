@@ -143,12 +143,13 @@ def test_placements_agree_and_match_oracle(oracle_mod, M):
     b_q, b_s = synth.mxfp4_weights(22, N, K)
     gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
     (a_q, a_tiles), r1 = rmsq.add_rmsnorm_quant_mxfp4_mma_scales(g["x"], g["gamma"], g["residual"])
-    fused = rmsq.mxfp4_gemm(a_q, a_tiles, gb, tb)
+    fused = rmsq.mxfp4_gemm(a_q, a_tiles, gb, tb)                       # library's own tile choice
     y, r2 = rmsq.add_rmsnorm(g["x"], g["gamma"], g["residual"])
-    pre = rmsq.a16wfp4_gemm(y, gb, tb)
+    same = rmsq.GemmOpts(bn=256)                                         # equal tiles and K split
+    pre = rmsq.a16wfp4_gemm(y, gb, tb, opts=same)
     torch.cuda.synchronize()
     assert torch.equal(r1, r2)
-    assert torch.equal(fused, pre), "the two placements differ"
+    assert torch.equal(rmsq.mxfp4_gemm(a_q, a_tiles, gb, tb, opts=same), pre), "the two placements differ"
     ref_q = oracle_mod.add_rmsnorm_quant_mxfp4(d_cpu["x"], d_cpu["residual"], d_cpu["gamma"])
     boundary = ref_q["margin"] < parity.BOUNDARY
     assert np.array_equal(parity.u16(y)[~boundary], ref_q["y"][~boundary])
@@ -172,7 +173,7 @@ def test_full_size_sampled(oracle_mod):
     y, _ = rmsq.add_rmsnorm(g["x"], g["gamma"], g["residual"])
     pre = rmsq.a16wfp4_gemm(y, gb, tb)
     torch.cuda.synchronize()
-    assert torch.equal(fused, pre)
+    assert torch.equal(fused, pre)          # both choose 256-row tiles and no K split here
     rows = [0, 1, 127, 128, 4095, 5000, 8190, 8191]
     sub = {k: (v[rows] if v.dim() == 2 else v) for k, v in d_cpu.items()}
     ref_q = oracle_mod.add_rmsnorm_quant_mxfp4(sub["x"], sub["residual"], sub["gamma"])
