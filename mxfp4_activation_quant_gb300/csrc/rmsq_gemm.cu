@@ -96,6 +96,7 @@ struct GemmParams {
     int32_t b_row_tiles;        // ceil(N / 128): 128-row scale tiles that exist for B
     int32_t a_box_rows;         // rows of A per TMA box: 128, or M rounded up to 8 when M < 128
     int32_t ksplit;             // CTAs of a cluster that split K (1 = no split)
+    int32_t debug_skip_stage;   // test hook: the loads of this local stage are never issued (-1 = off)
     int64_t wait_limit_ns;
     unsigned int *status;
 };
@@ -456,6 +457,7 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_sf = tmem + BN;   // scale-factor columns follow the accumulator
+    int issued = 0;                       // warp 0: stages whose loads were issued
 
     if (warp == 0) {
         // ---------------------------------------------------------- loads
@@ -468,12 +470,15 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
             atoms += (bt0 + t < p.b_row_tiles);
         const uint32_t tx = b_tx + atoms * 1024u +
                             (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kStageBytes + C::kSfaBytes));
-        int issued = 0;
         for (int i = 0; i < KL; ++i) {
             const int ks = ks0 + i, s = i % C::kStages;
             const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
             if (!warp_wait(saddr(empty + s), ph ^ 1u, abort, p))
                 break;
+            if (i == p.debug_skip_stage) {   // test hook: this stage never arrives
+                issued = i + 1;
+                continue;
+            }
             if (elect_one()) {
                 const uint32_t fb = saddr(full + s);
                 mbar_arrive_tx(fb, tx);
@@ -491,17 +496,6 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
             }
             __syncwarp();
             issued = i + 1;
-        }
-        if (*abort && lane == 0) {
-            // let the copies already issued land before the CTA goes away
-            // (one deadline for all of them)
-            const uint64_t t0 = gtimer();
-            for (int i = (issued > C::kStages ? issued - C::kStages : 0); i < issued; ++i) {
-                const uint32_t fb = saddr(full + i % C::kStages);
-                const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
-                while (!mbar_test(fb, ph) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
-                }
-            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -633,6 +627,20 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     // ------------------------------------------------------------ teardown
     tc_fence_before();
     __syncthreads();
+    if (*abort && threadIdx.x == 0) {
+        // every role has stopped, so the abort is final: let the copies this
+        // CTA issued and nobody consumed land before it goes away (one
+        // deadline for all of them)
+        const uint64_t t0 = gtimer();
+        for (int i = (issued > C::kStages ? issued - C::kStages : 0); i < issued; ++i) {
+            if (i == p.debug_skip_stage)
+                continue;
+            const uint32_t fb = saddr(full + i % C::kStages);
+            const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+            while (!mbar_test(fb, ph) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
+            }
+        }
+    }
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
@@ -738,6 +746,7 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
     // rest of the tile keeps whatever it held and feeds only discarded rows.
     p.a_box_rows = g.M >= kBM ? kBM : (int32_t)((g.M + 7) / 8 * 8);
     p.ksplit = g.ksplit;
+    p.debug_skip_stage = g.debug_skip_stage;
     if (p.ksplit < 1 || p.ksplit > 8 || p.ksplit > p.k_stages)
         return cudaErrorInvalidValue;
     p.wait_limit_ns = g.wait_limit_ns;

@@ -58,6 +58,7 @@ struct GemmLaunch {
     int64_t M, N, K;
     int bn;                    // 64, 128 or 256
     int ksplit;                // 1..8 CTAs (a cluster) per tile splitting K
+    int debug_skip_stage;      // test hook (-1 = off): a K stage whose loads are never issued
     int64_t wait_limit_ns;
     unsigned int *status;
 };

@@ -125,8 +125,11 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 
 def test_gemm_opts_layout_matches_header():
-    assert ctypes.sizeof(rmsq.GemmOpts) == 16
+    # int32 bn, ksplit; int64 wait_limit_ns; int32 debug_skip_stage, reserved
+    assert ctypes.sizeof(rmsq.GemmOpts) == 24
     assert rmsq.GemmOpts.wait_limit_ns.offset == 8
+    assert rmsq.GemmOpts.debug_skip_stage.offset == 16
+    assert rmsq.GemmOpts().debug_skip_stage == -1
 
 
 A_Q, A_S, B_Q, B_S, D = (BASE + i * (1 << 32) for i in range(5))

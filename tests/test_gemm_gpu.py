@@ -183,3 +183,27 @@ def test_full_size_sampled(oracle_mod):
     st = parity.compare_gemm(got, {k: v[keep] for k, v in ref.items()}, K, what="full size")
     assert rmsq.sync_status() == 0
     print(st)
+
+
+@pytest.mark.parametrize("pre,ksplit", [(False, 1), (False, 2), (True, 1)])
+def test_bounded_wait_reports_timeout(oracle_mod, pre, ksplit):
+    """A stage whose loads are never issued (test hook) makes a wait run
+    out: the kernel stops, drains and frees its tensor memory, the host reads
+    RMSQ_ERR_TIMEOUT, and the next GEMM on the same context is correct."""
+    M, N, K = 128, 256, 1024
+    a_q, a_s, b_q, b_s = operands(61, M, N, K)
+    ga, ta = a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV))
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    stuck = rmsq.GemmOpts(bn=128, ksplit=ksplit, wait_limit_ns=50_000_000, debug_skip_stage=1)
+    if pre:
+        y = synth.random_bf16(62, (M, K)).to(DEV)
+        rmsq.a16wfp4_gemm(y, gb, tb, opts=stuck)
+    else:
+        rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=stuck)
+    assert rmsq.sync_status() == 5                      # RMSQ_ERR_TIMEOUT
+    assert rmsq.sync_status() == 0                      # read and cleared
+    d = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=128, ksplit=ksplit))
+    torch.cuda.synchronize()
+    ref = oracle_mod.mxfp4_gemm(a_q.numpy(), a_s.numpy(), b_q.numpy(), b_s.numpy())
+    parity.compare_gemm(d, ref, K, what="after a timed-out launch")
+    assert rmsq.sync_status() == 0
