@@ -453,7 +453,7 @@ __global__ void mx_scale_tiles_kernel(const uint8_t *s, int64_t ld, int64_t R, i
     }
 }
 
-const rmsq_gemm_opts kDefaultGemmOpts = {0, 0, 0, -1, 0};
+const rmsq_gemm_opts kDefaultGemmOpts = {0, 0, 0, 0, 0};
 
 // Shared by both placements: a_q / ld_a (bytes) for MXFP4 A, a / ld_a
 // (elements) for bf16 A.
@@ -470,8 +470,8 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
         return fail(RMSQ_ERR_INVALID_ARG, "ksplit must be 0..8 (got %d)", o.ksplit);
     if (o.wait_limit_ns < 0)
         return fail(RMSQ_ERR_INVALID_ARG, "wait_limit_ns must be >= 0");
-    if (o.debug_skip_stage < -1)
-        return fail(RMSQ_ERR_INVALID_ARG, "debug_skip_stage must be >= -1");
+    if (o.debug_stall_stage < 0)
+        return fail(RMSQ_ERR_INVALID_ARG, "debug_stall_stage must be >= 0");
     if (K % 256)
         return fail(RMSQ_ERR_UNSUPPORTED, "K=%lld is not a multiple of 256", (long long)K);
     if (N % 8)
@@ -552,7 +552,7 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     g.K = K;
     g.bn = bn;
     g.ksplit = ksplit;
-    g.debug_skip_stage = o.debug_skip_stage;
+    g.debug_skip_stage = o.debug_stall_stage - 1;   // -1: off
     g.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
     g.status = status;
     cudaError_t e = launch_mxfp4_gemm(g, (cudaStream_t)stream);

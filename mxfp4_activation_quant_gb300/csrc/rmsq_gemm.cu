@@ -63,25 +63,39 @@ constexpr int pow2_at_least(int v)
     return p;
 }
 
-template <int BN>
+// A stage of the ring is kSpans K-spans of 256 elements (one 128-byte
+// swizzle span each: four MMAs of K = 64) behind ONE barrier phase. Measured
+// on GB300: a TMA completion phase costs ~0.25 us, serialised per SM,
+// whatever it carries (8 KB per phase gave 29 GB/s per CTA, 32 KB 80 GB/s,
+// and more phases in flight did not help), so stages carry as many bytes as
+// the ring allows -- except that the widest tile of the plain GEMM keeps a
+// deeper ring of single-span stages, which measured faster for it (M = 8192:
+// 65.7 us with 4 x 1 span against 86.7 us with 2 x 2 spans), while the
+// prequant kernel's widest tile takes 2 x 2 (8.7 against 11.9 us at 4
+// tokens, equal at 64 and more). 64-row tiles: 4 spans x 2 stages (6.1
+// against 6.8 us at 4 tokens); 128-row tiles: 2 spans x 3 stages.
+template <int BN, bool PRE = false>
 struct GemmCfg {
-    static constexpr int kStages = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-    static constexpr int kABytes = kBM * kStageBytes;
-    static constexpr int kBBytes = BN * kStageBytes;
-    static constexpr int kSfbAtoms = BN >= 128 ? BN / 128 : 1;   // 128-row scale tiles of B per stage chunk
-    static constexpr int kSfaBytes = 2 * 512;                    // two 128-element K chunks
-    static constexpr int kSfbBytes = kSfbAtoms * 2 * 512;
-    static constexpr int kSfCols = 8 + 8 * kSfbAtoms;            // scale-factor TMEM columns per stage
+    static constexpr int kSpans = BN == 64 ? 4 : (BN == 128 ? 2 : (PRE ? 2 : 1));
+    static constexpr int kStages = BN == 64 ? 2 : (BN == 128 ? 3 : (PRE ? 2 : 4));
+    static constexpr int kSfbAtoms = BN >= 128 ? BN / 128 : 1;   // 128-row scale tiles of B per K chunk
+    static constexpr int kSpanA = kBM * kStageBytes;             // A codes of one span (16 KB)
+    static constexpr int kSpanB = BN * kStageBytes;
+    static constexpr int kSpanAB = kSpanA + kSpanB;
+    static constexpr int kAB = kSpans * kSpanAB;                  // operand bytes of a stage
+    static constexpr int kSfaSpan = 2 * 512;                      // two 128-element K chunks
+    static constexpr int kSfbSpan = kSfbAtoms * 2 * 512;
+    static constexpr int kSfColsSpan = 8 + 8 * kSfbAtoms;        // scale-factor TMEM columns per span
+    static constexpr int kSfCols = kSpans * kSfColsSpan;          // ... per stage
     static constexpr int kTmemCols = pow2_at_least(BN + kStages * kSfCols);
-    static constexpr int kOffB = kABytes;
-    static constexpr int kAB = kABytes + kBBytes;
     static constexpr int kOffSfa = kStages * kAB;
-    static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
-    static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
+    static constexpr int kOffSfb = kOffSfa + kStages * kSpans * kSfaSpan;
+    static constexpr int kOffBar = kOffSfb + kStages * kSpans * kSfbSpan;
     static constexpr int kBarBytes = (2 * kStages + 2) * 8 + 16;
     static constexpr size_t kSmem = 1024 + kOffBar + kBarBytes;
     static_assert(kTmemCols <= 512, "tensor memory");
     static_assert(kSmem <= 232448, "shared memory");
+    static_assert(kBM * (BN + 4) * 4 <= kOffSfa, "split-K partials fit in the operand ring");
 };
 
 struct GemmParams {
@@ -268,65 +282,57 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 // ---------------------------------------------------- prequant (A in bf16)
 
 // The 256 threads of warps 4-11 quantise the valid rows R of the A tile for
-// each of this CTA's K stages. Item i = t + 256 j of a stage is 16-byte vector
+// each K span of this CTA. Item i = t + 256 j of a span is 16-byte vector
 // (i % 32) of row (i / 32): warp w takes rows w, w + 8, ..., a row's 32 lanes
 // read its 512 contiguous bytes, and the 4 lanes of a 32-element group find
 // the group's amax with two shuffles. The arithmetic is the fused kernel's:
 // X from the group's largest magnitude, elements times 2^-X (exact),
 // saturating round-to-nearest-even E2M1.
 //
-// A thread's items (NI per stage) run through its stages in order, in chunks
-// of up to 8: the next chunk's loads are issued before the current chunk is
-// processed (so with few rows, loads run several stages ahead), the waits
-// for the chunk's stage slots come before it and the arrivals after it, and
-// the chunk's items go through each step together without branches, which
-// lets their load -> shuffle -> convert chains overlap. A chunk spans at
-// most STAGES - 1 stages, so it never waits for a slot that only its own
-// arrivals could free.
-template <int STAGES, int AB, int OFF_SFA>
+// A thread's items of a stage (its spans x NI) go in chunks of up to 8 that
+// never cross a stage: the wait for the stage's slot comes before its first
+// chunk and the arrival after its last, and the next chunk's loads (possibly
+// the next stage's) are issued before the current chunk is processed. The
+// chunk's items go through each step together without branches, so their
+// load -> shuffle -> convert chains overlap.
+template <int BN>
 __device__ __forceinline__ bool prequant_loop(const GemmParams &p, int64_t m0, int R, int ks0, int KL,
                                               uint8_t *smem, uint64_t *full, uint64_t *empty, volatile int *abort)
 {
+    using C = GemmCfg<BN, true>;
     const int t = threadIdx.x - 128;          // 0 .. kQuantThreads - 1
     const int w = t >> 5, vec = t & 31, g = vec >> 2;
-    const int NI = (R + 7) >> 3;                       // items per thread per stage
-    const int total = KL * NI;
-    const int ch = min(8, (STAGES - 2) * NI + 1);      // items per chunk
+    const int NI = (R + 7) >> 3;              // items per thread per span
+    const int NST = (KL + C::kSpans - 1) / C::kSpans;
     const uint4 *base = p.a_bf16 + m0 * p.lda_v + vec;
+    auto items = [&](int j) { return min(C::kSpans, KL - j * C::kSpans) * NI; };
     uint4 cur[8], nxt[8];
 
-    auto load_chunk = [&](int c0, uint4 (&v)[8]) {
-        int i = c0 / NI, j = c0 - i * NI;
+    auto load_chunk = [&](int j, int c0, uint4 (&v)[8]) {
+        const int n = items(j);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int row = w + 8 * j;
-            const bool ok = u < ch && c0 + u < total && row < R;
-            v[u] = ok ? __ldg(base + row * p.lda_v + (int64_t)(ks0 + i) * (kStageK / 8)) : make_uint4(0, 0, 0, 0);
-            if (++j == NI) {
-                j = 0;
-                ++i;
-            }
+            const int idx = c0 + u, sp = idx / NI, row = w + 8 * (idx - sp * NI);
+            const bool ok = idx < n && row < R;
+            v[u] = ok ? __ldg(base + row * p.lda_v + (int64_t)(ks0 + j * C::kSpans + sp) * (kStageK / 8))
+                      : make_uint4(0, 0, 0, 0);
         }
     };
 
-    load_chunk(0, cur);
-    for (int c0 = 0; c0 < total; c0 += ch) {
-        if (c0 + ch < total)
-            load_chunk(c0 + ch, nxt);
-        const int ic = c0 / NI, jc = c0 - ic * NI;
-        // slots of the stages this chunk starts
-        {
-            int i = ic, j = jc;
-            for (int u = 0; u < ch && c0 + u < total; ++u) {
-                if (j == 0 && !warp_wait(saddr(empty + i % STAGES), ((uint32_t)(i / STAGES) & 1u) ^ 1u, abort, p))
-                    return false;
-                if (++j == NI) {
-                    j = 0;
-                    ++i;
-                }
-            }
+    int j = 0, c0 = 0;
+    if (NST > 0)
+        load_chunk(0, 0, cur);
+    while (j < NST) {
+        const int n = items(j), s = j % C::kStages;
+        int jn = j, cn = c0 + 8;
+        if (cn >= n) {
+            jn = j + 1;
+            cn = 0;
         }
-        // the chunk's items, step by step
+        if (jn < NST)
+            load_chunk(jn, cn, nxt);
+        if (c0 == 0 && !warp_wait(saddr(empty + s), ((uint32_t)(j / C::kStages) & 1u) ^ 1u, abort, p))
+            return false;
         uint32_t am[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -337,49 +343,33 @@ __device__ __forceinline__ bool prequant_loop(const GemmParams &p, int64_t m0, i
 #pragma unroll
         for (int u = 0; u < 8; ++u)
             am[u] = max(am[u], __shfl_xor_sync(0xffffffffu, am[u], 2));
-        {
-            int i = ic, j = jc;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int row = w + 8 * j;
-                const int s = i % STAGES;
-                const bool ok = u < ch && c0 + u < total && row < R;
-                const int X = mx_exponent_from_bits(am[u]);
-                const float2 mult = f2(__uint_as_float((uint32_t)(127 - X) << 23));   // 2^-X
-                const uint4 v = cur[u];
-                const uint32_t codes =
-                    e2m1x8(mul2(unpack_bf16x2(v.x), mult), mul2(unpack_bf16x2(v.y), mult),
-                           mul2(unpack_bf16x2(v.z), mult), mul2(unpack_bf16x2(v.w), mult));
-                if (ok) {
-                    *reinterpret_cast<uint32_t *>(smem + s * AB + row * kStageBytes + ((g ^ (row & 7)) << 4) +
-                                                  (vec & 3) * 4) = codes;
-                    if ((vec & 3) == 0)        // scale tile g/4: (row % 32) * 16 + (row / 32) * 4 + g % 4
-                        smem[OFF_SFA + s * 1024 + (g >> 2) * 512 + (row & 31) * 16 + (row >> 5) * 4 + (g & 3)] =
-                            (uint8_t)(X + 127);
-                }
-                if (++j == NI) {
-                    j = 0;
-                    ++i;
-                }
+        for (int u = 0; u < 8; ++u) {
+            const int idx = c0 + u, sp = idx / NI, row = w + 8 * (idx - sp * NI);
+            const bool ok = idx < n && row < R;
+            const int X = mx_exponent_from_bits(am[u]);
+            const float2 mult = f2(__uint_as_float((uint32_t)(127 - X) << 23));   // 2^-X
+            const uint4 v = cur[u];
+            const uint32_t codes = e2m1x8(mul2(unpack_bf16x2(v.x), mult), mul2(unpack_bf16x2(v.y), mult),
+                                          mul2(unpack_bf16x2(v.z), mult), mul2(unpack_bf16x2(v.w), mult));
+            if (ok) {
+                uint8_t *sA = smem + s * C::kAB + sp * C::kSpanAB;
+                *reinterpret_cast<uint32_t *>(sA + row * kStageBytes + ((g ^ (row & 7)) << 4) + (vec & 3) * 4) =
+                    codes;
+                if ((vec & 3) == 0)            // scale tile g/4: (row % 32) * 16 + (row / 32) * 4 + g % 4
+                    smem[C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan + (g >> 2) * 512 + (row & 31) * 16 +
+                         (row >> 5) * 4 + (g & 3)] = (uint8_t)(X + 127);
             }
         }
-        // stages this chunk completes
-        {
-            int i = ic, j = jc;
-            for (int u = 0; u < ch && c0 + u < total; ++u) {
-                if (j == NI - 1) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    mbar_arrive(saddr(full + i % STAGES));
-                }
-                if (++j == NI) {
-                    j = 0;
-                    ++i;
-                }
-            }
+        if (c0 + 8 >= n) {                     // the stage's last chunk
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(saddr(full + s));
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
             cur[u] = nxt[u];
+        j = jn;
+        c0 = cn;
     }
     return true;
 }
@@ -410,7 +400,7 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     mxfp4_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                       const __grid_constant__ CUtensorMap map_b)
 {
-    using C = GemmCfg<BN>;
+    using C = GemmCfg<BN, PREQUANT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *full = (uint64_t *)(smem + C::kOffBar);
@@ -459,43 +449,54 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     const uint32_t tmem_sf = tmem + BN;   // scale-factor columns follow the accumulator
     int issued = 0;                       // warp 0: stages whose loads were issued
 
+    const int NST = (KL + C::kSpans - 1) / C::kSpans;            // stages of this CTA
     if (warp == 0) {
         // ---------------------------------------------------------- loads
         // The whole warp runs the loop (its values stay warp-uniform) and one
         // elected lane issues the copies.
-        const uint32_t b_tx = C::kBBytes;
         const int bt0 = (int)(n0 >> 7);                           // first 128-row scale tile of B
         int atoms = 0;
         for (int t = 0; t < C::kSfbAtoms; ++t)
             atoms += (bt0 + t < p.b_row_tiles);
-        const uint32_t tx = b_tx + atoms * 1024u +
-                            (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kStageBytes + C::kSfaBytes));
-        for (int i = 0; i < KL; ++i) {
-            const int ks = ks0 + i, s = i % C::kStages;
-            const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
-            if (!warp_wait(saddr(empty + s), ph ^ 1u, abort, p))
-                break;
-            if (i == p.debug_skip_stage) {   // test hook: this stage never arrives
-                issued = i + 1;
-                continue;
-            }
-            if (elect_one()) {
-                const uint32_t fb = saddr(full + s);
-                mbar_arrive_tx(fb, tx);
-                uint8_t *stage = smem + s * C::kAB;
+        const uint32_t span_tx = C::kSpanB + atoms * 1024u +
+                                 (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kStageBytes + C::kSfaSpan));
+        auto issue = [&](int j) {            // one stage's copies, by the elected lane
+            if (j == p.debug_skip_stage)     // test hook: this stage never arrives
+                return;
+            const int s = j % C::kStages, nsp = min(C::kSpans, KL - j * C::kSpans);
+            const uint32_t fb = saddr(full + s);
+            mbar_arrive_tx(fb, span_tx * nsp);
+            for (int sp = 0; sp < nsp; ++sp) {
+                const int ks = ks0 + j * C::kSpans + sp;
+                uint8_t *a_dst = smem + s * C::kAB + sp * C::kSpanAB;
                 if (!PREQUANT) {
-                    tma_2d(saddr(stage), &map_a, ks * kStageBytes, (int)m0, fb);
-                    bulk_g2s(saddr(smem + C::kOffSfa + s * C::kSfaBytes),
+                    tma_2d(saddr(a_dst), &map_a, ks * kStageBytes, (int)m0, fb);
+                    bulk_g2s(saddr(smem + C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan),
                              p.a_scale + ((int64_t)m_tile * (2 * KS) + 2 * ks) * 512, 1024, fb);
                 }
-                tma_2d(saddr(stage + C::kOffB), &map_b, ks * kStageBytes, (int)n0, fb);
+                tma_2d(saddr(a_dst + C::kSpanA), &map_b, ks * kStageBytes, (int)n0, fb);
                 for (int t = 0; t < C::kSfbAtoms; ++t)
                     if (bt0 + t < p.b_row_tiles)
-                        bulk_g2s(saddr(smem + C::kOffSfb + s * C::kSfbBytes + t * 1024),
+                        bulk_g2s(saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan + t * 1024),
                                  p.b_scale + ((int64_t)(bt0 + t) * (2 * KS) + 2 * ks) * 512, 1024, fb);
             }
+        };
+        // The first pass over the ring finds every slot free: issue it back
+        // to back; then one stage per freed slot.
+        const int first = NST < C::kStages ? NST : C::kStages;
+        if (elect_one())
+            for (int j = 0; j < first; ++j)
+                issue(j);
+        __syncwarp();
+        issued = first;
+        for (int j = first; j < NST; ++j) {
+            const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
+            if (!warp_wait(saddr(empty + j % C::kStages), ph ^ 1u, abort, p))
+                break;
+            if (elect_one())
+                issue(j);
             __syncwarp();
-            issued = i + 1;
+            issued = j + 1;
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -504,31 +505,33 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
         // a 64-row B tile sits in the lower or upper half of its 128-row scale tile
         const uint32_t sfb_row_col = (BN == 64) ? (uint32_t)(((n0 >> 6) & 1) * 2) : 0u;
         bool any = false;
-        for (int i = 0; i < KL; ++i) {
-            const int s = i % C::kStages;
-            const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+        for (int j = 0; j < NST; ++j) {
+            const int s = j % C::kStages, nsp = min(C::kSpans, KL - j * C::kSpans);
+            const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
             if (!warp_wait(saddr(full + s), ph, abort, p))
                 break;
             tc_fence_after();
-            const uint32_t sfa_col = tmem_sf + s * C::kSfCols;
-            const uint32_t sfb_col = sfa_col + 8;
-            const uint32_t sfa_smem = saddr(smem + C::kOffSfa + s * C::kSfaBytes);
-            const uint32_t sfb_smem = saddr(smem + C::kOffSfb + s * C::kSfbBytes);
-            const uint32_t a_smem = saddr(smem + s * C::kAB), b_smem = a_smem + C::kOffB;
             if (elect_one()) {
+                for (int sp = 0; sp < nsp; ++sp) {
+                    const uint32_t sfa_col = tmem_sf + s * C::kSfCols + sp * C::kSfColsSpan;
+                    const uint32_t sfb_col = sfa_col + 8;
+                    const uint32_t sfa_smem = saddr(smem + C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan);
+                    const uint32_t sfb_smem = saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan);
+                    const uint32_t a_smem = saddr(smem + s * C::kAB + sp * C::kSpanAB), b_smem = a_smem + C::kSpanA;
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    cp_sf(sfa_col + 4 * j, desc_sf(sfa_smem + j * 512));
+                    for (int c = 0; c < 2; ++c) {
+                        cp_sf(sfa_col + 4 * c, desc_sf(sfa_smem + c * 512));
 #pragma unroll
-                    for (int t = 0; t < C::kSfbAtoms; ++t)
-                        cp_sf(sfb_col + 4 * C::kSfbAtoms * j + 4 * t, desc_sf(sfb_smem + t * 1024 + j * 512));
-                }
+                        for (int t = 0; t < C::kSfbAtoms; ++t)
+                            cp_sf(sfb_col + 4 * C::kSfbAtoms * c + 4 * t, desc_sf(sfb_smem + t * 1024 + c * 512));
+                    }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int j = k >> 1;
-                    mma_mxf4(tmem, desc_sw128(a_smem + 32 * k), desc_sw128(b_smem + 32 * k),
-                             idesc_mxf4(BN, (k & 1) * 2), sfa_col + 4 * j,
-                             sfb_col + 4 * C::kSfbAtoms * j + sfb_row_col, (i | k) != 0);
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = k >> 1;
+                        mma_mxf4(tmem, desc_sw128(a_smem + 32 * k), desc_sw128(b_smem + 32 * k),
+                                 idesc_mxf4(BN, (k & 1) * 2), sfa_col + 4 * c,
+                                 sfb_col + 4 * C::kSfbAtoms * c + sfb_row_col, (j | sp | k) != 0);
+                    }
                 }
                 mma_commit(saddr(empty + s));
             }
@@ -556,7 +559,7 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
         const int64_t m = m0 + r;
         bool ok = true;
         if (PREQUANT)
-            ok = prequant_loop<C::kStages, C::kAB, C::kOffSfa>(p, m0, R, ks0, KL, smem, full, empty, abort);
+            ok = prequant_loop<BN>(p, m0, R, ks0, KL, smem, full, empty, abort);
         // ------------------------------------------------------- epilogue
         if (ok && warp_wait(saddr(accum), 0, abort, p)) {
             tc_fence_after();
@@ -690,7 +693,7 @@ template <int BN, bool PRE>
 cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int m_tiles,
                           int n_tiles, cudaStream_t st)
 {
-    using C = GemmCfg<BN>;
+    using C = GemmCfg<BN, PRE>;
     static bool attr[128];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

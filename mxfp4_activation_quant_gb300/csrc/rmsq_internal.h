@@ -58,7 +58,8 @@ struct GemmLaunch {
     int64_t M, N, K;
     int bn;                    // 64, 128 or 256
     int ksplit;                // 1..8 CTAs (a cluster) per tile splitting K
-    int debug_skip_stage;      // test hook (-1 = off): a K stage whose loads are never issued
+    int debug_skip_stage;      // test hook: a local K stage whose loads are never issued (-1 = off;
+                               // a zero-initialised GemmLaunch must set it)
     int64_t wait_limit_ns;
     unsigned int *status;
 };

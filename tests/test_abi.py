@@ -125,11 +125,12 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 
 def test_gemm_opts_layout_matches_header():
-    # int32 bn, ksplit; int64 wait_limit_ns; int32 debug_skip_stage, reserved
+    # int32 bn, ksplit; int64 wait_limit_ns; int32 debug_stall_stage, reserved
     assert ctypes.sizeof(rmsq.GemmOpts) == 24
     assert rmsq.GemmOpts.wait_limit_ns.offset == 8
-    assert rmsq.GemmOpts.debug_skip_stage.offset == 16
-    assert rmsq.GemmOpts().debug_skip_stage == -1
+    assert rmsq.GemmOpts.debug_stall_stage.offset == 16
+    # zero-initialised options are the defaults (the hook is off)
+    assert bytes(rmsq.GemmOpts()) == bytes(24)
 
 
 A_Q, A_S, B_Q, B_S, D = (BASE + i * (1 << 32) for i in range(5))

@@ -190,11 +190,11 @@ def test_bounded_wait_reports_timeout(oracle_mod, pre, ksplit):
     """A stage whose loads are never issued (test hook) makes a wait run
     out: the kernel stops, drains and frees its tensor memory, the host reads
     RMSQ_ERR_TIMEOUT, and the next GEMM on the same context is correct."""
-    M, N, K = 128, 256, 1024
+    M, N, K = 128, 256, 2048           # at least two stages in every CTA
     a_q, a_s, b_q, b_s = operands(61, M, N, K)
     ga, ta = a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV))
     gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
-    stuck = rmsq.GemmOpts(bn=128, ksplit=ksplit, wait_limit_ns=50_000_000, debug_skip_stage=1)
+    stuck = rmsq.GemmOpts(bn=128, ksplit=ksplit, wait_limit_ns=50_000_000, debug_stall_stage=2)
     if pre:
         y = synth.random_bf16(62, (M, K)).to(DEV)
         rmsq.a16wfp4_gemm(y, gb, tb, opts=stuck)
