@@ -38,6 +38,7 @@
 //     + g copied by tcgen05.cp .32x128b.warpx4 (rows r % 32 -> lanes, the
 //     same data in all four lane quarters).
 #include <cuda.h>
+#include <cstdarg>
 #include <cstdio>
 
 #include "rmsq.h"
@@ -46,6 +47,25 @@
 
 namespace rmsq {
 namespace {
+
+// One MXFP4 GEMM launch: D[M, N] bf16 = A B^T (see rmsq_gemm.cu). A is
+// either MXFP4 codes + tiled scales (a_q, a_scale; lda in bytes) or bf16
+// (a_bf16; lda in elements, quantised in the kernel's prologue).
+struct GemmLaunch {
+    const void *a_q, *a_scale, *a_bf16;
+    int64_t lda;
+    const void *b_q, *b_scale;
+    int64_t ldb;               // bytes
+    void *d;
+    int64_t ldd;               // elements
+    int64_t M, N, K;
+    int bn;                    // 64, 128 or 256
+    int ksplit;                // 1..8 CTAs (a cluster) per tile splitting K
+    int debug_skip_stage;      // test hook: a local K stage whose loads are never issued (-1 = off;
+                               // a zero-initialised GemmLaunch must set it)
+    int64_t wait_limit_ns;
+    unsigned int *status;
+};
 
 constexpr int kBM = 128;          // MMA M: rows of A per tile
 constexpr int kStageBytes = 128;  // bytes of one operand row per stage (256 E2M1)
@@ -729,8 +749,6 @@ cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUte
     return cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<BN, PRE>, p, ma, mb);
 }
 
-}  // namespace
-
 cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
 {
     GemmParams p{};
@@ -777,4 +795,209 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
 
 bool tensor_map_encoder_available() { return encode_fn() != nullptr; }
 
+// --------------------------------------------------------- host checks
+
+rmsq_status failf(rmsq_status s, const char *fmt, ...)
+{
+    char msg[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(msg, sizeof msg, fmt, ap);
+    va_end(ap);
+    return set_error(s, msg);
+}
+
+struct Range {
+    uintptr_t lo, hi;
+};
+
+Range mat_range(const void *p, int64_t M, int64_t H, int64_t ld, int64_t elem)
+{
+    uintptr_t lo = (uintptr_t)p;
+    return Range{lo, lo + (uintptr_t)(((M - 1) * ld + H) * elem)};
+}
+
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+// ------------------------------------------------------------ consumer GEMM
+
+__global__ void mx_scale_tiles_kernel(const uint8_t *s, int64_t ld, int64_t R, int64_t G, uint8_t *out,
+                                      int64_t total, int64_t ktiles, uint8_t fill)
+{
+    for (int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; o < total;
+         o += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = o >> 9;
+        const int w = (int)(o & 511);
+        const int r = ((w & 15) >> 2) * 32 + (w >> 4), c = w & 3;   // inverse of (r%32)*16 + (r/32)*4 + c
+        const int64_t row = (tile / ktiles) * 128 + r, g = (tile % ktiles) * 4 + c;
+        out[o] = (row < R && g < G) ? s[row * ld + g] : fill;
+    }
+}
+
+const rmsq_gemm_opts kDefaultGemmOpts = {0, 0, 0, 0, 0};
+
+// Shared by both placements: a_q / ld_a (bytes) for MXFP4 A, a / ld_a
+// (elements) for bf16 A.
+rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *a_scale, const void *b_q,
+                        int64_t ld_b, const void *b_scale, void *d, int64_t ld_d, int64_t M, int64_t N,
+                        int64_t K, void *stream, const rmsq_gemm_opts *opts)
+{
+    const rmsq_gemm_opts o = opts ? *opts : kDefaultGemmOpts;
+    if (M < 0 || N < 0 || K <= 0)
+        return set_error(RMSQ_ERR_INVALID_ARG, "need M >= 0, N >= 0, K > 0");
+    if (o.bn != 0 && o.bn != 64 && o.bn != 128 && o.bn != 256)
+        return failf(RMSQ_ERR_INVALID_ARG, "bn must be 0, 64, 128 or 256 (got %d)", o.bn);
+    if (o.ksplit < 0 || o.ksplit > 8)
+        return failf(RMSQ_ERR_INVALID_ARG, "ksplit must be 0..8 (got %d)", o.ksplit);
+    if (o.wait_limit_ns < 0)
+        return failf(RMSQ_ERR_INVALID_ARG, "wait_limit_ns must be >= 0");
+    if (o.debug_stall_stage < 0)
+        return failf(RMSQ_ERR_INVALID_ARG, "debug_stall_stage must be >= 0");
+    if (K % 256)
+        return failf(RMSQ_ERR_UNSUPPORTED, "K=%lld is not a multiple of 256", (long long)K);
+    if (N % 8)
+        return failf(RMSQ_ERR_UNSUPPORTED, "N=%lld is not a multiple of 8", (long long)N);
+    if (M == 0 || N == 0)
+        return clear_error();
+    if (!a || !b_q || !b_scale || !d || (!prequant && !a_scale))
+        return failf(RMSQ_ERR_INVALID_ARG, "operand, scale and output pointers are required");
+    const int64_t a_row_bytes = prequant ? K * 2 : K / 2;
+    const int64_t lda_bytes = prequant ? ld_a * 2 : ld_a;
+    if (lda_bytes < a_row_bytes || ld_b < K / 2 || ld_d < N)
+        return failf(RMSQ_ERR_INVALID_ARG, "leading dimensions must cover a row");
+    if (!aligned(a, 16) || !aligned(b_q, 16) || !aligned(b_scale, 16) || !aligned(d, 16) ||
+        (!prequant && !aligned(a_scale, 16)) || lda_bytes % 16 || ld_b % 16 || ld_d % 8)
+        return failf(RMSQ_ERR_MISALIGNED,
+                    "operands, scale tiles and D need 16-byte aligned bases and 16-byte row pitches");
+    const int64_t m_tiles = (M + 127) / 128;
+    if (m_tiles > 65535)
+        return failf(RMSQ_ERR_UNSUPPORTED, "M=%lld exceeds %d rows", (long long)M, 65535 * 128);
+    const int64_t tile_bytes = (K / 128) * 512;
+    Range rd = mat_range(d, M, N, ld_d, 2);
+    Range ins[4] = {mat_range(a, M, a_row_bytes, lda_bytes, 1), mat_range(b_q, N, K / 2, ld_b, 1),
+                    mat_range(b_scale, 1, (N + 127) / 128 * tile_bytes, 0, 1), {0, 0}};
+    if (!prequant)
+        ins[3] = mat_range(a_scale, 1, m_tiles * tile_bytes, 0, 1);
+    for (const Range &r : ins)
+        if (r.hi > r.lo && overlaps(rd, r))
+            return failf(RMSQ_ERR_INVALID_ARG, "D overlaps an input");
+    if (!tensor_map_encoder_available())
+        return failf(RMSQ_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return failf(RMSQ_ERR_CUDA, "no current device");
+    unsigned int *status = device_status_word(dev);
+    if (!status)
+        return failf(RMSQ_ERR_CUDA, "status word address unavailable");
+    // Tile width, from measurements on GB300 (N = 2112, K = 7168): the
+    // prequant kernel quantises A once per B tile, so it always takes the
+    // widest tile; the plain GEMM takes 256-row B tiles once they give at
+    // least half the SMs a tile, 128 from two row tiles of A on, and 64 for a
+    // single row tile (decode). With fewer tiles than SMs, K is split over a
+    // cluster of up to 8 CTAs (each at least one K stage).
+    const int sms = device_sm_count();
+    int bn = o.bn;
+    if (!bn) {
+        if (prequant || m_tiles * ((N + 255) / 256) * 2 >= sms)
+            bn = 256;
+        else
+            bn = m_tiles >= 2 ? 128 : 64;
+    }
+    const int64_t tiles = m_tiles * ((N + bn - 1) / bn);
+    int ksplit = o.ksplit;
+    if (!ksplit) {
+        int64_t k = tiles >= sms ? 1 : sms / tiles;
+        if (k > 8)
+            k = 8;
+        if (k > K / 256)
+            k = K / 256;
+        ksplit = (int)(k < 1 ? 1 : k);
+    }
+    if (ksplit > K / 256)
+        return failf(RMSQ_ERR_INVALID_ARG, "ksplit=%d exceeds the %lld K stages", ksplit, (long long)(K / 256));
+    GemmLaunch g{};
+    if (prequant) {
+        g.a_bf16 = a;
+    } else {
+        g.a_q = a;
+        g.a_scale = a_scale;
+    }
+    g.lda = ld_a;
+    g.b_q = b_q;
+    g.b_scale = b_scale;
+    g.ldb = ld_b;
+    g.d = d;
+    g.ldd = ld_d;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.bn = bn;
+    g.ksplit = ksplit;
+    g.debug_skip_stage = o.debug_stall_stage - 1;   // -1: off
+    g.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
+    g.status = status;
+    cudaError_t e = launch_mxfp4_gemm(g, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return failf(RMSQ_ERR_CUDA, "GEMM launch failed: %s", cudaGetErrorString(e));
+    return clear_error();
+}
+
+}  // namespace
 }  // namespace rmsq
+
+using namespace rmsq;
+
+extern "C" {
+
+rmsq_status rmsq_mxfp4_gemm_ex(
+    const void *a_q, int64_t ld_a, const void *a_scale_tiles, const void *b_q, int64_t ld_b,
+    const void *b_scale_tiles, void *d, int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream,
+    const rmsq_gemm_opts *opts)
+{
+    return gemm_common(false, a_q, ld_a, a_scale_tiles, b_q, ld_b, b_scale_tiles, d, ld_d, M, N, K, stream,
+                       opts);
+}
+
+rmsq_status rmsq_mxfp4_gemm(
+    const void *a_q, int64_t ld_a, const void *a_scale_tiles, const void *b_q, int64_t ld_b,
+    const void *b_scale_tiles, void *d, int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream)
+{
+    return gemm_common(false, a_q, ld_a, a_scale_tiles, b_q, ld_b, b_scale_tiles, d, ld_d, M, N, K, stream,
+                       nullptr);
+}
+
+rmsq_status rmsq_a16wfp4_gemm_ex(
+    const void *a, int64_t ld_a, const void *b_q, int64_t ld_b, const void *b_scale_tiles, void *d,
+    int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream, const rmsq_gemm_opts *opts)
+{
+    return gemm_common(true, a, ld_a, nullptr, b_q, ld_b, b_scale_tiles, d, ld_d, M, N, K, stream, opts);
+}
+
+rmsq_status rmsq_a16wfp4_gemm(
+    const void *a, int64_t ld_a, const void *b_q, int64_t ld_b, const void *b_scale_tiles, void *d,
+    int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream)
+{
+    return gemm_common(true, a, ld_a, nullptr, b_q, ld_b, b_scale_tiles, d, ld_d, M, N, K, stream, nullptr);
+}
+
+rmsq_status rmsq_mx_scale_tiles(const uint8_t *scale, int64_t ld, int64_t R, int64_t G, uint8_t *out,
+                                uint8_t fill, void *stream)
+{
+    if (R < 0 || G <= 0 || ld < G)
+        return failf(RMSQ_ERR_INVALID_ARG, "need R >= 0, G > 0, ld >= G");
+    if (R == 0)
+        return clear_error();
+    if (!scale || !out)
+        return failf(RMSQ_ERR_INVALID_ARG, "scale and out are required");
+    const int64_t ktiles = (G + 3) / 4, total = (R + 127) / 128 * ktiles * 512;
+    if (overlaps(mat_range(out, 1, total, 0, 1), mat_range(scale, R, G, ld, 1)))
+        return failf(RMSQ_ERR_INVALID_ARG, "out overlaps scale");
+    int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+    mx_scale_tiles_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(scale, ld, R, G, out, total, ktiles, fill);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? clear_error() : failf(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+}
+
+}  // extern "C"

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "rmsq.h"
+
 namespace rmsq {
 
 // One tensor (a "segment") handled by a launch. A launch covers one segment,
@@ -45,27 +47,13 @@ struct BulkParams {
     unsigned int *status;     // device status word (set on a timed-out wait)
 };
 
-// One MXFP4 GEMM launch: D[M, N] bf16 = A B^T (see rmsq_gemm.cu). A is
-// either MXFP4 codes + tiled scales (a_q, a_scale; lda in bytes) or bf16
-// (a_bf16; lda in elements, quantised in the kernel's prologue).
-struct GemmLaunch {
-    const void *a_q, *a_scale, *a_bf16;
-    int64_t lda;
-    const void *b_q, *b_scale;
-    int64_t ldb;               // bytes
-    void *d;
-    int64_t ldd;               // elements
-    int64_t M, N, K;
-    int bn;                    // 64, 128 or 256
-    int ksplit;                // 1..8 CTAs (a cluster) per tile splitting K
-    int debug_skip_stage;      // test hook: a local K stage whose loads are never issued (-1 = off;
-                               // a zero-initialised GemmLaunch must set it)
-    int64_t wait_limit_ns;
-    unsigned int *status;
-};
-
-cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st);
-bool tensor_map_encoder_available();
+// Error reporting and device queries of the C-ABI layer (rmsq_api.cu), for
+// the GEMM's host code: set_error records the message of the failing call
+// on this host thread; the status word is the one bounded waits report to.
+rmsq_status set_error(rmsq_status s, const char *msg);
+rmsq_status clear_error();
+int device_sm_count();
+unsigned int *device_status_word(int dev);
 
 constexpr int kMaxThreads = 512;
 
