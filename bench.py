@@ -544,6 +544,67 @@ def make_e2e_step(run, M: int, inputs, outputs, chunks: int, dev):
     return step
 
 
+def make_e2e_step_packed(w, d_cpu, M: int, chunks: int, dev):
+    """End-to-end step of the FP8 prefill workload with each row chunk's
+    inputs (x rows, then residual rows) contiguous in one pinned host buffer
+    and its outputs (residual, y, E4M3 codes, scales) contiguous in another, so
+    that a chunk moves with one host->device and one device->host copy; chunks
+    rotate over three streams so that copies in both directions overlap the
+    kernels of other chunks. Returns (step, h2d_bytes, d2h_bytes)."""
+    import torch
+    from mxfp4_activation_quant_gb300 import rmsq
+    H, G = w.H, w.H // 128
+    in_row, out_row = 4 * H, 4 * H + H + 4 * G
+    bounds = [(M * i // chunks, M * (i + 1) // chunks) for i in range(chunks)]
+    host_in = torch.empty(M * in_row, dtype=torch.uint8).pin_memory()
+    xb = d_cpu["x"].contiguous().view(torch.uint8).view(M, 2 * H)
+    rb = d_cpu["residual"].contiguous().view(torch.uint8).view(M, 2 * H)
+    for r0, r1 in bounds:
+        seg = host_in[r0 * in_row:r1 * in_row].view(2, r1 - r0, 2 * H)
+        seg[0].copy_(xb[r0:r1])
+        seg[1].copy_(rb[r0:r1])
+    dev_in = torch.empty_like(host_in, device=dev)
+    dev_out = torch.empty(M * out_row, dtype=torch.uint8, device=dev)
+    host_out = torch.empty(M * out_row, dtype=torch.uint8).pin_memory()
+    gamma_h = d_cpu["gamma"].contiguous().pin_memory()
+    gamma_d = torch.empty_like(gamma_h, device=dev)
+    streams = [torch.cuda.current_stream(dev)] + [torch.cuda.Stream(dev) for _ in range(2)]
+
+    def views(r0, r1):
+        n = r1 - r0
+        i = dev_in[r0 * in_row:r1 * in_row]
+        o = dev_out[r0 * out_row:r1 * out_row]
+        bf = lambda t: t.view(torch.bfloat16).view(n, H)
+        x, res = bf(i[:2 * H * n]), bf(i[2 * H * n:])
+        ro, y = bf(o[:2 * H * n]), bf(o[2 * H * n:4 * H * n])
+        q = o[4 * H * n:5 * H * n].view(n, H)
+        sc = o[5 * H * n:].view(torch.float32).view(n, G)
+        return x, res, ro, y, q, sc
+    chunk_views = [views(r0, r1) for r0, r1 in bounds]
+
+    def step():
+        s0 = streams[0]
+        with torch.cuda.stream(s0):
+            gamma_d.copy_(gamma_h, non_blocking=True)
+        start = torch.cuda.Event()
+        start.record(s0)
+        for s in streams[1:]:
+            s.wait_event(start)
+        for c, (r0, r1) in enumerate(bounds):
+            s = streams[c % len(streams)]
+            x, res, ro, y, q, sc = chunk_views[c]
+            with torch.cuda.stream(s):
+                dev_in[r0 * in_row:r1 * in_row].copy_(host_in[r0 * in_row:r1 * in_row], non_blocking=True)
+                rmsq.add_rmsnorm_quant_fp8_into(x, gamma_d, res, q, sc, ro, y, eps=w.eps, stream=s.cuda_stream)
+                host_out[r0 * out_row:r1 * out_row].copy_(dev_out[r0 * out_row:r1 * out_row], non_blocking=True)
+        for s in streams[1:]:
+            e = torch.cuda.Event()
+            e.record(s)
+            s0.wait_event(e)
+
+    return step, host_in.numel() + gamma_h.numel() * 2, host_out.numel()
+
+
 def run_ours(args) -> None:
     import torch
     import torch.distributed as dist
@@ -598,7 +659,11 @@ def run_ours(args) -> None:
     # end to end through the public API: pinned host buffers, copies inside the
     # timed region, row chunks pipelined over three streams
     chunks = args.e2e_chunks if chunkable else 1
-    e2e_step = make_e2e_step(run, M, io_in, io_out, chunks, dev)
+    packed = w.kind == "fp8" and w.scale_layout == "row" and w.keep_bf16 and w.residual and chunkable
+    if packed:      # the headline workload: one copy each way per chunk
+        e2e_step, h2d_packed, d2h_packed = make_e2e_step_packed(rank_workload(w, rank), d_cpu, M, chunks, dev)
+    else:
+        e2e_step = make_e2e_step(run, M, io_in, io_out, chunks, dev)
     e2e_value = None
     if not args.no_e2e:
         e2e_steps = max(3, min(20, args.steps))
@@ -610,6 +675,8 @@ def run_ours(args) -> None:
         e2e_value = round(world * bytes_step * e2e_steps / (max_over_ranks(e2e_ms, world, dev) * 1e-3) / 1e9, 1)
     h2d = sum(hv.numel() * hv.element_size() for _, hv, _ in io_in)
     d2h = sum(hv.numel() * hv.element_size() for _, hv, _ in io_out)
+    if packed:
+        h2d, d2h = h2d_packed, d2h_packed
 
     headline = args.workload == WORKLOAD and not args.rows
     extra = other_workloads(dev, stream) if (rank == 0 and headline and not args.no_extra) else None
@@ -637,7 +704,9 @@ def run_ours(args) -> None:
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} HBM copy"},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "row_chunks": chunks, "streams": 3},
+                    "d2h_bytes_per_step": d2h, "row_chunks": chunks, "streams": 3,
+                    "copies": "one each way per chunk (packed chunk buffers)" if packed else
+                              "one per tensor and chunk"},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -763,7 +832,7 @@ def main() -> None:
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / qknorm / MXFP4 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
-    ap.add_argument("--e2e-chunks", type=int, default=8, help="row chunks pipelined in the e2e leg")
+    ap.add_argument("--e2e-chunks", type=int, default=24, help="row chunks pipelined in the e2e leg")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="replay the K timed steps from a CUDA graph (auto: decode and qknorm)")
     ap.add_argument("--rows", type=int, default=0,
