@@ -207,3 +207,30 @@ def test_bounded_wait_reports_timeout(oracle_mod, pre, ksplit):
     ref = oracle_mod.mxfp4_gemm(a_q.numpy(), a_s.numpy(), b_q.numpy(), b_s.numpy())
     parity.compare_gemm(d, ref, K, what="after a timed-out launch")
     assert rmsq.sync_status() == 0
+
+
+def test_strided_operands(oracle_mod):
+    """Leading dimensions wider than a row for A (codes and bf16), B and D."""
+    M, N, K = 150, 200, 768
+    a_q, a_s, b_q, b_s = operands(71, M, N, K)
+    pa = torch.zeros((M, K // 2 + 48), dtype=torch.uint8)
+    pa[:, :K // 2] = a_q
+    pb = torch.zeros((N, K // 2 + 80), dtype=torch.uint8)
+    pb[:, :K // 2] = b_q
+    ga, gb = pa.to(DEV)[:, :K // 2], pb.to(DEV)[:, :K // 2]
+    ta, tb = rmsq.mx_scale_tiles(a_s.to(DEV)), rmsq.mx_scale_tiles(b_s.to(DEV))
+    dbig = torch.zeros((M, N + 24), dtype=torch.bfloat16, device=DEV)
+    d = rmsq.mxfp4_gemm(ga, ta, gb, tb, out=dbig[:, :N])
+    torch.cuda.synchronize()
+    ref = oracle_mod.mxfp4_gemm(a_q.numpy(), a_s.numpy(), b_q.numpy(), b_s.numpy())
+    parity.compare_gemm(d, ref, K, what="strided A, B, D")
+    assert (dbig[:, N:] == 0).all()
+    # bf16 A with a wider row pitch, quantised in the GEMM
+    y_cpu = synth.random_bf16(72, (M, K + 64))
+    y = y_cpu.to(DEV)[:, :K]
+    same = rmsq.GemmOpts(bn=256)
+    pre = rmsq.a16wfp4_gemm(y, gb, tb, opts=same)
+    q, s = oracle_mod.group_quant_mxfp4(parity.u16(y_cpu[:, :K].contiguous()))
+    ref = oracle_mod.mxfp4_gemm(q, s, b_q.numpy(), b_s.numpy())
+    parity.compare_gemm(pre, ref, K, what="strided bf16 A")
+    assert rmsq.sync_status() == 0
