@@ -290,18 +290,19 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
  *                  differ between ksplit values in the last bits (both
  *                  placements agree bit for bit at equal ksplit and bn).
  *   wait_limit_ns  limit of every wait inside the kernel, 0 = 2 s
- *   debug_skip_stage  test hook: every CTA leaves the loads of this K stage
- *                  (counted within the CTA's share of K) unissued, so a wait
- *                  runs out; the kernel then stops, drains, frees its tensor
- *                  memory and sets the status word (rmsq_sync_status returns
- *                  RMSQ_ERR_TIMEOUT, D is incomplete); -1 = off. Zero-
- *                  initialised options must set it to -1.
+ *   debug_stall_stage  test hook, 0 = off (so zero-initialised options are
+ *                  the defaults): with s > 0 every CTA leaves the loads of its
+ *                  K stage s - 1 (counted within the CTA's share of K)
+ *                  unissued, so a wait runs out; the kernel then stops,
+ *                  drains, frees its tensor memory and sets the status word
+ *                  (rmsq_sync_status returns RMSQ_ERR_TIMEOUT, D is
+ *                  incomplete).
  */
 typedef struct rmsq_gemm_opts {
     int32_t bn;
     int32_t ksplit;
     int64_t wait_limit_ns;
-    int32_t debug_skip_stage;
+    int32_t debug_stall_stage;
     int32_t reserved;
 } rmsq_gemm_opts;
 
