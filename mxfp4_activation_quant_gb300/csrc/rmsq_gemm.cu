@@ -9,12 +9,15 @@
 // concurrency 4):
 //   * A already quantised -- codes [M, K/2] and scales in the MMA tile layout,
 //     as rmsq_add_rmsnorm_quant_mxfp4_mma_scales writes them -- loaded by TMA;
-//   * A in bf16 (prequant): four warps quantise every 128 x 256 stage of A into
-//     shared memory with the fused kernel's own group-32 rule.
+//   * A in bf16 (prequant): eight warps quantise each K span of A into shared
+//     memory with the fused kernel's own group-32 rule.
 //
 // One CTA computes a 128 x BN tile (BN = 64, 128 or 256): the MMA's M = 128
-// rows of A, N = BN rows of B. K advances in stages of 256 elements = 128
-// bytes per row, one 128-byte swizzle span, i.e. four MMAs of K = 64.
+// rows of A, N = BN rows of B. K advances in spans of 256 elements = 128
+// bytes per row (one 128-byte swizzle span, four MMAs of K = 64); a ring
+// stage holds one to four spans behind one barrier phase (GemmCfg). With
+// fewer tiles than SMs, the CTAs of a thread-block cluster split K and add
+// their fp32 partial sums through distributed shared memory, in rank order.
 // Warp roles (256 threads): warp 0 issues the TMA and bulk loads; warp 1
 // owns the tensor memory and issues tcgen05.cp (scale factors, shared ->
 // tensor memory) and tcgen05.mma (one elected lane each); warps 4-7 run the
@@ -48,9 +51,9 @@
 namespace rmsq {
 namespace {
 
-// One MXFP4 GEMM launch: D[M, N] bf16 = A B^T (see rmsq_gemm.cu). A is
-// either MXFP4 codes + tiled scales (a_q, a_scale; lda in bytes) or bf16
-// (a_bf16; lda in elements, quantised in the kernel's prologue).
+// One GEMM launch as the host checks leave it. A is either MXFP4 codes +
+// tiled scales (a_q, a_scale; lda in bytes) or bf16 (a_bf16; lda in
+// elements, quantised in the kernel).
 struct GemmLaunch {
     const void *a_q, *a_scale, *a_bf16;
     int64_t lda;
@@ -68,8 +71,8 @@ struct GemmLaunch {
 };
 
 constexpr int kBM = 128;          // MMA M: rows of A per tile
-constexpr int kStageBytes = 128;  // bytes of one operand row per stage (256 E2M1)
-constexpr int kStageK = 256;      // K elements per stage
+constexpr int kSpanBytes = 128;   // bytes of one operand row per span (256 E2M1)
+constexpr int kSpanK = 256;       // K elements per span
 // 8 warps; the prequant kernel has 4 more, so that 8 warps quantise A
 template <bool PREQUANT>
 constexpr int gemm_threads() { return PREQUANT ? 384 : 256; }
@@ -99,8 +102,8 @@ struct GemmCfg {
     static constexpr int kSpans = BN == 64 ? 4 : (BN == 128 ? 2 : (PRE ? 2 : 1));
     static constexpr int kStages = BN == 64 ? 2 : (BN == 128 ? 3 : (PRE ? 2 : 4));
     static constexpr int kSfbAtoms = BN >= 128 ? BN / 128 : 1;   // 128-row scale tiles of B per K chunk
-    static constexpr int kSpanA = kBM * kStageBytes;             // A codes of one span (16 KB)
-    static constexpr int kSpanB = BN * kStageBytes;
+    static constexpr int kSpanA = kBM * kSpanBytes;             // A codes of one span (16 KB)
+    static constexpr int kSpanB = BN * kSpanBytes;
     static constexpr int kSpanAB = kSpanA + kSpanB;
     static constexpr int kAB = kSpans * kSpanAB;                  // operand bytes of a stage
     static constexpr int kSfaSpan = 2 * 512;                      // two 128-element K chunks
@@ -126,7 +129,7 @@ struct GemmParams {
     uint16_t *d;                // bf16 [M, ldd]
     int64_t ldd;
     int64_t M, N;
-    int32_t k_stages;           // K / 256
+    int32_t k_spans;            // K / 256: spans of K (a ring stage holds one or more)
     int32_t b_row_tiles;        // ceil(N / 128): 128-row scale tiles that exist for B
     int32_t a_box_rows;         // rows of A per TMA box: 128, or M rounded up to 8 when M < 128
     int32_t ksplit;             // CTAs of a cluster that split K (1 = no split)
@@ -334,7 +337,7 @@ __device__ __forceinline__ bool prequant_loop(const GemmParams &p, int64_t m0, i
         for (int u = 0; u < 8; ++u) {
             const int idx = c0 + u, sp = idx / NI, row = w + 8 * (idx - sp * NI);
             const bool ok = idx < n && row < R;
-            v[u] = ok ? __ldg(base + row * p.lda_v + (int64_t)(ks0 + j * C::kSpans + sp) * (kStageK / 8))
+            v[u] = ok ? __ldg(base + row * p.lda_v + (int64_t)(ks0 + j * C::kSpans + sp) * (kSpanK / 8))
                       : make_uint4(0, 0, 0, 0);
         }
     };
@@ -374,7 +377,7 @@ __device__ __forceinline__ bool prequant_loop(const GemmParams &p, int64_t m0, i
                                           mul2(unpack_bf16x2(v.z), mult), mul2(unpack_bf16x2(v.w), mult));
             if (ok) {
                 uint8_t *sA = smem + s * C::kAB + sp * C::kSpanAB;
-                *reinterpret_cast<uint32_t *>(sA + row * kStageBytes + ((g ^ (row & 7)) << 4) + (vec & 3) * 4) =
+                *reinterpret_cast<uint32_t *>(sA + row * kSpanBytes + ((g ^ (row & 7)) << 4) + (vec & 3) * 4) =
                     codes;
                 if ((vec & 3) == 0)            // scale tile g/4: (row % 32) * 16 + (row / 32) * 4 + g % 4
                     smem[C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan + (g >> 2) * 512 + (row & 31) * 16 +
@@ -433,8 +436,8 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tile = blockIdx.x, m_tile = blockIdx.y;
     const int64_t m0 = (int64_t)m_tile * kBM, n0 = (int64_t)n_tile * BN;
-    // this CTA's stages of K: all of them, or its share when a cluster splits K
-    const int KS = p.k_stages;
+    // this CTA's spans of K: all of them, or its share when a cluster splits K
+    const int KS = p.k_spans;
     const int kz = (int)blockIdx.z;
     const int ks0 = (int)((int64_t)KS * kz / p.ksplit), KL = (int)((int64_t)KS * (kz + 1) / p.ksplit) - ks0;
     const int R = (int)min((int64_t)kBM, p.M - m0);    // rows of the tile that exist
@@ -479,7 +482,7 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
         for (int t = 0; t < C::kSfbAtoms; ++t)
             atoms += (bt0 + t < p.b_row_tiles);
         const uint32_t span_tx = C::kSpanB + atoms * 1024u +
-                                 (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kStageBytes + C::kSfaSpan));
+                                 (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kSpanBytes + C::kSfaSpan));
         auto issue = [&](int j) {            // one stage's copies, by the elected lane
             if (j == p.debug_skip_stage)     // test hook: this stage never arrives
                 return;
@@ -490,11 +493,11 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                 const int ks = ks0 + j * C::kSpans + sp;
                 uint8_t *a_dst = smem + s * C::kAB + sp * C::kSpanAB;
                 if (!PREQUANT) {
-                    tma_2d(saddr(a_dst), &map_a, ks * kStageBytes, (int)m0, fb);
+                    tma_2d(saddr(a_dst), &map_a, ks * kSpanBytes, (int)m0, fb);
                     bulk_g2s(saddr(smem + C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan),
                              p.a_scale + ((int64_t)m_tile * (2 * KS) + 2 * ks) * 512, 1024, fb);
                 }
-                tma_2d(saddr(a_dst + C::kSpanA), &map_b, ks * kStageBytes, (int)n0, fb);
+                tma_2d(saddr(a_dst + C::kSpanA), &map_b, ks * kSpanBytes, (int)n0, fb);
                 for (int t = 0; t < C::kSfbAtoms; ++t)
                     if (bt0 + t < p.b_row_tiles)
                         bulk_g2s(saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan + t * 1024),
@@ -702,7 +705,7 @@ bool make_code_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row
         return false;
     cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld};
-    cuuint32_t box[2] = {(cuuint32_t)kStageBytes, (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)kSpanBytes, (cuuint32_t)box_rows};
     cuuint32_t es[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -760,7 +763,7 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
     p.ldd = g.ldd;
     p.M = g.M;
     p.N = g.N;
-    p.k_stages = (int32_t)(g.K / kStageK);
+    p.k_spans = (int32_t)(g.K / kSpanK);
     p.b_row_tiles = (int32_t)((g.N + 127) / 128);
     // Rows of the A tile past M are never stored, so with fewer than 128
     // rows only those (rounded up to a swizzle atom of 8) are loaded; the
@@ -768,7 +771,7 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
     p.a_box_rows = g.M >= kBM ? kBM : (int32_t)((g.M + 7) / 8 * 8);
     p.ksplit = g.ksplit;
     p.debug_skip_stage = g.debug_skip_stage;
-    if (p.ksplit < 1 || p.ksplit > 8 || p.ksplit > p.k_stages)
+    if (p.ksplit < 1 || p.ksplit > 8 || p.ksplit > p.k_spans)
         return cudaErrorInvalidValue;
     p.wait_limit_ns = g.wait_limit_ns;
     p.status = g.status;
@@ -896,8 +899,10 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     // widest tile; the plain GEMM takes 256-row B tiles once they give at
     // least half the SMs a tile, 128 from two row tiles of A on, and 64 for a
     // single row tile (decode). With fewer tiles than SMs, K is split over a
-    // cluster of up to 8 CTAs (each at least one K stage).
+    // cluster of up to 8 CTAs (each at least one 256-element span of K).
     const int sms = device_sm_count();
+    if (sms <= 0)
+        return failf(RMSQ_ERR_CUDA, "SM count query failed");
     int bn = o.bn;
     if (!bn) {
         if (prequant || m_tiles * ((N + 255) / 256) * 2 >= sms)
@@ -916,7 +921,8 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
         ksplit = (int)(k < 1 ? 1 : k);
     }
     if (ksplit > K / 256)
-        return failf(RMSQ_ERR_INVALID_ARG, "ksplit=%d exceeds the %lld K stages", ksplit, (long long)(K / 256));
+        return failf(RMSQ_ERR_INVALID_ARG, "ksplit=%d exceeds the %lld 256-element spans of K", ksplit,
+                     (long long)(K / 256));
     GemmLaunch g{};
     if (prequant) {
         g.a_bf16 = a;
