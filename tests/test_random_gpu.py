@@ -1,0 +1,104 @@
+"""Seeded random shapes and options for every entry point, against the oracle.
+
+The hand-picked parity cases cover the workloads and the known edges; this
+sweep draws shapes, leading dimensions and launch options from a fixed seed
+so that combinations nobody picked (one token, eight output columns, a K
+split that leaves one span per CTA, ...) are exercised too. Same bars as
+tests/parity.py."""
+
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_activation_quant_gb300 import rmsq, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.fail("these tests need a CUDA GPU")
+
+
+def _rows(seed, M, H, var=1.0, pad=0, tensor="x"):
+    t = synth.random_bf16(seed, (M, H + pad), var=var, tensor=tensor)
+    return t, t[:, :H]
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_random_norm_quant(oracle_mod, case):
+    rng = np.random.default_rng(1000 + case)
+    M = int(rng.choice([1, 2, 3, 7, 33, 129, 300]))
+    H = int(rng.choice([128, 256, 640, 1024, 1536, 2048, 3072, 7168]))
+    pad = int(rng.choice([0, 8, 64]))
+    eps = float(rng.choice([1e-6, 1e-5, 0.0]))
+    use_res = bool(rng.integers(0, 2)) and eps != 0.0
+    x_full, x = _rows(2000 + case, M, H, pad=pad)
+    r_full, r = _rows(3000 + case, M, H, var=4.0, pad=pad, tensor="residual")
+    g = synth.gaussian_bf16(4000 + case, "gamma", (H,), mean=1.0, var=0.1)
+    if eps == 0.0:                       # no residual, and every row kept away from zero
+        x_full = x_full.clone()
+        x_full[:, 0] = 1.0
+        x = x_full[:, :H]
+    gx = x_full.to(DEV)[:, :H]
+    gr = r_full.to(DEV)[:, :H] if use_res else None
+    gg = g.to(DEV)
+    res = r if use_res else None
+    if rng.integers(0, 2):
+        layout = str(rng.choice(["row", "col", "col_pad4"]))
+        keep = bool(rng.integers(0, 2))
+        out, res_out = rmsq.add_rmsnorm_quant_fp8(gx, gg, gr, eps=eps, scale_layout=layout, keep_bf16=keep)
+        torch.cuda.synchronize()
+        ref = oracle_mod.add_rmsnorm_quant_fp8(x.contiguous(), None if res is None else res.contiguous(), g, eps,
+                                               layout=layout)
+        got = {"q": out[-2], "scale": out[-1], "residual_out": res_out, "y": out[0] if keep else None}
+        sc = got["scale"]
+        if layout == "col_pad4":           # compare the first M columns of the padded scale matrix
+            got["scale"] = sc[:, :M]
+            ref["scale"] = ref["scale"][:, :M]
+        parity.compare_fp8(got, ref, "col" if layout != "row" else "row", what=f"case {case}")
+    else:
+        if H % 32:
+            pytest.skip("MXFP4 needs H % 32 == 0")
+        keep = bool(rng.integers(0, 2))
+        out, res_out = rmsq.add_rmsnorm_quant_mxfp4(gx, gg, gr, eps=eps, keep_bf16=keep)
+        torch.cuda.synchronize()
+        ref = oracle_mod.add_rmsnorm_quant_mxfp4(x.contiguous(), None if res is None else res.contiguous(), g, eps)
+        got = {"q": out[-2], "scale": out[-1], "residual_out": res_out, "y": out[0] if keep else None}
+        parity.compare_mx(got, ref, what=f"case {case}")
+    assert rmsq.sync_status() == 0
+
+
+@pytest.mark.parametrize("case", range(48))
+def test_random_gemm(oracle_mod, case):
+    rng = np.random.default_rng(5000 + case)
+    M = int(rng.choice([1, 4, 8, 63, 128, 129, 257]))
+    N = int(rng.choice([8, 16, 64, 136, 256, 264, 520]))
+    K = 256 * int(rng.choice([1, 2, 3, 5, 8]))
+    bn = int(rng.choice([0, 64, 128, 256]))
+    ks_max = min(8, K // 256)
+    ksplit = int(rng.integers(0, ks_max + 1))
+    prequant = bool(rng.integers(0, 2))
+    b_q, b_s = synth.mxfp4_weights(6000 + case, N, K)
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    opts = rmsq.GemmOpts(bn=bn, ksplit=ksplit)
+    if prequant:
+        y = synth.random_bf16(7000 + case, (M, K))
+        d = rmsq.a16wfp4_gemm(y.to(DEV), gb, tb, opts=opts)
+        a_q, a_s = oracle_mod.group_quant_mxfp4(parity.u16(y))
+    else:
+        a_q_t, a_s_t = synth.mxfp4_weights(8000 + case, M, K, scale_lo=124, scale_hi=131)
+        d = rmsq.mxfp4_gemm(a_q_t.to(DEV), rmsq.mx_scale_tiles(a_s_t.to(DEV)), gb, tb, opts=opts)
+        a_q, a_s = a_q_t.numpy(), a_s_t.numpy()
+    torch.cuda.synchronize()
+    ref = oracle_mod.mxfp4_gemm(a_q, a_s, b_q.numpy(), b_s.numpy())
+    st = parity.compare_gemm(d, ref, K, what=f"case {case}: M={M} N={N} K={K} bn={bn} ksplit={ksplit} "
+                                              f"prequant={prequant}")
+    assert st["bit_equal_fraction"] > 0.95, st
+    assert rmsq.sync_status() == 0
