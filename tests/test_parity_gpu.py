@@ -490,3 +490,32 @@ def test_empty_batch_is_a_no_op():
     (mq, ms), _ = rmsq.add_rmsnorm_quant_mxfp4(x, g)
     torch.cuda.synchronize()
     assert q.shape == (0, 7168) and s.shape == (0, 56) and mq.shape == (0, 3584)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+def test_device_encoder_every_fp32_pattern(oracle_mod, fmt):
+    """All 2^32 fp32 bit patterns through the kernels' hardware conversion
+    (cvt.rn.satfinite) against the oracle's encoder, in 64 chunks, the oracle
+    threaded over the host cores. Non-NaN inputs must agree exactly; NaN
+    inputs (outside every workload) must give the E4M3 NaN code, and for
+    E2M1, which has no NaN, only their count of disagreements is reported."""
+    from concurrent.futures import ThreadPoolExecutor
+    enc_gpu = rmsq.encode_e4m3 if fmt == "e4m3" else rmsq.encode_e2m1
+    enc_cpu = oracle_mod.e4m3_encode if fmt == "e4m3" else oracle_mod.e2m1_encode
+    chunk = 1 << 26
+    bad, nan_diff, checked = 0, 0, 0
+    with ThreadPoolExecutor(max_workers=16) as ex:
+        for c in range(1 << 6):
+            v = np.arange(c * chunk, (c + 1) * chunk, dtype=np.uint64).astype(np.uint32).view(np.float32)
+            got = enc_gpu(torch.from_numpy(v).to(DEV)).cpu().numpy()
+            want = np.concatenate(list(ex.map(enc_cpu, np.array_split(v, 16))))
+            nan = np.isnan(v)
+            bad += int(((got != want) & ~nan).sum())
+            if fmt == "e4m3":
+                assert np.all((got[nan] & 0x7F) == 0x7F), "a NaN input did not give the NaN code"
+            else:
+                nan_diff += int(((got != want) & nan).sum())
+            checked += v.size
+    assert checked == 1 << 32
+    assert bad == 0, f"{bad} fp32 patterns encode differently"
+    print(fmt, "patterns checked:", checked, "NaN inputs encoded differently (E2M1 only):", nan_diff)
