@@ -102,3 +102,30 @@ def test_random_gemm(oracle_mod, case):
                                               f"prequant={prequant}")
     assert st["bit_equal_fraction"] > 0.95, st
     assert rmsq.sync_status() == 0
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_random_qknorm(oracle_mod, case):
+    rng = np.random.default_rng(9000 + case)
+    M = int(rng.choice([1, 5, 64, 257]))
+    mx = bool(rng.integers(0, 2))
+    unit = 32 if mx else 128
+    Hq = unit * int(rng.choice([4, 12, 16, 48]))
+    Hkv = unit * int(rng.choice([2, 4, 8]))
+    q_a = synth.random_bf16(9100 + case, (M, Hq), tensor="q_a")
+    kv_a = synth.random_bf16(9200 + case, (M, Hkv), var=2.0, tensor="kv_a")
+    gq = synth.gaussian_bf16(9300 + case, "gamma_q", (Hq,), mean=1.0, var=0.1)
+    gk = synth.gaussian_bf16(9400 + case, "gamma_kv", (Hkv,), mean=1.0, var=0.1)
+    keep = bool(rng.integers(0, 2))
+    fn = rmsq.qknorm_quant_mxfp4 if mx else rmsq.qknorm_quant_fp8
+    outq, outk = fn(q_a.to(DEV), kv_a.to(DEV), gq.to(DEV), gk.to(DEV), keep_bf16=keep)
+    torch.cuda.synchronize()
+    for out, x, g in ((outq, q_a, gq), (outk, kv_a, gk)):
+        got = {"q": out[-2], "scale": out[-1], "y": out[0] if keep else None}
+        if mx:
+            ref = oracle_mod.add_rmsnorm_quant_mxfp4(x, None, g)
+            parity.compare_mx(got, ref, what=f"qknorm case {case}")
+        else:
+            ref = oracle_mod.add_rmsnorm_quant_fp8(x, None, g)
+            parity.compare_fp8(got, ref, "row", what=f"qknorm case {case}")
+    assert rmsq.sync_status() == 0
