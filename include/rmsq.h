@@ -57,7 +57,8 @@ typedef enum rmsq_status {
     RMSQ_ERR_MISALIGNED = 2,    /* pointer or leading dimension alignment */
     RMSQ_ERR_UNSUPPORTED = 3,   /* valid but not implemented (e.g. group != 128 for FP8) */
     RMSQ_ERR_CUDA = 4,          /* a CUDA runtime call failed */
-    RMSQ_ERR_TIMEOUT = 5        /* a bounded device wait gave up (rmsq_sync_status) */
+    RMSQ_ERR_TIMEOUT = 5,       /* a bounded device wait gave up (rmsq_sync_status) */
+    RMSQ_ERR_BOUNDS = 6         /* debug build only: a store's index check failed (rmsq_sync_status) */
 } rmsq_status;
 
 typedef enum rmsq_scale_layout {
@@ -222,7 +223,9 @@ const char *rmsq_last_error(void);
  * Waits for `stream`, then reads and clears the library's device status
  * word on the current device. Returns RMSQ_ERR_TIMEOUT if a kernel launched
  * since the last read gave up a bounded wait (its outputs are then
- * incomplete), RMSQ_ERR_CUDA if the synchronisation failed, else RMSQ_OK.
+ * incomplete), RMSQ_ERR_BOUNDS if, in a library built with RMSQ_DEBUG, an
+ * index check before a store failed (the store was skipped),
+ * RMSQ_ERR_CUDA if the synchronisation failed, else RMSQ_OK.
  */
 rmsq_status rmsq_sync_status(void *stream);
 
@@ -337,6 +340,15 @@ rmsq_status rmsq_encode_e2m1(const float *in, uint8_t *out, int64_t n, void *str
  * must be zero). Enqueued on `stream`.
  */
 rmsq_status rmsq_check_group_division(unsigned long long *counts, void *stream);
+
+/*
+ * Positive control of the debug build's store checks: in a library built
+ * with RMSQ_DEBUG, enqueues a one-thread kernel whose single check fails on
+ * purpose (nothing is stored), so that the next rmsq_sync_status returns
+ * RMSQ_ERR_BOUNDS. In release builds it returns RMSQ_ERR_UNSUPPORTED and
+ * launches nothing.
+ */
+rmsq_status rmsq_debug_bounds_selftest(void *stream);
 
 #ifdef __cplusplus
 }

@@ -231,6 +231,21 @@ unsigned int *status_word_ptr(int dev)
     return ptrs[dev];
 }
 
+// Debug build: point the segment's bounds checks at the status word and
+// give them the scale buffer's capacity. Nothing in release builds.
+void debug_bind(Seg &s, int64_t scale_elems)
+{
+#ifdef RMSQ_DEBUG
+    int dev = 0;
+    cudaGetDevice(&dev);
+    s.debug_flag = status_word_ptr(dev);
+    s.scale_elems = scale_elems;
+#else
+    (void)s;
+    (void)scale_elems;
+#endif
+}
+
 rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_t st)
 {
     const int gv = mx ? 4 : 16;
@@ -307,6 +322,17 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
     return fail(RMSQ_ERR_INVALID_ARG, "unknown kernel %d", o.kernel);
 }
 
+// ------------------------------------------------ debug-build self-test
+
+#ifdef RMSQ_DEBUG
+__global__ void debug_bounds_selftest_kernel(unsigned int *flag, int64_t n)
+{
+    // an index equal to the extent: the check fails and the store is skipped
+    if (RMSQ_IN_BOUNDS(flag, n < n))
+        flag[0] |= 0u;
+}
+#endif
+
 // ------------------------------------------------------- encoder kernels
 
 __global__ void encode_e4m3_kernel(const float *in, uint8_t *out, int64_t n)
@@ -370,6 +396,8 @@ rmsq_status qknorm_common(bool mx, const void *q_a, int64_t ld_q, const void *kv
                       scale_layout, nullptr, out_q_bf16);
     Seg sk = make_seg(kv_a, ld_kv, nullptr, 0, gamma_kv, eps, M, Hkv, out_kv_q, out_kv_scale,
                       scale_layout, nullptr, out_kv_bf16);
+    debug_bind(sq, (Hq / group) * M);
+    debug_bind(sk, (Hkv / group) * M);
     // Team shapes: the compiled-in MLA pair shape when it fits exactly,
     // otherwise one vectors-per-thread value for both latents, least padding
     // first.
@@ -435,6 +463,7 @@ rmsq_status mxfp4_common(const void *x, int64_t ld_x, const void *residual, int6
     Seg s = make_seg(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q, out_scale, layout,
                      out_residual, out_bf16);
     s.scale_ld = ktiles;
+    debug_bind(s, sbytes);
     return launch_single(s, true, opts ? *opts : kDefaultOpts, (cudaStream_t)stream);
 }
 
@@ -461,6 +490,7 @@ const char *rmsq_status_string(rmsq_status s)
     case RMSQ_ERR_UNSUPPORTED: return "unsupported shape or option";
     case RMSQ_ERR_CUDA: return "CUDA error";
     case RMSQ_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case RMSQ_ERR_BOUNDS: return "a bounds check of the debug build failed";
     }
     return "unknown status";
 }
@@ -489,6 +519,7 @@ rmsq_status rmsq_add_rmsnorm_quant_group_fp8_ex(
     Seg s = make_seg(x, ld_x, residual, ld_res, gamma, eps, M, H, out_q, out_scale,
                      scale_layout == RMSQ_SCALE_ROW_MAJOR ? 0 : 1, out_residual, out_bf16);
     s.scale_ld = sld;
+    debug_bind(s, (H / group) * sld);
     return launch_single(s, false, opts ? *opts : kDefaultOpts, (cudaStream_t)stream);
 }
 
@@ -566,6 +597,7 @@ rmsq_status rmsq_add_rmsnorm(
         return st == RMSQ_OK ? ok() : st;
     Seg s = make_seg(x, ld_x, residual, ld_res, gamma, eps, M, H, nullptr, nullptr, 0, out_residual,
                      out_bf16);
+    debug_bind(s, 0);
     return launch_single(s, true, kDefaultOpts, (cudaStream_t)stream);
 }
 
@@ -580,9 +612,29 @@ rmsq_status rmsq_sync_status(void *stream)
         e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
     if (e != cudaSuccess)
         return fail(RMSQ_ERR_CUDA, "status word access failed: %s", cudaGetErrorString(e));
+    if (word & 4u)
+        return fail(RMSQ_ERR_BOUNDS, "a debug-build bounds check failed, the store was skipped (status 0x%x)", word);
     if (word)
         return fail(RMSQ_ERR_TIMEOUT, "a bounded wait gave up (status 0x%x)", word);
     return ok();
+}
+
+rmsq_status rmsq_debug_bounds_selftest(void *stream)
+{
+#ifdef RMSQ_DEBUG
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return fail(RMSQ_ERR_CUDA, "no current device");
+    unsigned int *status = status_word_ptr(dev);
+    if (!status)
+        return fail(RMSQ_ERR_CUDA, "status word address unavailable");
+    debug_bounds_selftest_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(status, 1);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ok() : fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+#else
+    (void)stream;
+    return fail(RMSQ_ERR_UNSUPPORTED, "the bounds checks exist only in the RMSQ_DEBUG build");
+#endif
 }
 
 rmsq_status rmsq_encode_e4m3(const float *in, uint8_t *out, int64_t n, void *stream)

@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kMaxThreads) bulk_kernel(const __grid_constant
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const int v = k * tpr + t;
-                if (!GUARD || v < nvec)
+                if ((!GUARD || v < nvec) && RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && v < nvec))
                     s.out_res[row * nv + v] = r[k];
             }
         }

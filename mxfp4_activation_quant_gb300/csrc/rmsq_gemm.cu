@@ -614,7 +614,8 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                         o.y = pack_bf16x2(__uint_as_float(acc[8 * v + 2]), __uint_as_float(acc[8 * v + 3]));
                         o.z = pack_bf16x2(__uint_as_float(acc[8 * v + 4]), __uint_as_float(acc[8 * v + 5]));
                         o.w = pack_bf16x2(__uint_as_float(acc[8 * v + 6]), __uint_as_float(acc[8 * v + 7]));
-                        *reinterpret_cast<uint4 *>(drow + c0 + 8 * v) = o;
+                        if (RMSQ_IN_BOUNDS(p.status, m < p.M && n0 + c0 + 8 * (v + 1) <= p.N))
+                            *reinterpret_cast<uint4 *>(drow + c0 + 8 * v) = o;
                     }
                 }
             }
@@ -644,8 +645,9 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                 acc.z += v.z;
                 acc.w += v.w;
             }
-            *reinterpret_cast<uint2 *>(p.d + (m0 + row) * p.ldd + n0 + c) =
-                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+            if (RMSQ_IN_BOUNDS(p.status, m0 + row < p.M && n0 + c + 4 <= p.N))
+                *reinterpret_cast<uint2 *>(p.d + (m0 + row) * p.ldd + n0 + c) =
+                    make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
         }
         cluster_sync();
     }

@@ -31,6 +31,10 @@ struct Seg {
     float eps;
     float inv_h;           // fp32 rounding of 1/H
     int64_t prefetch_rows; // row kernel: rows ahead whose x / residual are prefetched into L2 (0 = off)
+#ifdef RMSQ_DEBUG
+    unsigned int *debug_flag;   // status word; bounds checks of the debug build set bit 2
+    int64_t scale_elems;        // capacity of out_scale in elements
+#endif
 };
 
 struct LaunchParams {

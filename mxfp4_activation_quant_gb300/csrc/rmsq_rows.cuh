@@ -197,7 +197,7 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         uint4 *yrow = s.out_bf16 + row * nvec + t;
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
-            if (!GUARD || k * tpr + t < nvec)
+            if ((!GUARD || k * tpr + t < nvec) && RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && k * tpr + t < nvec))
                 yrow[k * tpr] = y[k];
     }
     if (!s.out_q)   // norm only (rmsq_add_rmsnorm)
@@ -234,7 +234,9 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
             if (leader) {
                 const int64_t g = v >> 4, G = s.H >> 7;
                 float *sc = (float *)s.out_scale;
-                sc[s.layout == 0 ? row * G + g : g * s.scale_ld + row] = scale;
+                const int64_t si = s.layout == 0 ? row * G + g : g * s.scale_ld + row;
+                if (RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && si < s.scale_elems))
+                    sc[si] = scale;
             }
             const GroupDivisor gd = make_group_divisor(d);
             float2 qv[4];
@@ -248,19 +250,23 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
                     qv[j] = make_float2(__fdiv_rn(bf_lo(yw[j]), d), __fdiv_rn(bf_hi(yw[j]), d));
             }
             const uint2 q = make_uint2(e4m3x4(qv[0], qv[1]), e4m3x4(qv[2], qv[3]));
-            reinterpret_cast<uint2 *>(s.out_q + row * (int64_t)s.H)[v] = q;
+            if (RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && v < nvec))
+                reinterpret_cast<uint2 *>(s.out_q + row * (int64_t)s.H)[v] = q;
         } else {
             const int X = mx_exponent_from_bits(am[k]);
             const float2 mult = f2(__uint_as_float((uint32_t)(127 - X) << 23));   // 2^-X
             if (leader) {
                 uint8_t *sc = (uint8_t *)s.out_scale;
                 const int64_t g = v >> 2;
-                sc[s.layout == 0 ? row * (int64_t)(s.H >> 5) + g : mma_scale_offset(row, g, s.scale_ld)] =
-                    (uint8_t)(X + 127);
+                const int64_t si =
+                    s.layout == 0 ? row * (int64_t)(s.H >> 5) + g : mma_scale_offset(row, g, s.scale_ld);
+                if (RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && si < s.scale_elems))
+                    sc[si] = (uint8_t)(X + 127);
             }
-            reinterpret_cast<uint32_t *>(s.out_q + row * (int64_t)(s.H >> 1))[v] =
-                e2m1x8(mul2(unpack_bf16x2(yw[0]), mult), mul2(unpack_bf16x2(yw[1]), mult),
-                       mul2(unpack_bf16x2(yw[2]), mult), mul2(unpack_bf16x2(yw[3]), mult));
+            if (RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && v < nvec))
+                reinterpret_cast<uint32_t *>(s.out_q + row * (int64_t)(s.H >> 1))[v] =
+                    e2m1x8(mul2(unpack_bf16x2(yw[0]), mult), mul2(unpack_bf16x2(yw[1]), mult),
+                           mul2(unpack_bf16x2(yw[2]), mult), mul2(unpack_bf16x2(yw[3]), mult));
         }
     }
 }
@@ -290,7 +296,7 @@ __device__ __forceinline__ void row_from_global(const Seg &s, int64_t row, int t
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             r[k] = add_bf16x8(xv[k], rv[k]);
-            if (!GUARD || k * tpr + t < nvec)
+            if ((!GUARD || k * tpr + t < nvec) && RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && k * tpr + t < nvec))
                 orow[k * tpr] = r[k];
         }
     } else {

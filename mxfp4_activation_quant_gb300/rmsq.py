@@ -18,11 +18,13 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "_build", "librmsq.so")
+# RMSQ_DEBUG=1 selects the bounds-checking debug build (tests only)
+LIB_PATH = os.path.join(HERE, "_build",
+                        "librmsq_debug.so" if os.environ.get("RMSQ_DEBUG") == "1" else "librmsq.so")
 
 RMSQ_OK = 0
 STATUS_NAMES = {0: "RMSQ_OK", 1: "RMSQ_ERR_INVALID_ARG", 2: "RMSQ_ERR_MISALIGNED",
-                3: "RMSQ_ERR_UNSUPPORTED", 4: "RMSQ_ERR_CUDA", 5: "RMSQ_ERR_TIMEOUT"}
+                3: "RMSQ_ERR_UNSUPPORTED", 4: "RMSQ_ERR_CUDA", 5: "RMSQ_ERR_TIMEOUT", 6: "RMSQ_ERR_BOUNDS"}
 KERNEL_AUTO, KERNEL_ROWS, KERNEL_PERSISTENT = 0, 1, 2
 SCALE_ROW_MAJOR, SCALE_COL_MAJOR, SCALE_COL_MAJOR_PAD4 = 0, 1, 2
 
@@ -77,6 +79,7 @@ _SIGNATURES = {
     "rmsq_encode_e4m3": [_p, _p, _i64, _p],
     "rmsq_encode_e2m1": [_p, _p, _i64, _p],
     "rmsq_check_group_division": [_p, _p],
+    "rmsq_debug_bounds_selftest": [_p],
 }
 
 

@@ -17,3 +17,13 @@ def oracle_mod():
     from oracle import oracle
     oracle.lib()
     return oracle
+
+
+@pytest.fixture(autouse=True)
+def _debug_build_bounds_check(request):
+    """With the bounds-checking debug library (RMSQ_DEBUG=1), no GPU test may
+    leave a failed store check behind in the status word."""
+    yield
+    if os.environ.get("RMSQ_DEBUG") == "1" and request.node.get_closest_marker("gpu"):
+        from mxfp4_activation_quant_gb300 import rmsq
+        assert rmsq.sync_status() == 0, "a debug-build bounds check failed (or a wait timed out)"

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings(L):
-    for s in range(6):
+    for s in range(7):
         assert L.rmsq_status_string(s)
     assert L.rmsq_status_string(99) == b"unknown status"
 
@@ -190,3 +190,9 @@ def test_norm_only_and_tiles_reject_bad_arguments(L):
     assert tiles(None, 8, 10, 8, B_S, 0, None) == 1
     assert tiles(A_S, 8, 1000, 8, A_S + 512, 0, None) == 1                 # out overlaps the input
     assert tiles(A_S, 8, 0, 8, B_S, 0, None) == 0
+
+
+def test_bounds_selftest_needs_the_debug_build(L):
+    if os.environ.get("RMSQ_DEBUG") == "1":
+        pytest.skip("release-build behaviour")
+    assert L.rmsq_debug_bounds_selftest(None) == 3         # RMSQ_ERR_UNSUPPORTED, nothing launched

@@ -519,3 +519,13 @@ def test_device_encoder_every_fp32_pattern(oracle_mod, fmt):
     assert checked == 1 << 32
     assert bad == 0, f"{bad} fp32 patterns encode differently"
     print(fmt, "patterns checked:", checked, "NaN inputs encoded differently (E2M1 only):", nan_diff)
+
+
+def test_debug_build_bounds_check_fires():
+    """Positive control of the debug build's store checks (skipped in release
+    builds): a deliberately failing check is reported as RMSQ_ERR_BOUNDS."""
+    if os.environ.get("RMSQ_DEBUG") != "1":
+        pytest.skip("runs against the RMSQ_DEBUG library (tests/test_zz_debug_build_gpu.py)")
+    assert rmsq.lib().rmsq_debug_bounds_selftest(torch.cuda.current_stream().cuda_stream) == 0
+    assert rmsq.sync_status() == 6                     # RMSQ_ERR_BOUNDS
+    assert rmsq.sync_status() == 0
