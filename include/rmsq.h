@@ -299,14 +299,21 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
  *                  unissued, so a wait runs out; the kernel then stops,
  *                  drains, frees its tensor memory and sets the status word
  *                  (rmsq_sync_status returns RMSQ_ERR_TIMEOUT, D is
- *                  incomplete).
+ *                  incomplete). With the persistent schedule the stage is
+ *                  counted over the CTA's tiles.
+ *   schedule       0 = auto (persistent when quantised A, no K split and
+ *                  more tiles than SMs), 1 = one tile per CTA, 2 =
+ *                  persistent: one CTA per SM walks the tiles, so a tile's
+ *                  set-up, first loads and epilogue overlap its neighbours'
+ *                  work (quantised A and ksplit 1 only). Results do not
+ *                  depend on it.
  */
 typedef struct rmsq_gemm_opts {
     int32_t bn;
     int32_t ksplit;
     int64_t wait_limit_ns;
     int32_t debug_stall_stage;
-    int32_t reserved;
+    int32_t schedule;
 } rmsq_gemm_opts;
 
 rmsq_status rmsq_mxfp4_gemm_ex(

@@ -64,6 +64,7 @@ struct GemmLaunch {
     int64_t M, N, K;
     int bn;                    // 64, 128 or 256
     int ksplit;                // 1..8 CTAs (a cluster) per tile splitting K
+    int persistent_ctas;       // > 0: a persistent grid of this many CTAs walks the tiles
     int debug_skip_stage;      // test hook: a local K stage whose loads are never issued (-1 = off;
                                // a zero-initialised GemmLaunch must set it)
     int64_t wait_limit_ns;
@@ -114,7 +115,7 @@ struct GemmCfg {
     static constexpr int kOffSfa = kStages * kAB;
     static constexpr int kOffSfb = kOffSfa + kStages * kSpans * kSfaSpan;
     static constexpr int kOffBar = kOffSfb + kStages * kSpans * kSfbSpan;
-    static constexpr int kBarBytes = (2 * kStages + 2) * 8 + 16;
+    static constexpr int kBarBytes = (2 * kStages + 3) * 8 + 16;
     static constexpr size_t kSmem = 1024 + kOffBar + kBarBytes;
     static_assert(kTmemCols <= 512, "tensor memory");
     static_assert(kSmem <= 232448, "shared memory");
@@ -133,6 +134,8 @@ struct GemmParams {
     int32_t b_row_tiles;        // ceil(N / 128): 128-row scale tiles that exist for B
     int32_t a_box_rows;         // rows of A per TMA box: 128, or M rounded up to 8 when M < 128
     int32_t ksplit;             // CTAs of a cluster that split K (1 = no split)
+    int32_t persistent;         // 1: a grid of gridDim.x CTAs walks the m_tiles x n_tiles tiles
+    int32_t m_tiles, n_tiles;
     int32_t debug_skip_stage;   // test hook: the loads of this local stage are never issued (-1 = off)
     int64_t wait_limit_ns;
     unsigned int *status;
@@ -429,12 +432,31 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     uint64_t *full = (uint64_t *)(smem + C::kOffBar);
     uint64_t *empty = full + C::kStages;
     uint64_t *accum = empty + C::kStages;
-    uint64_t *drain = accum + 1;
+    uint64_t *tmem_empty = accum + 1;
+    uint64_t *drain = tmem_empty + 1;
     uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     volatile int *abort = (volatile int *)(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tile = blockIdx.x, m_tile = blockIdx.y;
+    // Tiles: one per CTA from the grid, or -- persistent launches -- tiles
+    // blockIdx.x, blockIdx.x + gridDim.x, ... of the n-fastest tile order.
+    // (m0, n0, R) below are the CTA's first tile; the split-K reduction, which
+    // only one-tile launches use, refers to them.
+    auto tile_at = [&](int i, int &mt, int &nt) -> bool {
+        if (!p.persistent) {
+            mt = (int)blockIdx.y;
+            nt = (int)blockIdx.x;
+            return i == 0;
+        }
+        const int64_t t = (int64_t)blockIdx.x + (int64_t)i * gridDim.x;
+        if (t >= (int64_t)p.m_tiles * p.n_tiles)
+            return false;
+        mt = (int)(t / p.n_tiles);
+        nt = (int)(t % p.n_tiles);
+        return true;
+    };
+    int m_tile = 0, n_tile = 0;
+    tile_at(0, m_tile, n_tile);
     const int64_t m0 = (int64_t)m_tile * kBM, n0 = (int64_t)n_tile * BN;
     // this CTA's spans of K: all of them, or its share when a cluster splits K
     const int KS = p.k_spans;
@@ -455,6 +477,8 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(empty + s)));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(accum)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(tmem_empty)),
+                     "r"(PREQUANT ? kQuantThreads : 128));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(drain)));
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -470,106 +494,120 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_sf = tmem + BN;   // scale-factor columns follow the accumulator
-    int issued = 0;                       // warp 0: stages whose loads were issued
+    int issued = 0;                       // warp 0: stages (counted over all tiles) whose loads were issued
 
-    const int NST = (KL + C::kSpans - 1) / C::kSpans;            // stages of this CTA
+    // Stages are counted over all of the CTA's tiles (g): the ring runs on
+    // from one tile into the next.
+    const int NST = (KL + C::kSpans - 1) / C::kSpans;            // stages per tile
     if (warp == 0) {
         // ---------------------------------------------------------- loads
         // The whole warp runs the loop (its values stay warp-uniform) and one
         // elected lane issues the copies.
-        const int bt0 = (int)(n0 >> 7);                           // first 128-row scale tile of B
-        int atoms = 0;
-        for (int t = 0; t < C::kSfbAtoms; ++t)
-            atoms += (bt0 + t < p.b_row_tiles);
-        const uint32_t span_tx = C::kSpanB + atoms * 1024u +
-                                 (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kSpanBytes + C::kSfaSpan));
-        auto issue = [&](int j) {            // one stage's copies, by the elected lane
-            if (j == p.debug_skip_stage)     // test hook: this stage never arrives
-                return;
-            const int s = j % C::kStages, nsp = min(C::kSpans, KL - j * C::kSpans);
-            const uint32_t fb = saddr(full + s);
-            mbar_arrive_tx(fb, span_tx * nsp);
-            for (int sp = 0; sp < nsp; ++sp) {
-                const int ks = ks0 + j * C::kSpans + sp;
-                uint8_t *a_dst = smem + s * C::kAB + sp * C::kSpanAB;
-                if (!PREQUANT) {
-                    tma_2d(saddr(a_dst), &map_a, ks * kSpanBytes, (int)m0, fb);
-                    bulk_g2s(saddr(smem + C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan),
-                             p.a_scale + ((int64_t)m_tile * (2 * KS) + 2 * ks) * 512, 1024, fb);
+        int g = 0;
+        int mt, nt;
+        for (int ti = 0; tile_at(ti, mt, nt); ++ti) {
+            const int64_t tm0 = (int64_t)mt * kBM, tn0 = (int64_t)nt * BN;
+            const int bt0 = (int)(tn0 >> 7);                         // first 128-row scale tile of B
+            int atoms = 0;
+            for (int t = 0; t < C::kSfbAtoms; ++t)
+                atoms += (bt0 + t < p.b_row_tiles);
+            const uint32_t span_tx = C::kSpanB + atoms * 1024u +
+                                     (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kSpanBytes + C::kSfaSpan));
+            bool stop = false;
+            for (int j = 0; j < NST; ++j, ++g) {
+                const int s = g % C::kStages;
+                if (g >= C::kStages &&
+                    !warp_wait(saddr(empty + s), ((uint32_t)(g / C::kStages) & 1u) ^ 1u, abort, p)) {
+                    stop = true;
+                    break;
                 }
-                tma_2d(saddr(a_dst + C::kSpanA), &map_b, ks * kSpanBytes, (int)n0, fb);
-                for (int t = 0; t < C::kSfbAtoms; ++t)
-                    if (bt0 + t < p.b_row_tiles)
-                        bulk_g2s(saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan + t * 1024),
-                                 p.b_scale + ((int64_t)(bt0 + t) * (2 * KS) + 2 * ks) * 512, 1024, fb);
+                if (g != p.debug_skip_stage && elect_one()) {   // test hook: that stage never arrives
+                    const int nsp = min(C::kSpans, KL - j * C::kSpans);
+                    const uint32_t fb = saddr(full + s);
+                    mbar_arrive_tx(fb, span_tx * nsp);
+                    for (int sp = 0; sp < nsp; ++sp) {
+                        const int ks = ks0 + j * C::kSpans + sp;
+                        uint8_t *a_dst = smem + s * C::kAB + sp * C::kSpanAB;
+                        if (!PREQUANT) {
+                            tma_2d(saddr(a_dst), &map_a, ks * kSpanBytes, (int)tm0, fb);
+                            bulk_g2s(saddr(smem + C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan),
+                                     p.a_scale + ((int64_t)mt * (2 * KS) + 2 * ks) * 512, 1024, fb);
+                        }
+                        tma_2d(saddr(a_dst + C::kSpanA), &map_b, ks * kSpanBytes, (int)tn0, fb);
+                        for (int t = 0; t < C::kSfbAtoms; ++t)
+                            if (bt0 + t < p.b_row_tiles)
+                                bulk_g2s(saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan + t * 1024),
+                                         p.b_scale + ((int64_t)(bt0 + t) * (2 * KS) + 2 * ks) * 512, 1024, fb);
+                    }
+                }
+                __syncwarp();
+                issued = g + 1;
             }
-        };
-        // The first pass over the ring finds every slot free: issue it back
-        // to back; then one stage per freed slot.
-        const int first = NST < C::kStages ? NST : C::kStages;
-        if (elect_one())
-            for (int j = 0; j < first; ++j)
-                issue(j);
-        __syncwarp();
-        issued = first;
-        for (int j = first; j < NST; ++j) {
-            const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
-            if (!warp_wait(saddr(empty + j % C::kStages), ph ^ 1u, abort, p))
+            if (stop)
                 break;
-            if (elect_one())
-                issue(j);
-            __syncwarp();
-            issued = j + 1;
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
         // warp-uniform loop, one elected lane issues the tensor-core work
-        // a 64-row B tile sits in the lower or upper half of its 128-row scale tile
-        const uint32_t sfb_row_col = (BN == 64) ? (uint32_t)(((n0 >> 6) & 1) * 2) : 0u;
-        bool any = false;
-        for (int j = 0; j < NST; ++j) {
-            const int s = j % C::kStages, nsp = min(C::kSpans, KL - j * C::kSpans);
-            const uint32_t ph = (uint32_t)(j / C::kStages) & 1u;
-            if (!warp_wait(saddr(full + s), ph, abort, p))
-                break;
-            tc_fence_after();
-            if (elect_one()) {
-                for (int sp = 0; sp < nsp; ++sp) {
-                    const uint32_t sfa_col = tmem_sf + s * C::kSfCols + sp * C::kSfColsSpan;
-                    const uint32_t sfb_col = sfa_col + 8;
-                    const uint32_t sfa_smem = saddr(smem + C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan);
-                    const uint32_t sfb_smem = saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan);
-                    const uint32_t a_smem = saddr(smem + s * C::kAB + sp * C::kSpanAB), b_smem = a_smem + C::kSpanA;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        cp_sf(sfa_col + 4 * c, desc_sf(sfa_smem + c * 512));
-#pragma unroll
-                        for (int t = 0; t < C::kSfbAtoms; ++t)
-                            cp_sf(sfb_col + 4 * C::kSfbAtoms * c + 4 * t, desc_sf(sfb_smem + t * 1024 + c * 512));
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int c = k >> 1;
-                        mma_mxf4(tmem, desc_sw128(a_smem + 32 * k), desc_sw128(b_smem + 32 * k),
-                                 idesc_mxf4(BN, (k & 1) * 2), sfa_col + 4 * c,
-                                 sfb_col + 4 * C::kSfbAtoms * c + sfb_row_col, (j | sp | k) != 0);
-                    }
-                }
-                mma_commit(saddr(empty + s));
+        int g = 0;
+        int mt, nt;
+        bool any = false, stop = false;
+        for (int ti = 0; !stop && tile_at(ti, mt, nt); ++ti) {
+            // the accumulator is free once the epilogue has read the previous tile
+            if (ti > 0) {
+                if (!warp_wait(saddr(tmem_empty), (uint32_t)((ti - 1) & 1), abort, p))
+                    break;
+                tc_fence_after();
             }
-            __syncwarp();
-            any = true;
-        }
-        if (elect_one()) {
-            if (!*abort) {
-                mma_commit(saddr(accum));
-            } else if (any) {
-                // drain the tensor core before the tensor memory is freed
-                mma_commit(saddr(drain));
-                const uint64_t t0 = gtimer();
-                while (!mbar_test(saddr(drain), 0) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
+            // a tile that starts half-way into a 128-row scale tile (64-row
+            // tiles) reads its rows' scale columns from 2 on
+            const uint32_t sfb_row_col = (BN == 64) ? (uint32_t)((((int64_t)nt * BN) >> 6 & 1) * 2) : 0u;
+            for (int j = 0; j < NST; ++j, ++g) {
+                const int s = g % C::kStages, nsp = min(C::kSpans, KL - j * C::kSpans);
+                if (!warp_wait(saddr(full + s), (uint32_t)(g / C::kStages) & 1u, abort, p)) {
+                    stop = true;
+                    break;
                 }
+                tc_fence_after();
+                if (elect_one()) {
+                    for (int sp = 0; sp < nsp; ++sp) {
+                        const uint32_t sfa_col = tmem_sf + s * C::kSfCols + sp * C::kSfColsSpan;
+                        const uint32_t sfb_col = sfa_col + 8;
+                        const uint32_t sfa_smem = saddr(smem + C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan);
+                        const uint32_t sfb_smem = saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan);
+                        const uint32_t a_smem = saddr(smem + s * C::kAB + sp * C::kSpanAB),
+                                       b_smem = a_smem + C::kSpanA;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            cp_sf(sfa_col + 4 * c, desc_sf(sfa_smem + c * 512));
+#pragma unroll
+                            for (int t = 0; t < C::kSfbAtoms; ++t)
+                                cp_sf(sfb_col + 4 * C::kSfbAtoms * c + 4 * t,
+                                      desc_sf(sfb_smem + t * 1024 + c * 512));
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int c = k >> 1;
+                            mma_mxf4(tmem, desc_sw128(a_smem + 32 * k), desc_sw128(b_smem + 32 * k),
+                                     idesc_mxf4(BN, (k & 1) * 2), sfa_col + 4 * c,
+                                     sfb_col + 4 * C::kSfbAtoms * c + sfb_row_col, (j | sp | k) != 0);
+                        }
+                    }
+                    mma_commit(saddr(empty + s));
+                }
+                __syncwarp();
+                any = true;
+            }
+            if (!stop && elect_one())
+                mma_commit(saddr(accum));    // this tile's accumulator is complete
+            __syncwarp();
+        }
+        if (*abort && any && elect_one()) {
+            // drain the tensor core before the tensor memory is freed
+            mma_commit(saddr(drain));
+            const uint64_t t0 = gtimer();
+            while (!mbar_test(saddr(drain), 0) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
             }
         }
         __syncwarp();
@@ -579,23 +617,28 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
         // prequant: warps 4-7 and 8-11 share the epilogue by column halves
         const int c_lo = (PREQUANT && warp >= 8) ? BN / 2 : 0;
         const int c_hi = (PREQUANT && warp < 8) ? BN / 2 : BN;
-        const int64_t m = m0 + r;
         bool ok = true;
         if (PREQUANT)
             ok = prequant_loop<BN>(p, m0, R, ks0, KL, smem, full, empty, abort);
         // ------------------------------------------------------- epilogue
-        if (ok && warp_wait(saddr(accum), 0, abort, p)) {
+        int mt, nt;
+        for (int ti = 0; ok && tile_at(ti, mt, nt); ++ti) {
+            if (!warp_wait(saddr(accum), (uint32_t)(ti & 1), abort, p))
+                break;
             tc_fence_after();
+            const int64_t tm0 = (int64_t)mt * kBM, tn0 = (int64_t)nt * BN;
+            const int64_t m = tm0 + r;
+            const int tR = (int)min((int64_t)kBM, p.M - tm0);
             const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-            uint16_t *drow = p.d + m * p.ldd + n0;
-            // split K: this CTA's partial sums go to its shared memory (the
+            uint16_t *drow = p.d + m * p.ldd + tn0;
+            // split-K: this CTA's partial sums go to its shared memory (the
             // operand ring is free now), padded rows against bank conflicts
             float *red = (float *)smem + r * (BN + 4);
 #pragma unroll 1
             for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
                 uint32_t acc[32];
                 tmem_ld32(trow + c0, acc);
-                if (r >= R)
+                if (r >= tR)
                     continue;
                 if (p.ksplit > 1) {
 #pragma unroll
@@ -605,7 +648,7 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                                         __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3]));
                     continue;
                 }
-                const int64_t valid = p.N - (n0 + c0);
+                const int64_t valid = p.N - (tn0 + c0);
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     if (valid >= 8 * (v + 1)) {
@@ -614,11 +657,14 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                         o.y = pack_bf16x2(__uint_as_float(acc[8 * v + 2]), __uint_as_float(acc[8 * v + 3]));
                         o.z = pack_bf16x2(__uint_as_float(acc[8 * v + 4]), __uint_as_float(acc[8 * v + 5]));
                         o.w = pack_bf16x2(__uint_as_float(acc[8 * v + 6]), __uint_as_float(acc[8 * v + 7]));
-                        if (RMSQ_IN_BOUNDS(p.status, m < p.M && n0 + c0 + 8 * (v + 1) <= p.N))
+                        if (RMSQ_IN_BOUNDS(p.status, m < p.M && tn0 + c0 + 8 * (v + 1) <= p.N))
                             *reinterpret_cast<uint4 *>(drow + c0 + 8 * v) = o;
                     }
                 }
             }
+            // the accumulator may be overwritten by the next tile's MMAs
+            tc_fence_before();
+            mbar_arrive(saddr(tmem_empty));
         }
     }
 
@@ -716,7 +762,7 @@ bool make_code_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row
 
 template <int BN, bool PRE>
 cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int m_tiles,
-                          int n_tiles, cudaStream_t st)
+                          int n_tiles, int persistent_ctas, cudaStream_t st)
 {
     using C = GemmCfg<BN, PRE>;
     static bool attr[128];
@@ -732,6 +778,10 @@ cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUte
         if (e != cudaSuccess)
             return e;
         attr[dev] = true;
+    }
+    if (p.persistent) {     // one CTA per SM walks the tiles
+        mxfp4_gemm_kernel<BN, PRE><<<dim3(persistent_ctas, 1, 1), gemm_threads<PRE>(), C::kSmem, st>>>(p, ma, mb);
+        return cudaGetLastError();
     }
     if (p.ksplit == 1) {
         mxfp4_gemm_kernel<BN, PRE><<<dim3(n_tiles, m_tiles, 1), gemm_threads<PRE>(), C::kSmem, st>>>(p, ma, mb);
@@ -754,6 +804,8 @@ cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUte
     return cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<BN, PRE>, p, ma, mb);
 }
 
+bool pre_of(const GemmLaunch &g) { return g.a_bf16 != nullptr; }
+
 cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
 {
     GemmParams p{};
@@ -773,6 +825,7 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
     p.a_box_rows = g.M >= kBM ? kBM : (int32_t)((g.M + 7) / 8 * 8);
     p.ksplit = g.ksplit;
     p.debug_skip_stage = g.debug_skip_stage;
+    p.persistent = g.persistent_ctas > 0;
     if (p.ksplit < 1 || p.ksplit > 8 || p.ksplit > p.k_spans)
         return cudaErrorInvalidValue;
     p.wait_limit_ns = g.wait_limit_ns;
@@ -786,14 +839,18 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
         return cudaErrorInvalidValue;
     }
     const int m_tiles = (int)((g.M + kBM - 1) / kBM), n_tiles = (int)((g.N + g.bn - 1) / g.bn);
+    p.m_tiles = m_tiles;
+    p.n_tiles = n_tiles;
+    if (p.persistent && (pre_of(g) || p.ksplit != 1))
+        return cudaErrorInvalidValue;
     const bool pre = g.a_bf16 != nullptr;
     switch (g.bn) {
-    case 64: return pre ? launch_gemm_t<64, true>(p, ma, mb, m_tiles, n_tiles, st)
-                        : launch_gemm_t<64, false>(p, ma, mb, m_tiles, n_tiles, st);
-    case 128: return pre ? launch_gemm_t<128, true>(p, ma, mb, m_tiles, n_tiles, st)
-                         : launch_gemm_t<128, false>(p, ma, mb, m_tiles, n_tiles, st);
-    case 256: return pre ? launch_gemm_t<256, true>(p, ma, mb, m_tiles, n_tiles, st)
-                         : launch_gemm_t<256, false>(p, ma, mb, m_tiles, n_tiles, st);
+    case 64: return pre ? launch_gemm_t<64, true>(p, ma, mb, m_tiles, n_tiles, g.persistent_ctas, st)
+                        : launch_gemm_t<64, false>(p, ma, mb, m_tiles, n_tiles, g.persistent_ctas, st);
+    case 128: return pre ? launch_gemm_t<128, true>(p, ma, mb, m_tiles, n_tiles, g.persistent_ctas, st)
+                         : launch_gemm_t<128, false>(p, ma, mb, m_tiles, n_tiles, g.persistent_ctas, st);
+    case 256: return pre ? launch_gemm_t<256, true>(p, ma, mb, m_tiles, n_tiles, g.persistent_ctas, st)
+                         : launch_gemm_t<256, false>(p, ma, mb, m_tiles, n_tiles, g.persistent_ctas, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -860,6 +917,8 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
         return failf(RMSQ_ERR_INVALID_ARG, "wait_limit_ns must be >= 0");
     if (o.debug_stall_stage < 0)
         return failf(RMSQ_ERR_INVALID_ARG, "debug_stall_stage must be >= 0");
+    if (o.schedule < 0 || o.schedule > 2)
+        return failf(RMSQ_ERR_INVALID_ARG, "schedule must be 0, 1 or 2 (got %d)", o.schedule);
     if (K % 256)
         return failf(RMSQ_ERR_UNSUPPORTED, "K=%lld is not a multiple of 256", (long long)K);
     if (N % 8)
@@ -925,6 +984,17 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     if (ksplit > K / 256)
         return failf(RMSQ_ERR_INVALID_ARG, "ksplit=%d exceeds the %lld 256-element spans of K", ksplit,
                      (long long)(K / 256));
+    // More tiles than SMs (no K split, A quantised): one persistent CTA per
+    // SM walks the tiles, so set-up, the ring's first fill and the epilogue
+    // overlap the neighbouring tiles' work.
+    bool persistent = !prequant && ksplit == 1 && tiles > sms;
+    if (o.schedule == 1)
+        persistent = false;
+    else if (o.schedule == 2) {
+        if (prequant || ksplit != 1)
+            return failf(RMSQ_ERR_UNSUPPORTED, "the persistent schedule needs quantised A and no K split");
+        persistent = true;
+    }
     GemmLaunch g{};
     if (prequant) {
         g.a_bf16 = a;
@@ -943,6 +1013,7 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     g.K = K;
     g.bn = bn;
     g.ksplit = ksplit;
+    g.persistent_ctas = persistent ? (int)(tiles < sms ? tiles : sms) : 0;
     g.debug_skip_stage = o.debug_stall_stage - 1;   // -1: off
     g.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
     g.status = status;

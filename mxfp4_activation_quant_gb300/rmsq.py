@@ -47,10 +47,10 @@ class LaunchOpts(ctypes.Structure):
 class GemmOpts(ctypes.Structure):
     """Mirror of ``rmsq_gemm_opts``."""
     _fields_ = [("bn", _i32), ("ksplit", _i32), ("wait_limit_ns", _i64), ("debug_stall_stage", _i32),
-                ("reserved", _i32)]
+                ("schedule", _i32)]
 
-    def __init__(self, bn=0, ksplit=0, wait_limit_ns=0, debug_stall_stage=0):
-        super().__init__(bn, ksplit, wait_limit_ns, debug_stall_stage, 0)
+    def __init__(self, bn=0, ksplit=0, wait_limit_ns=0, debug_stall_stage=0, schedule=0):
+        super().__init__(bn, ksplit, wait_limit_ns, debug_stall_stage, schedule)
 
 
 class RmsqError(RuntimeError):

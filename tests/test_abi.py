@@ -125,10 +125,11 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 
 def test_gemm_opts_layout_matches_header():
-    # int32 bn, ksplit; int64 wait_limit_ns; int32 debug_stall_stage, reserved
+    # int32 bn, ksplit; int64 wait_limit_ns; int32 debug_stall_stage, schedule
     assert ctypes.sizeof(rmsq.GemmOpts) == 24
     assert rmsq.GemmOpts.wait_limit_ns.offset == 8
     assert rmsq.GemmOpts.debug_stall_stage.offset == 16
+    assert rmsq.GemmOpts.schedule.offset == 20
     # zero-initialised options are the defaults (the hook is off)
     assert bytes(rmsq.GemmOpts()) == bytes(24)
 
@@ -173,9 +174,9 @@ def test_gemm_specific_checks(L):
     assert gemm(L, True, lda=1000) == 1                      # bf16 A rows are K elements
     assert gemm(L, True, lda=1028) == 2                      # bf16 leading dimension % 8
     assert gemm(L, False, M=0) == 0 and gemm(L, True, N=0) == 0
-    opts = rmsq.GemmOpts(bn=96)
-    assert L.rmsq_mxfp4_gemm_ex(A_Q, 512, A_S, B_Q, 512, B_S, D, 256, 64, 256, 1024, None,
-                                ctypes.byref(opts)) == 1
+    for opts in (rmsq.GemmOpts(bn=96), rmsq.GemmOpts(schedule=3), rmsq.GemmOpts(schedule=-1)):
+        assert L.rmsq_mxfp4_gemm_ex(A_Q, 512, A_S, B_Q, 512, B_S, D, 256, 64, 256, 1024, None,
+                                    ctypes.byref(opts)) == 1
 
 
 def test_norm_only_and_tiles_reject_bad_arguments(L):

@@ -86,6 +86,44 @@ def test_tile_choices_agree_bitwise():
         assert torch.equal(o, outs[0])
 
 
+@pytest.mark.parametrize("bn,M,N", [(64, 1100, 1032), (128, 2050, 1352), (256, 4100, 1160)])
+def test_persistent_schedule(oracle_mod, bn, M, N):
+    """More tiles than SMs: a persistent grid (each CTA walks several tiles,
+    the stage ring and the accumulator carried from one tile into the next)
+    gives the one-tile-per-CTA result bit for bit, and the oracle's on
+    sampled rows, ragged last row and column tiles included."""
+    K = 1024
+    a_q, a_s, b_q, b_s = operands(300 + bn, M, N, K)
+    ga, gb = a_q.to(DEV), b_q.to(DEV)
+    ta, tb = rmsq.mx_scale_tiles(a_s.to(DEV)), rmsq.mx_scale_tiles(b_s.to(DEV))
+    one = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=bn, ksplit=1, schedule=1))
+    walk = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=bn, ksplit=1, schedule=2))
+    auto = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=bn))
+    torch.cuda.synchronize()
+    tiles = -(-M // 128) * -(-N // bn)
+    assert tiles > torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert torch.equal(one, walk) and torch.equal(one, auto)
+    rows = np.unique(np.concatenate([np.arange(0, M, 97), [M - 1]]))
+    ref = oracle_mod.mxfp4_gemm(a_q.numpy()[rows], a_s.numpy()[rows], b_q.numpy(), b_s.numpy())
+    st = parity.compare_gemm(walk[torch.from_numpy(rows).to(DEV)], ref, K, what=f"persistent bn={bn}")
+    assert rmsq.sync_status() == 0
+    print(bn, tiles, st)
+
+
+def test_persistent_schedule_rejects():
+    """The persistent schedule walks whole tiles with quantised A only."""
+    M, N, K = 128, 256, 512
+    a_q, a_s, b_q, b_s = operands(31, M, N, K)
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    y = synth.random_bf16(32, (M, K)).to(DEV)
+    with pytest.raises(RuntimeError, match="persistent"):
+        rmsq.a16wfp4_gemm(y, gb, tb, opts=rmsq.GemmOpts(schedule=2))
+    with pytest.raises(RuntimeError, match="persistent"):
+        rmsq.mxfp4_gemm(a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV)), gb, tb,
+                        opts=rmsq.GemmOpts(ksplit=2, schedule=2))
+    assert rmsq.sync_status() == 0
+
+
 def test_long_k_wraps_the_stage_ring(oracle_mod):
     """K = 7168 is 28 stages: every ring slot is reused several times."""
     M, N, K = 130, 136, 7168
@@ -206,6 +244,28 @@ def test_bounded_wait_reports_timeout(oracle_mod, pre, ksplit):
     torch.cuda.synchronize()
     ref = oracle_mod.mxfp4_gemm(a_q.numpy(), a_s.numpy(), b_q.numpy(), b_s.numpy())
     parity.compare_gemm(d, ref, K, what="after a timed-out launch")
+    assert rmsq.sync_status() == 0
+
+
+def test_bounded_wait_in_a_later_tile():
+    """Persistent schedule: the stalled stage sits in the second tile of the
+    CTAs that walk two (160 tiles of 128 x 128 on fewer SMs, four stages
+    per tile). Those CTAs stop and drain, the host reads RMSQ_ERR_TIMEOUT,
+    and the next launch matches the one-tile schedule bit for bit."""
+    M, N, K = 2048, 1280, 2048
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    assert 80 <= sms < 160
+    a_q, a_s, b_q, b_s = operands(63, M, N, K)
+    ga, ta = a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV))
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    stuck = rmsq.GemmOpts(bn=128, ksplit=1, wait_limit_ns=50_000_000, debug_stall_stage=6, schedule=2)
+    rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=stuck)
+    assert rmsq.sync_status() == 5                      # RMSQ_ERR_TIMEOUT
+    assert rmsq.sync_status() == 0
+    walk = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=128, ksplit=1, schedule=2))
+    one = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=128, ksplit=1, schedule=1))
+    torch.cuda.synchronize()
+    assert torch.equal(walk, one)
     assert rmsq.sync_status() == 0
 
 

@@ -87,7 +87,10 @@ def test_random_gemm(oracle_mod, case):
     prequant = bool(rng.integers(0, 2))
     b_q, b_s = synth.mxfp4_weights(6000 + case, N, K)
     gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
-    opts = rmsq.GemmOpts(bn=bn, ksplit=ksplit)
+    # drawn last so that the cases above keep their shapes: the persistent
+    # schedule where it applies (quantised A, no K split)
+    schedule = 2 if (not prequant and ksplit == 1 and rng.integers(0, 2)) else 0
+    opts = rmsq.GemmOpts(bn=bn, ksplit=ksplit, schedule=schedule)
     if prequant:
         y = synth.random_bf16(7000 + case, (M, K))
         d = rmsq.a16wfp4_gemm(y.to(DEV), gb, tb, opts=opts)
@@ -99,7 +102,7 @@ def test_random_gemm(oracle_mod, case):
     torch.cuda.synchronize()
     ref = oracle_mod.mxfp4_gemm(a_q, a_s, b_q.numpy(), b_s.numpy())
     st = parity.compare_gemm(d, ref, K, what=f"case {case}: M={M} N={N} K={K} bn={bn} ksplit={ksplit} "
-                                              f"prequant={prequant}")
+                                              f"prequant={prequant} schedule={schedule}")
     assert st["bit_equal_fraction"] > 0.95, st
     assert rmsq.sync_status() == 0
 
