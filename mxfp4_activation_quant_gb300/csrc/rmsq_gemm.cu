@@ -114,7 +114,10 @@ struct GemmCfg {
     static constexpr int kTmemCols = pow2_at_least(BN + kStages * kSfCols);
     static constexpr int kOffSfa = kStages * kAB;
     static constexpr int kOffSfb = kOffSfa + kStages * kSpans * kSfaSpan;
-    static constexpr int kOffBar = kOffSfb + kStages * kSpans * kSfbSpan;
+    // plain GEMM: each epilogue warp stages 32 rows x 128 bytes of D here
+    static constexpr int kOffOut = kOffSfb + kStages * kSpans * kSfbSpan;
+    static constexpr int kOutBytes = PRE ? 0 : 4 * 2 * 2048;
+    static constexpr int kOffBar = kOffOut + kOutBytes;
     static constexpr int kBarBytes = (2 * kStages + 3) * 8 + 16;
     static constexpr size_t kSmem = 1024 + kOffBar + kBarBytes;
     static_assert(kTmemCols <= 512, "tensor memory");
@@ -291,8 +294,9 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 lanes x 32 columns of fp32 from tensor memory.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+// 32 lanes x 32 columns of fp32 from tensor memory (issue only; the values
+// are valid after tmem_ld_wait + tmem_hold).
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32])
 {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -302,7 +306,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Ties the registers of a tensor-memory load to a point after the wait, so
+// that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_hold(uint32_t (&r)[32])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    tmem_ld32_issue(taddr, r);
+    tmem_ld_wait();
+    tmem_hold(r);
 }
 
 // ---------------------------------------------------- prequant (A in bf16)
@@ -621,6 +645,8 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
         if (PREQUANT)
             ok = prequant_loop<BN>(p, m0, R, ks0, KL, smem, full, empty, abort);
         // ------------------------------------------------------- epilogue
+        // plain GEMM: this warp's staging rows for the stores of D
+        uint8_t *const stage_w = smem + C::kOffOut + (warp - 4) * 4096;
         int mt, nt;
         for (int ti = 0; ok && tile_at(ti, mt, nt); ++ti) {
             if (!warp_wait(saddr(accum), (uint32_t)(ti & 1), abort, p))
@@ -634,21 +660,61 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
             // split-K: this CTA's partial sums go to its shared memory (the
             // operand ring is free now), padded rows against bank conflicts
             float *red = (float *)smem + r * (BN + 4);
+            if (!PREQUANT && p.ksplit == 1) {
+                // Stores of D, 64 columns at a time: each lane holds its row's
+                // 128 bytes; they pass through shared memory (16-byte chunk j
+                // of row i at j ^ (i mod 8): no bank conflicts either way) so
+                // that every store instruction writes four whole 128-byte
+                // lines of D (eight lanes per row) instead of 32 rows' pieces.
+                const int64_t row0 = tm0 + q * 32;
+                const int cj = lane & 7;
 #pragma unroll 1
-            for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+                for (int c0 = 0; c0 < BN && row0 < p.M && tn0 + c0 < p.N; c0 += 64) {   // warp-uniform
+                    uint32_t lo[32], hi[32];
+                    tmem_ld32_issue(trow + c0, lo);
+                    tmem_ld32_issue(trow + c0 + 32, hi);
+                    tmem_ld_wait();
+                    tmem_hold(lo);
+                    tmem_hold(hi);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t *a = j < 4 ? lo + 8 * j : hi + 8 * (j - 4);
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(a[0]), __uint_as_float(a[1]));
+                        o.y = pack_bf16x2(__uint_as_float(a[2]), __uint_as_float(a[3]));
+                        o.z = pack_bf16x2(__uint_as_float(a[4]), __uint_as_float(a[5]));
+                        o.w = pack_bf16x2(__uint_as_float(a[6]), __uint_as_float(a[7]));
+                        *reinterpret_cast<uint4 *>(stage_w + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = it * 4 + (lane >> 3);
+                        const uint4 v = *reinterpret_cast<const uint4 *>(stage_w + rr * 128 + ((cj ^ (rr & 7)) << 4));
+                        const int64_t gm = row0 + rr, gn = tn0 + c0 + cj * 8;
+                        if (gm < p.M && gn < p.N && RMSQ_IN_BOUNDS(p.status, gn + 8 <= p.N))
+                            *reinterpret_cast<uint4 *>(p.d + gm * p.ldd + gn) = v;
+                    }
+                    __syncwarp();                // the rows are read before they are overwritten
+                }
+            }
+#pragma unroll 1
+            for (int c0 = c_lo; c0 < c_hi && (PREQUANT || p.ksplit > 1); c0 += 32) {
                 uint32_t acc[32];
                 tmem_ld32(trow + c0, acc);
-                if (r >= tR)
-                    continue;
                 if (p.ksplit > 1) {
+                    if (r < tR) {
 #pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        *reinterpret_cast<float4 *>(red + c0 + 4 * v) =
-                            make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
-                                        __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3]));
+                        for (int v = 0; v < 8; ++v)
+                            *reinterpret_cast<float4 *>(red + c0 + 4 * v) =
+                                make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
+                                            __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3]));
+                    }
                     continue;
                 }
                 const int64_t valid = p.N - (tn0 + c0);
+                if (r >= tR)
+                    continue;
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     if (valid >= 8 * (v + 1)) {
