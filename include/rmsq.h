@@ -301,12 +301,15 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
  *                  (rmsq_sync_status returns RMSQ_ERR_TIMEOUT, D is
  *                  incomplete). With the persistent schedule the stage is
  *                  counted over the CTA's tiles.
- *   schedule       0 = auto (persistent when quantised A, no K split and
+ *   schedule       0 = auto (CTA pairs when quantised A takes 256-row B
+ *                  tiles without a K split; else persistent when there are
  *                  more tiles than SMs), 1 = one tile per CTA, 2 =
  *                  persistent: one CTA per SM walks the tiles, so a tile's
  *                  set-up, first loads and epilogue overlap its neighbours'
- *                  work (quantised A and ksplit 1 only). Results do not
- *                  depend on it.
+ *                  work (quantised A and ksplit 1 only), 3 = persistent CTA
+ *                  pairs: a cluster of two CTAs computes 256 x 256 tiles
+ *                  with the tensor cores of both SMs (quantised A, bn 0 or
+ *                  256, ksplit 0 or 1). Results do not depend on it.
  */
 typedef struct rmsq_gemm_opts {
     int32_t bn;

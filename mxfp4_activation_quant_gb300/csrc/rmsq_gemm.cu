@@ -65,6 +65,7 @@ struct GemmLaunch {
     int bn;                    // 64, 128 or 256
     int ksplit;                // 1..8 CTAs (a cluster) per tile splitting K
     int persistent_ctas;       // > 0: a persistent grid of this many CTAs walks the tiles
+    bool pair;                 // 256 x 256 tiles on CTA pairs (persistent, bn 256, quantised A)
     int debug_skip_stage;      // test hook: a local K stage whose loads are never issued (-1 = off;
                                // a zero-initialised GemmLaunch must set it)
     int64_t wait_limit_ns;
@@ -262,10 +263,10 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t addr)
 }
 
 // Instruction descriptor of kind::mxf4 (E2M1 x E2M1, UE8M0 scales, fp32
-// accumulator, both operands K-major, M = 128).
-__host__ __device__ constexpr uint32_t idesc_mxf4(int n, int sf_id)
+// accumulator, both operands K-major; M = 128, or 256 for a CTA pair).
+__host__ __device__ constexpr uint32_t idesc_mxf4(int n, int sf_id, int m = kBM)
 {
-    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(kBM >> 4) << 24) |
+    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(m >> 4) << 24) |
            ((uint32_t)sf_id << 29) | ((uint32_t)sf_id << 4);
 }
 
@@ -289,6 +290,60 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// ---- the same for a CTA pair (cta_group::2), issued by the even CTA. Measured
+// with a self-checking probe on GB300: the MMA reads A rows 128r.. and B rows
+// (N/2)r.. from CTA r's shared memory at the same offsets, and each CTA's
+// tensor memory holds D for its 128 rows, the scale factors of its rows of A
+// and those of ALL N rows of B; tcgen05.cp copies each CTA's own shared memory
+// into its own tensor memory; the commit can arrive on both CTAs' barriers.
+__device__ __forceinline__ void mma_mxf4_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                              uint32_t sfb, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void cp_sf_pair(uint32_t taddr, uint64_t desc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+// arrives on the barrier at this offset in every CTA of `mask`
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     bar),
+                 "h"(mask)
+                 : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion counts on a
+// barrier of either CTA of the pair (a cluster address)
+__device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -787,6 +842,276 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     }
 }
 
+// ------------------------------------------------------ CTA-pair kernel
+// A cluster of two CTAs computes 256 x 256 tiles of D (persistent: pair
+// blockIdx.x / 2 walks tiles pair, pair + pairs, ... in N-fastest order) with
+// M = 256 MMAs issued by the even CTA. CTA r loads its 128 rows of A and rows
+// 128r.. of the tile's 256 rows of B, so a span of K costs each SM 32 KB of
+// operands (48 KB for a 128 x 256 tile of its own): the ring holds six
+// stages instead of four. Each CTA also loads the tile's A scales for its
+// rows and ALL of its B scales (the MMA reads both from each SM's own tensor
+// memory); every copy of both CTAs completes on the even CTA's `full`
+// barrier, which the even CTA arms for both. The MMA commits arrive on both
+// CTAs' `empty` and `accum` barriers; both epilogues (their own 128 rows, in
+// their own tensor memory) arrive on the even CTA's `tmem_empty`.
+// Stage shape measured on GB300 (N = 2112, K = 7168, M = 8192): one span x
+// six stages 50.7 us, one x five 51.6 us, two spans x three stages 56.2 us.
+struct PairCfg {
+    static constexpr int BN = 256;                     // columns of D per tile
+    static constexpr int kRowsB = BN / 2;              // rows of B per CTA
+    static constexpr int kSpanA = kBM * kSpanBytes;
+    static constexpr int kSpanB = kRowsB * kSpanBytes;
+    static constexpr int kSpanAB = kSpanA + kSpanB;
+    static constexpr int kSpans = 1;                   // spans of K per stage (one barrier phase)
+    static constexpr int kStage = kSpans * kSpanAB;
+    static constexpr int kSfbAtoms = BN / 128;
+    static constexpr int kStages = 6;
+    static constexpr int kOffSfa = kStages * kStage;
+    static constexpr int kOffSfb = kOffSfa + kStages * kSpans * 1024;
+    static constexpr int kOffOut = kOffSfb + kStages * kSpans * kSfbAtoms * 1024;
+    static constexpr int kOutBytes = 4 * 2048;         // each epilogue warp: 32 rows x 64 bytes of D
+    static constexpr int kOffBar = kOffOut + kOutBytes;
+    static constexpr int kBarBytes = (2 * kStages + 3) * 8 + 16;
+    static constexpr size_t kSmem = 1024 + kOffBar + kBarBytes;
+    static constexpr int kSfColsSpan = 8 + 8 * kSfbAtoms;   // scale-factor TMEM columns per span
+    static constexpr int kSfCols = kSpans * kSfColsSpan;     // ... per stage
+    static constexpr int kTmemCols = pow2_at_least(BN + kStages * kSfCols);
+    static constexpr uint32_t kCtaTx = kSpanA + kSpanB + 1024 + kSfbAtoms * 1024;   // bytes per CTA per span
+    static_assert(kTmemCols <= 512, "tensor memory");
+    static_assert(kSmem <= 232448, "shared memory");
+};
+
+__global__ void __launch_bounds__(256, 1)
+    mxfp4_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
+                           const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sfa,
+                           const __grid_constant__ CUtensorMap map_sfb)
+{
+    using C = PairCfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = (uint64_t *)(smem + C::kOffBar);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *accum = empty + C::kStages;
+    uint64_t *tmem_empty = accum + 1;
+    uint64_t *drain = tmem_empty + 1;
+    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
+    volatile int *abort = (volatile int *)(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+    auto tile_at = [&](int i, int &mt, int &nt) -> bool {   // mt: 256-row tile of A, nt: 256-row tile of B
+        const int64_t t = (int64_t)pair + (int64_t)i * npairs;
+        if (t >= (int64_t)p.m_tiles * p.n_tiles)
+            return false;
+        mt = (int)(t / p.n_tiles);
+        nt = (int)(t % p.n_tiles);
+        return true;
+    };
+    const int KS = p.k_spans;
+    const int NST = (KS + C::kSpans - 1) / C::kSpans;   // stages per tile
+
+    if (threadIdx.x == 32) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_a) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_b) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_sfa) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_sfb) : "memory");
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(full + s)));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(empty + s)));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(accum)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(saddr(tmem_empty)));   // 4 epilogue warps x 2 CTAs
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(drain)));
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                     "r"(C::kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' barriers exist before either signals the other's
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_sf = tmem + C::BN;
+    const uint32_t full_lead = cluster_addr(saddr(full), 0);
+    int issued = 0;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- loads
+        int g = 0, mt, nt;
+        bool stop = false;
+        for (int ti = 0; !stop && tile_at(ti, mt, nt); ++ti) {
+            const int a_row = mt * 256 + kBM * (int)rank;
+            const int b_row = nt * C::BN + C::kRowsB * (int)rank;
+            const int bt0 = (nt * C::BN) >> 7;                       // the tile's first 128-row scale tile of B
+            const int sfa_tile = mt * 2 + (int)rank;
+            for (int j = 0; j < NST; ++j, ++g) {
+                const int s = g % C::kStages;
+                if (g >= C::kStages &&
+                    !warp_wait(saddr(empty + s), ((uint32_t)(g / C::kStages) & 1u) ^ 1u, abort, p)) {
+                    stop = true;
+                    break;
+                }
+                if (g != p.debug_skip_stage && elect_one()) {   // test hook: that stage never arrives
+                    const int nsp = min(C::kSpans, KS - j * C::kSpans);
+                    if (rank == 0)
+                        mbar_arrive_tx(saddr(full + s), 2 * C::kCtaTx * nsp);
+                    const uint32_t fb = full_lead + 8 * s;
+                    for (int sp = 0; sp < nsp; ++sp) {
+                        const int ks = j * C::kSpans + sp;
+                        uint8_t *st = smem + s * C::kStage + sp * C::kSpanAB;
+                        const int slot = s * C::kSpans + sp;
+                        tma_2d_pair(saddr(st), &map_a, ks * kSpanBytes, a_row, fb);
+                        tma_2d_pair(saddr(st + C::kSpanA), &map_b, ks * kSpanBytes, b_row, fb);
+                        tma_2d_pair(saddr(smem + C::kOffSfa + slot * 1024), &map_sfa, 0, 4 * (sfa_tile * KS + ks), fb);
+#pragma unroll
+                        for (int t = 0; t < C::kSfbAtoms; ++t)
+                            tma_2d_pair(saddr(smem + C::kOffSfb + (slot * C::kSfbAtoms + t) * 1024), &map_sfb, 0,
+                                        4 * ((bt0 + t) * KS + ks), fb);
+                    }
+                }
+                __syncwarp();
+                issued = g + 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1 && rank == 0) {
+        // ------------------------------------------------------------ MMA
+        int g = 0, mt, nt;
+        bool any = false, stop = false;
+        for (int ti = 0; !stop && tile_at(ti, mt, nt); ++ti) {
+            if (ti > 0) {   // both epilogues have read the previous tile's accumulator
+                if (!warp_wait(saddr(tmem_empty), (uint32_t)((ti - 1) & 1), abort, p))
+                    break;
+                tc_fence_after();
+            }
+            for (int j = 0; j < NST; ++j, ++g) {
+                const int s = g % C::kStages;
+                if (!warp_wait(saddr(full + s), (uint32_t)(g / C::kStages) & 1u, abort, p)) {
+                    stop = true;
+                    break;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+                    const int nsp = min(C::kSpans, KS - j * C::kSpans);
+                    for (int sp = 0; sp < nsp; ++sp) {
+                        const int slot = s * C::kSpans + sp;
+                        const uint32_t sfa_col = tmem_sf + s * C::kSfCols + sp * C::kSfColsSpan, sfb_col = sfa_col + 8;
+                        const uint32_t sfa_smem = saddr(smem + C::kOffSfa + slot * 1024);
+                        const uint32_t sfb_smem = saddr(smem + C::kOffSfb + slot * C::kSfbAtoms * 1024);
+                        const uint32_t a_smem = saddr(smem + s * C::kStage + sp * C::kSpanAB),
+                                       b_smem = a_smem + C::kSpanA;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            cp_sf_pair(sfa_col + 4 * c, desc_sf(sfa_smem + c * 512));
+#pragma unroll
+                            for (int t = 0; t < C::kSfbAtoms; ++t)
+                                cp_sf_pair(sfb_col + 4 * C::kSfbAtoms * c + 4 * t,
+                                           desc_sf(sfb_smem + t * 1024 + c * 512));
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int c = k >> 1;
+                            mma_mxf4_pair(tmem, desc_sw128(a_smem + 32 * k), desc_sw128(b_smem + 32 * k),
+                                          idesc_mxf4(C::BN, (k & 1) * 2, 2 * kBM), sfa_col + 4 * c,
+                                          sfb_col + 4 * C::kSfbAtoms * c, (j | sp | k) != 0);
+                        }
+                    }
+                    mma_commit_pair(saddr(empty + s), 3);
+                }
+                __syncwarp();
+                any = true;
+            }
+            if (!stop && elect_one())
+                mma_commit_pair(saddr(accum), 3);   // this tile's accumulators are complete
+            __syncwarp();
+        }
+        if (*abort && any && elect_one()) {
+            // drain the tensor cores before the tensor memory is freed
+            mma_commit_pair(saddr(drain), 1);
+            const uint64_t t0 = gtimer();
+            while (!mbar_test(saddr(drain), 0) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------- epilogue
+        // This CTA's 128 rows of the tile, 32 columns at a time, through
+        // shared memory so that each store instruction writes eight rows'
+        // whole 64-byte pieces (16-byte chunk j of row i at j ^ ((i/2) mod 4):
+        // conflict-free both ways).
+        const int q = warp & 3;
+        uint8_t *const stage_w = smem + C::kOffOut + (warp - 4) * 2048;
+        const uint32_t tmem_empty_lead = cluster_addr(saddr(tmem_empty), 0);
+        const int cj = lane & 3;
+        int mt, nt;
+        for (int ti = 0; tile_at(ti, mt, nt); ++ti) {
+            if (!warp_wait(saddr(accum), (uint32_t)(ti & 1), abort, p))
+                break;
+            tc_fence_after();
+            const int64_t row0 = (int64_t)mt * 256 + kBM * (int)rank + q * 32, n0 = (int64_t)nt * C::BN;
+            const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+            for (int c0 = 0; c0 < C::BN && row0 < p.M && n0 + c0 < p.N; c0 += 32) {   // warp-uniform
+                uint32_t acc[32];
+                tmem_ld32(trow + c0, acc);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 o;
+                    o.x = pack_bf16x2(__uint_as_float(acc[8 * j + 0]), __uint_as_float(acc[8 * j + 1]));
+                    o.y = pack_bf16x2(__uint_as_float(acc[8 * j + 2]), __uint_as_float(acc[8 * j + 3]));
+                    o.z = pack_bf16x2(__uint_as_float(acc[8 * j + 4]), __uint_as_float(acc[8 * j + 5]));
+                    o.w = pack_bf16x2(__uint_as_float(acc[8 * j + 6]), __uint_as_float(acc[8 * j + 7]));
+                    *reinterpret_cast<uint4 *>(stage_w + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = o;
+                }
+                __syncwarp();
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int rr = it * 8 + (lane >> 2);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(stage_w + rr * 64 + ((cj ^ ((rr >> 1) & 3)) << 4));
+                    const int64_t gm = row0 + rr, gn = n0 + c0 + cj * 8;
+                    if (gm < p.M && gn < p.N && RMSQ_IN_BOUNDS(p.status, gn + 8 <= p.N))
+                        *reinterpret_cast<uint4 *>(p.d + gm * p.ldd + gn) = v;
+                }
+                __syncwarp();
+            }
+            // the accumulator may be overwritten by the next tile's MMAs
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(tmem_empty_lead);
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (*abort && threadIdx.x == 0 && rank == 0) {
+        // let the copies of stages this pair armed land before either CTA goes
+        const uint64_t t0 = gtimer();
+        for (int i = (issued > C::kStages ? issued - C::kStages : 0); i < issued; ++i) {
+            if (i == p.debug_skip_stage)
+                continue;
+            const uint32_t fb = saddr(full + i % C::kStages);
+            const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
+            while (!mbar_test(fb, ph) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
+            }
+        }
+    }
+    cluster_sync();   // neither CTA leaves while the other may still signal its barriers or read its memory
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
+    }
+}
+
 // ----------------------------------------------------------------- host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -872,8 +1197,103 @@ cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUte
 
 bool pre_of(const GemmLaunch &g) { return g.a_bf16 != nullptr; }
 
+// 2-D map over a scale-tile array viewed as rows of 256 bytes (one K span of
+// a 128-row tile is four such rows, 1 KB); rows past the end read as zero.
+bool make_scale_map(CUtensorMap *map, const void *base, int64_t rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {256, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {256, 4};
+    cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// CTA pairs resident at once with the pair kernel's shared memory (cached per device)
+int pair_capacity(int dev)
+{
+    static int cap[128];
+    if (dev < 0 || dev >= 128)
+        return 0;
+    if (!cap[dev]) {
+        if (cudaFuncSetAttribute(mxfp4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)PairCfg::kSmem) != cudaSuccess)
+            return 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.dynamicSmemBytes = PairCfg::kSmem;
+        cudaLaunchAttribute cl[1];
+        cl[0].id = cudaLaunchAttributeClusterDimension;
+        cl[0].val.clusterDim.x = 2;
+        cl[0].val.clusterDim.y = 1;
+        cl[0].val.clusterDim.z = 1;
+        cfg.attrs = cl;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mxfp4_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0)
+            return 0;
+        cap[dev] = n;
+    }
+    return cap[dev];
+}
+
+cudaError_t launch_pair(const GemmLaunch &g, cudaStream_t st)
+{
+    GemmParams p{};
+    p.d = (uint16_t *)g.d;
+    p.ldd = g.ldd;
+    p.M = g.M;
+    p.N = g.N;
+    p.k_spans = (int32_t)(g.K / kSpanK);
+    p.b_row_tiles = (int32_t)((g.N + 127) / 128);
+    p.a_box_rows = kBM;
+    p.ksplit = 1;
+    p.persistent = 1;
+    p.m_tiles = (int32_t)((g.M + 255) / 256);
+    p.n_tiles = (int32_t)((g.N + PairCfg::BN - 1) / PairCfg::BN);
+    p.debug_skip_stage = g.debug_skip_stage;
+    p.wait_limit_ns = g.wait_limit_ns;
+    p.status = g.status;
+    const int64_t m_tiles128 = (g.M + 127) / 128;
+    CUtensorMap ma, mb, msa, msb;
+    if (!make_code_map(&ma, g.a_q, g.M, g.K / 2, g.lda, kBM) ||
+        !make_code_map(&mb, g.b_q, g.N, g.K / 2, g.ldb, PairCfg::kRowsB) ||
+        !make_scale_map(&msa, g.a_scale, m_tiles128 * p.k_spans * 4) ||
+        !make_scale_map(&msb, g.b_scale, (int64_t)p.b_row_tiles * p.k_spans * 4))
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const int cap = pair_capacity(dev);
+    if (cap <= 0)
+        return cudaErrorInvalidConfiguration;
+    const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+    const int pairs = (int)(tiles < cap ? tiles : cap);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = PairCfg::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute cl[1];
+    cl[0].id = cudaLaunchAttributeClusterDimension;
+    cl[0].val.clusterDim.x = 2;
+    cl[0].val.clusterDim.y = 1;
+    cl[0].val.clusterDim.z = 1;
+    cfg.attrs = cl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_pair_kernel, p, ma, mb, msa, msb);
+}
+
 cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
 {
+    if (g.pair)
+        return pre_of(g) ? cudaErrorInvalidValue : launch_pair(g, st);
     GemmParams p{};
     p.a_scale = (const uint8_t *)g.a_scale;
     p.b_scale = (const uint8_t *)g.b_scale;
@@ -983,8 +1403,8 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
         return failf(RMSQ_ERR_INVALID_ARG, "wait_limit_ns must be >= 0");
     if (o.debug_stall_stage < 0)
         return failf(RMSQ_ERR_INVALID_ARG, "debug_stall_stage must be >= 0");
-    if (o.schedule < 0 || o.schedule > 2)
-        return failf(RMSQ_ERR_INVALID_ARG, "schedule must be 0, 1 or 2 (got %d)", o.schedule);
+    if (o.schedule < 0 || o.schedule > 3)
+        return failf(RMSQ_ERR_INVALID_ARG, "schedule must be 0, 1, 2 or 3 (got %d)", o.schedule);
     if (K % 256)
         return failf(RMSQ_ERR_UNSUPPORTED, "K=%lld is not a multiple of 256", (long long)K);
     if (N % 8)
@@ -1031,6 +1451,11 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     if (sms <= 0)
         return failf(RMSQ_ERR_CUDA, "SM count query failed");
     int bn = o.bn;
+    if (o.schedule == 3) {
+        if (prequant || (bn && bn != 256) || (o.ksplit && o.ksplit != 1))
+            return failf(RMSQ_ERR_UNSUPPORTED, "the CTA-pair schedule needs quantised A, bn 256 and no K split");
+        bn = 256;
+    }
     if (!bn) {
         if (prequant || m_tiles * ((N + 255) / 256) * 2 >= sms)
             bn = 256;
@@ -1038,7 +1463,7 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
             bn = m_tiles >= 2 ? 128 : 64;
     }
     const int64_t tiles = m_tiles * ((N + bn - 1) / bn);
-    int ksplit = o.ksplit;
+    int ksplit = o.schedule == 3 ? 1 : o.ksplit;
     if (!ksplit) {
         int64_t k = tiles >= sms ? 1 : sms / tiles;
         if (k > 8)
@@ -1053,8 +1478,12 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     // More tiles than SMs (no K split, A quantised): one persistent CTA per
     // SM walks the tiles, so set-up, the ring's first fill and the epilogue
     // overlap the neighbouring tiles' work.
+    // 256-row tiles without a K split (the widest tiles already fill the
+    // SMs): CTA pairs with 256 x 256 tiles, the fastest form measured from
+    // 2048 tokens on (N = 2112, K = 7168).
     bool persistent = !prequant && ksplit == 1 && tiles > sms;
-    if (o.schedule == 1)
+    bool pair = o.schedule == 3 || (o.schedule == 0 && !prequant && ksplit == 1 && bn == 256);
+    if (o.schedule == 1 || pair)
         persistent = false;
     else if (o.schedule == 2) {
         if (prequant || ksplit != 1)
@@ -1080,6 +1509,7 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     g.bn = bn;
     g.ksplit = ksplit;
     g.persistent_ctas = persistent ? (int)(tiles < sms ? tiles : sms) : 0;
+    g.pair = pair;
     g.debug_skip_stage = o.debug_stall_stage - 1;   // -1: off
     g.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
     g.status = status;

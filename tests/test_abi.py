@@ -174,7 +174,7 @@ def test_gemm_specific_checks(L):
     assert gemm(L, True, lda=1000) == 1                      # bf16 A rows are K elements
     assert gemm(L, True, lda=1028) == 2                      # bf16 leading dimension % 8
     assert gemm(L, False, M=0) == 0 and gemm(L, True, N=0) == 0
-    for opts in (rmsq.GemmOpts(bn=96), rmsq.GemmOpts(schedule=3), rmsq.GemmOpts(schedule=-1)):
+    for opts in (rmsq.GemmOpts(bn=96), rmsq.GemmOpts(schedule=4), rmsq.GemmOpts(schedule=-1)):
         assert L.rmsq_mxfp4_gemm_ex(A_Q, 512, A_S, B_Q, 512, B_S, D, 256, 64, 256, 1024, None,
                                     ctypes.byref(opts)) == 1
 

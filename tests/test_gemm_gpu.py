@@ -110,6 +110,42 @@ def test_persistent_schedule(oracle_mod, bn, M, N):
     print(bn, tiles, st)
 
 
+@pytest.mark.parametrize("M,N,K", [(4100, 1160, 1024), (1100, 2112, 2048), (300, 264, 256), (129, 520, 512),
+                                   (1, 256, 768), (600, 8, 1280)])
+def test_pair_schedule(oracle_mod, M, N, K):
+    """CTA pairs (256 x 256 tiles, M = 256 MMAs over two SMs): bit for bit the
+    one-tile-per-CTA result, and the oracle's on sampled rows -- ragged M and
+    N, a pair whose odd CTA has no rows of A (M = 129, M = 1), one span of K."""
+    a_q, a_s, b_q, b_s = operands(400 + M % 97, M, N, K)
+    ga, gb = a_q.to(DEV), b_q.to(DEV)
+    ta, tb = rmsq.mx_scale_tiles(a_s.to(DEV)), rmsq.mx_scale_tiles(b_s.to(DEV))
+    one = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=256, ksplit=1, schedule=1))
+    pair = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(schedule=3))
+    again = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=256, ksplit=1, schedule=3))
+    torch.cuda.synchronize()
+    assert torch.equal(one, pair) and torch.equal(pair, again)
+    rows = np.unique(np.concatenate([np.arange(0, M, 61), [M - 1]]))
+    ref = oracle_mod.mxfp4_gemm(a_q.numpy()[rows], a_s.numpy()[rows], b_q.numpy(), b_s.numpy())
+    st = parity.compare_gemm(pair[torch.from_numpy(rows).to(DEV)], ref, K, what=f"pair M={M} N={N} K={K}")
+    assert st["bit_equal_fraction"] > 0.95, st
+    assert rmsq.sync_status() == 0
+    print(M, N, K, st)
+
+
+def test_pair_schedule_rejects():
+    M, N, K = 256, 256, 512
+    a_q, a_s, b_q, b_s = operands(33, M, N, K)
+    ga, ta = a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV))
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    y = synth.random_bf16(34, (M, K)).to(DEV)
+    for bad in (rmsq.GemmOpts(schedule=3, bn=128), rmsq.GemmOpts(schedule=3, ksplit=2)):
+        with pytest.raises(RuntimeError, match="CTA-pair"):
+            rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=bad)
+    with pytest.raises(RuntimeError, match="CTA-pair"):
+        rmsq.a16wfp4_gemm(y, gb, tb, opts=rmsq.GemmOpts(schedule=3))
+    assert rmsq.sync_status() == 0
+
+
 def test_persistent_schedule_rejects():
     """The persistent schedule walks whole tiles with quantised A only."""
     M, N, K = 128, 256, 512
@@ -266,6 +302,27 @@ def test_bounded_wait_in_a_later_tile():
     one = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=128, ksplit=1, schedule=1))
     torch.cuda.synchronize()
     assert torch.equal(walk, one)
+    assert rmsq.sync_status() == 0
+
+
+def test_pair_bounded_wait_in_a_later_tile():
+    """CTA pairs: the stalled stage (never loaded by either CTA) sits in the
+    second tile of the pairs that walk two (M = 4096, N = 2560: 160 tiles of
+    256 x 256, four stages each). Both CTAs of a stalled pair stop within
+    their wait limits; the host reads RMSQ_ERR_TIMEOUT; the next launch
+    matches the one-tile schedule bit for bit."""
+    M, N, K = 4096, 2560, 1024
+    a_q, a_s, b_q, b_s = operands(64, M, N, K)
+    ga, ta = a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV))
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    stuck = rmsq.GemmOpts(wait_limit_ns=50_000_000, debug_stall_stage=6, schedule=3)
+    rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=stuck)
+    assert rmsq.sync_status() == 5                      # RMSQ_ERR_TIMEOUT
+    assert rmsq.sync_status() == 0
+    pair = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(schedule=3))
+    one = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=256, ksplit=1, schedule=1))
+    torch.cuda.synchronize()
+    assert torch.equal(pair, one)
     assert rmsq.sync_status() == 0
 
 
