@@ -17,12 +17,17 @@
 // bytes per row (one 128-byte swizzle span, four MMAs of K = 64); a ring
 // stage holds one to four spans behind one barrier phase (GemmCfg). With
 // fewer tiles than SMs, the CTAs of a thread-block cluster split K and add
-// their fp32 partial sums through distributed shared memory, in rank order.
+// their fp32 partial sums through distributed shared memory, in rank order;
+// with more, a persistent grid walks the tiles (the ring runs on from one
+// tile into the next). For 256-row B tiles without a K split, CTA pairs
+// (mxfp4_gemm_pair_kernel, tcgen05 cta_group::2) compute 256 x 256 tiles
+// with the tensor cores of two SMs.
 // Warp roles (256 threads): warp 0 issues the TMA and bulk loads; warp 1
 // owns the tensor memory and issues tcgen05.cp (scale factors, shared ->
 // tensor memory) and tcgen05.mma (one elected lane each); warps 4-7 run the
-// epilogue (tcgen05.ld -> bf16 -> global). The prequant kernel has 384
-// threads: warps 4-11 quantise A and then share the epilogue.
+// epilogue (tcgen05.ld -> bf16 -> shared memory -> whole 128-byte lines of
+// D). The prequant kernel has 384 threads: warps 4-11 quantise A and then
+// share the epilogue.
 // Every mbarrier wait is bounded; a wait that runs out sets the status word,
 // makes the other roles stop, drains what is in flight and frees the tensor
 // memory before the CTA exits.
@@ -66,8 +71,8 @@ struct GemmLaunch {
     int ksplit;                // 1..8 CTAs (a cluster) per tile splitting K
     int persistent_ctas;       // > 0: a persistent grid of this many CTAs walks the tiles
     bool pair;                 // 256 x 256 tiles on CTA pairs (persistent, bn 256, quantised A)
-    int debug_skip_stage;      // test hook: a local K stage whose loads are never issued (-1 = off;
-                               // a zero-initialised GemmLaunch must set it)
+    int debug_skip_stage;      // test hook: a ring stage (counted over the CTA's tiles) whose loads
+                               // are never issued (-1 = off; a zero-initialised GemmLaunch must set it)
     int64_t wait_limit_ns;
     unsigned int *status;
 };
@@ -139,8 +144,8 @@ struct GemmParams {
     int32_t a_box_rows;         // rows of A per TMA box: 128, or M rounded up to 8 when M < 128
     int32_t ksplit;             // CTAs of a cluster that split K (1 = no split)
     int32_t persistent;         // 1: a grid of gridDim.x CTAs walks the m_tiles x n_tiles tiles
-    int32_t m_tiles, n_tiles;
-    int32_t debug_skip_stage;   // test hook: the loads of this local stage are never issued (-1 = off)
+    int32_t m_tiles, n_tiles;   // tiles of the launch (the pair kernel: 256-row tiles of A and B)
+    int32_t debug_skip_stage;   // test hook: this ring stage (counted over the CTA's tiles) is never loaded (-1 = off)
     int64_t wait_limit_ns;
     unsigned int *status;
 };
