@@ -403,8 +403,8 @@ rmsq_status qknorm_common(bool mx, const void *q_a, int64_t ld_q, const void *kv
     // first.
     int v0 = 0, v1 = 0, tq = 0, tk = 0, t0s = 0, t1s = 0;
     const int gv = mx ? 4 : 16;
-    if (Hq == 3 * 64 * 8 && Hkv == 4 * 16 * 8) {
-        v0 = 3; tq = 64; v1 = 4; tk = 16; t0s = 64; t1s = 16;
+    if (Hq == 6 * 32 * 8 && Hkv == 4 * 16 * 8) {
+        v0 = 6; tq = 32; v1 = 4; tk = 16; t0s = 32; t1s = 16;
     } else {
         int64_t best_waste = -1;
         for (int v : kVptPreference) {

@@ -3,9 +3,13 @@
 
 namespace rmsq {
 
+// The MLA latent pair (q_a 1536, kv_a 512): one warp per q_a row with six
+// vectors per thread (no cross-warp step: 14.73 against 15.59 us for the
+// FP8 pair at M = 8192 with a two-warp team of three vectors each), and
+// 16-thread teams of four vectors for kv_a.
 bool static_dual_shape(int v0, int t0, int v1, int t1)
 {
-    return v0 == 3 && t0 == 64 && v1 == 4 && t1 == 16;
+    return v0 == 6 && t0 == 32 && v1 == 4 && t1 == 16;
 }
 
 template <bool MX>
@@ -14,7 +18,7 @@ cudaError_t launch_dual_impl(int v0, int t0, int v1, int t1, const LaunchParams 
 {
     if (t0 || t1) {
         if (static_dual_shape(v0, t0, v1, t1))
-            dual_kernel<3, 64, 4, 16, MX><<<grid, threads, 0, st>>>(p);
+            dual_kernel<6, 32, 4, 16, MX><<<grid, threads, 0, st>>>(p);
         else
             return cudaErrorInvalidValue;
         return cudaGetLastError();

@@ -132,6 +132,28 @@ def test_pair_schedule(oracle_mod, M, N, K):
     print(M, N, K, st)
 
 
+def test_pair_schedule_strided(oracle_mod):
+    """CTA pairs with leading dimensions wider than a row for A, B and D."""
+    M, N, K = 700, 520, 1536
+    a_q, a_s, b_q, b_s = operands(75, M, N, K)
+    pa = torch.zeros((M, K // 2 + 176), dtype=torch.uint8)
+    pa[:, :K // 2] = a_q
+    pb = torch.zeros((N, K // 2 + 48), dtype=torch.uint8)
+    pb[:, :K // 2] = b_q
+    ga, gb = pa.to(DEV)[:, :K // 2], pb.to(DEV)[:, :K // 2]
+    ta, tb = rmsq.mx_scale_tiles(a_s.to(DEV)), rmsq.mx_scale_tiles(b_s.to(DEV))
+    dbig = torch.zeros((M, N + 40), dtype=torch.bfloat16, device=DEV)
+    d = rmsq.mxfp4_gemm(ga, ta, gb, tb, out=dbig[:, :N], opts=rmsq.GemmOpts(schedule=3))
+    one = rmsq.mxfp4_gemm(a_q.to(DEV), ta, b_q.to(DEV), tb, opts=rmsq.GemmOpts(bn=256, ksplit=1, schedule=1))
+    torch.cuda.synchronize()
+    assert torch.equal(d, one)
+    assert (dbig[:, N:] == 0).all()
+    rows = np.unique(np.concatenate([np.arange(0, M, 37), [M - 1]]))
+    ref = oracle_mod.mxfp4_gemm(a_q.numpy()[rows], a_s.numpy()[rows], b_q.numpy(), b_s.numpy())
+    parity.compare_gemm(d[torch.from_numpy(rows).to(DEV)], ref, K, what="pair, strided A, B, D")
+    assert rmsq.sync_status() == 0
+
+
 def test_pair_schedule_rejects():
     M, N, K = 256, 256, 512
     a_q, a_s, b_q, b_s = operands(33, M, N, K)
