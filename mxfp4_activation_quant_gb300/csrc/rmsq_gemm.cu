@@ -346,9 +346,14 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank)
     return r;
 }
 
+// Relaxed arrival on a barrier of either CTA of the pair. The epilogue uses it
+// to hand the accumulator back: the only ordering needed is that its
+// tensor-memory loads are complete, which tcgen05.wait::ld has established
+// before the arrival is issued. (A cluster-scope release here would also wait
+// for the warp's outstanding stores of D.)
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -1063,10 +1068,9 @@ __global__ void __launch_bounds__(256, 1)
             tc_fence_after();
             const int64_t row0 = (int64_t)mt * 256 + kBM * (int)rank + q * 32, n0 = (int64_t)nt * C::BN;
             const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-            for (int c0 = 0; c0 < C::BN && row0 < p.M && n0 + c0 < p.N; c0 += 32) {   // warp-uniform
-                uint32_t acc[32];
-                tmem_ld32(trow + c0, acc);
+            // 32-column chunks of D this warp writes (warp-uniform; N is a multiple of 8)
+            const int nch = row0 < p.M ? (int)((min((int64_t)C::BN, p.N - n0) + 31) / 32) : 0;
+            auto store_chunk = [&](const uint32_t(&acc)[32], int c0) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     uint4 o;
@@ -1086,12 +1090,45 @@ __global__ void __launch_bounds__(256, 1)
                         *reinterpret_cast<uint4 *>(p.d + gm * p.ldd + gn) = v;
                 }
                 __syncwarp();
+            };
+            // the accumulator may be overwritten by the next tile's MMAs once
+            // this warp's last tensor-memory load is complete
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster(tmem_empty_lead);
+            };
+            // Chunk c + 1 is loaded from tensor memory while chunk c goes to D.
+            uint32_t a[32], b[32];
+            if (nch > 0) {
+                tmem_ld32_issue(trow, a);
+                tmem_ld_wait();
+                tmem_hold(a);
+            } else {
+                release();
             }
-            // the accumulator may be overwritten by the next tile's MMAs
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive_cluster(tmem_empty_lead);
+#pragma unroll 1
+            for (int c = 0; c < nch; c += 2) {
+                if (c + 1 < nch)
+                    tmem_ld32_issue(trow + (c + 1) * 32, b);
+                else
+                    release();
+                store_chunk(a, c * 32);
+                if (c + 1 < nch) {
+                    tmem_ld_wait();
+                    tmem_hold(b);
+                    if (c + 2 < nch)
+                        tmem_ld32_issue(trow + (c + 2) * 32, a);
+                    else
+                        release();
+                    store_chunk(b, (c + 1) * 32);
+                    if (c + 2 < nch) {
+                        tmem_ld_wait();
+                        tmem_hold(a);
+                    }
+                }
+            }
         }
     }
 
