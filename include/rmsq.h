@@ -280,10 +280,13 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
 /*
  * Optional control of the GEMM launch (NULL = defaults), for tests and
  * tuning; results do not depend on it.
- *   bn             rows of B per CTA tile: 64, 128 or 256; 0 = auto (256 for
- *                  the prequant GEMM, which quantises A once per B tile; for
- *                  the plain GEMM 256 once that gives half the SMs a tile,
- *                  else 128 with two or more 128-row tiles of A, else 64)
+ *   bn             rows of B per CTA tile: 64, 128 or 256, or 192 with the
+ *                  CTA-pair schedule only (then rows of B per pair tile);
+ *                  0 = auto (256 for the prequant GEMM, which quantises A
+ *                  once per B tile; for the plain GEMM 256 once that gives
+ *                  half the SMs a tile, else 128 with two or more 128-row
+ *                  tiles of A, else 64; CTA pairs take 256 or 192, whichever
+ *                  leaves the busiest pair the least work)
  *   ksplit         CTAs, launched as one thread-block cluster, that split K
  *                  for each tile and add their fp32 partial sums through
  *                  distributed shared memory (rank order, so deterministic):
@@ -307,9 +310,10 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
  *                  persistent: one CTA per SM walks the tiles, so a tile's
  *                  set-up, first loads and epilogue overlap its neighbours'
  *                  work (quantised A and ksplit 1 only), 3 = persistent CTA
- *                  pairs: a cluster of two CTAs computes 256 x 256 tiles
- *                  with the tensor cores of both SMs (quantised A, bn 0 or
- *                  256, ksplit 0 or 1). Results do not depend on it.
+ *                  pairs: a cluster of two CTAs computes 256 x 256 (or
+ *                  256 x 192, two accumulators) tiles with the tensor cores
+ *                  of both SMs (quantised A, bn 0, 192 or 256, ksplit 0 or
+ *                  1). Results do not depend on it.
  */
 typedef struct rmsq_gemm_opts {
     int32_t bn;

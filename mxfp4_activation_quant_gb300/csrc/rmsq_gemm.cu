@@ -862,57 +862,66 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
 }
 
 // ------------------------------------------------------ CTA-pair kernel
-// A cluster of two CTAs computes 256 x 256 tiles of D (persistent: pair
+// A cluster of two CTAs computes 256 x BN tiles of D (persistent: pair
 // blockIdx.x / 2 walks tiles pair, pair + pairs, ... in N-fastest order) with
 // M = 256 MMAs issued by the even CTA. CTA r loads its 128 rows of A and rows
-// 128r.. of the tile's 256 rows of B, so a span of K costs each SM 32 KB of
-// operands (48 KB for a 128 x 256 tile of its own): the ring holds six
-// stages instead of four. Each CTA also loads the tile's A scales for its
-// rows and ALL of its B scales (the MMA reads both from each SM's own tensor
-// memory); every copy of both CTAs completes on the even CTA's `full`
-// barrier, which the even CTA arms for both. The MMA commits arrive on both
-// CTAs' `empty` and `accum` barriers; both epilogues (their own 128 rows, in
-// their own tensor memory) arrive on the even CTA's `tmem_empty`.
-// Stage shape measured on GB300 (N = 2112, K = 7168, M = 8192): one span x
-// six stages 50.7 us, one x five 51.6 us, two spans x three stages 56.2 us.
+// (BN/2)r.. of the tile's BN rows of B, so a span of K costs each SM 32 KB of
+// operands at BN = 256 (48 KB for a 128 x 256 tile of its own). Each CTA also
+// loads the tile's A scales for its rows and ALL of its B scales (the MMA
+// reads both from each SM's own tensor memory); every copy of both CTAs
+// completes on the even CTA's `full` barrier, which the even CTA arms for
+// both. The MMA commits arrive on both CTAs' `empty` and `accum` barriers;
+// both epilogues (their own 128 rows, in their own tensor memory) arrive on
+// the even CTA's `tmem_empty`.
+// BN = 256: one accumulator, six ring stages. BN = 192: two accumulators
+// (the MMAs of the next tile run while the epilogue drains the last) and five
+// stages; 2 x 192 accumulator columns leave room for five stages' scale
+// factors. Each stage's scale factors keep their own tensor-memory slot, so
+// a slot is free again when the producer may refill the stage. (A separate
+// ring of five slots under seven stages, where the MMA warp waited for the
+// commit of stage g - 5 before reusing a slot, starved the tensor pipe:
+// 64.4 us at M = 8192 against 48.2 us.)
+// Stage shape measured on GB300 (BN = 256, N = 2112, K = 7168, M = 8192): one
+// span x six stages 50.7 us, one x five 51.6 us, two spans x three 56.2 us.
+template <int BN_>
 struct PairCfg {
-    static constexpr int BN = 256;                     // columns of D per tile
+    static constexpr int BN = BN_;                     // columns of D per tile
     static constexpr int kRowsB = BN / 2;              // rows of B per CTA
     static constexpr int kSpanA = kBM * kSpanBytes;
     static constexpr int kSpanB = kRowsB * kSpanBytes;
-    static constexpr int kSpanAB = kSpanA + kSpanB;
-    static constexpr int kSpans = 1;                   // spans of K per stage (one barrier phase)
-    static constexpr int kStage = kSpans * kSpanAB;
-    static constexpr int kSfbAtoms = BN / 128;
-    static constexpr int kStages = 6;
+    static constexpr int kStage = kSpanA + kSpanB;     // one span of K per stage
+    static constexpr int kSfbAtoms = 2;                // 128-row scale tiles of B a tile touches
+    static constexpr int kStages = BN == 256 ? 6 : 5;
+    static constexpr int kAcc = BN == 256 ? 1 : 2;     // accumulators in tensor memory
     static constexpr int kOffSfa = kStages * kStage;
-    static constexpr int kOffSfb = kOffSfa + kStages * kSpans * 1024;
-    static constexpr int kOffOut = kOffSfb + kStages * kSpans * kSfbAtoms * 1024;
+    static constexpr int kOffSfb = kOffSfa + kStages * 1024;
+    static constexpr int kOffOut = kOffSfb + kStages * kSfbAtoms * 1024;
     static constexpr int kOutBytes = 4 * 2048;         // each epilogue warp: 32 rows x 64 bytes of D
     static constexpr int kOffBar = kOffOut + kOutBytes;
-    static constexpr int kBarBytes = (2 * kStages + 3) * 8 + 16;
+    static constexpr int kBarBytes = (2 * kStages + 2 * kAcc + 1) * 8 + 16;
     static constexpr size_t kSmem = 1024 + kOffBar + kBarBytes;
-    static constexpr int kSfColsSpan = 8 + 8 * kSfbAtoms;   // scale-factor TMEM columns per span
-    static constexpr int kSfCols = kSpans * kSfColsSpan;     // ... per stage
-    static constexpr int kTmemCols = pow2_at_least(BN + kStages * kSfCols);
-    static constexpr uint32_t kCtaTx = kSpanA + kSpanB + 1024 + kSfbAtoms * 1024;   // bytes per CTA per span
-    static_assert(kTmemCols <= 512, "tensor memory");
+    static constexpr int kSfCols = 8 + 8 * kSfbAtoms;  // scale-factor TMEM columns per stage
+    static constexpr int kTmemCols = pow2_at_least(kAcc * BN + kStages * kSfCols);
+    static constexpr uint32_t kCtaTx = kSpanA + kSpanB + 1024 + kSfbAtoms * 1024;   // bytes per CTA per stage
+    static_assert(BN == 256 || BN == 192, "tile width");
+    static_assert(kAcc * BN + kStages * kSfCols <= 512, "tensor memory");
     static_assert(kSmem <= 232448, "shared memory");
 };
 
+template <int BN>
 __global__ void __launch_bounds__(256, 1)
     mxfp4_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                            const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sfa,
                            const __grid_constant__ CUtensorMap map_sfb)
 {
-    using C = PairCfg;
+    using C = PairCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *full = (uint64_t *)(smem + C::kOffBar);
     uint64_t *empty = full + C::kStages;
-    uint64_t *accum = empty + C::kStages;
-    uint64_t *tmem_empty = accum + 1;
-    uint64_t *drain = tmem_empty + 1;
+    uint64_t *accum = empty + C::kStages;          // [kAcc]
+    uint64_t *tmem_empty = accum + C::kAcc;        // [kAcc]
+    uint64_t *drain = tmem_empty + C::kAcc;
     uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     volatile int *abort = (volatile int *)(tmem_slot + 1);
 
@@ -920,7 +929,7 @@ __global__ void __launch_bounds__(256, 1)
     uint32_t rank;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
     const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
-    auto tile_at = [&](int i, int &mt, int &nt) -> bool {   // mt: 256-row tile of A, nt: 256-row tile of B
+    auto tile_at = [&](int i, int &mt, int &nt) -> bool {   // mt: 256-row tile of A, nt: BN-row tile of B
         const int64_t t = (int64_t)pair + (int64_t)i * npairs;
         if (t >= (int64_t)p.m_tiles * p.n_tiles)
             return false;
@@ -928,8 +937,7 @@ __global__ void __launch_bounds__(256, 1)
         nt = (int)(t % p.n_tiles);
         return true;
     };
-    const int KS = p.k_spans;
-    const int NST = (KS + C::kSpans - 1) / C::kSpans;   // stages per tile
+    const int KS = p.k_spans;   // stages per tile
 
     if (threadIdx.x == 32) {
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_a) : "memory");
@@ -942,8 +950,10 @@ __global__ void __launch_bounds__(256, 1)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(full + s)));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(empty + s)));
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(accum)));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(saddr(tmem_empty)));   // 4 epilogue warps x 2 CTAs
+        for (int a = 0; a < C::kAcc; ++a) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(accum + a)));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(saddr(tmem_empty + a)));   // 4 warps x 2 CTAs
+        }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(drain)));
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -958,7 +968,7 @@ __global__ void __launch_bounds__(256, 1)
     cluster_sync();   // both CTAs' barriers exist before either signals the other's
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_sf = tmem + C::BN;
+    const uint32_t tmem_sf = tmem + C::kAcc * BN;
     const uint32_t full_lead = cluster_addr(saddr(full), 0);
     int issued = 0;
 
@@ -968,10 +978,10 @@ __global__ void __launch_bounds__(256, 1)
         bool stop = false;
         for (int ti = 0; !stop && tile_at(ti, mt, nt); ++ti) {
             const int a_row = mt * 256 + kBM * (int)rank;
-            const int b_row = nt * C::BN + C::kRowsB * (int)rank;
-            const int bt0 = (nt * C::BN) >> 7;                       // the tile's first 128-row scale tile of B
+            const int b_row = nt * BN + C::kRowsB * (int)rank;
+            const int bt0 = (nt * BN) >> 7;                       // the tile's first 128-row scale tile of B
             const int sfa_tile = mt * 2 + (int)rank;
-            for (int j = 0; j < NST; ++j, ++g) {
+            for (int j = 0; j < KS; ++j, ++g) {
                 const int s = g % C::kStages;
                 if (g >= C::kStages &&
                     !warp_wait(saddr(empty + s), ((uint32_t)(g / C::kStages) & 1u) ^ 1u, abort, p)) {
@@ -979,22 +989,17 @@ __global__ void __launch_bounds__(256, 1)
                     break;
                 }
                 if (g != p.debug_skip_stage && elect_one()) {   // test hook: that stage never arrives
-                    const int nsp = min(C::kSpans, KS - j * C::kSpans);
                     if (rank == 0)
-                        mbar_arrive_tx(saddr(full + s), 2 * C::kCtaTx * nsp);
+                        mbar_arrive_tx(saddr(full + s), 2 * C::kCtaTx);
                     const uint32_t fb = full_lead + 8 * s;
-                    for (int sp = 0; sp < nsp; ++sp) {
-                        const int ks = j * C::kSpans + sp;
-                        uint8_t *st = smem + s * C::kStage + sp * C::kSpanAB;
-                        const int slot = s * C::kSpans + sp;
-                        tma_2d_pair(saddr(st), &map_a, ks * kSpanBytes, a_row, fb);
-                        tma_2d_pair(saddr(st + C::kSpanA), &map_b, ks * kSpanBytes, b_row, fb);
-                        tma_2d_pair(saddr(smem + C::kOffSfa + slot * 1024), &map_sfa, 0, 4 * (sfa_tile * KS + ks), fb);
+                    uint8_t *st = smem + s * C::kStage;
+                    tma_2d_pair(saddr(st), &map_a, j * kSpanBytes, a_row, fb);
+                    tma_2d_pair(saddr(st + C::kSpanA), &map_b, j * kSpanBytes, b_row, fb);
+                    tma_2d_pair(saddr(smem + C::kOffSfa + s * 1024), &map_sfa, 0, 4 * (sfa_tile * KS + j), fb);
 #pragma unroll
-                        for (int t = 0; t < C::kSfbAtoms; ++t)
-                            tma_2d_pair(saddr(smem + C::kOffSfb + (slot * C::kSfbAtoms + t) * 1024), &map_sfb, 0,
-                                        4 * ((bt0 + t) * KS + ks), fb);
-                    }
+                    for (int t = 0; t < C::kSfbAtoms; ++t)
+                        tma_2d_pair(saddr(smem + C::kOffSfb + (s * C::kSfbAtoms + t) * 1024), &map_sfb, 0,
+                                    4 * ((bt0 + t) * KS + j), fb);
                 }
                 __syncwarp();
                 issued = g + 1;
@@ -1006,12 +1011,17 @@ __global__ void __launch_bounds__(256, 1)
         int g = 0, mt, nt;
         bool any = false, stop = false;
         for (int ti = 0; !stop && tile_at(ti, mt, nt); ++ti) {
-            if (ti > 0) {   // both epilogues have read the previous tile's accumulator
-                if (!warp_wait(saddr(tmem_empty), (uint32_t)((ti - 1) & 1), abort, p))
+            const int acc_slot = ti % C::kAcc, use = ti / C::kAcc;
+            if (use > 0) {   // both epilogues have read this accumulator's previous tile
+                if (!warp_wait(saddr(tmem_empty + acc_slot), (uint32_t)((use - 1) & 1), abort, p))
                     break;
                 tc_fence_after();
             }
-            for (int j = 0; j < NST; ++j, ++g) {
+            const uint32_t d_tmem = tmem + acc_slot * BN;
+            // a tile that starts half-way into a 128-row scale tile of B (BN =
+            // 192, odd tiles) reads its rows' scale columns from 2 on
+            const uint32_t sfb_row_col = (uint32_t)(((nt * BN) >> 6) & 1) * 2;
+            for (int j = 0; j < KS; ++j, ++g) {
                 const int s = g % C::kStages;
                 if (!warp_wait(saddr(full + s), (uint32_t)(g / C::kStages) & 1u, abort, p)) {
                     stop = true;
@@ -1019,29 +1029,23 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 tc_fence_after();
                 if (elect_one()) {
-                    const int nsp = min(C::kSpans, KS - j * C::kSpans);
-                    for (int sp = 0; sp < nsp; ++sp) {
-                        const int slot = s * C::kSpans + sp;
-                        const uint32_t sfa_col = tmem_sf + s * C::kSfCols + sp * C::kSfColsSpan, sfb_col = sfa_col + 8;
-                        const uint32_t sfa_smem = saddr(smem + C::kOffSfa + slot * 1024);
-                        const uint32_t sfb_smem = saddr(smem + C::kOffSfb + slot * C::kSfbAtoms * 1024);
-                        const uint32_t a_smem = saddr(smem + s * C::kStage + sp * C::kSpanAB),
-                                       b_smem = a_smem + C::kSpanA;
+                    const uint32_t sfa_col = tmem_sf + s * C::kSfCols, sfb_col = sfa_col + 8;
+                    const uint32_t sfa_smem = saddr(smem + C::kOffSfa + s * 1024);
+                    const uint32_t sfb_smem = saddr(smem + C::kOffSfb + s * C::kSfbAtoms * 1024);
+                    const uint32_t a_smem = saddr(smem + s * C::kStage), b_smem = a_smem + C::kSpanA;
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            cp_sf_pair(sfa_col + 4 * c, desc_sf(sfa_smem + c * 512));
+                    for (int c = 0; c < 2; ++c) {
+                        cp_sf_pair(sfa_col + 4 * c, desc_sf(sfa_smem + c * 512));
 #pragma unroll
-                            for (int t = 0; t < C::kSfbAtoms; ++t)
-                                cp_sf_pair(sfb_col + 4 * C::kSfbAtoms * c + 4 * t,
-                                           desc_sf(sfb_smem + t * 1024 + c * 512));
-                        }
+                        for (int t = 0; t < C::kSfbAtoms; ++t)
+                            cp_sf_pair(sfb_col + 4 * C::kSfbAtoms * c + 4 * t, desc_sf(sfb_smem + t * 1024 + c * 512));
+                    }
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int c = k >> 1;
-                            mma_mxf4_pair(tmem, desc_sw128(a_smem + 32 * k), desc_sw128(b_smem + 32 * k),
-                                          idesc_mxf4(C::BN, (k & 1) * 2, 2 * kBM), sfa_col + 4 * c,
-                                          sfb_col + 4 * C::kSfbAtoms * c, (j | sp | k) != 0);
-                        }
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = k >> 1;
+                        mma_mxf4_pair(d_tmem, desc_sw128(a_smem + 32 * k), desc_sw128(b_smem + 32 * k),
+                                      idesc_mxf4(BN, (k & 1) * 2, 2 * kBM), sfa_col + 4 * c,
+                                      sfb_col + 4 * C::kSfbAtoms * c + sfb_row_col, (j | k) != 0);
                     }
                     mma_commit_pair(saddr(empty + s), 3);
                 }
@@ -1049,7 +1053,7 @@ __global__ void __launch_bounds__(256, 1)
                 any = true;
             }
             if (!stop && elect_one())
-                mma_commit_pair(saddr(accum), 3);   // this tile's accumulators are complete
+                mma_commit_pair(saddr(accum + acc_slot), 3);   // this tile's accumulators are complete
             __syncwarp();
         }
         if (*abort && any && elect_one()) {
@@ -1068,17 +1072,18 @@ __global__ void __launch_bounds__(256, 1)
         // conflict-free both ways).
         const int q = warp & 3;
         uint8_t *const stage_w = smem + C::kOffOut + (warp - 4) * 2048;
-        const uint32_t tmem_empty_lead = cluster_addr(saddr(tmem_empty), 0);
         const int cj = lane & 3;
         int mt, nt;
         for (int ti = 0; tile_at(ti, mt, nt); ++ti) {
-            if (!warp_wait(saddr(accum), (uint32_t)(ti & 1), abort, p))
+            const int acc_slot = ti % C::kAcc, use = ti / C::kAcc;
+            if (!warp_wait(saddr(accum + acc_slot), (uint32_t)(use & 1), abort, p))
                 break;
             tc_fence_after();
-            const int64_t row0 = (int64_t)mt * 256 + kBM * (int)rank + q * 32, n0 = (int64_t)nt * C::BN;
-            const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+            const int64_t row0 = (int64_t)mt * 256 + kBM * (int)rank + q * 32, n0 = (int64_t)nt * BN;
+            const uint32_t trow = tmem + acc_slot * BN + ((uint32_t)(q * 32) << 16);
+            const uint32_t tmem_empty_lead = cluster_addr(saddr(tmem_empty + acc_slot), 0);
             // 32-column chunks of D this warp writes (warp-uniform; N is a multiple of 8)
-            const int nch = row0 < p.M ? (int)((min((int64_t)C::BN, p.N - n0) + 31) / 32) : 0;
+            const int nch = row0 < p.M ? (int)((min((int64_t)BN, p.N - n0) + 31) / 32) : 0;
             auto store_chunk = [&](const uint32_t(&acc)[32], int c0) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -1100,8 +1105,8 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 __syncwarp();
             };
-            // the accumulator may be overwritten by the next tile's MMAs once
-            // this warp's last tensor-memory load is complete
+            // the accumulator may be overwritten by the MMAs of a later tile
+            // once this warp's last tensor-memory load is complete
             auto release = [&]() {
                 tc_fence_before();
                 __syncwarp();
@@ -1265,19 +1270,21 @@ bool make_scale_map(CUtensorMap *map, const void *base, int64_t rows)
 }
 
 // CTA pairs resident at once with the pair kernel's shared memory (cached per device)
+template <int BN>
 int pair_capacity(int dev)
 {
+    using C = PairCfg<BN>;
     static int cap[128];
     if (dev < 0 || dev >= 128)
         return 0;
     if (!cap[dev]) {
-        if (cudaFuncSetAttribute(mxfp4_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)PairCfg::kSmem) != cudaSuccess)
+        if (cudaFuncSetAttribute(mxfp4_gemm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::kSmem) != cudaSuccess)
             return 0;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2, 1, 1);
         cfg.blockDim = dim3(256, 1, 1);
-        cfg.dynamicSmemBytes = PairCfg::kSmem;
+        cfg.dynamicSmemBytes = C::kSmem;
         cudaLaunchAttribute cl[1];
         cl[0].id = cudaLaunchAttributeClusterDimension;
         cl[0].val.clusterDim.x = 2;
@@ -1286,15 +1293,17 @@ int pair_capacity(int dev)
         cfg.attrs = cl;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, mxfp4_gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveClusters(&n, mxfp4_gemm_pair_kernel<BN>, &cfg) != cudaSuccess || n <= 0)
             return 0;
         cap[dev] = n;
     }
     return cap[dev];
 }
 
-cudaError_t launch_pair(const GemmLaunch &g, cudaStream_t st)
+template <int BN>
+cudaError_t launch_pair_t(const GemmLaunch &g, cudaStream_t st)
 {
+    using C = PairCfg<BN>;
     GemmParams p{};
     p.d = (uint16_t *)g.d;
     p.ldd = g.ldd;
@@ -1306,14 +1315,14 @@ cudaError_t launch_pair(const GemmLaunch &g, cudaStream_t st)
     p.ksplit = 1;
     p.persistent = 1;
     p.m_tiles = (int32_t)((g.M + 255) / 256);
-    p.n_tiles = (int32_t)((g.N + PairCfg::BN - 1) / PairCfg::BN);
+    p.n_tiles = (int32_t)((g.N + BN - 1) / BN);
     p.debug_skip_stage = g.debug_skip_stage;
     p.wait_limit_ns = g.wait_limit_ns;
     p.status = g.status;
     const int64_t m_tiles128 = (g.M + 127) / 128;
     CUtensorMap ma, mb, msa, msb;
     if (!make_code_map(&ma, g.a_q, g.M, g.K / 2, g.lda, kBM) ||
-        !make_code_map(&mb, g.b_q, g.N, g.K / 2, g.ldb, PairCfg::kRowsB) ||
+        !make_code_map(&mb, g.b_q, g.N, g.K / 2, g.ldb, C::kRowsB) ||
         !make_scale_map(&msa, g.a_scale, m_tiles128 * p.k_spans * 4) ||
         !make_scale_map(&msb, g.b_scale, (int64_t)p.b_row_tiles * p.k_spans * 4))
         return cudaErrorInvalidValue;
@@ -1321,7 +1330,7 @@ cudaError_t launch_pair(const GemmLaunch &g, cudaStream_t st)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    const int cap = pair_capacity(dev);
+    const int cap = pair_capacity<BN>(dev);
     if (cap <= 0)
         return cudaErrorInvalidConfiguration;
     const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
@@ -1329,7 +1338,7 @@ cudaError_t launch_pair(const GemmLaunch &g, cudaStream_t st)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
-    cfg.dynamicSmemBytes = PairCfg::kSmem;
+    cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute cl[1];
     cl[0].id = cudaLaunchAttributeClusterDimension;
@@ -1338,7 +1347,16 @@ cudaError_t launch_pair(const GemmLaunch &g, cudaStream_t st)
     cl[0].val.clusterDim.z = 1;
     cfg.attrs = cl;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_pair_kernel, p, ma, mb, msa, msb);
+    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_pair_kernel<BN>, p, ma, mb, msa, msb);
+}
+
+cudaError_t launch_pair(const GemmLaunch &g, cudaStream_t st)
+{
+    switch (g.bn) {
+    case 256: return launch_pair_t<256>(g, st);
+    case 192: return launch_pair_t<192>(g, st);
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
@@ -1446,8 +1464,10 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     const rmsq_gemm_opts o = opts ? *opts : kDefaultGemmOpts;
     if (M < 0 || N < 0 || K <= 0)
         return set_error(RMSQ_ERR_INVALID_ARG, "need M >= 0, N >= 0, K > 0");
-    if (o.bn != 0 && o.bn != 64 && o.bn != 128 && o.bn != 256)
-        return failf(RMSQ_ERR_INVALID_ARG, "bn must be 0, 64, 128 or 256 (got %d)", o.bn);
+    if (o.bn != 0 && o.bn != 64 && o.bn != 128 && o.bn != 192 && o.bn != 256)
+        return failf(RMSQ_ERR_INVALID_ARG, "bn must be 0, 64, 128, 192 or 256 (got %d)", o.bn);
+    if (o.bn == 192 && o.schedule != 3)
+        return failf(RMSQ_ERR_UNSUPPORTED, "bn 192 is a width of the CTA-pair schedule only");
     if (o.ksplit < 0 || o.ksplit > 8)
         return failf(RMSQ_ERR_INVALID_ARG, "ksplit must be 0..8 (got %d)", o.ksplit);
     if (o.wait_limit_ns < 0)
@@ -1503,9 +1523,11 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
         return failf(RMSQ_ERR_CUDA, "SM count query failed");
     int bn = o.bn;
     if (o.schedule == 3) {
-        if (prequant || (bn && bn != 256) || (o.ksplit && o.ksplit != 1))
-            return failf(RMSQ_ERR_UNSUPPORTED, "the CTA-pair schedule needs quantised A, bn 256 and no K split");
-        bn = 256;
+        if (prequant || (bn && bn != 256 && bn != 192) || (o.ksplit && o.ksplit != 1))
+            return failf(RMSQ_ERR_UNSUPPORTED,
+                         "the CTA-pair schedule needs quantised A, bn 192 or 256 and no K split");
+        if (!bn)
+            bn = 256;
     }
     if (!bn) {
         if (prequant || m_tiles * ((N + 255) / 256) * 2 >= sms)
@@ -1536,6 +1558,19 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     bool pair = o.schedule == 3 || (o.schedule == 0 && !prequant && ksplit == 1 && bn == 256);
     if (o.schedule == 1 || pair)
         persistent = false;
+    if (pair && !o.bn) {
+        // Pair tile width: the one whose busiest pair does the least work,
+        // counting a 192-wide tile as 0.75 of a 256-wide one and charging it
+        // 4 % for its lower efficiency per column (measured: 12.8 against
+        // 12.3 us per 256-column unit at N = 2112, K = 7168).
+        const int cap256 = pair_capacity<256>(dev), cap192 = pair_capacity<192>(dev);
+        if (cap256 <= 0 || cap192 <= 0)
+            return failf(RMSQ_ERR_CUDA, "cluster occupancy query failed");
+        const int64_t mt2 = (M + 255) / 256;
+        const int64_t w256 = (mt2 * ((N + 255) / 256) + cap256 - 1) / cap256 * 256;
+        const int64_t w192 = (mt2 * ((N + 191) / 192) + cap192 - 1) / cap192 * 192;
+        bn = w192 * 104 < w256 * 100 ? 192 : 256;
+    }
     else if (o.schedule == 2) {
         if (prequant || ksplit != 1)
             return failf(RMSQ_ERR_UNSUPPORTED, "the persistent schedule needs quantised A and no K split");

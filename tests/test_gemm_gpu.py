@@ -110,18 +110,21 @@ def test_persistent_schedule(oracle_mod, bn, M, N):
     print(bn, tiles, st)
 
 
+@pytest.mark.parametrize("bn", [256, 192])
 @pytest.mark.parametrize("M,N,K", [(4100, 1160, 1024), (1100, 2112, 2048), (300, 264, 256), (129, 520, 512),
-                                   (1, 256, 768), (600, 8, 1280)])
-def test_pair_schedule(oracle_mod, M, N, K):
-    """CTA pairs (256 x 256 tiles, M = 256 MMAs over two SMs): bit for bit the
+                                   (1, 256, 768), (600, 8, 1280), (8192, 2112, 512)])
+def test_pair_schedule(oracle_mod, M, N, K, bn):
+    """CTA pairs (256 x bn tiles, M = 256 MMAs over two SMs; bn 192 with two
+    accumulators and a ring of scale-factor slots): bit for bit the
     one-tile-per-CTA result, and the oracle's on sampled rows -- ragged M and
-    N, a pair whose odd CTA has no rows of A (M = 129, M = 1), one span of K."""
+    N, a pair whose odd CTA has no rows of A (M = 129, M = 1), one span of K,
+    several tiles per pair (M = 8192)."""
     a_q, a_s, b_q, b_s = operands(400 + M % 97, M, N, K)
     ga, gb = a_q.to(DEV), b_q.to(DEV)
     ta, tb = rmsq.mx_scale_tiles(a_s.to(DEV)), rmsq.mx_scale_tiles(b_s.to(DEV))
     one = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=256, ksplit=1, schedule=1))
-    pair = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(schedule=3))
-    again = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=256, ksplit=1, schedule=3))
+    pair = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=bn if bn != 256 else 0, schedule=3))
+    again = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=bn, ksplit=1, schedule=3))
     torch.cuda.synchronize()
     assert torch.equal(one, pair) and torch.equal(pair, again)
     rows = np.unique(np.concatenate([np.arange(0, M, 61), [M - 1]]))
@@ -161,6 +164,9 @@ def test_pair_schedule_rejects():
     gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
     y = synth.random_bf16(34, (M, K)).to(DEV)
     for bad in (rmsq.GemmOpts(schedule=3, bn=128), rmsq.GemmOpts(schedule=3, ksplit=2)):
+        with pytest.raises(RuntimeError, match="CTA-pair"):
+            rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=bad)
+    for bad in (rmsq.GemmOpts(bn=192), rmsq.GemmOpts(bn=192, schedule=2)):
         with pytest.raises(RuntimeError, match="CTA-pair"):
             rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=bad)
     with pytest.raises(RuntimeError, match="CTA-pair"):
@@ -327,7 +333,8 @@ def test_bounded_wait_in_a_later_tile():
     assert rmsq.sync_status() == 0
 
 
-def test_pair_bounded_wait_in_a_later_tile():
+@pytest.mark.parametrize("bn", [256, 192])
+def test_pair_bounded_wait_in_a_later_tile(bn):
     """CTA pairs: the stalled stage (never loaded by either CTA) sits in the
     second tile of the pairs that walk two (M = 4096, N = 2560: 160 tiles of
     256 x 256, four stages each). Both CTAs of a stalled pair stop within
@@ -337,11 +344,11 @@ def test_pair_bounded_wait_in_a_later_tile():
     a_q, a_s, b_q, b_s = operands(64, M, N, K)
     ga, ta = a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV))
     gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
-    stuck = rmsq.GemmOpts(wait_limit_ns=50_000_000, debug_stall_stage=6, schedule=3)
+    stuck = rmsq.GemmOpts(bn=bn, wait_limit_ns=50_000_000, debug_stall_stage=6, schedule=3)
     rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=stuck)
     assert rmsq.sync_status() == 5                      # RMSQ_ERR_TIMEOUT
     assert rmsq.sync_status() == 0
-    pair = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(schedule=3))
+    pair = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=bn, schedule=3))
     one = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=256, ksplit=1, schedule=1))
     torch.cuda.synchronize()
     assert torch.equal(pair, one)

@@ -91,7 +91,9 @@ def test_random_gemm(oracle_mod, case):
     # schedule where it applies (quantised A, no K split)
     schedule = 2 if (not prequant and ksplit == 1 and rng.integers(0, 2)) else 0
     if not prequant and ksplit <= 1 and bn in (0, 256) and rng.integers(0, 2):
-        schedule = 3                     # CTA pairs
+        schedule = 3                     # CTA pairs, 256- or 192-wide tiles
+        if rng.integers(0, 2):
+            bn = 192
     opts = rmsq.GemmOpts(bn=bn, ksplit=ksplit, schedule=schedule)
     if prequant:
         y = synth.random_bf16(7000 + case, (M, K))
