@@ -87,7 +87,9 @@ def measured_fp4_peak() -> tuple[float, str]:
         return FALLBACK_BF16_TFLOPS * FP4_OVER_BF16, "fallback bf16 x nominal fp4/bf16 ratio 6"
 
 
-GEMM_SOURCES = ("rmsq_gemm.cu", "rmsq_device.cuh", "rmsq_internal.h")
+# the GEMM's own files (left out of the norm + quant digest) and the shared headers it also uses
+GEMM_ONLY = ("rmsq_gemm.cu", "rmsq_gemm_pair.cu", "rmsq_gemm_common.cuh")
+GEMM_SOURCES = GEMM_ONLY + ("rmsq_device.cuh", "rmsq_internal.h")
 
 
 def kernel_source_digest(kind: str = "rows") -> str:
@@ -98,7 +100,7 @@ def kernel_source_digest(kind: str = "rows") -> str:
     for f in sorted(os.listdir(csrc)):
         if not f.endswith((".cu", ".cuh", ".h")):
             continue
-        if (kind == "gemm" and f not in GEMM_SOURCES) or (kind == "rows" and f == GEMM_SOURCES[0]):
+        if (kind == "gemm" and f not in GEMM_SOURCES) or (kind == "rows" and f in GEMM_ONLY):
             continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())

@@ -20,8 +20,8 @@
 // their fp32 partial sums through distributed shared memory, in rank order;
 // with more, a persistent grid walks the tiles (the ring runs on from one
 // tile into the next). For 256-row B tiles without a K split, CTA pairs
-// (mxfp4_gemm_pair_kernel, tcgen05 cta_group::2) compute 256 x 256 tiles
-// with the tensor cores of two SMs.
+// (mxfp4_gemm_pair_kernel in rmsq_gemm_pair.cu, tcgen05 cta_group::2)
+// compute 256 x 256 or 256 x 192 tiles with the tensor cores of two SMs.
 // Warp roles (256 threads): warp 0 issues the TMA and bulk loads; warp 1
 // owns the tensor memory and issues tcgen05.cp (scale factors, shared ->
 // tensor memory) and tcgen05.mma (one elected lane each); warps 4-7 run the
@@ -45,53 +45,10 @@
 //     the 512-byte tile of 128 rows x 4 groups at (r % 32) * 16 + (r / 32) * 4
 //     + g copied by tcgen05.cp .32x128b.warpx4 (rows r % 32 -> lanes, the
 //     same data in all four lane quarters).
-#include <cuda.h>
-#include <cstdarg>
-#include <cstdio>
-
-#include "rmsq.h"
-#include "rmsq_device.cuh"
-#include "rmsq_internal.h"
+#include "rmsq_gemm_common.cuh"
 
 namespace rmsq {
-namespace {
-
-// One GEMM launch as the host checks leave it. A is either MXFP4 codes +
-// tiled scales (a_q, a_scale; lda in bytes) or bf16 (a_bf16; lda in
-// elements, quantised in the kernel).
-struct GemmLaunch {
-    const void *a_q, *a_scale, *a_bf16;
-    int64_t lda;
-    const void *b_q, *b_scale;
-    int64_t ldb;               // bytes
-    void *d;
-    int64_t ldd;               // elements
-    int64_t M, N, K;
-    int bn;                    // 64, 128 or 256
-    int ksplit;                // 1..8 CTAs (a cluster) per tile splitting K
-    int persistent_ctas;       // > 0: a persistent grid of this many CTAs walks the tiles
-    bool pair;                 // 256 x 256 tiles on CTA pairs (persistent, bn 256, quantised A)
-    int debug_skip_stage;      // test hook: a ring stage (counted over the CTA's tiles) whose loads
-                               // are never issued (-1 = off; a zero-initialised GemmLaunch must set it)
-    int64_t wait_limit_ns;
-    unsigned int *status;
-};
-
-constexpr int kBM = 128;          // MMA M: rows of A per tile
-constexpr int kSpanBytes = 128;   // bytes of one operand row per span (256 E2M1)
-constexpr int kSpanK = 256;       // K elements per span
-// 8 warps; the prequant kernel has 4 more, so that 8 warps quantise A
-template <bool PREQUANT>
-constexpr int gemm_threads() { return PREQUANT ? 384 : 256; }
-constexpr int kQuantThreads = 256;   // warps 4-11 of the prequant kernel
-
-constexpr int pow2_at_least(int v)
-{
-    int p = 32;
-    while (p < v)
-        p <<= 1;
-    return p;
-}
+namespace gemm {
 
 // A stage of the ring is kSpans K-spans of 256 elements (one 128-byte
 // swizzle span each: four MMAs of K = 64) behind ONE barrier phase. Measured
@@ -130,269 +87,6 @@ struct GemmCfg {
     static_assert(kSmem <= 232448, "shared memory");
     static_assert(kBM * (BN + 4) * 4 <= kOffSfa, "split-K partials fit in the operand ring");
 };
-
-struct GemmParams {
-    const uint8_t *a_scale;     // MMA tile layout, ceil(M/128) x K/128 tiles of 512 bytes
-    const uint8_t *b_scale;     // same for B
-    const uint4 *a_bf16;        // prequant: bf16 rows, 16-byte vectors
-    int64_t lda_v;              // prequant: leading dimension in vectors
-    uint16_t *d;                // bf16 [M, ldd]
-    int64_t ldd;
-    int64_t M, N;
-    int32_t k_spans;            // K / 256: spans of K (a ring stage holds one or more)
-    int32_t b_row_tiles;        // ceil(N / 128): 128-row scale tiles that exist for B
-    int32_t a_box_rows;         // rows of A per TMA box: 128, or M rounded up to 8 when M < 128
-    int32_t ksplit;             // CTAs of a cluster that split K (1 = no split)
-    int32_t persistent;         // 1: a grid of gridDim.x CTAs walks the m_tiles x n_tiles tiles
-    int32_t m_tiles, n_tiles;   // tiles of the launch (the pair kernel: 256-row tiles of A and B)
-    int32_t debug_skip_stage;   // test hook: this ring stage (counted over the CTA's tiles) is never loaded (-1 = off)
-    int64_t wait_limit_ns;
-    unsigned int *status;
-};
-
-// ------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t gtimer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase of `bar` with the given parity. Returns false
-// (after raising the CTA's abort flag and the status word) if it ran out, or
-// if another role of the CTA already aborted.
-// The clock and the abort flag are looked at only every 64 polls: reading
-// %globaltimer on every poll made the waiting thread notice a completed
-// phase hundreds of nanoseconds late (measured on GB300).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          const GemmParams &p)
-{
-    if (mbar_test(bar, parity))
-        return true;
-    uint64_t t0 = 0;
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_test(bar, parity))
-            return true;
-        if ((n & 63) == 0) {
-            if (*abort)
-                return false;
-            const uint64_t t = gtimer();
-            if (!t0) {
-                t0 = t;
-            } else if (t - t0 > (uint64_t)p.wait_limit_ns) {
-                *abort = 1;
-                atomicOr(p.status, 2u);
-                return false;
-            }
-        }
-    }
-}
-
-// The same wait taken by lane 0 for the whole warp (warp-uniform result, so
-// that the .sync.aligned tensor-memory instructions after it see all lanes).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          const GemmParams &p)
-{
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0)
-        ok = mbar_wait(bar, parity, abort, p) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// One lane of the (fully active) warp, chosen by the hardware.
-__device__ __forceinline__ bool elect_one()
-{
-    uint32_t pred;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "elect.sync _|p, 0xffffffff;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(pred));
-    return pred != 0;
-}
-
-__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr)
-{
-    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Descriptor of a 32-row x 16-byte scale tile (no swizzle, 8-row core
-// matrices 128 bytes apart) for tcgen05.cp.
-__device__ __forceinline__ uint64_t desc_sf(uint32_t addr)
-{
-    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
-}
-
-// Instruction descriptor of kind::mxf4 (E2M1 x E2M1, UE8M0 scales, fp32
-// accumulator, both operands K-major; M = 128, or 256 for a CTA pair).
-__host__ __device__ constexpr uint32_t idesc_mxf4(int n, int sf_id, int m = kBM)
-{
-    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(m >> 4) << 24) |
-           ((uint32_t)sf_id << 29) | ((uint32_t)sf_id << 4);
-}
-
-__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                                         uint32_t sfb, uint32_t acc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void cp_sf(uint32_t taddr, uint64_t desc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// ---- the same for a CTA pair (cta_group::2), issued by the even CTA. Measured
-// with a self-checking probe on GB300: the MMA reads A rows 128r.. and B rows
-// (N/2)r.. from CTA r's shared memory at the same offsets, and each CTA's
-// tensor memory holds D for its 128 rows, the scale factors of its rows of A
-// and those of ALL N rows of B; tcgen05.cp copies each CTA's own shared memory
-// into its own tensor memory; the commit can arrive on both CTAs' barriers.
-__device__ __forceinline__ void mma_mxf4_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                                              uint32_t sfb, uint32_t acc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void cp_sf_pair(uint32_t taddr, uint64_t desc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
-
-// arrives on the barrier at this offset in every CTA of `mask`
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask)
-{
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     bar),
-                 "h"(mask)
-                 : "memory");
-}
-
-// TMA load into this CTA's shared memory whose completion counts on a
-// barrier of either CTA of the pair (a cluster address)
-__device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-
-// Relaxed arrival on a barrier of either CTA of the pair. The epilogue uses it
-// to hand the accumulator back: the only ordering needed is that its
-// tensor-memory loads are complete, which tcgen05.wait::ld has established
-// before the arrival is issued. (A cluster-scope release here would also wait
-// for the warp's outstanding stores of D.)
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr)
-{
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 lanes x 32 columns of fp32 from tensor memory (issue only; the values
-// are valid after tmem_ld_wait + tmem_hold).
-__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Ties the registers of a tensor-memory load to a point after the wait, so
-// that no use of them is scheduled before it.
-__device__ __forceinline__ void tmem_hold(uint32_t (&r)[32])
-{
-    asm volatile(""
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
-                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
-{
-    tmem_ld32_issue(taddr, r);
-    tmem_ld_wait();
-    tmem_hold(r);
-}
 
 // ---------------------------------------------------- prequant (A in bf16)
 
@@ -487,34 +181,6 @@ __device__ __forceinline__ bool prequant_loop(const GemmParams &p, int64_t m0, i
         c0 = cn;
     }
     return true;
-}
-
-// ------------------------------------------------------- cluster (split K)
-
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// The split-K cluster's last barrier, before its CTAs leave: each CTA's reads
-// of the others' shared memory have returned (their values were used) before
-// it arrives, so a relaxed arrival suffices -- measured 2.5-4 % faster than a
-// release at 4-512 tokens.
-__device__ __forceinline__ void cluster_sync_exit()
-{
-    asm volatile("barrier.cluster.arrive.relaxed;\n\tbarrier.cluster.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ float4 ld_peer_f4(const float *local, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(saddr(local)), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(remote)
-                 : "memory");
-    return v;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -861,313 +527,6 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     }
 }
 
-// ------------------------------------------------------ CTA-pair kernel
-// A cluster of two CTAs computes 256 x BN tiles of D (persistent: pair
-// blockIdx.x / 2 walks tiles pair, pair + pairs, ... in N-fastest order) with
-// M = 256 MMAs issued by the even CTA. CTA r loads its 128 rows of A and rows
-// (BN/2)r.. of the tile's BN rows of B, so a span of K costs each SM 32 KB of
-// operands at BN = 256 (48 KB for a 128 x 256 tile of its own). Each CTA also
-// loads the tile's A scales for its rows and ALL of its B scales (the MMA
-// reads both from each SM's own tensor memory); every copy of both CTAs
-// completes on the even CTA's `full` barrier, which the even CTA arms for
-// both. The MMA commits arrive on both CTAs' `empty` and `accum` barriers;
-// both epilogues (their own 128 rows, in their own tensor memory) arrive on
-// the even CTA's `tmem_empty`.
-// BN = 256: one accumulator, six ring stages. BN = 192: two accumulators
-// (the MMAs of the next tile run while the epilogue drains the last) and five
-// stages; 2 x 192 accumulator columns leave room for five stages' scale
-// factors. Each stage's scale factors keep their own tensor-memory slot, so
-// a slot is free again when the producer may refill the stage. (A separate
-// ring of five slots under seven stages, where the MMA warp waited for the
-// commit of stage g - 5 before reusing a slot, starved the tensor pipe:
-// 64.4 us at M = 8192 against 48.2 us.)
-// Stage shape measured on GB300 (BN = 256, N = 2112, K = 7168, M = 8192): one
-// span x six stages 50.7 us, one x five 51.6 us, two spans x three 56.2 us.
-template <int BN_>
-struct PairCfg {
-    static constexpr int BN = BN_;                     // columns of D per tile
-    static constexpr int kRowsB = BN / 2;              // rows of B per CTA
-    static constexpr int kSpanA = kBM * kSpanBytes;
-    static constexpr int kSpanB = kRowsB * kSpanBytes;
-    static constexpr int kStage = kSpanA + kSpanB;     // one span of K per stage
-    static constexpr int kSfbAtoms = 2;                // 128-row scale tiles of B a tile touches
-    static constexpr int kStages = BN == 256 ? 6 : 5;
-    static constexpr int kAcc = BN == 256 ? 1 : 2;     // accumulators in tensor memory
-    static constexpr int kOffSfa = kStages * kStage;
-    static constexpr int kOffSfb = kOffSfa + kStages * 1024;
-    static constexpr int kOffOut = kOffSfb + kStages * kSfbAtoms * 1024;
-    static constexpr int kOutBytes = 4 * 2048;         // each epilogue warp: 32 rows x 64 bytes of D
-    static constexpr int kOffBar = kOffOut + kOutBytes;
-    static constexpr int kBarBytes = (2 * kStages + 2 * kAcc + 1) * 8 + 16;
-    static constexpr size_t kSmem = 1024 + kOffBar + kBarBytes;
-    static constexpr int kSfCols = 8 + 8 * kSfbAtoms;  // scale-factor TMEM columns per stage
-    static constexpr int kTmemCols = pow2_at_least(kAcc * BN + kStages * kSfCols);
-    static constexpr uint32_t kCtaTx = kSpanA + kSpanB + 1024 + kSfbAtoms * 1024;   // bytes per CTA per stage
-    static_assert(BN == 256 || BN == 192, "tile width");
-    static_assert(kAcc * BN + kStages * kSfCols <= 512, "tensor memory");
-    static_assert(kSmem <= 232448, "shared memory");
-};
-
-template <int BN>
-__global__ void __launch_bounds__(256, 1)
-    mxfp4_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
-                           const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sfa,
-                           const __grid_constant__ CUtensorMap map_sfb)
-{
-    using C = PairCfg<BN>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *full = (uint64_t *)(smem + C::kOffBar);
-    uint64_t *empty = full + C::kStages;
-    uint64_t *accum = empty + C::kStages;          // [kAcc]
-    uint64_t *tmem_empty = accum + C::kAcc;        // [kAcc]
-    uint64_t *drain = tmem_empty + C::kAcc;
-    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
-    volatile int *abort = (volatile int *)(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint32_t rank;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
-    auto tile_at = [&](int i, int &mt, int &nt) -> bool {   // mt: 256-row tile of A, nt: BN-row tile of B
-        const int64_t t = (int64_t)pair + (int64_t)i * npairs;
-        if (t >= (int64_t)p.m_tiles * p.n_tiles)
-            return false;
-        mt = (int)(t / p.n_tiles);
-        nt = (int)(t % p.n_tiles);
-        return true;
-    };
-    const int KS = p.k_spans;   // stages per tile
-
-    if (threadIdx.x == 32) {
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_a) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_b) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_sfa) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&map_sfb) : "memory");
-    }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(full + s)));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(empty + s)));
-        }
-        for (int a = 0; a < C::kAcc; ++a) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(accum + a)));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(saddr(tmem_empty + a)));   // 4 warps x 2 CTAs
-        }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(drain)));
-        *abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
-                     "r"(C::kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();   // both CTAs' barriers exist before either signals the other's
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_sf = tmem + C::kAcc * BN;
-    const uint32_t full_lead = cluster_addr(saddr(full), 0);
-    int issued = 0;
-
-    if (warp == 0) {
-        // ---------------------------------------------------------- loads
-        int g = 0, mt, nt;
-        bool stop = false;
-        for (int ti = 0; !stop && tile_at(ti, mt, nt); ++ti) {
-            const int a_row = mt * 256 + kBM * (int)rank;
-            const int b_row = nt * BN + C::kRowsB * (int)rank;
-            const int bt0 = (nt * BN) >> 7;                       // the tile's first 128-row scale tile of B
-            const int sfa_tile = mt * 2 + (int)rank;
-            for (int j = 0; j < KS; ++j, ++g) {
-                const int s = g % C::kStages;
-                if (g >= C::kStages &&
-                    !warp_wait(saddr(empty + s), ((uint32_t)(g / C::kStages) & 1u) ^ 1u, abort, p)) {
-                    stop = true;
-                    break;
-                }
-                if (g != p.debug_skip_stage && elect_one()) {   // test hook: that stage never arrives
-                    if (rank == 0)
-                        mbar_arrive_tx(saddr(full + s), 2 * C::kCtaTx);
-                    const uint32_t fb = full_lead + 8 * s;
-                    uint8_t *st = smem + s * C::kStage;
-                    tma_2d_pair(saddr(st), &map_a, j * kSpanBytes, a_row, fb);
-                    tma_2d_pair(saddr(st + C::kSpanA), &map_b, j * kSpanBytes, b_row, fb);
-                    tma_2d_pair(saddr(smem + C::kOffSfa + s * 1024), &map_sfa, 0, 4 * (sfa_tile * KS + j), fb);
-#pragma unroll
-                    for (int t = 0; t < C::kSfbAtoms; ++t)
-                        tma_2d_pair(saddr(smem + C::kOffSfb + (s * C::kSfbAtoms + t) * 1024), &map_sfb, 0,
-                                    4 * ((bt0 + t) * KS + j), fb);
-                }
-                __syncwarp();
-                issued = g + 1;
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1 && rank == 0) {
-        // ------------------------------------------------------------ MMA
-        int g = 0, mt, nt;
-        bool any = false, stop = false;
-        for (int ti = 0; !stop && tile_at(ti, mt, nt); ++ti) {
-            const int acc_slot = ti % C::kAcc, use = ti / C::kAcc;
-            if (use > 0) {   // both epilogues have read this accumulator's previous tile
-                if (!warp_wait(saddr(tmem_empty + acc_slot), (uint32_t)((use - 1) & 1), abort, p))
-                    break;
-                tc_fence_after();
-            }
-            const uint32_t d_tmem = tmem + acc_slot * BN;
-            // a tile that starts half-way into a 128-row scale tile of B (BN =
-            // 192, odd tiles) reads its rows' scale columns from 2 on
-            const uint32_t sfb_row_col = (uint32_t)(((nt * BN) >> 6) & 1) * 2;
-            for (int j = 0; j < KS; ++j, ++g) {
-                const int s = g % C::kStages;
-                if (!warp_wait(saddr(full + s), (uint32_t)(g / C::kStages) & 1u, abort, p)) {
-                    stop = true;
-                    break;
-                }
-                tc_fence_after();
-                if (elect_one()) {
-                    const uint32_t sfa_col = tmem_sf + s * C::kSfCols, sfb_col = sfa_col + 8;
-                    const uint32_t sfa_smem = saddr(smem + C::kOffSfa + s * 1024);
-                    const uint32_t sfb_smem = saddr(smem + C::kOffSfb + s * C::kSfbAtoms * 1024);
-                    const uint32_t a_smem = saddr(smem + s * C::kStage), b_smem = a_smem + C::kSpanA;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        cp_sf_pair(sfa_col + 4 * c, desc_sf(sfa_smem + c * 512));
-#pragma unroll
-                        for (int t = 0; t < C::kSfbAtoms; ++t)
-                            cp_sf_pair(sfb_col + 4 * C::kSfbAtoms * c + 4 * t, desc_sf(sfb_smem + t * 1024 + c * 512));
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int c = k >> 1;
-                        mma_mxf4_pair(d_tmem, desc_sw128(a_smem + 32 * k), desc_sw128(b_smem + 32 * k),
-                                      idesc_mxf4(BN, (k & 1) * 2, 2 * kBM), sfa_col + 4 * c,
-                                      sfb_col + 4 * C::kSfbAtoms * c + sfb_row_col, (j | k) != 0);
-                    }
-                    mma_commit_pair(saddr(empty + s), 3);
-                }
-                __syncwarp();
-                any = true;
-            }
-            if (!stop && elect_one())
-                mma_commit_pair(saddr(accum + acc_slot), 3);   // this tile's accumulators are complete
-            __syncwarp();
-        }
-        if (*abort && any && elect_one()) {
-            // drain the tensor cores before the tensor memory is freed
-            mma_commit_pair(saddr(drain), 1);
-            const uint64_t t0 = gtimer();
-            while (!mbar_test(saddr(drain), 0) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
-            }
-        }
-        __syncwarp();
-    } else if (warp >= 4) {
-        // ------------------------------------------------------- epilogue
-        // This CTA's 128 rows of the tile, 32 columns at a time, through
-        // shared memory so that each store instruction writes eight rows'
-        // whole 64-byte pieces (16-byte chunk j of row i at j ^ ((i/2) mod 4):
-        // conflict-free both ways).
-        const int q = warp & 3;
-        uint8_t *const stage_w = smem + C::kOffOut + (warp - 4) * 2048;
-        const int cj = lane & 3;
-        int mt, nt;
-        for (int ti = 0; tile_at(ti, mt, nt); ++ti) {
-            const int acc_slot = ti % C::kAcc, use = ti / C::kAcc;
-            if (!warp_wait(saddr(accum + acc_slot), (uint32_t)(use & 1), abort, p))
-                break;
-            tc_fence_after();
-            const int64_t row0 = (int64_t)mt * 256 + kBM * (int)rank + q * 32, n0 = (int64_t)nt * BN;
-            const uint32_t trow = tmem + acc_slot * BN + ((uint32_t)(q * 32) << 16);
-            const uint32_t tmem_empty_lead = cluster_addr(saddr(tmem_empty + acc_slot), 0);
-            // 32-column chunks of D this warp writes (warp-uniform; N is a multiple of 8)
-            const int nch = row0 < p.M ? (int)((min((int64_t)BN, p.N - n0) + 31) / 32) : 0;
-            auto store_chunk = [&](const uint32_t(&acc)[32], int c0) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 o;
-                    o.x = pack_bf16x2(__uint_as_float(acc[8 * j + 0]), __uint_as_float(acc[8 * j + 1]));
-                    o.y = pack_bf16x2(__uint_as_float(acc[8 * j + 2]), __uint_as_float(acc[8 * j + 3]));
-                    o.z = pack_bf16x2(__uint_as_float(acc[8 * j + 4]), __uint_as_float(acc[8 * j + 5]));
-                    o.w = pack_bf16x2(__uint_as_float(acc[8 * j + 6]), __uint_as_float(acc[8 * j + 7]));
-                    *reinterpret_cast<uint4 *>(stage_w + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = o;
-                }
-                __syncwarp();
-#pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int rr = it * 8 + (lane >> 2);
-                    const uint4 v = *reinterpret_cast<const uint4 *>(stage_w + rr * 64 + ((cj ^ ((rr >> 1) & 3)) << 4));
-                    const int64_t gm = row0 + rr, gn = n0 + c0 + cj * 8;
-                    if (gm < p.M && gn < p.N && RMSQ_IN_BOUNDS(p.status, gn + 8 <= p.N))
-                        *reinterpret_cast<uint4 *>(p.d + gm * p.ldd + gn) = v;
-                }
-                __syncwarp();
-            };
-            // the accumulator may be overwritten by the MMAs of a later tile
-            // once this warp's last tensor-memory load is complete
-            auto release = [&]() {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive_cluster(tmem_empty_lead);
-            };
-            // Chunk c + 1 is loaded from tensor memory while chunk c goes to D.
-            uint32_t a[32], b[32];
-            if (nch > 0) {
-                tmem_ld32_issue(trow, a);
-                tmem_ld_wait();
-                tmem_hold(a);
-            } else {
-                release();
-            }
-#pragma unroll 1
-            for (int c = 0; c < nch; c += 2) {
-                if (c + 1 < nch)
-                    tmem_ld32_issue(trow + (c + 1) * 32, b);
-                else
-                    release();
-                store_chunk(a, c * 32);
-                if (c + 1 < nch) {
-                    tmem_ld_wait();
-                    tmem_hold(b);
-                    if (c + 2 < nch)
-                        tmem_ld32_issue(trow + (c + 2) * 32, a);
-                    else
-                        release();
-                    store_chunk(b, (c + 1) * 32);
-                    if (c + 2 < nch) {
-                        tmem_ld_wait();
-                        tmem_hold(a);
-                    }
-                }
-            }
-        }
-    }
-
-    // ------------------------------------------------------------ teardown
-    tc_fence_before();
-    __syncthreads();
-    if (*abort && threadIdx.x == 0 && rank == 0) {
-        // let the copies of stages this pair armed land before either CTA goes
-        const uint64_t t0 = gtimer();
-        for (int i = (issued > C::kStages ? issued - C::kStages : 0); i < issued; ++i) {
-            if (i == p.debug_skip_stage)
-                continue;
-            const uint32_t fb = saddr(full + i % C::kStages);
-            const uint32_t ph = (uint32_t)(i / C::kStages) & 1u;
-            while (!mbar_test(fb, ph) && gtimer() - t0 < (uint64_t)p.wait_limit_ns) {
-            }
-        }
-    }
-    cluster_sync();   // neither CTA leaves while the other may still signal its barriers or read its memory
-    if (warp == 1) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
-    }
-}
-
 // ----------------------------------------------------------------- host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -1269,96 +628,6 @@ bool make_scale_map(CUtensorMap *map, const void *base, int64_t rows)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// CTA pairs resident at once with the pair kernel's shared memory (cached per device)
-template <int BN>
-int pair_capacity(int dev)
-{
-    using C = PairCfg<BN>;
-    static int cap[128];
-    if (dev < 0 || dev >= 128)
-        return 0;
-    if (!cap[dev]) {
-        if (cudaFuncSetAttribute(mxfp4_gemm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)C::kSmem) != cudaSuccess)
-            return 0;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2, 1, 1);
-        cfg.blockDim = dim3(256, 1, 1);
-        cfg.dynamicSmemBytes = C::kSmem;
-        cudaLaunchAttribute cl[1];
-        cl[0].id = cudaLaunchAttributeClusterDimension;
-        cl[0].val.clusterDim.x = 2;
-        cl[0].val.clusterDim.y = 1;
-        cl[0].val.clusterDim.z = 1;
-        cfg.attrs = cl;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, mxfp4_gemm_pair_kernel<BN>, &cfg) != cudaSuccess || n <= 0)
-            return 0;
-        cap[dev] = n;
-    }
-    return cap[dev];
-}
-
-template <int BN>
-cudaError_t launch_pair_t(const GemmLaunch &g, cudaStream_t st)
-{
-    using C = PairCfg<BN>;
-    GemmParams p{};
-    p.d = (uint16_t *)g.d;
-    p.ldd = g.ldd;
-    p.M = g.M;
-    p.N = g.N;
-    p.k_spans = (int32_t)(g.K / kSpanK);
-    p.b_row_tiles = (int32_t)((g.N + 127) / 128);
-    p.a_box_rows = kBM;
-    p.ksplit = 1;
-    p.persistent = 1;
-    p.m_tiles = (int32_t)((g.M + 255) / 256);
-    p.n_tiles = (int32_t)((g.N + BN - 1) / BN);
-    p.debug_skip_stage = g.debug_skip_stage;
-    p.wait_limit_ns = g.wait_limit_ns;
-    p.status = g.status;
-    const int64_t m_tiles128 = (g.M + 127) / 128;
-    CUtensorMap ma, mb, msa, msb;
-    if (!make_code_map(&ma, g.a_q, g.M, g.K / 2, g.lda, kBM) ||
-        !make_code_map(&mb, g.b_q, g.N, g.K / 2, g.ldb, C::kRowsB) ||
-        !make_scale_map(&msa, g.a_scale, m_tiles128 * p.k_spans * 4) ||
-        !make_scale_map(&msb, g.b_scale, (int64_t)p.b_row_tiles * p.k_spans * 4))
-        return cudaErrorInvalidValue;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    const int cap = pair_capacity<BN>(dev);
-    if (cap <= 0)
-        return cudaErrorInvalidConfiguration;
-    const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
-    const int pairs = (int)(tiles < cap ? tiles : cap);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * pairs, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmem;
-    cfg.stream = st;
-    cudaLaunchAttribute cl[1];
-    cl[0].id = cudaLaunchAttributeClusterDimension;
-    cl[0].val.clusterDim.x = 2;
-    cl[0].val.clusterDim.y = 1;
-    cl[0].val.clusterDim.z = 1;
-    cfg.attrs = cl;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mxfp4_gemm_pair_kernel<BN>, p, ma, mb, msa, msb);
-}
-
-cudaError_t launch_pair(const GemmLaunch &g, cudaStream_t st)
-{
-    switch (g.bn) {
-    case 256: return launch_pair_t<256>(g, st);
-    case 192: return launch_pair_t<192>(g, st);
-    }
-    return cudaErrorInvalidValue;
-}
-
 cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
 {
     if (g.pair)
@@ -1411,6 +680,8 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
 }
 
 bool tensor_map_encoder_available() { return encode_fn() != nullptr; }
+
+namespace {
 
 // --------------------------------------------------------- host checks
 
@@ -1563,7 +834,7 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
         // counting a 192-wide tile as 0.75 of a 256-wide one and charging it
         // 4 % for its lower efficiency per column (measured: 12.8 against
         // 12.3 us per 256-column unit at N = 2112, K = 7168).
-        const int cap256 = pair_capacity<256>(dev), cap192 = pair_capacity<192>(dev);
+        const int cap256 = pair_capacity(dev, 256), cap192 = pair_capacity(dev, 192);
         if (cap256 <= 0 || cap192 <= 0)
             return failf(RMSQ_ERR_CUDA, "cluster occupancy query failed");
         const int64_t mt2 = (M + 255) / 256;
@@ -1606,9 +877,11 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
 }
 
 }  // namespace
+}  // namespace gemm
 }  // namespace rmsq
 
 using namespace rmsq;
+using namespace rmsq::gemm;
 
 extern "C" {
 
