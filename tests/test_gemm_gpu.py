@@ -78,6 +78,44 @@ def test_split_k_matches_oracle(oracle_mod, bn, ksplit):
     print(bn, ksplit, st)
 
 
+@pytest.mark.parametrize("bn,ksplit", [(64, 4), (64, 2), (256, 8), (128, 3)])
+def test_split_k_rows_independent_of_m(oracle_mod, bn, ksplit):
+    """Split K adds the cluster's partial sums in rank order whatever the
+    tile's row count, so the rows a 4-token launch computes equal the same
+    rows of a 200-token launch bit for bit, and match the oracle."""
+    M, N, K = 200, 264, 2048
+    a_q, a_s, b_q, b_s = operands(91, M, N, K)
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    opts = rmsq.GemmOpts(bn=bn, ksplit=ksplit)
+    full = rmsq.mxfp4_gemm(a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV)), gb, tb, opts=opts)
+    few = rmsq.mxfp4_gemm(a_q[:4].to(DEV), rmsq.mx_scale_tiles(a_s[:4].to(DEV)), gb, tb, opts=opts)
+    torch.cuda.synchronize()
+    assert torch.equal(few, full[:4])
+    ref = oracle_mod.mxfp4_gemm(a_q[:4].numpy(), a_s[:4].numpy(), b_q.numpy(), b_s.numpy())
+    parity.compare_gemm(few, ref, K, what=f"split K, 4 rows, bn={bn} ksplit={ksplit}")
+    assert rmsq.sync_status() == 0
+
+
+def test_bounded_wait_split_k_decode(oracle_mod):
+    """A stalled stage at decode size (8 tokens, K split over 2 CTAs, two
+    4-span stages per CTA, the second never loaded): the stalled CTA stops,
+    both still meet at the cluster barriers, the host reads
+    RMSQ_ERR_TIMEOUT and the next launch matches the oracle."""
+    M, N, K = 8, 256, 4096
+    a_q, a_s, b_q, b_s = operands(93, M, N, K)
+    ga, ta = a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV))
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=64, ksplit=2, wait_limit_ns=50_000_000,
+                                                       debug_stall_stage=2))
+    assert rmsq.sync_status() == 5                      # RMSQ_ERR_TIMEOUT
+    assert rmsq.sync_status() == 0
+    again = rmsq.mxfp4_gemm(ga, ta, gb, tb, opts=rmsq.GemmOpts(bn=64, ksplit=2))
+    torch.cuda.synchronize()
+    ref = oracle_mod.mxfp4_gemm(a_q.numpy(), a_s.numpy(), b_q.numpy(), b_s.numpy())
+    parity.compare_gemm(again, ref, K, what="after a timed-out split-K launch")
+    assert rmsq.sync_status() == 0
+
+
 def test_tile_choices_agree_bitwise():
     """Tiles of 64, 128 and 256 B rows run the same MMAs in the same K order."""
     a_q, a_s, b_q, b_s = operands(5, 256, 512, 1024)
