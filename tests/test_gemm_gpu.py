@@ -253,6 +253,28 @@ def test_degenerate_operands():
     assert out.shape == (0, N)
 
 
+@pytest.mark.parametrize("bn", [256, 192])
+def test_degenerate_operands_pair(bn):
+    """The same degenerate operands through CTA pairs: zero codes under 2^127
+    scales give exact zeros (no NaN / Inf), 2^-127 scales give finite output,
+    and a pair whose odd CTA has rows of A only past M (M = 130) is fine."""
+    M, N, K = 130, 264, 512
+    opts = rmsq.GemmOpts(bn=bn, schedule=3)
+    z = torch.zeros((M, K // 2), dtype=torch.uint8)
+    s_hi = torch.full((M, K // 32), 254, dtype=torch.uint8)
+    b_q, b_s = synth.mxfp4_weights(3, N, K)
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    d = rmsq.mxfp4_gemm(z.to(DEV), rmsq.mx_scale_tiles(s_hi.to(DEV)), gb, tb, opts=opts)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(d.float()).item() == 0
+    s_lo = torch.zeros((M, K // 32), dtype=torch.uint8)
+    a_q, _ = synth.mxfp4_weights(4, M, K)
+    d = rmsq.mxfp4_gemm(a_q.to(DEV), rmsq.mx_scale_tiles(s_lo.to(DEV)), gb, tb, opts=opts)
+    torch.cuda.synchronize()
+    assert torch.isfinite(d.float()).all()
+    assert rmsq.sync_status() == 0
+
+
 def test_output_guard_band():
     """The GEMM writes exactly D[:M, :N]: canary bytes around a strided D stay."""
     M, N, K = 70, 136, 512
