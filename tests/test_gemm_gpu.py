@@ -183,12 +183,12 @@ def test_pair_schedule_strided(oracle_mod):
     pb[:, :K // 2] = b_q
     ga, gb = pa.to(DEV)[:, :K // 2], pb.to(DEV)[:, :K // 2]
     ta, tb = rmsq.mx_scale_tiles(a_s.to(DEV)), rmsq.mx_scale_tiles(b_s.to(DEV))
-    dbig = torch.zeros((M, N + 40), dtype=torch.bfloat16, device=DEV)
-    d = rmsq.mxfp4_gemm(ga, ta, gb, tb, out=dbig[:, :N], opts=rmsq.GemmOpts(schedule=3))
+    dbig = torch.zeros((M + 9, N + 40), dtype=torch.bfloat16, device=DEV)
+    d = rmsq.mxfp4_gemm(ga, ta, gb, tb, out=dbig[:M, :N], opts=rmsq.GemmOpts(schedule=3))
     one = rmsq.mxfp4_gemm(a_q.to(DEV), ta, b_q.to(DEV), tb, opts=rmsq.GemmOpts(bn=256, ksplit=1, schedule=1))
     torch.cuda.synchronize()
     assert torch.equal(d, one)
-    assert (dbig[:, N:] == 0).all()
+    assert (dbig[:, N:] == 0).all() and (dbig[M:] == 0).all()   # nothing past D[:M, :N] is written
     rows = np.unique(np.concatenate([np.arange(0, M, 37), [M - 1]]))
     ref = oracle_mod.mxfp4_gemm(a_q.numpy()[rows], a_s.numpy()[rows], b_q.numpy(), b_s.numpy())
     parity.compare_gemm(d[torch.from_numpy(rows).to(DEV)], ref, K, what="pair, strided A, B, D")
