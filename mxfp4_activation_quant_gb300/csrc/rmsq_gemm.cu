@@ -783,12 +783,17 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     unsigned int *status = device_status_word(dev);
     if (!status)
         return failf(RMSQ_ERR_CUDA, "status word address unavailable");
-    // Tile width, from measurements on GB300 (N = 2112, K = 7168): the
-    // prequant kernel quantises A once per B tile, so it always takes the
-    // widest tile; the plain GEMM takes 256-row B tiles once they give at
-    // least half the SMs a tile, 128 from two row tiles of A on, and 64 for a
-    // single row tile (decode). With fewer tiles than SMs, K is split over a
-    // cluster of up to 8 CTAs (each at least one 256-element span of K).
+    // Tile width, from measurements on GB300 (N = 2112, K = 7168). The
+    // prequant kernel quantises A once per B tile, so it mostly takes the
+    // widest tile, except: up to 16 tokens, 64-row tiles (K split 4; 8.4
+    // against 8.7 us at 4 tokens), where quantising is nearly free and the
+    // CTAs load less of B; and with two row tiles of A, 128-row tiles (K
+    // split 4: 37.8 against 52.4 us at 256 tokens), because 18 clusters of
+    // 8 CTAs do not all fit on the GPU at once and the last ones run in a
+    // second wave. The plain GEMM takes 256-row B tiles once they give at
+    // least half the SMs a tile, 128 from two row tiles of A on, and 64 for
+    // a single row tile (decode). With fewer tiles than SMs, K is split over
+    // a cluster of up to 8 CTAs (each at least one 256-element span of K).
     const int sms = device_sm_count();
     if (sms <= 0)
         return failf(RMSQ_ERR_CUDA, "SM count query failed");
@@ -801,7 +806,9 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
             bn = 256;
     }
     if (!bn) {
-        if (prequant || m_tiles * ((N + 255) / 256) * 2 >= sms)
+        if (prequant)
+            bn = m_tiles == 2 ? 128 : (M <= 16 ? 64 : 256);
+        else if (m_tiles * ((N + 255) / 256) * 2 >= sms)
             bn = 256;
         else
             bn = m_tiles >= 2 ? 128 : 64;

@@ -322,6 +322,35 @@ def test_placements_agree_and_match_oracle(oracle_mod, M):
     print(M, st)
 
 
+@pytest.mark.parametrize("M", [1, 4, 16, 64, 128, 256])
+def test_placements_agree_at_few_tokens(oracle_mod, M):
+    """Up to two row tiles of A, at every tile width and K split the library
+    picks or may be asked for there: the quantising GEMM equals the
+    quantised-A GEMM bit for bit under the same options, and sampled rows
+    (rows are independent) match the oracle's composition."""
+    K, N = 7168, 2112
+    g, d_cpu = _pipeline_inputs(M, K, 41)
+    b_q, b_s = synth.mxfp4_weights(42, N, K)
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    (a_q, a_tiles), _ = rmsq.add_rmsnorm_quant_mxfp4_mma_scales(g["x"], g["gamma"], g["residual"])
+    y, _ = rmsq.add_rmsnorm(g["x"], g["gamma"], g["residual"])
+    rows = sorted(r for r in {0, 1, M // 3, M // 2, 127, 128, M - 2, M - 1} if 0 <= r < M)
+    sub = {k: (v[rows] if v.dim() == 2 else v) for k, v in d_cpu.items()}
+    ref_q = oracle_mod.add_rmsnorm_quant_mxfp4(sub["x"], sub["residual"], sub["gamma"])
+    keep = ref_q["margin"] >= parity.BOUNDARY
+    ref = oracle_mod.mxfp4_gemm(ref_q["q"], ref_q["scale"], b_q.numpy(), b_s.numpy())
+    ref = {k: v[keep] for k, v in ref.items()}
+    pick = torch.tensor(rows, device=DEV)[torch.from_numpy(keep).to(DEV)]
+    for bn, ksplit in [(0, 0), (64, 0), (128, 0), (128, 4), (128, 6), (256, 0), (256, 4)]:
+        o = rmsq.GemmOpts(bn=bn, ksplit=ksplit)
+        pre = rmsq.a16wfp4_gemm(y, gb, tb, opts=o)
+        plain = rmsq.mxfp4_gemm(a_q, a_tiles, gb, tb, opts=o)
+        torch.cuda.synchronize()
+        assert torch.equal(pre, plain), (M, bn, ksplit)
+        parity.compare_gemm(pre[pick], ref, K, what=f"M={M} bn={bn} ksplit={ksplit}")
+    assert rmsq.sync_status() == 0
+
+
 def test_full_size_sampled(oracle_mod):
     """The benchmarked shape (M=8192 tokens, N=2112, K=7168): the placements
     agree on every output; sampled rows (rows are independent) against the
