@@ -282,11 +282,12 @@ rmsq_status rmsq_add_rmsnorm_quant_mxfp4_ex(
  * tuning; results do not depend on it.
  *   bn             rows of B per CTA tile: 64, 128 or 256, or 192 with the
  *                  CTA-pair schedule only (then rows of B per pair tile);
- *                  0 = auto (256 for the prequant GEMM, which quantises A
- *                  once per B tile; for the plain GEMM 256 once that gives
- *                  half the SMs a tile, else 128 with two or more 128-row
- *                  tiles of A, else 64; CTA pairs take 256 or 192, whichever
- *                  leaves the busiest pair the least work)
+ *                  0 = auto (for the prequant GEMM, which quantises A once
+ *                  per B tile: 64 up to 16 rows of A, 128 with exactly two
+ *                  128-row tiles of A, else 256; for the plain GEMM 256 once
+ *                  that gives half the SMs a tile, else 128 with two or more
+ *                  128-row tiles of A, else 64; CTA pairs take 256 or 192,
+ *                  whichever leaves the busiest pair the least work)
  *   ksplit         CTAs, launched as one thread-block cluster, that split K
  *                  for each tile and add their fp32 partial sums through
  *                  distributed shared memory (rank order, so deterministic):
@@ -331,6 +332,38 @@ rmsq_status rmsq_mxfp4_gemm_ex(
 rmsq_status rmsq_a16wfp4_gemm_ex(
     const void *a, int64_t ld_a, const void *b_q, int64_t ld_b, const void *b_scale_tiles, void *d,
     int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream, const rmsq_gemm_opts *opts);
+
+/*
+ * The launch rmsq_mxfp4_gemm_ex (prequant = 0) or rmsq_a16wfp4_gemm_ex
+ * (prequant != 0) makes for an M x N x K product with these options (NULL =
+ * defaults), on a device with `sms` SMs on which `pairs_256` / `pairs_192`
+ * CTA pairs of the 256- / 192-wide pair kernel fit at once (the GEMM entry
+ * points ask the current device for the three numbers; here the caller gives
+ * them). Pure host arithmetic: no CUDA call, no device needed. The choice is
+ * the one the GEMM calls make, so it applies their option and shape checks
+ * and returns the same status for the same arguments (pointer, pitch and
+ * alignment checks aside); a pair capacity is needed only when the library
+ * picks the pair width, and a non-positive one then gives
+ * RMSQ_ERR_INVALID_ARG.
+ *   plan->bn               B-tile width (rows of B per CTA, or per CTA pair)
+ *   plan->ksplit           CTAs of one cluster that split each tile's K (1: none)
+ *   plan->schedule         1 one tile per CTA (or per cluster), 2 persistent,
+ *                          3 CTA pairs
+ *   plan->persistent_ctas  CTAs of the persistent grid (schedule 2), else 0
+ * With M = 0 or N = 0 nothing is launched and *plan is all zeros. *plan is
+ * zeroed first, so it is all zeros after any error. plan is required
+ * (caller-owned host memory).
+ */
+typedef struct rmsq_gemm_plan {
+    int32_t bn;
+    int32_t ksplit;
+    int32_t schedule;
+    int32_t persistent_ctas;
+} rmsq_gemm_plan;
+
+rmsq_status rmsq_gemm_plan_for(
+    int32_t prequant, int64_t M, int64_t N, int64_t K, const rmsq_gemm_opts *opts, int32_t sms,
+    int32_t pairs_256, int32_t pairs_192, rmsq_gemm_plan *plan);
 
 /*
  * The device encoders the kernels use, applied elementwise to n fp32 values

@@ -726,13 +726,9 @@ __global__ void mx_scale_tiles_kernel(const uint8_t *s, int64_t ld, int64_t R, i
 
 const rmsq_gemm_opts kDefaultGemmOpts = {0, 0, 0, 0, 0};
 
-// Shared by both placements: a_q / ld_a (bytes) for MXFP4 A, a / ld_a
-// (elements) for bf16 A.
-rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *a_scale, const void *b_q,
-                        int64_t ld_b, const void *b_scale, void *d, int64_t ld_d, int64_t M, int64_t N,
-                        int64_t K, void *stream, const rmsq_gemm_opts *opts)
+// Option and shape checks shared by the GEMM entry points and the plan query.
+rmsq_status check_gemm_args(int64_t M, int64_t N, int64_t K, const rmsq_gemm_opts &o)
 {
-    const rmsq_gemm_opts o = opts ? *opts : kDefaultGemmOpts;
     if (M < 0 || N < 0 || K <= 0)
         return set_error(RMSQ_ERR_INVALID_ARG, "need M >= 0, N >= 0, K > 0");
     if (o.bn != 0 && o.bn != 64 && o.bn != 128 && o.bn != 192 && o.bn != 256)
@@ -751,38 +747,27 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
         return failf(RMSQ_ERR_UNSUPPORTED, "K=%lld is not a multiple of 256", (long long)K);
     if (N % 8)
         return failf(RMSQ_ERR_UNSUPPORTED, "N=%lld is not a multiple of 8", (long long)N);
-    if (M == 0 || N == 0)
-        return clear_error();
-    if (!a || !b_q || !b_scale || !d || (!prequant && !a_scale))
-        return failf(RMSQ_ERR_INVALID_ARG, "operand, scale and output pointers are required");
-    const int64_t a_row_bytes = prequant ? K * 2 : K / 2;
-    const int64_t lda_bytes = prequant ? ld_a * 2 : ld_a;
-    if (lda_bytes < a_row_bytes || ld_b < K / 2 || ld_d < N)
-        return failf(RMSQ_ERR_INVALID_ARG, "leading dimensions must cover a row");
-    if (!aligned(a, 16) || !aligned(b_q, 16) || !aligned(b_scale, 16) || !aligned(d, 16) ||
-        (!prequant && !aligned(a_scale, 16)) || lda_bytes % 16 || ld_b % 16 || ld_d % 8)
-        return failf(RMSQ_ERR_MISALIGNED,
-                    "operands, scale tiles and D need 16-byte aligned bases and 16-byte row pitches");
+    return RMSQ_OK;
+}
+
+// What one GEMM launches: B-tile width, K split (CTAs of a cluster per
+// tile), CTA pairs or not, and the persistent grid's size (0: one CTA, or
+// one cluster, per tile).
+struct GemmPlan {
+    int bn, ksplit;
+    bool pair;
+    int persistent_ctas;
+};
+
+// The launch for a shape (M, N > 0; arguments already checked) on a device
+// with `sms` SMs. pair_caps(w) gives how many CTA pairs of width w fit on the
+// device at once; it is asked only when the library picks the pair width,
+// and a non-positive answer fails with caps_status.
+template <class PairCaps>
+rmsq_status plan_gemm(bool prequant, int64_t M, int64_t N, int64_t K, const rmsq_gemm_opts &o, int sms,
+                      PairCaps &&pair_caps, rmsq_status caps_status, GemmPlan &plan)
+{
     const int64_t m_tiles = (M + 127) / 128;
-    if (m_tiles > 65535)
-        return failf(RMSQ_ERR_UNSUPPORTED, "M=%lld exceeds %d rows", (long long)M, 65535 * 128);
-    const int64_t tile_bytes = (K / 128) * 512;
-    Range rd = mat_range(d, M, N, ld_d, 2);
-    Range ins[4] = {mat_range(a, M, a_row_bytes, lda_bytes, 1), mat_range(b_q, N, K / 2, ld_b, 1),
-                    mat_range(b_scale, 1, (N + 127) / 128 * tile_bytes, 0, 1), {0, 0}};
-    if (!prequant)
-        ins[3] = mat_range(a_scale, 1, m_tiles * tile_bytes, 0, 1);
-    for (const Range &r : ins)
-        if (r.hi > r.lo && overlaps(rd, r))
-            return failf(RMSQ_ERR_INVALID_ARG, "D overlaps an input");
-    if (!tensor_map_encoder_available())
-        return failf(RMSQ_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return failf(RMSQ_ERR_CUDA, "no current device");
-    unsigned int *status = device_status_word(dev);
-    if (!status)
-        return failf(RMSQ_ERR_CUDA, "status word address unavailable");
     // Tile width, from measurements on GB300 (N = 2112, K = 7168). The
     // prequant kernel quantises A once per B tile, so it mostly takes the
     // widest tile, except: up to 16 tokens, 64-row tiles (K split 4; 8.4
@@ -794,9 +779,6 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     // least half the SMs a tile, 128 from two row tiles of A on, and 64 for
     // a single row tile (decode). With fewer tiles than SMs, K is split over
     // a cluster of up to 8 CTAs (each at least one 256-element span of K).
-    const int sms = device_sm_count();
-    if (sms <= 0)
-        return failf(RMSQ_ERR_CUDA, "SM count query failed");
     int bn = o.bn;
     if (o.schedule == 3) {
         if (prequant || (bn && bn != 256 && bn != 192) || (o.ksplit && o.ksplit != 1))
@@ -841,9 +823,10 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
         // counting a 192-wide tile as 0.75 of a 256-wide one and charging it
         // 4 % for its lower efficiency per column (measured: 12.8 against
         // 12.3 us per 256-column unit at N = 2112, K = 7168).
-        const int cap256 = pair_capacity(dev, 256), cap192 = pair_capacity(dev, 192);
+        const int cap256 = pair_caps(256), cap192 = pair_caps(192);
         if (cap256 <= 0 || cap192 <= 0)
-            return failf(RMSQ_ERR_CUDA, "cluster occupancy query failed");
+            return failf(caps_status,
+                         "CTA-pair capacity unavailable (cluster occupancy query failed or not given)");
         const int64_t mt2 = (M + 255) / 256;
         const int64_t w256 = (mt2 * ((N + 255) / 256) + cap256 - 1) / cap256 * 256;
         const int64_t w192 = (mt2 * ((N + 191) / 192) + cap192 - 1) / cap192 * 192;
@@ -854,6 +837,63 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
             return failf(RMSQ_ERR_UNSUPPORTED, "the persistent schedule needs quantised A and no K split");
         persistent = true;
     }
+    plan.bn = bn;
+    plan.ksplit = ksplit;
+    plan.pair = pair;
+    plan.persistent_ctas = persistent ? (int)(tiles < sms ? tiles : sms) : 0;
+    return RMSQ_OK;
+}
+
+// Shared by both placements: a_q / ld_a (bytes) for MXFP4 A, a / ld_a
+// (elements) for bf16 A.
+rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *a_scale, const void *b_q,
+                        int64_t ld_b, const void *b_scale, void *d, int64_t ld_d, int64_t M, int64_t N,
+                        int64_t K, void *stream, const rmsq_gemm_opts *opts)
+{
+    const rmsq_gemm_opts o = opts ? *opts : kDefaultGemmOpts;
+    const rmsq_status cs = check_gemm_args(M, N, K, o);
+    if (cs != RMSQ_OK)
+        return cs;
+    if (M == 0 || N == 0)
+        return clear_error();
+    if (!a || !b_q || !b_scale || !d || (!prequant && !a_scale))
+        return failf(RMSQ_ERR_INVALID_ARG, "operand, scale and output pointers are required");
+    const int64_t a_row_bytes = prequant ? K * 2 : K / 2;
+    const int64_t lda_bytes = prequant ? ld_a * 2 : ld_a;
+    if (lda_bytes < a_row_bytes || ld_b < K / 2 || ld_d < N)
+        return failf(RMSQ_ERR_INVALID_ARG, "leading dimensions must cover a row");
+    if (!aligned(a, 16) || !aligned(b_q, 16) || !aligned(b_scale, 16) || !aligned(d, 16) ||
+        (!prequant && !aligned(a_scale, 16)) || lda_bytes % 16 || ld_b % 16 || ld_d % 8)
+        return failf(RMSQ_ERR_MISALIGNED,
+                    "operands, scale tiles and D need 16-byte aligned bases and 16-byte row pitches");
+    const int64_t m_tiles = (M + 127) / 128;
+    if (m_tiles > 65535)
+        return failf(RMSQ_ERR_UNSUPPORTED, "M=%lld exceeds %d rows", (long long)M, 65535 * 128);
+    const int64_t tile_bytes = (K / 128) * 512;
+    Range rd = mat_range(d, M, N, ld_d, 2);
+    Range ins[4] = {mat_range(a, M, a_row_bytes, lda_bytes, 1), mat_range(b_q, N, K / 2, ld_b, 1),
+                    mat_range(b_scale, 1, (N + 127) / 128 * tile_bytes, 0, 1), {0, 0}};
+    if (!prequant)
+        ins[3] = mat_range(a_scale, 1, m_tiles * tile_bytes, 0, 1);
+    for (const Range &r : ins)
+        if (r.hi > r.lo && overlaps(rd, r))
+            return failf(RMSQ_ERR_INVALID_ARG, "D overlaps an input");
+    if (!tensor_map_encoder_available())
+        return failf(RMSQ_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return failf(RMSQ_ERR_CUDA, "no current device");
+    unsigned int *status = device_status_word(dev);
+    if (!status)
+        return failf(RMSQ_ERR_CUDA, "status word address unavailable");
+    const int sms = device_sm_count();
+    if (sms <= 0)
+        return failf(RMSQ_ERR_CUDA, "SM count query failed");
+    GemmPlan plan{};
+    const rmsq_status ps = plan_gemm(
+        prequant, M, N, K, o, sms, [dev](int w) { return pair_capacity(dev, w); }, RMSQ_ERR_CUDA, plan);
+    if (ps != RMSQ_OK)
+        return ps;
     GemmLaunch g{};
     if (prequant) {
         g.a_bf16 = a;
@@ -870,10 +910,10 @@ rmsq_status gemm_common(bool prequant, const void *a, int64_t ld_a, const void *
     g.M = M;
     g.N = N;
     g.K = K;
-    g.bn = bn;
-    g.ksplit = ksplit;
-    g.persistent_ctas = persistent ? (int)(tiles < sms ? tiles : sms) : 0;
-    g.pair = pair;
+    g.bn = plan.bn;
+    g.ksplit = plan.ksplit;
+    g.persistent_ctas = plan.persistent_ctas;
+    g.pair = plan.pair;
     g.debug_skip_stage = o.debug_stall_stage - 1;   // -1: off
     g.wait_limit_ns = o.wait_limit_ns > 0 ? o.wait_limit_ns : 2000000000LL;
     g.status = status;
@@ -921,6 +961,35 @@ rmsq_status rmsq_a16wfp4_gemm(
     int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream)
 {
     return gemm_common(true, a, ld_a, nullptr, b_q, ld_b, b_scale_tiles, d, ld_d, M, N, K, stream, nullptr);
+}
+
+rmsq_status rmsq_gemm_plan_for(int32_t prequant, int64_t M, int64_t N, int64_t K, const rmsq_gemm_opts *opts,
+                               int32_t sms, int32_t pairs_256, int32_t pairs_192, rmsq_gemm_plan *plan)
+{
+    if (!plan)
+        return failf(RMSQ_ERR_INVALID_ARG, "plan is required");
+    *plan = rmsq_gemm_plan{0, 0, 0, 0};
+    const rmsq_gemm_opts o = opts ? *opts : kDefaultGemmOpts;
+    const rmsq_status cs = check_gemm_args(M, N, K, o);
+    if (cs != RMSQ_OK)
+        return cs;
+    if (sms <= 0)
+        return failf(RMSQ_ERR_INVALID_ARG, "sms must be > 0 (got %d)", sms);
+    if (M == 0 || N == 0)
+        return clear_error();
+    if ((M + 127) / 128 > 65535)
+        return failf(RMSQ_ERR_UNSUPPORTED, "M=%lld exceeds %d rows", (long long)M, 65535 * 128);
+    GemmPlan p{};
+    const rmsq_status ps = plan_gemm(
+        prequant != 0, M, N, K, o, sms, [=](int w) { return w == 192 ? pairs_192 : pairs_256; },
+        RMSQ_ERR_INVALID_ARG, p);
+    if (ps != RMSQ_OK)
+        return ps;
+    plan->bn = p.bn;
+    plan->ksplit = p.ksplit;
+    plan->schedule = p.pair ? 3 : (p.persistent_ctas > 0 ? 2 : 1);
+    plan->persistent_ctas = p.persistent_ctas;
+    return clear_error();
 }
 
 rmsq_status rmsq_mx_scale_tiles(const uint8_t *scale, int64_t ld, int64_t R, int64_t G, uint8_t *out,

@@ -53,6 +53,11 @@ class GemmOpts(ctypes.Structure):
         super().__init__(bn, ksplit, wait_limit_ns, debug_stall_stage, schedule)
 
 
+class GemmPlan(ctypes.Structure):
+    """Mirror of ``rmsq_gemm_plan``."""
+    _fields_ = [("bn", _i32), ("ksplit", _i32), ("schedule", _i32), ("persistent_ctas", _i32)]
+
+
 class RmsqError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
@@ -74,6 +79,7 @@ _SIGNATURES = {
     "rmsq_mxfp4_gemm_ex": [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _p],
     "rmsq_a16wfp4_gemm": [_p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p],
     "rmsq_a16wfp4_gemm_ex": [_p, _i64, _p, _i64, _p, _p, _i64, _i64, _i64, _i64, _p, _p],
+    "rmsq_gemm_plan_for": [_i32, _i64, _i64, _i64, _p, _i32, _i32, _i32, _p],
     "rmsq_mx_scale_tiles": [_p, _i64, _i64, _i64, _p, ctypes.c_uint8, _p],
     "rmsq_sync_status": [_p],
     "rmsq_encode_e4m3": [_p, _p, _i64, _p],
@@ -408,6 +414,21 @@ def a16wfp4_gemm(a: torch.Tensor, b_q: torch.Tensor, b_scale_tiles: torch.Tensor
     else:
         _check(lib().rmsq_a16wfp4_gemm_ex(*args, ctypes.byref(opts)))
     return d
+
+
+def gemm_plan(M: int, N: int, K: int, *, sms: int, pairs_256: int, pairs_192: int, prequant: bool = False,
+              opts: GemmOpts | None = None) -> GemmPlan:
+    """The launch mxfp4_gemm (or, with prequant, a16wfp4_gemm) makes for an
+    M x N x K product on a device with ``sms`` SMs that holds ``pairs_256`` /
+    ``pairs_192`` CTA pairs at once: B-tile width, K split, schedule (1 one
+    tile per CTA, 2 persistent, 3 CTA pairs) and persistent grid size. Host
+    arithmetic only (rmsq_gemm_plan_for); raises on the arguments the GEMM
+    calls reject."""
+    plan = GemmPlan()
+    o = ctypes.byref(opts) if opts is not None else None
+    _check(lib().rmsq_gemm_plan_for(1 if prequant else 0, M, N, K, o, sms, pairs_256, pairs_192,
+                                    ctypes.byref(plan)))
+    return plan
 
 
 def add_rmsnorm_quant_mxfp4_mma_scales_into(x, gamma, residual, q, scale_tiles, res_out=None, y=None,
