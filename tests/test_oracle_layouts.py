@@ -1,7 +1,8 @@
 """Pins of the oracle's GEMM-ready scale layouts: hand-evaluated positions of
 the block-scaled MMA tile layout (tests/golden/mx_scale_tiles.json), the
-layout being a bijection onto the non-padding bytes, and the padded
-column-major FP8 scales equalling the plain column-major ones."""
+layout being a bijection onto the non-padding bytes, padding bytes holding the
+requested fill, and the padded column-major FP8 scales equalling the plain
+column-major ones."""
 
 import json
 import os
@@ -34,6 +35,17 @@ def test_mx_scale_tiles_is_a_bijection(oracle_mod):
         assert int(mark.sum()) == M * G                       # every entry lands on its own byte
         got = np.sort((planes[0] + (planes[1] << 8) + (planes[2] << 16))[mark == 1])
         np.testing.assert_array_equal(got, idx)
+
+
+def test_mx_scale_tiles_padding_is_fill(oracle_mod):
+    """Bytes of the padded tiles that hold no entry (rows past M, groups past
+    G) carry the requested fill; the entries keep their values."""
+    for M, G, fill in ((130, 5, 0xAB), (1, 1, 7), (128, 4, 255)):
+        data = np.full((M, G), 3, np.uint8)                   # no entry equals the fill
+        out = oracle_mod.mx_scale_tiles(data, fill=fill)
+        assert out.size == -(-M // 128) * -(-G // 4) * 512
+        assert int((out == 3).sum()) == M * G
+        assert int((out == fill).sum()) == out.size - M * G
 
 
 def test_fp8_padded_column_major(oracle_mod):

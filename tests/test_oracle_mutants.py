@@ -1,11 +1,13 @@
 """The oracle's pins are strong enough to catch plausible mistakes.
 
-Each case plants one mistake in a copy of the oracle's C source, compiles it
-on the CPU, swaps it in for the real oracle, and runs the pins (hand-worked
-rows, encoder brute force, library cross-checks, invariants): at least one of
-them must fail. Nothing here touches the GPU or the real oracle build.
+Each case plants one mistake in a copy of the oracle's C source (compiled on
+the CPU and swapped in for the real oracle) or of its numpy layer (loaded over
+the real C library), and runs the pins (hand-worked rows, encoder brute force,
+library cross-checks, invariants, structural identities): at least one of them
+must fail. Nothing here touches the GPU or the real oracle build.
 """
 
+import importlib.util
 import os
 import shutil
 
@@ -16,6 +18,7 @@ from oracle import build as oracle_build
 from oracle import oracle as O
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "rmsq_oracle.c")
+PY_SRC = os.path.join(os.path.dirname(SRC), "oracle.py")
 
 MUTANTS = {
     "drop_eps": ("sqrt(S / (double)c->H + (double)c->eps)", "sqrt(S / (double)c->H)"),
@@ -51,6 +54,21 @@ MUTANTS = {
     "gemm_output_truncated": ("c->dbf16[o] = f32_to_bf16_rne((float)d);",
                               "c->dbf16[o] = (uint16_t)(*(uint32_t *)&(float){(float)d} >> 16);"),
     "zero_group_nan": ("float quot = (amax == 0.0f) ? v : v / scale;", "float quot = v / scale;"),
+    "margin_to_the_far_boundary": ("fmin(fabs(t64 - mid_up), fabs(t64 - mid_dn))",
+                                   "fmax(fabs(t64 - mid_up), fabs(t64 - mid_dn))"),
+}
+
+# Mistakes in the numpy layer that chains the C steps (oracle/oracle.py).
+PY_MUTANTS = {
+    "residual_skipped": ("        r = add_residual(x, residual, nthreads)\n    else:\n        r = x",
+                         "        r = x\n    else:\n        r = x"),
+    "scale_layout_ignored": ("q, scale = group_quant_fp8(y, group, _layout_code(layout), nthreads)",
+                             "q, scale = group_quant_fp8(y, group, SCALE_ROW_MAJOR, nthreads)"),
+    "kv_half_is_the_q_half": ('    return {"q": a, "kv": b}', '    return {"q": a, "kv": a}'),
+    "prequant_drops_activation_scales": ("    out = mxfp4_gemm(q, s, b_q, b_scale, nthreads)",
+                                         "    out = mxfp4_gemm(q, np.full_like(s, 127), b_q, b_scale, nthreads)"),
+    "tile_padding_fill_ignored": ("out = np.full(((M + 127) // 128) * ((G + 3) // 4) * 512, fill, dtype=np.uint8)",
+                                  "out = np.full(((M + 127) // 128) * ((G + 3) // 4) * 512, 0, dtype=np.uint8)"),
 }
 
 
@@ -74,8 +92,12 @@ def _pins(oracle_mod):
     yield "norm:fp8_invariants", lambda: norm.test_fp8_quant_invariants(oracle_mod, b)
     yield "norm:col_major", lambda: norm.test_fp8_column_major_is_transpose(oracle_mod, b)
     yield "norm:mxfp4_invariants", lambda: norm.test_mxfp4_invariants(oracle_mod)
+    yield "norm:margin", lambda: norm.test_margin_is_the_distance_to_the_fp32_rounding_boundary(oracle_mod, b)
+    yield "norm:qknorm_halves", lambda: norm.test_qknorm_halves_equal_single_calls(oracle_mod)
+    yield "norm:mxfp4_qknorm_halves", lambda: norm.test_mxfp4_qknorm_halves_equal_single_calls(oracle_mod)
     from tests import test_oracle_layouts as lay
     yield "layout:mx_tiles", lambda: lay.test_mx_scale_tiles_hand_positions(oracle_mod)
+    yield "layout:mx_tiles_fill", lambda: lay.test_mx_scale_tiles_padding_is_fill(oracle_mod)
     yield "layout:col_pad4", lambda: lay.test_fp8_padded_column_major(oracle_mod)
     from tests import test_oracle_gemm as gemm
     yield "gemm:hand", lambda: gemm.test_hand_worked_product(oracle_mod)
@@ -84,6 +106,7 @@ def _pins(oracle_mod):
     yield "gemm:numpy_fp64", lambda: gemm.test_exact_fp64_matrix_product(oracle_mod)
     yield "gemm:scale_group", lambda: gemm.test_scale_byte_scales_its_group_only(oracle_mod)
     yield "gemm:cancellation", lambda: gemm.test_cancellation_keeps_small_terms(oracle_mod)
+    yield "gemm:prequant", lambda: gemm.test_prequant_is_quant_then_gemm(oracle_mod)
 
 
 def _batch():
@@ -96,6 +119,31 @@ def _batch():
 def test_real_oracle_passes_every_pin(oracle_mod):
     for name, run in _pins(oracle_mod):
         run()
+
+
+def _first_failing_pin(oracle_mod):
+    for name, run in _pins(oracle_mod):
+        try:
+            run()
+        except AssertionError:
+            return name
+    return None
+
+
+@pytest.mark.parametrize("mutant", sorted(PY_MUTANTS))
+def test_planted_mistake_in_the_composition_is_caught(mutant, tmp_path):
+    """The same for the numpy layer: a copy of oracle.py with one mistake,
+    loaded as a module of the oracle package over the real C library."""
+    find, repl = PY_MUTANTS[mutant]
+    src = open(PY_SRC).read()
+    assert src.count(find) == 1, f"mutation site for {mutant} not found exactly once"
+    path = tmp_path / "oracle_mutant.py"
+    path.write_text(src.replace(find, repl))
+    spec = importlib.util.spec_from_file_location("oracle.oracle_mutant", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod._lib = O.lib()
+    assert _first_failing_pin(mod), f"no pin caught the planted mistake {mutant!r}"
 
 
 @pytest.mark.parametrize("mutant", sorted(MUTANTS))
@@ -111,11 +159,4 @@ def test_planted_mistake_is_caught(mutant, tmp_path, monkeypatch):
     path.write_text(src)
     lib = oracle_build.compile_source(str(path), str(tmp_path / "libmutant.so"))
     monkeypatch.setattr(O, "_lib", O.load_library(lib))
-    caught = []
-    for name, run in _pins(O):
-        try:
-            run()
-        except AssertionError:
-            caught.append(name)
-            break
-    assert caught, f"no pin caught the planted mistake {mutant!r}"
+    assert _first_failing_pin(O), f"no pin caught the planted mistake {mutant!r}"
