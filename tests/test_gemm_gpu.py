@@ -322,7 +322,7 @@ def test_placements_agree_and_match_oracle(oracle_mod, M):
     print(M, st)
 
 
-@pytest.mark.parametrize("M", [1, 4, 16, 64, 128, 256])
+@pytest.mark.parametrize("M", [1, 4, 16, 64, 128, 129, 200, 256])
 def test_placements_agree_at_few_tokens(oracle_mod, M):
     """Up to two row tiles of A, at every tile width and K split the library
     picks or may be asked for there: the quantising GEMM equals the
