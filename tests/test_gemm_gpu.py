@@ -364,7 +364,7 @@ def test_full_size_sampled(oracle_mod):
     y, _ = rmsq.add_rmsnorm(g["x"], g["gamma"], g["residual"])
     pre = rmsq.a16wfp4_gemm(y, gb, tb)
     torch.cuda.synchronize()
-    assert torch.equal(fused, pre)          # both choose 256-row tiles and no K split here
+    assert torch.equal(fused, pre)          # neither splits K here: every sum runs in the same order
     rows = [0, 1, 127, 128, 4095, 5000, 8190, 8191]
     sub = {k: (v[rows] if v.dim() == 2 else v) for k, v in d_cpu.items()}
     ref_q = oracle_mod.add_rmsnorm_quant_mxfp4(sub["x"], sub["residual"], sub["gamma"])
