@@ -2,6 +2,7 @@
 // kernel and team shape, launch, and status reporting. Nothing here
 // allocates device memory; the only device state is the status word that
 // bounded waits report through.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -203,32 +204,34 @@ Seg make_seg(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
 // Number of SMs of the current device (0 if the query fails).
 int sm_count()
 {
-    static int cached[128];
+    static std::atomic<int> cached[128];   // every thread stores the same value
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
         return 0;
-    if (!cached[dev]) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_acquire);
+    if (!n) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return 0;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_release);
     }
-    return cached[dev];
+    return n;
 }
 
 // Device address of the status word, looked up once per device.
 unsigned int *status_word_ptr(int dev)
 {
-    static unsigned int *ptrs[128];
+    static std::atomic<unsigned int *> ptrs[128];   // every thread stores the same value
     if (dev < 0 || dev >= 128)
         return nullptr;
-    if (!ptrs[dev]) {
+    unsigned int *ptr = ptrs[dev].load(std::memory_order_acquire);
+    if (!ptr) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess)
             return nullptr;
-        ptrs[dev] = (unsigned int *)p;
+        ptr = (unsigned int *)p;
+        ptrs[dev].store(ptr, std::memory_order_release);
     }
-    return ptrs[dev];
+    return ptr;
 }
 
 // Debug build: point the segment's bounds checks at the status word and

@@ -535,17 +535,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 EncodeTiledFn encode_fn()
 {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once; the initialisation of a function-local static is thread-safe
+    static const EncodeTiledFn fn = [] {
         void *f = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = (EncodeTiledFn)f;
-    }
+            return (EncodeTiledFn)f;
+        return (EncodeTiledFn) nullptr;
+    }();
     return fn;
 }
 
@@ -571,19 +570,19 @@ cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUte
                           int n_tiles, int persistent_ctas, cudaStream_t st)
 {
     using C = GemmCfg<BN, PRE>;
-    static bool attr[128];
+    static std::atomic<bool> attr[128];   // shared-memory limit raised on this device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev < 0 || dev >= 128)
         return cudaErrorInvalidDevice;
-    if (!attr[dev]) {
+    if (!attr[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(mxfp4_gemm_kernel<BN, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::kSmem);
         if (e != cudaSuccess)
             return e;
-        attr[dev] = true;
+        attr[dev].store(true, std::memory_order_release);
     }
     if (p.persistent) {     // one CTA per SM walks the tiles
         mxfp4_gemm_kernel<BN, PRE><<<dim3(persistent_ctas, 1, 1), gemm_threads<PRE>(), C::kSmem, st>>>(p, ma, mb);

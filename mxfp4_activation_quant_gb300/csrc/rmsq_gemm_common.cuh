@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 

@@ -321,10 +321,11 @@ template <int BN>
 int pair_capacity_t(int dev)
 {
     using C = PairCfg<BN>;
-    static int cap[128];
+    static std::atomic<int> cap[128];   // every thread stores the same value
     if (dev < 0 || dev >= 128)
         return 0;
-    if (!cap[dev]) {
+    int c = cap[dev].load(std::memory_order_acquire);
+    if (!c) {
         if (cudaFuncSetAttribute(mxfp4_gemm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::kSmem) != cudaSuccess)
             return 0;
@@ -342,9 +343,10 @@ int pair_capacity_t(int dev)
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, mxfp4_gemm_pair_kernel<BN>, &cfg) != cudaSuccess || n <= 0)
             return 0;
-        cap[dev] = n;
+        cap[dev].store(n, std::memory_order_release);
+        c = n;
     }
-    return cap[dev];
+    return c;
 }
 
 template <int BN>
