@@ -1,5 +1,7 @@
 """Host-side pieces of the benchmark: algorithmic byte counts per call (the
-roofline's numerator) equal the per-row derivation for each workload, and the
+roofline's numerator) equal the per-row derivation for each workload, ncu
+traffic records count only while their kernel family's sources are unchanged,
+the roofline peaks come from the measured file (else the fallback), and the
 JSON helpers behave without a GPU."""
 
 import os
@@ -28,6 +30,53 @@ def test_traffic_record_requires_current_sources(tmp_path, monkeypatch):
     assert len(bench.kernel_source_digest()) == 16
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.recorded_traffic("prefill:rows") is None
+
+
+def _fake_tree(root):
+    csrc = root / "mxfp4_activation_quant_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("rmsq_rows.cuh", "rmsq_api.cu", "rmsq_gemm.cu", "rmsq_device.cuh", "notes.txt"):
+        (csrc / f).write_text(f"// {f}\n")
+    (root / "profiles").mkdir()
+    return csrc
+
+
+def _stamp(root, monkeypatch):
+    import json
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    rec = {"prefill:rows": {"kernel_source_digest": bench.kernel_source_digest("rows"), "dram_bytes_per_launch": 11},
+           "consumer:gemm": {"kernel_source_digest": bench.kernel_source_digest("gemm"), "dram_bytes_per_launch": 22}}
+    (root / "profiles" / "traffic.json").write_text(json.dumps(rec))
+
+
+def test_traffic_stamps_follow_their_own_sources(tmp_path, monkeypatch):
+    """A capture stays valid while the sources of its kernel family are
+    unchanged: a GEMM-only file voids the GEMM's record only, a file of the
+    norm + quant kernels voids theirs only, a header both include voids both,
+    and files that are not sources count for neither."""
+    csrc = _fake_tree(tmp_path)
+    _stamp(tmp_path, monkeypatch)
+    assert bench.recorded_traffic("prefill:rows") == 11 and bench.recorded_traffic("consumer:gemm") == 22
+    (csrc / "notes.txt").write_text("changed")
+    assert bench.recorded_traffic("prefill:rows") == 11 and bench.recorded_traffic("consumer:gemm") == 22
+    (csrc / "rmsq_gemm.cu").write_text("// changed\n")
+    assert bench.recorded_traffic("prefill:rows") == 11 and bench.recorded_traffic("consumer:gemm") is None
+    _stamp(tmp_path, monkeypatch)
+    (csrc / "rmsq_rows.cuh").write_text("// changed\n")
+    assert bench.recorded_traffic("prefill:rows") is None and bench.recorded_traffic("consumer:gemm") == 22
+    _stamp(tmp_path, monkeypatch)
+    (csrc / "rmsq_device.cuh").write_text("// changed\n")
+    assert bench.recorded_traffic("prefill:rows") is None and bench.recorded_traffic("consumer:gemm") is None
+    assert bench.recorded_traffic("no:such") is None
+
+
+def test_fp4_peak_is_the_bf16_rate_times_six(monkeypatch, tmp_path):
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 1.0, "bf16_tflops": 1800.0}')
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_fp4_peak()[0] == 10800.0
+    (tmp_path / "MEASURED_PEAKS.json").unlink()
+    peak, how = bench.measured_fp4_peak()
+    assert peak == bench.FALLBACK_BF16_TFLOPS * 6 and "fallback" in how
 
 
 def test_measured_peak_is_read(monkeypatch, tmp_path):
