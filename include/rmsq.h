@@ -339,11 +339,12 @@ rmsq_status rmsq_a16wfp4_gemm_ex(
  * defaults), on a device with `sms` SMs on which `pairs_256` / `pairs_192`
  * CTA pairs of the 256- / 192-wide pair kernel fit at once (the GEMM entry
  * points ask the current device for the three numbers; here the caller gives
- * them). Pure host arithmetic: no CUDA call, no device needed. The choice is
- * the one the GEMM calls make, so it applies their option and shape checks
- * and returns the same status for the same arguments (pointer, pitch and
- * alignment checks aside); a pair capacity is needed only when the library
- * picks the pair width, and a non-positive one then gives
+ * them). This is the library's own launch choice, not an operation of the
+ * source pages. Pure host arithmetic: no CUDA call, no device needed. The
+ * choice is the one the GEMM calls make, so it applies their option and shape
+ * checks and returns the same status for the same arguments (pointer, pitch
+ * and alignment checks aside); a pair capacity is needed only when the
+ * library picks the pair width, and a non-positive one then gives
  * RMSQ_ERR_INVALID_ARG.
  *   plan->bn               B-tile width (rows of B per CTA, or per CTA pair)
  *   plan->ksplit           CTAs of one cluster that split each tile's K (1: none)
