@@ -53,6 +53,10 @@ MUTANTS = {
     "gemm_plain_running_sum": ("double d = sum + comp;", "double d = sum;"),
     "gemm_output_truncated": ("c->dbf16[o] = f32_to_bf16_rne((float)d);",
                               "c->dbf16[o] = (uint16_t)(*(uint32_t *)&(float){(float)d} >> 16);"),
+    "gemm_b_nibbles_swapped": ("mx_element(brow, bsc, k)", "mx_element(brow, bsc, k ^ 1)"),
+    "gemm_magnitude_signed": ("mag += fabs(term);", "mag += term;"),
+    "gemm_last_group_dropped": ("for (int64_t k = 0; k < K; ++k) {\n                double term",
+                                "for (int64_t k = 0; k < K - 32; ++k) {\n                double term"),
     "zero_group_nan": ("float quot = (amax == 0.0f) ? v : v / scale;", "float quot = v / scale;"),
     "margin_to_the_far_boundary": ("fmin(fabs(t64 - mid_up), fabs(t64 - mid_dn))",
                                    "fmax(fabs(t64 - mid_up), fabs(t64 - mid_dn))"),
