@@ -38,6 +38,37 @@ def test_every_declared_symbol_is_exported(L):
     assert not missing, missing
 
 
+def _kind_of_c(param: str) -> str:
+    if "*" in param:
+        return "ptr"
+    base = param.split()[-2] if len(param.split()) > 1 else param
+    return {"int64_t": "i64", "int32_t": "i32", "int": "i32", "float": "f32", "uint8_t": "u8"}[base]
+
+
+def _kind_of_ctypes(t) -> str:
+    return {ctypes.c_void_p: "ptr", ctypes.c_char_p: "ptr", ctypes.c_int64: "i64", ctypes.c_int32: "i32",
+            ctypes.c_float: "f32", ctypes.c_uint8: "u8"}[t]
+
+
+def test_binding_signatures_match_the_header():
+    """Every function the header declares has a ctypes signature in the
+    binding (the two error-reporting calls aside), with the same number of
+    arguments and the same kind (pointer, int64, int32, float, byte) at every
+    position, so no call passes its arguments in the wrong registers."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decls = re.findall(r"\b(rmsq_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text)
+    checked = 0
+    for name, params in decls:
+        if name in ("rmsq_status_string", "rmsq_last_error"):
+            continue
+        assert name in rmsq._SIGNATURES, f"{name} has no ctypes signature"
+        want = [_kind_of_c(p.strip()) for p in params.split(",")] if params.strip() not in ("", "void") else []
+        got = [_kind_of_ctypes(t) for t in rmsq._SIGNATURES[name]]
+        assert got == want, (name, want, got)
+        checked += 1
+    assert checked == len(rmsq._SIGNATURES)
+
+
 def test_status_strings(L):
     for s in range(7):
         assert L.rmsq_status_string(s)
