@@ -69,6 +69,19 @@ def test_binding_signatures_match_the_header():
     assert checked == len(rmsq._SIGNATURES)
 
 
+def test_binding_structs_match_the_header():
+    """Each struct the header defines has a ctypes mirror with the same
+    fields, in the same order, of the same widths."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    structs = dict(re.findall(r"typedef struct (rmsq_[a-z_]+) \{([^}]*)\}", text))
+    mirrors = {"rmsq_launch_opts": rmsq.LaunchOpts, "rmsq_gemm_opts": rmsq.GemmOpts, "rmsq_gemm_plan": rmsq.GemmPlan}
+    assert set(structs) == set(mirrors)
+    for name, body in structs.items():
+        want = [(f.split()[1], _kind_of_c(f)) for f in (x.strip() for x in body.split(";")) if f]
+        got = [(fname, _kind_of_ctypes(t)) for fname, t in mirrors[name]._fields_]
+        assert got == want, (name, want, got)
+
+
 def test_status_strings(L):
     for s in range(7):
         assert L.rmsq_status_string(s)
