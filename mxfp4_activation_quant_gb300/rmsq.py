@@ -115,7 +115,13 @@ def _check(status: int) -> None:
 
 
 def _ptr(t):
-    return None if t is None else t.data_ptr()
+    """Device address of a tensor argument (None for an absent optional one).
+    Host tensors are refused here: a kernel given a host address would fault."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor arguments must be CUDA tensors (got a CPU tensor)")
+    return t.data_ptr()
 
 
 def _stream(device) -> int:

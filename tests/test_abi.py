@@ -161,6 +161,14 @@ def test_launch_opts_layout_matches_header():
     assert rmsq.LaunchOpts.debug_skip_row.offset == 16
 
 
+def test_host_tensors_are_refused():
+    """The binding never hands a kernel the address of host memory."""
+    import torch
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        rmsq._ptr(torch.zeros(4))
+    assert rmsq._ptr(None) is None
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(rmsq, "_lib", None)
     monkeypatch.setattr(rmsq, "LIB_PATH", str(tmp_path / "nope.so"))
