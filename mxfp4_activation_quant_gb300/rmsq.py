@@ -124,6 +124,36 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _buf(t, name: str, nbytes: int):
+    """Address of a buffer the library addresses without a pitch (gamma, the
+    outputs, scale tiles): a contiguous CUDA tensor holding at least nbytes
+    bytes, or None when absent. The C calls see only pointers, so the sizes
+    are checked here."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes; this call needs {nbytes}")
+    return t.data_ptr()
+
+
+def _scale_bytes(M: int, H: int, group: int, layout: int) -> int:
+    r, c = scale_shape(M, H, group, layout)
+    return 4 * r * c
+
+
+def _like_x(t, name: str, M: int, H: int) -> int:
+    """A second [M, H] bf16 input (the residual); returns its leading dimension."""
+    ld = _rows_view(t, name)
+    if tuple(t.shape) != (M, H):
+        raise ValueError(f"{name} must have the shape of x, [{M}, {H}]")
+    return ld
+
+
 def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
@@ -170,7 +200,7 @@ def add_rmsnorm_quant_fp8(x: torch.Tensor, gamma: torch.Tensor, residual: torch.
     """
     ldx = _rows_view(x, "x")
     M, H = x.shape
-    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    ldr = _like_x(residual, "residual", M, H) if residual is not None else 0
     dev = x.device
     layout = _layout(scale_layout)
     q = torch.empty((M, H), dtype=torch.float8_e4m3fn, device=dev)
@@ -179,8 +209,8 @@ def add_rmsnorm_quant_fp8(x: torch.Tensor, gamma: torch.Tensor, residual: torch.
     if residual is not None:
         res_out = out_residual if out_residual is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
-    args = (_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H, group, _ptr(q), _ptr(scale),
-            layout, _ptr(res_out), _ptr(y), _stream(dev))
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H, group, _ptr(q),
+            _ptr(scale), layout, _buf(res_out, "out_residual", 2 * M * H), _ptr(y), _stream(dev))
     if opts is None:
         _check(lib().rmsq_add_rmsnorm_quant_group_fp8(*args))
     else:
@@ -194,10 +224,12 @@ def add_rmsnorm_quant_fp8_into(x, gamma, residual, q, scale, res_out=None, y=Non
     """As add_rmsnorm_quant_fp8, writing into caller-allocated outputs (no allocation)."""
     ldx = _rows_view(x, "x")
     M, H = x.shape
-    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    ldr = _like_x(residual, "residual", M, H) if residual is not None else 0
     st = _stream(x.device) if stream is None else stream
-    args = (_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H, group, _ptr(q), _ptr(scale),
-            _layout(scale_layout), _ptr(res_out), _ptr(y), st)
+    layout = _layout(scale_layout)
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H, group,
+            _buf(q, "q", M * H), _buf(scale, "scale", _scale_bytes(M, H, group, layout)), layout,
+            _buf(res_out, "res_out", 2 * M * H), _buf(y, "y", 2 * M * H), st)
     if opts is None:
         _check(lib().rmsq_add_rmsnorm_quant_group_fp8(*args))
     else:
@@ -209,10 +241,11 @@ def add_rmsnorm_quant_mxfp4_into(x, gamma, residual, q, scale, res_out=None, y=N
     """As add_rmsnorm_quant_mxfp4, writing into caller-allocated outputs."""
     ldx = _rows_view(x, "x")
     M, H = x.shape
-    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    ldr = _like_x(residual, "residual", M, H) if residual is not None else 0
     st = _stream(x.device) if stream is None else stream
-    args = (_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H, _ptr(q), _ptr(scale),
-            _ptr(res_out), _ptr(y), st)
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H,
+            _buf(q, "q", M * (H // 2)), _buf(scale, "scale", M * (H // 32)), _buf(res_out, "res_out", 2 * M * H),
+            _buf(y, "y", 2 * M * H), st)
     if opts is None:
         _check(lib().rmsq_add_rmsnorm_quant_mxfp4(*args))
     else:
@@ -226,11 +259,16 @@ def qknorm_quant_fp8_into(q_a, kv_a, gamma_q, gamma_kv, qq, qs, kq, ks, qy=None,
     ldq = _rows_view(q_a, "q_a")
     ldk = _rows_view(kv_a, "kv_a")
     M, Hq = q_a.shape
-    Hkv = kv_a.shape[1]
+    Mk, Hkv = kv_a.shape
+    if Mk != M:
+        raise ValueError("q_a and kv_a must have the same number of rows")
     st = _stream(q_a.device) if stream is None else stream
-    _check(lib().rmsq_qknorm_quant_fp8(_ptr(q_a), ldq, _ptr(kv_a), ldk, _ptr(gamma_q), _ptr(gamma_kv), eps,
-                                       M, Hq, Hkv, group, _ptr(qq), _ptr(qs), _ptr(kq), _ptr(ks),
-                                       _layout(scale_layout), _ptr(qy), _ptr(ky), st))
+    layout = _layout(scale_layout)
+    _check(lib().rmsq_qknorm_quant_fp8(
+        _ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq), _buf(gamma_kv, "gamma_kv", 2 * Hkv),
+        eps, M, Hq, Hkv, group, _buf(qq, "qq", M * Hq), _buf(qs, "qs", _scale_bytes(M, Hq, group, layout)),
+        _buf(kq, "kq", M * Hkv), _buf(ks, "ks", _scale_bytes(M, Hkv, group, layout)), layout,
+        _buf(qy, "qy", 2 * M * Hq), _buf(ky, "ky", 2 * M * Hkv), st))
 
 
 def qknorm_quant_fp8(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Tensor,
@@ -256,8 +294,8 @@ def qknorm_quant_fp8(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Tenso
 
     qq, qs, qy = outs(Hq)
     kq, ks, ky = outs(Hkv)
-    _check(lib().rmsq_qknorm_quant_fp8(_ptr(q_a), ldq, _ptr(kv_a), ldk, _ptr(gamma_q), _ptr(gamma_kv),
-                                       eps, M, Hq, Hkv, group, _ptr(qq), _ptr(qs), _ptr(kq), _ptr(ks),
+    _check(lib().rmsq_qknorm_quant_fp8(_ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq),
+                                       _buf(gamma_kv, "gamma_kv", 2 * Hkv), eps, M, Hq, Hkv, group, _ptr(qq), _ptr(qs), _ptr(kq), _ptr(ks),
                                        layout, _ptr(qy), _ptr(ky), _stream(dev)))
     if keep_bf16:
         return (qy, qq, qs), (ky, kq, ks)
@@ -284,7 +322,8 @@ def qknorm_quant_mxfp4(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Ten
 
     qq, qs, qy = outs(Hq)
     kq, ks, ky = outs(Hkv)
-    _check(lib().rmsq_qknorm_quant_mxfp4(_ptr(q_a), ldq, _ptr(kv_a), ldk, _ptr(gamma_q), _ptr(gamma_kv), eps,
+    _check(lib().rmsq_qknorm_quant_mxfp4(_ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq),
+                                         _buf(gamma_kv, "gamma_kv", 2 * Hkv), eps,
                                          M, Hq, Hkv, _ptr(qq), _ptr(qs), _ptr(kq), _ptr(ks), _ptr(qy),
                                          _ptr(ky), _stream(dev)))
     if keep_bf16:
@@ -299,7 +338,7 @@ def add_rmsnorm_quant_mxfp4(x: torch.Tensor, gamma: torch.Tensor, residual: torc
     the low nibble), E8M0 scales [M, H/32] uint8. Same tuple forms as the FP8 call."""
     ldx = _rows_view(x, "x")
     M, H = x.shape
-    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    ldr = _like_x(residual, "residual", M, H) if residual is not None else 0
     dev = x.device
     q = torch.empty((M, H // 2), dtype=torch.uint8, device=dev)
     scale = torch.empty((M, H // 32), dtype=torch.uint8, device=dev)
@@ -307,8 +346,8 @@ def add_rmsnorm_quant_mxfp4(x: torch.Tensor, gamma: torch.Tensor, residual: torc
     if residual is not None:
         res_out = out_residual if out_residual is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
-    args = (_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H, _ptr(q), _ptr(scale),
-            _ptr(res_out), _ptr(y), _stream(dev))
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H, _ptr(q), _ptr(scale),
+            _buf(res_out, "out_residual", 2 * M * H), _ptr(y), _stream(dev))
     if opts is None:
         _check(lib().rmsq_add_rmsnorm_quant_mxfp4(*args))
     else:
@@ -324,16 +363,17 @@ def add_rmsnorm_quant_mxfp4_mma_scales(x: torch.Tensor, gamma: torch.Tensor,
     are in ``scale_out``, zero-filled when it is allocated here)."""
     ldx = _rows_view(x, "x")
     M, H = x.shape
-    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    ldr = _like_x(residual, "residual", M, H) if residual is not None else 0
     dev = x.device
     q = torch.empty((M, H // 2), dtype=torch.uint8, device=dev)
     scale = scale_out if scale_out is not None else torch.zeros(mma_scale_bytes(M, H), dtype=torch.uint8,
                                                                 device=dev)
     res_out = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if residual is not None else None
     y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
-    _check(lib().rmsq_add_rmsnorm_quant_mxfp4_mma_scales(_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps,
-                                                         M, H, _ptr(q), _ptr(scale), _ptr(res_out), _ptr(y),
-                                                         _stream(dev)))
+    _check(lib().rmsq_add_rmsnorm_quant_mxfp4_mma_scales(_ptr(x), ldx, _ptr(residual), ldr,
+                                                         _buf(gamma, "gamma", 2 * H), eps, M, H, _ptr(q),
+                                                         _buf(scale, "scale_out", mma_scale_bytes(M, H)),
+                                                         _ptr(res_out), _ptr(y), _stream(dev)))
     return ((y, q, scale) if keep_bf16 else (q, scale)), res_out
 
 
@@ -344,15 +384,15 @@ def add_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, residual: torch.Tensor | N
     (``residual_out`` None without a residual). H must be a multiple of 32."""
     ldx = _rows_view(x, "x")
     M, H = x.shape
-    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    ldr = _like_x(residual, "residual", M, H) if residual is not None else 0
     dev = x.device
     y = out if out is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     res_out = None
     if residual is not None:
         res_out = out_residual if out_residual is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     st = _stream(dev) if stream is None else stream
-    _check(lib().rmsq_add_rmsnorm(_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H, _ptr(res_out),
-                                  _ptr(y), st))
+    _check(lib().rmsq_add_rmsnorm(_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H,
+                                  _buf(res_out, "out_residual", 2 * M * H), _buf(y, "out", 2 * M * H), st))
     return y, res_out
 
 
@@ -393,7 +433,8 @@ def mxfp4_gemm(a_q: torch.Tensor, a_scale_tiles: torch.Tensor, b_q: torch.Tensor
         raise ValueError("A and B have different K")
     d = _gemm_out(M, N, a_q.device, out)
     st = _stream(a_q.device) if stream is None else stream
-    args = (_ptr(a_q), lda, _ptr(a_scale_tiles), _ptr(b_q), ldb, _ptr(b_scale_tiles), _ptr(d), d.stride(0),
+    args = (_ptr(a_q), lda, _buf(a_scale_tiles, "a_scale_tiles", mma_scale_bytes(M, K)), _ptr(b_q), ldb,
+            _buf(b_scale_tiles, "b_scale_tiles", mma_scale_bytes(N, K)), _ptr(d), d.stride(0),
             M, N, K, st)
     if opts is None:
         _check(lib().rmsq_mxfp4_gemm(*args))
@@ -414,7 +455,8 @@ def a16wfp4_gemm(a: torch.Tensor, b_q: torch.Tensor, b_scale_tiles: torch.Tensor
         raise ValueError("A and B have different K")
     d = _gemm_out(M, N, a.device, out)
     st = _stream(a.device) if stream is None else stream
-    args = (_ptr(a), lda, _ptr(b_q), ldb, _ptr(b_scale_tiles), _ptr(d), d.stride(0), M, N, K, st)
+    args = (_ptr(a), lda, _ptr(b_q), ldb, _buf(b_scale_tiles, "b_scale_tiles", mma_scale_bytes(N, K)), _ptr(d),
+            d.stride(0), M, N, K, st)
     if opts is None:
         _check(lib().rmsq_a16wfp4_gemm(*args))
     else:
@@ -442,10 +484,12 @@ def add_rmsnorm_quant_mxfp4_mma_scales_into(x, gamma, residual, q, scale_tiles, 
     """As add_rmsnorm_quant_mxfp4_mma_scales, writing into caller-allocated outputs."""
     ldx = _rows_view(x, "x")
     M, H = x.shape
-    ldr = _rows_view(residual, "residual") if residual is not None else 0
+    ldr = _like_x(residual, "residual", M, H) if residual is not None else 0
     st = _stream(x.device) if stream is None else stream
-    _check(lib().rmsq_add_rmsnorm_quant_mxfp4_mma_scales(_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, H,
-                                                         _ptr(q), _ptr(scale_tiles), _ptr(res_out), _ptr(y), st))
+    _check(lib().rmsq_add_rmsnorm_quant_mxfp4_mma_scales(
+        _ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H, _buf(q, "q", M * (H // 2)),
+        _buf(scale_tiles, "scale_tiles", mma_scale_bytes(M, H)), _buf(res_out, "res_out", 2 * M * H),
+        _buf(y, "y", 2 * M * H), st))
 
 
 def sync_status(device=None) -> int:
@@ -456,6 +500,8 @@ def sync_status(device=None) -> int:
 
 def encode_e4m3(v: torch.Tensor) -> torch.Tensor:
     """The kernels' E4M3 conversion applied elementwise (fp32 CUDA tensor -> uint8)."""
+    if v.dtype != torch.float32:
+        raise ValueError("v must be float32")
     v = v.contiguous()
     out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
     _check(lib().rmsq_encode_e4m3(_ptr(v), _ptr(out), v.numel(), _stream(v.device)))
@@ -464,6 +510,8 @@ def encode_e4m3(v: torch.Tensor) -> torch.Tensor:
 
 def encode_e2m1(v: torch.Tensor) -> torch.Tensor:
     """The kernels' E2M1 conversion applied elementwise (one code per byte)."""
+    if v.dtype != torch.float32:
+        raise ValueError("v must be float32")
     v = v.contiguous()
     out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
     _check(lib().rmsq_encode_e2m1(_ptr(v), _ptr(out), v.numel(), _stream(v.device)))
