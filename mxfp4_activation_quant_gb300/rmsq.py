@@ -331,6 +331,24 @@ def qknorm_quant_mxfp4(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Ten
     return (qq, qs), (kq, ks)
 
 
+def qknorm_quant_mxfp4_into(q_a, kv_a, gamma_q, gamma_kv, qq, qs, kq, ks, qy=None, ky=None,
+                            eps: float = 1e-6, stream: int | None = None) -> None:
+    """As qknorm_quant_mxfp4, writing into caller-allocated outputs: codes
+    [M, H/2] uint8 and E8M0 scales [M, H/32] uint8 per latent."""
+    ldq = _rows_view(q_a, "q_a")
+    ldk = _rows_view(kv_a, "kv_a")
+    M, Hq = q_a.shape
+    Mk, Hkv = kv_a.shape
+    if Mk != M:
+        raise ValueError("q_a and kv_a must have the same number of rows")
+    st = _stream(q_a.device) if stream is None else stream
+    _check(lib().rmsq_qknorm_quant_mxfp4(
+        _ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq), _buf(gamma_kv, "gamma_kv", 2 * Hkv),
+        eps, M, Hq, Hkv, _buf(qq, "qq", M * (Hq // 2)), _buf(qs, "qs", M * (Hq // 32)),
+        _buf(kq, "kq", M * (Hkv // 2)), _buf(ks, "ks", M * (Hkv // 32)), _buf(qy, "qy", 2 * M * Hq),
+        _buf(ky, "ky", 2 * M * Hkv), st))
+
+
 def add_rmsnorm_quant_mxfp4(x: torch.Tensor, gamma: torch.Tensor, residual: torch.Tensor | None = None,
                             eps: float = 1e-6, keep_bf16: bool = False,
                             out_residual: torch.Tensor | None = None, opts: LaunchOpts | None = None):

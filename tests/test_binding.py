@@ -99,6 +99,13 @@ def qk_into_args():
                 ky=FakeCuda((M, HKV), BF16))
 
 
+def qk_mx_into_args():
+    return dict(q_a=FakeCuda((M, HQ), BF16), kv_a=FakeCuda((M, HKV), BF16), gamma_q=FakeCuda((HQ,), BF16),
+                gamma_kv=FakeCuda((HKV,), BF16), qq=FakeCuda((M, HQ // 2), U8), qs=FakeCuda((M, HQ // 32), U8),
+                kq=FakeCuda((M, HKV // 2), U8), ks=FakeCuda((M, HKV // 32), U8), qy=FakeCuda((M, HQ), BF16),
+                ky=FakeCuda((M, HKV), BF16))
+
+
 def norm_args():
     return dict(x=FakeCuda((M, H), BF16), gamma=FakeCuda((H,), BF16), residual=FakeCuda((M, H), BF16),
                 out=FakeCuda((M, H), BF16), out_residual=FakeCuda((M, H), BF16))
@@ -124,6 +131,7 @@ CALLS = {
     "mxfp4": (lambda a: rmsq.add_rmsnorm_quant_mxfp4_into(**a, stream=0), mx_into_args),
     "mma_scales": (lambda a: rmsq.add_rmsnorm_quant_mxfp4_mma_scales_into(**a, stream=0), mma_into_args),
     "qknorm": (lambda a: rmsq.qknorm_quant_fp8_into(**a, scale_layout="col", stream=0), qk_into_args),
+    "qknorm_mx": (lambda a: rmsq.qknorm_quant_mxfp4_into(**a, stream=0), qk_mx_into_args),
     "norm": (lambda a: rmsq.add_rmsnorm(**a, stream=0), norm_args),
     "gemm": (lambda a: rmsq.mxfp4_gemm(**a, stream=0), gemm_args),
     "prequant": (lambda a: rmsq.a16wfp4_gemm(**a, stream=0), pre_args),
@@ -180,8 +188,9 @@ def test_residual_must_have_the_shape_of_x(fake, call):
     assert not fake.calls
 
 
-def test_kv_rows_must_match_q_rows(fake):
-    run, make = CALLS["qknorm"]
+@pytest.mark.parametrize("call", ["qknorm", "qknorm_mx"])
+def test_kv_rows_must_match_q_rows(fake, call):
+    run, make = CALLS[call]
     args = make()
     args["kv_a"] = FakeCuda((M - 1, HKV), BF16)
     with pytest.raises(ValueError, match="same number of rows"):
@@ -197,6 +206,11 @@ def test_declared_argument_order(fake):
     _, p = fake.calls[-1]
     assert p[:9] == (a["x"].addr, H, a["residual"].addr, H, a["gamma"].addr, 1e-6, M, H, 128)
     assert p[9:] == (a["q"].addr, a["scale"].addr, rmsq.SCALE_COL_MAJOR, a["res_out"].addr, a["y"].addr, 7)
+    k = qk_mx_into_args()
+    rmsq.qknorm_quant_mxfp4_into(**k, eps=1e-5, stream=3)
+    _, p = fake.calls[-1]
+    assert p == (k["q_a"].addr, HQ, k["kv_a"].addr, HKV, k["gamma_q"].addr, k["gamma_kv"].addr, 1e-5, M, HQ, HKV,
+                 k["qq"].addr, k["qs"].addr, k["kq"].addr, k["ks"].addr, k["qy"].addr, k["ky"].addr, 3)
     g = gemm_args()
     rmsq.mxfp4_gemm(**g, stream=9)
     _, p = fake.calls[-1]
