@@ -225,7 +225,7 @@ def mx_scale_tiles(scale, fill: int = 0) -> np.ndarray:
 
 def add_rmsnorm_quant_fp8(x, residual, gamma, eps: float = 1e-6, group: int = 128,
                           layout="row", nthreads: int | None = None) -> dict:
-    """add -> RMSNorm -> per-group FP8 quant, each step a separate oracle call."""
+    """add, then RMSNorm, then FP8 quantisation by groups: each step a separate oracle call."""
     x = as_u16(x)
     if residual is not None:
         r = add_residual(x, residual, nthreads)

@@ -24,10 +24,10 @@
  *             y_i = bf16_rne((f32(r_i) * inv) * f32(gamma_i)), two fp32
  *             multiplies in that order, no fused multiply-add. y is the bf16
  *             side output ("keep_bf16", (bf16, fp8, scale), same PR).
- *   3a. FP8 group quant, group G = 128 ("group scale FP8 quantization
- *             (group_size=128)", page "fused rmsnorm quant fp8 work",
- *             Motivation): amax = max |y_i| over the group, scale =
- *             f32(amax / 448) by IEEE fp32 division, q_i =
+ *   3a. FP8 group quant, group G = 128 (one FP8 scale per 128 elements:
+ *             page "fused rmsnorm quant fp8 work", Motivation): amax =
+ *             max |y_i| over the group, scale = f32(amax / 448) by IEEE
+ *             fp32 division, q_i =
  *             e4m3(f32(y_i / scale)) by IEEE fp32 division by the stored
  *             scale followed by the saturating round-to-nearest-even E4M3
  *             encoder (OCP 8-bit floating point, E4M3, largest finite 448).
