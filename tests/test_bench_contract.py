@@ -79,6 +79,31 @@ def test_fp4_peak_is_the_bf16_rate_times_six(monkeypatch, tmp_path):
     assert peak == bench.FALLBACK_BF16_TFLOPS * 6 and "fallback" in how
 
 
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference (the CPU oracle, timed on a bounded sample)
+    prints one JSON line with the headline's metric and unit, its own
+    cpu_baseline and an e2e block that moves nothing between host and device."""
+    import json
+    import subprocess
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in rec, key
+    assert rec["impl"] == "reference" and rec["metric"] == bench.METRIC and rec["unit"] == "GB/s"
+    assert rec["steps"] == 1 and rec["warmup"] == 3 and rec["n_gpus"] == 1 and rec["value"] > 0
+    assert "workload" in rec["config"]
+    cb = rec["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == rec["value"] and cb["cores"] >= 1 and cb["sample"]
+    e2e = rec["e2e"]
+    assert e2e["value"] == rec["value"] and e2e["unit"] == rec["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
 def test_measured_peak_is_read(monkeypatch, tmp_path):
     (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 1234.5}')
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
