@@ -42,7 +42,9 @@ if ROOT not in sys.path:
 
 METRIC = "HBM GB/s (% of peak) & rows/s, fused add+RMSNorm+1x128 FP8 quant, M=16384 H=7168"
 WORKLOAD = "prefill"
-FALLBACK_HBM_GBS = 6800.0
+# bench-only variants of the prefill workload: the decode config's
+# column-major scale layouts at the prefill size
+VARIANTS = {"prefill_col": ("prefill", "col"), "prefill_col_pad4": ("prefill", "col_pad4")}
 
 
 def algorithmic_bytes(M: int, H: int, residual: bool = True, keep_bf16: bool = True) -> int:
@@ -63,28 +65,73 @@ def qk_bytes(M: int, Hq: int, Hkv: int) -> int:
     return sum(M * (2 * h + h + 4 * (h // 128)) + 2 * h for h in (Hq, Hkv))
 
 
-def measured_peaks() -> tuple[float, str]:
+def copy_peak_gbs(dev) -> float:
+    """Read + write GB/s of the library's own streaming copy kernel (rmsq_copy)
+    over 1 GiB, best of 10 (CUDA events): the HBM peak where no separately
+    measured one is recorded."""
+    import torch
+    from mxfp4_activation_quant_gb300 import rmsq
+    n = 1 << 30
+    src = torch.empty(n, dtype=torch.uint8, device=dev).fill_(1)
+    dst = torch.empty_like(src)
+    best = float("inf")
+    for _ in range(12):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        rmsq.copy_(dst, src)
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del src, dst
+    return round(2 * n / (best * 1e-3) / 1e9, 1)
+
+
+def measured_peaks(dev=None) -> tuple[float | None, str]:
+    """The HBM peak: the measured copy rate in MEASURED_PEAKS.json, else
+    the rate of the library's own copy kernel measured now on `dev`."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
             return float(json.load(fh)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
-        return FALLBACK_HBM_GBS, "fallback"
+        if dev is None:
+            return None, "unavailable: no MEASURED_PEAKS.json and no device to measure on"
+        return copy_peak_gbs(dev), "measured here: the library's copy kernel, 1 GiB read + written, best of 10"
 
 
 # Dense FP4 (E2M1) tensor rate over dense bf16 on GB300, from the nominal
 # figures (13.5 and 2.25 PFLOP/s); the measured bf16 GEMM rate times this is
 # the FP4 roofline.
 FP4_OVER_BF16 = 6.0
-FALLBACK_BF16_TFLOPS = 1900.0
 
 
-def measured_fp4_peak() -> tuple[float, str]:
+def bf16_gemm_tflops(dev) -> float:
+    """cuBLAS bf16 GEMM rate (torch.matmul, 8192^3, best of 10), as the
+    driver measures it, for boxes without MEASURED_PEAKS.json."""
+    import torch
+    n = 8192
+    a = torch.randn((n, n), device=dev).to(torch.bfloat16)
+    b = torch.randn((n, n), device=dev).to(torch.bfloat16)
+    best = float("inf")
+    for _ in range(12):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+
+
+def measured_fp4_peak(dev=None) -> tuple[float | None, str]:
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
             bf16 = float(json.load(fh)["bf16_tflops"])
         return bf16 * FP4_OVER_BF16, "measured bf16 burst x nominal fp4/bf16 ratio 6"
     except (OSError, KeyError, ValueError):
-        return FALLBACK_BF16_TFLOPS * FP4_OVER_BF16, "fallback bf16 x nominal fp4/bf16 ratio 6"
+        if dev is None:
+            return None, "unavailable: no MEASURED_PEAKS.json and no device to measure on"
+        return (round(bf16_gemm_tflops(dev) * FP4_OVER_BF16, 1),
+                "bf16 GEMM measured here (8192^3, best of 10) x nominal fp4/bf16 ratio 6")
 
 
 # the GEMM's own files (left out of the norm + quant digest) and the shared headers it also uses
@@ -118,6 +165,8 @@ def recorded_traffic(kernel_name: str) -> float | None:
     ent = rec.get(kernel_name)
     kind = "gemm" if kernel_name.startswith("consumer") else "rows"
     if not ent or ent.get("kernel_source_digest") != kernel_source_digest(kind):
+        return None
+    if any(k.startswith("restamped") for k in ent):      # a digest re-keyed by hand is no capture
         return None
     return float(ent["dram_bytes_per_launch"])
 
@@ -171,8 +220,19 @@ def gpu_id_for(dev) -> str:
 
 # ------------------------------------------------------------ reference arm
 
+def workload_config(name: str, M: int, world: int, bytes_step: int) -> dict:
+    """The ``config`` block of a line: what the workload is, nothing about the
+    arm that ran it (both arms print the same block for the same workload)."""
+    return {"workload": WORKLOAD_TEXT[name].format(M=M), "global_rows": M * world,
+            "parallelism": f"rows sharded, {world} independent batch(es)", "bytes_per_step": bytes_step,
+            "l2": ("inputs larger than L2 (129 MB); no flush needed" if bytes_step > 400e6 else
+                   "inputs smaller than L2: back-to-back steps are partly L2-resident")}
+
+
 def run_reference(args) -> None:
-    """The CPU oracle as it stands, on host cores, bounded samples of the workload."""
+    """The CPU oracle as it stands, on the host cores, on the full headline
+    workload: every step is one pass over all 16384 rows (about 0.1 s on 16
+    cores), so the line's config is the headline's own."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
@@ -180,9 +240,9 @@ def run_reference(args) -> None:
     from oracle import oracle
 
     w = synth.WORKLOADS[WORKLOAD]
-    rows = 1024
-    d = synth.make_inputs(w, M=rows)
+    d = synth.make_inputs(w)
     x, r, g = oracle.as_u16(d["x"]), oracle.as_u16(d["residual"]), oracle.as_u16(d["gamma"])
+    rows = x.shape[0]
     cores = oracle.default_threads()
     for _ in range(args.warmup):
         oracle.add_rmsnorm_quant_fp8(x, r, g, w.eps, nthreads=cores)
@@ -192,14 +252,14 @@ def run_reference(args) -> None:
     dt = (time.perf_counter() - t0) / args.steps
     b = algorithmic_bytes(rows, w.H)
     value = b / dt / 1e9
-    sample = f"first {rows} rows of the prefill workload per step (H={w.H}, keep_bf16)"
+    sample = f"all {rows} rows of the prefill workload per step (H={w.H}, keep_bf16)"
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64/f32", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD} M=16384 H=7168 FP8 1x128 keep_bf16 (sampled {rows} rows/step)",
-                   "rows_per_step": rows},
+        "config": workload_config(WORKLOAD, rows, 1, b),
+        "timing": "wall clock of K oracle passes on the host cores",
         "rows_per_s": round(rows / dt, 1),
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
@@ -207,8 +267,10 @@ def run_reference(args) -> None:
     }))
 
 
-def cpu_baseline(d_cpu, w) -> dict:
-    """The oracle timed on the host cores on the full prefill workload (3 passes)."""
+def cpu_baseline(d_cpu, w) -> tuple[dict, dict]:
+    """The oracle timed on the host cores on the full prefill workload (3
+    passes). Returns the timing and the oracle's outputs of the last pass,
+    against which the GPU's outputs of the same inputs are compared."""
     from oracle import oracle
     x, r, g = oracle.as_u16(d_cpu["x"]), oracle.as_u16(d_cpu["residual"]), oracle.as_u16(d_cpu["gamma"])
     cores = oracle.default_threads()
@@ -216,12 +278,60 @@ def cpu_baseline(d_cpu, w) -> dict:
     passes = 3
     t0 = time.perf_counter()
     for _ in range(passes):
-        oracle.add_rmsnorm_quant_fp8(x, r, g, w.eps, nthreads=cores)
+        ref = oracle.add_rmsnorm_quant_fp8(x, r, g, w.eps, nthreads=cores)
     dt = (time.perf_counter() - t0) / passes
     M = x.shape[0]
-    return {"value": round(algorithmic_bytes(M, w.H) / dt / 1e9, 3), "unit": "GB/s", "cores": cores,
-            "kind": "oracle", "sample": f"all {M} rows of the prefill workload, {passes} passes",
-            "rows_per_s": round(M / dt, 1), "ms_per_pass": round(dt * 1e3, 2)}
+    return ({"value": round(algorithmic_bytes(M, w.H) / dt / 1e9, 3), "unit": "GB/s", "cores": cores,
+             "kind": "oracle", "sample": f"all {M} rows of the prefill workload, {passes} passes",
+             "rows_per_s": round(M / dt, 1), "ms_per_pass": round(dt * 1e3, 2)}, ref)
+
+
+PARITY_RULE = ("residual_out and bf16 y bit-exact; scales within 1e-5 relative; every code within 1 ULP; "
+               "at most 0.1 % of codes differing. Rows whose fp64 inv_rms lies within 2^-40 of an fp32 "
+               "rounding boundary (boundary_rows) may round the other way; everywhere else every output "
+               "must be bit-exact")
+
+
+def _verdict(st: dict) -> dict:
+    """The parity bar applied to one call's figures (tests/parity.py's rule)."""
+    ok = (st.get("residual_out_bit_exact", True) and st.get("y_bit_exact_outside_boundary", True)
+          and st["max_code_ulp"] <= 1 and st["mismatch_fraction"] <= 1e-3
+          and st["codes_bit_exact_outside_boundary"] and st.get("scale_max_rel", 0.0) <= 1e-5
+          and st.get("scales_bit_exact_outside_boundary", True) and st.get("scale_max_step", 0) <= 1)
+    return {**st, "passes": bool(ok)}
+
+
+def parity_report(gpu: dict, prefill_ref: dict) -> dict:
+    """Part of the CPU-baseline leg: the GPU outputs of every config (0-4)
+    against the oracle run on the same inputs, all rows, with the mismatch
+    fraction of the codes. ``gpu`` maps a config name to (workload, CPU
+    inputs, GPU outputs copied to the host); the prefill oracle outputs come
+    from the timed CPU baseline."""
+    from oracle import oracle
+    from tests import parity
+    out = {"rule": PARITY_RULE}
+    for name, (w, d, got) in gpu.items():
+        if name == "prefill":
+            out[name] = _verdict(parity.fp8_stats(got, prefill_ref, w.scale_layout))
+        elif w.kind == "fp8":
+            ref = oracle.add_rmsnorm_quant_fp8(d["x"], d.get("residual"), d["gamma"], w.eps,
+                                               layout=w.scale_layout)
+            out[name] = _verdict(parity.fp8_stats(got, ref, w.scale_layout))
+        elif w.kind == "qknorm":
+            ref = oracle.qknorm_quant_fp8(d["q_a"], d["kv_a"], d["gamma_q"], d["gamma_kv"], w.eps)
+            a = _verdict(parity.fp8_stats(got["q_a"], ref["q"]))
+            b = _verdict(parity.fp8_stats(got["kv_a"], ref["kv"]))
+            codes = got["q_a"]["q"].numel() + got["kv_a"]["q"].numel()
+            out[name] = {"q_a": a, "kv_a": b, "rows": a["rows"],
+                         "boundary_rows": a["boundary_rows"] + b["boundary_rows"],
+                         "codes_differing": a["codes_differing"] + b["codes_differing"],
+                         "mismatch_fraction": (a["codes_differing"] + b["codes_differing"]) / codes,
+                         "passes": a["passes"] and b["passes"]}
+        else:
+            ref = oracle.add_rmsnorm_quant_mxfp4(d["x"], d.get("residual"), d["gamma"], w.eps)
+            out[name] = _verdict(parity.mx_stats(got, ref))
+    out["all_pass"] = all(v["passes"] for k, v in out.items() if isinstance(v, dict))
+    return out
 
 
 # -------------------------------------------------------------- our arm
@@ -284,15 +394,63 @@ def time_graph(fn, steps: int, stream) -> float:
     return ms
 
 
-def other_workloads(dev, stream) -> dict:
-    """Decode latency (M=64), MLA latent pair and MXFP4 throughput (reported beside the headline)."""
+def _cold_us(fn, dev, calls: int = 50) -> float:
+    """Median microseconds of `calls` calls, each timed alone (CUDA events)
+    after 256 MB (twice L2) have been written, so no input is L2-resident."""
+    import torch
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    each = []
+    for _ in range(calls):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        each.append(e0.elapsed_time(e1) * 1e3)
+    del flush
+    return statistics.median(each)
+
+
+def _graph_us(fn, reps: int) -> float:
+    """Microseconds per call of fn() replayed from a CUDA graph of `reps` calls
+    captured on torch's capture stream (warm L2 across calls)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps
+
+
+def other_workloads(dev, stream, peak: float) -> tuple[dict, dict]:
+    """Decode latency (M=64), the MLA latent pair, MXFP4 throughput and the
+    tiny config, reported beside the headline. Returns the report and, per
+    config, (workload, CPU inputs, GPU outputs on the host) for the parity
+    report of the CPU-baseline leg."""
     import torch
     from mxfp4_activation_quant_gb300 import rmsq, synth
 
-    out = {}
+    out, gpu = {}, {}
+    # tiny: M=4, H=256, row-major scales
+    w = synth.WORKLOADS["tiny"]
+    dc = synth.make_inputs(w)
+    d = {k: v.to(dev) for k, v in dc.items()}
+    (tq, ts), tr = rmsq.add_rmsnorm_quant_fp8(d["x"], d["gamma"], d["residual"], eps=w.eps)
+    torch.cuda.synchronize()
+    gpu["tiny"] = (w, dc, {"q": tq.cpu(), "scale": ts.cpu(), "residual_out": tr.cpu()})
+
     # decode: M=64, H=7168, column-major scales; launch-free latency via a graph
     w = synth.WORKLOADS["decode"]
-    d = {k: v.to(dev) for k, v in synth.make_inputs(w).items()}
+    dc = synth.make_inputs(w)
+    d = {k: v.to(dev) for k, v in dc.items()}
     M, H = w.M, w.H
     q = torch.empty((M, H), dtype=torch.uint8, device=dev)
     s = torch.empty((H // 128, M), dtype=torch.float32, device=dev)
@@ -304,37 +462,17 @@ def other_workloads(dev, stream) -> dict:
     for _ in range(10):
         dec()
     torch.cuda.synchronize()
-    reps = 200
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for _ in range(reps):
-            dec()
-    g.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    g.replay()
-    b.record()
-    torch.cuda.synchronize()
-    warm_us = a.elapsed_time(b) * 1e3 / reps
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    cold = []
-    for _ in range(50):
-        flush.fill_(1)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        dec()
-        e1.record()
-        torch.cuda.synchronize()
-        cold.append(e0.elapsed_time(e1) * 1e3)
+    gpu["decode"] = (w, dc, {"q": q.cpu(), "scale": s.cpu(), "residual_out": ro.cpu()})
+    warm_us = _graph_us(dec, 200)
     out["decode_m64"] = {"us_per_call_graph_warm_l2": round(warm_us, 3),
-                         "us_per_call_cold_l2_median": round(statistics.median(cold), 3),
-                         "GBps_graph_warm": round(algorithmic_bytes(M, H, True, False) / warm_us / 1e3, 1)}
-    del flush
+                         "us_per_call_cold_l2_median": round(_cold_us(dec, dev), 3),
+                         "GBps_graph_warm": round(algorithmic_bytes(M, H, True, False) / warm_us / 1e3, 1),
+                         "form": "latency (one block per SM or fewer)"}
 
     # MLA q_a / kv_a latents, M=8192
     w = synth.WORKLOADS["qknorm"]
-    d = {k: v.to(dev) for k, v in synth.make_inputs(w).items()}
+    dc = synth.make_inputs(w)
+    d = {k: v.to(dev) for k, v in dc.items()}
     M = w.M
     qq = torch.empty((M, w.Hq), dtype=torch.uint8, device=dev)
     qs = torch.empty((M, w.Hq // 128), dtype=torch.float32, device=dev)
@@ -345,24 +483,21 @@ def other_workloads(dev, stream) -> dict:
         rmsq.qknorm_quant_fp8_into(d["q_a"], d["kv_a"], d["gamma_q"], d["gamma_kv"], qq, qs, kq, ks, eps=w.eps)
     for _ in range(10):
         qk()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for _ in range(50):
-            qk()
-    g.replay()
     torch.cuda.synchronize()
-    a.record()
-    g.replay()
-    b.record()
-    torch.cuda.synchronize()
-    us = a.elapsed_time(b) * 1e3 / 50
-    out["qknorm_m8192"] = {"us_per_call_graph": round(us, 3),
-                           "GBps": round(qk_bytes(M, w.Hq, w.Hkv) / us / 1e3, 1),
-                           "note": "50.9 MB per call: mostly L2-resident across back-to-back calls"}
+    gpu["qknorm"] = (w, dc, {"q_a": {"q": qq.cpu(), "scale": qs.cpu()}, "kv_a": {"q": kq.cpu(), "scale": ks.cpu()}})
+    nb = qk_bytes(M, w.Hq, w.Hkv)
+    us = _graph_us(qk, 50)
+    cold = _cold_us(qk, dev)
+    out["qknorm_m8192"] = {"us_per_call_graph": round(us, 3), "GBps": round(nb / us / 1e3, 1),
+                           "note": "50.9 MB per call: mostly L2-resident across back-to-back calls",
+                           "us_per_call_cold_l2_median": round(cold, 3),
+                           "GBps_cold_l2": round(nb / cold / 1e3, 1),
+                           "frac_of_hbm_peak_cold_l2": round(nb / cold / 1e3 / peak, 4) if peak else None}
 
     # MXFP4, M=8192, H=7168
     w = synth.WORKLOADS["mxfp4"]
-    d = {k: v.to(dev) for k, v in synth.make_inputs(w).items()}
+    dc = synth.make_inputs(w)
+    d = {k: v.to(dev) for k, v in dc.items()}
     M, H = w.M, w.H
     mq = torch.empty((M, H // 2), dtype=torch.uint8, device=dev)
     ms = torch.empty((M, H // 32), dtype=torch.uint8, device=dev)
@@ -374,6 +509,7 @@ def other_workloads(dev, stream) -> dict:
     for _ in range(5):
         mx()
     total, each = time_launches(mx, 50, stream)
+    gpu["mxfp4"] = (w, dc, {"q": mq.cpu(), "scale": ms.cpu(), "residual_out": mr.cpu()})
     us = statistics.mean(each) * 1e3
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
@@ -382,7 +518,7 @@ def other_workloads(dev, stream) -> dict:
     out["mxfp4_m8192"] = {"us_per_call_graph": round(g_us, 2), "GBps_graph": round(mx_bytes(M, H) / g_us / 1e3, 1),
                           "us_per_call_back_to_back": round(us, 2), "GBps_back_to_back": round(mx_bytes(M, H) / us / 1e3, 1)}
     out["quant_placement"] = consumer_placements(dev)
-    return out
+    return out, gpu
 
 
 # The consumer of the input RMSNorm in the DeepSeek-V3 MLA block: the fused
@@ -466,15 +602,20 @@ def rank_workload(w, rank: int):
 def make_step(name: str, dev, rank: int, rows: int, opts):
     """Inputs, outputs and a launcher of one workload.
 
-    Returns (run, nbytes, M, inputs, outputs, w, d_cpu, chunkable): ``run(r0,
-    r1, stream)`` calls the library on rows [r0, r1) on ``stream``; inputs and
-    outputs are (device tensor, pinned host tensor, row-indexed) triples for
-    the end-to-end leg; ``chunkable`` says whether every per-row tensor is
-    row-major (so a row range is a contiguous slice)."""
+    Returns (run, nbytes, M, inputs, outputs, w, d_cpu, chunkable, outs):
+    ``run(r0, r1, stream)`` calls the library on rows [r0, r1) on ``stream``;
+    inputs and outputs are (device tensor, pinned host tensor, row-indexed)
+    triples for the end-to-end leg; ``chunkable`` says whether every per-row
+    tensor is row-major (so a row range is a contiguous slice); ``outs`` are
+    the device outputs by name."""
     import torch
     from mxfp4_activation_quant_gb300 import rmsq, synth
 
-    w = synth.WORKLOADS[name]
+    if name in VARIANTS:
+        base, layout = VARIANTS[name]
+        w = synth.Workload(**{**synth.WORKLOADS[base].__dict__, "name": name, "scale_layout": layout})
+    else:
+        w = synth.WORKLOADS[name]
     if rows:
         w = synth.Workload(**{**w.__dict__, "M": rows})
     wr = rank_workload(w, rank)
@@ -504,10 +645,11 @@ def make_step(name: str, dev, rank: int, rows: int, opts):
                                               stream=st)
         nbytes = mx_bytes(M, w.H)
     else:
-        col = w.scale_layout == "col"
+        col = w.scale_layout != "row"
         chunkable = not col
         outs = {"q": torch.empty((M, w.H), dtype=torch.uint8, device=dev),
-                "s": torch.empty(((w.H // 128, M) if col else (M, w.H // 128)), dtype=torch.float32, device=dev),
+                "s": torch.empty(rmsq.scale_shape(M, w.H, 128, rmsq._layout(w.scale_layout)), dtype=torch.float32,
+                                 device=dev),
                 "r": torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)}
         if w.keep_bf16:
             outs["y"] = torch.empty((M, w.H), dtype=torch.bfloat16, device=dev)
@@ -522,11 +664,11 @@ def make_step(name: str, dev, rank: int, rows: int, opts):
     inputs = [(d[k], d_cpu[k].pin_memory(), d[k].dim() == 2) for k in d]
     outputs = [(v, torch.empty(v.shape, dtype=v.dtype).pin_memory(), not (col_scales(w) and k == "s"))
                for k, v in outs.items()]
-    return run, nbytes, M, inputs, outputs, w, d_cpu, chunkable
+    return run, nbytes, M, inputs, outputs, w, d_cpu, chunkable, outs
 
 
 def col_scales(w) -> bool:
-    return w.kind == "fp8" and w.scale_layout == "col"
+    return w.kind == "fp8" and w.scale_layout != "row"
 
 
 def make_e2e_step(run, M: int, inputs, outputs, chunks: int, dev):
@@ -649,13 +791,14 @@ def run_ours(args) -> None:
 
     kernel = {"auto": rmsq.KERNEL_AUTO, "rows": rmsq.KERNEL_ROWS, "persistent": rmsq.KERNEL_PERSISTENT}[args.kernel]
     opts = rmsq.LaunchOpts(kernel=kernel) if kernel != rmsq.KERNEL_AUTO else None
-    run, bytes_step, M, io_in, io_out, w, d_cpu, chunkable = make_step(args.workload, dev, rank, args.rows, opts)
+    run, bytes_step, M, io_in, io_out, w, d_cpu, chunkable, outs = make_step(args.workload, dev, rank, args.rows,
+                                                                             opts)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         run(0, M, stream.cuda_stream)
 
-    peak, peak_kind = measured_peaks()
+    peak, peak_kind = measured_peaks(dev)
     sampler = ClockSampler(gpu_id_for(dev)) if rank == 0 else None
     time.sleep(0.25 if sampler else 0)
     for _ in range(args.warmup):
@@ -696,58 +839,81 @@ def run_ours(args) -> None:
     # timed region, row chunks pipelined over three streams
     chunks = args.e2e_chunks if chunkable else 1
     packed = w.kind == "fp8" and w.scale_layout == "row" and w.keep_bf16 and w.residual and chunkable
+    plain_step = make_e2e_step(run, M, io_in, io_out, chunks, dev)
     if packed:      # the headline workload: one copy each way per chunk
         e2e_step, h2d_packed, d2h_packed = make_e2e_step_packed(rank_workload(w, rank), d_cpu, M, chunks, dev)
     else:
-        e2e_step = make_e2e_step(run, M, io_in, io_out, chunks, dev)
-    e2e_value = None
-    if not args.no_e2e:
-        e2e_steps = max(3, min(20, args.steps))
-        for _ in range(2):
-            e2e_step()
-        if world > 1:
-            dist.barrier()
-        e2e_ms, _ = time_launches(e2e_step, e2e_steps, stream)
-        e2e_value = round(world * bytes_step * e2e_steps / (max_over_ranks(e2e_ms, world, dev) * 1e-3) / 1e9, 1)
+        e2e_step = plain_step
     h2d = sum(hv.numel() * hv.element_size() for _, hv, _ in io_in)
     d2h = sum(hv.numel() * hv.element_size() for _, hv, _ in io_out)
+
+    def time_e2e(fn):
+        n = max(3, min(20, args.steps))
+        for _ in range(2):
+            fn()
+        if world > 1:
+            dist.barrier()
+        ms, _ = time_launches(fn, n, stream)
+        return round(world * bytes_step * n / (max_over_ranks(ms, world, dev) * 1e-3) / 1e9, 1)
+    e2e = {"value": None, "unit": "GB/s", "h2d_bytes_per_step": h2d_packed if packed else h2d,
+           "d2h_bytes_per_step": d2h_packed if packed else d2h, "row_chunks": chunks, "streams": 3}
+    if not args.no_e2e:
+        e2e["value"] = time_e2e(e2e_step)
     if packed:
-        h2d, d2h = h2d_packed, d2h_packed
+        e2e["copies"] = "one each way per chunk"
+        e2e["host_layout"] = ("chunk-packed pinned buffers: each chunk's x then residual rows in one buffer, its "
+                              "outputs in another, arranged once before the timed region")
+        e2e["plain"] = {"value": None if args.no_e2e else time_e2e(plain_step), "unit": "GB/s",
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "copies": "one per tensor and chunk",
+                        "host_layout": "plain [M, H] pinned tensors, as a caller holds them"}
+    else:
+        e2e["copies"] = "one per tensor and chunk"
+        e2e["host_layout"] = "plain pinned tensors, as a caller holds them"
 
     headline = args.workload == WORKLOAD and not args.rows
-    extra = other_workloads(dev, stream) if (rank == 0 and headline and not args.no_extra) else None
-    cpu = cpu_baseline(d_cpu, w) if (rank == 0 and world == 1 and headline and not args.no_cpu) else None
+    extra, gpu_out = (other_workloads(dev, stream, peak) if (rank == 0 and headline and not args.no_extra)
+                      else (None, {}))
+    cpu, parity = None, None
+    if rank == 0 and world == 1 and headline and not args.no_cpu:
+        # the CPU-baseline leg: the oracle timed on the host cores, and the
+        # GPU's outputs of the timed steps compared with the oracle's
+        cpu, ref = cpu_baseline(d_cpu, w)
+        torch.cuda.synchronize()
+        gpu_out["prefill"] = (w, d_cpu, {"q": outs["q"].cpu(), "scale": outs["s"].cpu(),
+                                         "residual_out": outs["r"].cpu(), "y": outs["y"].cpu()})
+        parity = parity_report({k: gpu_out[k] for k in ("tiny", "decode", "prefill", "qknorm", "mxfp4")
+                                if k in gpu_out}, ref)
+        del ref
     if world > 1:
         dist.barrier()
     if rank == 0:
         kernel_name = f"{args.workload}:{'bulk' if kernel == rmsq.KERNEL_PERSISTENT else 'rows'}"
         traffic = recorded_traffic(kernel_name)
+        text_key = w.kind if w.kind != "fp8" else args.workload
         line = {
             "metric": METRIC if headline else f"HBM GB/s & rows/s, {args.workload} workload",
             "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[w.kind if w.kind != "fp8" else args.workload].format(M=M),
-                       "global_rows": M * world, "parallelism": f"rows sharded, {world} independent batch(es)",
-                       "l2": ("inputs larger than L2 (129 MB); no flush needed" if bytes_step > 400e6 else
-                              "inputs smaller than L2: back-to-back steps are partly L2-resident"),
-                       "kernel": args.kernel, "bytes_per_step": bytes_step,
-                       "timing": "CUDA graph of the K steps" if use_graph else "K back-to-back calls"},
+            "config": workload_config(text_key, M, world, bytes_step),
+            "kernel": args.kernel,
+            "timing": "CUDA graph of the K steps" if use_graph else "K back-to-back calls",
             "rows_per_s": round(world * M * args.steps / (max_ms * 1e-3), 1),
-            "pct_of_peak": round(100 * value / world / peak, 2),
+            "pct_of_peak": round(100 * value / world / peak, 2) if peak else None,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "frac": round(achieved / peak, 4) if peak else None, "traffic": traffic,
                          "peak_kind": f"{peak_kind} HBM copy"},
-            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "row_chunks": chunks, "streams": 3,
-                    "copies": "one each way per chunk (packed chunk buffers)" if packed else
-                              "one per tensor and chunk"},
+            "mismatch_fraction": parity["prefill"]["mismatch_fraction"] if parity else None,
+            "e2e": e2e,
             "gpu_launches": args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "parity": parity,
             "back_to_back": back_to_back,
             "other_workloads": extra,
+            "source_digest": {"rows": kernel_source_digest("rows"), "gemm": kernel_source_digest("gemm")},
         }
         print(json.dumps(line))
     if world > 1:
@@ -790,7 +956,7 @@ def run_consumer(args) -> None:
     flops = 2.0 * M * N * K
     value = flops * args.steps / (total_ms * 1e-3) / 1e12
     achieved = flops / (statistics.mean(each) * 1e-3) / 1e12
-    peak, peak_kind = measured_fp4_peak()
+    peak, peak_kind = measured_fp4_peak(dev)
     # end to end: A codes + scale tiles in from pinned host memory, D out
     a_q = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
     a_t = torch.empty(rmsq.mma_scale_bytes(M, K), dtype=torch.uint8, device=dev)
@@ -851,6 +1017,10 @@ def run_consumer(args) -> None:
 WORKLOAD_TEXT = {
     "prefill": "prefill input RMSNorm: M={M} H=7168 bf16, residual add, FP8 E4M3 1x128 groups, "
                "fp32 scales [M,56], keep_bf16 y",
+    "prefill_col": "prefill input RMSNorm: M={M} H=7168 bf16, residual add, FP8 E4M3 1x128 groups, "
+                   "fp32 scales column-major [56,M], keep_bf16 y",
+    "prefill_col_pad4": "prefill input RMSNorm: M={M} H=7168 bf16, residual add, FP8 E4M3 1x128 groups, "
+                        "fp32 scales column-major [56,M rounded up to 4], keep_bf16 y",
     "decode": "decode input RMSNorm: M={M} H=7168 bf16, residual add, FP8 E4M3 1x128, column-major scales",
     "qknorm": "MLA latents: q_a [M,1536] + kv_a [M,512], no residual, FP8 E4M3 1x128, one launch",
     "mxfp4": "input RMSNorm M={M} H=7168, residual add, MXFP4 (E8M0 per 32, E2M1 packed)",
@@ -875,8 +1045,10 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--kernel", choices=["auto", "rows", "persistent"], default="auto")
-    ap.add_argument("--workload", choices=["prefill", "decode", "qknorm", "mxfp4", "consumer"], default=WORKLOAD,
-                    help="the timed step (the headline line is prefill; consumer: the MXFP4 GEMM)")
+    ap.add_argument("--workload", choices=["prefill", "decode", "qknorm", "mxfp4", "consumer", *VARIANTS],
+                    default=WORKLOAD,
+                    help="the timed step (the headline line is prefill; consumer: the MXFP4 GEMM; prefill_col, "
+                         "prefill_col_pad4: the prefill step with column-major scales)")
     ap.add_argument("--no-extra", action="store_true", help="skip the decode / qknorm / MXFP4 lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")

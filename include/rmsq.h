@@ -198,6 +198,19 @@ rmsq_status rmsq_add_rmsnorm(
 rmsq_status rmsq_mxfp4_gemm(
     const void *a_q, int64_t ld_a, const void *a_scale_tiles, const void *b_q, int64_t ld_b,
     const void *b_scale_tiles, void *d, int64_t ld_d, int64_t M, int64_t N, int64_t K, void *stream);
+/*
+ * Every wait inside the GEMM kernels (a CTA waiting for its operand copies,
+ * for the tensor cores, or for its cluster peers) is bounded, 2 s by default
+ * (rmsq_gemm_opts.wait_limit_ns). A CTA whose wait runs out stops, drains its
+ * copies, frees its tensor memory and sets the status word; the call itself
+ * has already returned RMSQ_OK at launch. D is then incomplete, and only
+ * rmsq_sync_status reports it (RMSQ_ERR_TIMEOUT): a caller that cannot rule
+ * out a stalled GPU (time-slicing with other work, a debugger) checks
+ * rmsq_sync_status before trusting D. The limit is more than a thousand
+ * times the slowest launch measured on GB300 (the quantising GEMM at
+ * M = 16384, N = 2112, K = 7168: about a millisecond; the GEMM on quantised
+ * A: about 0.1 ms).
+ */
 
 rmsq_status rmsq_a16wfp4_gemm(
     const void *a, int64_t ld_a, const void *b_q, int64_t ld_b, const void *b_scale_tiles, void *d,
@@ -213,6 +226,16 @@ rmsq_status rmsq_mx_scale_tiles(const uint8_t *scale, int64_t ld, int64_t R, int
 
 /* ------------------------------------------------------------ utilities */
 
+/*
+ * Copies `bytes` bytes from src to dst (device pointers, 16-byte aligned,
+ * not overlapping, bytes a multiple of 16) with a plain streaming kernel:
+ * every byte is read from and written to HBM once. This is not an operation
+ * of the source pages; it is the read + write copy whose rate serves as the
+ * HBM roofline's peak where no separately measured peak is available.
+ * Enqueued on `stream`; RMSQ_ERR_INVALID_ARG for bad arguments.
+ */
+rmsq_status rmsq_copy(const void *src, void *dst, int64_t bytes, void *stream);
+
 /* Static description of a status code. */
 const char *rmsq_status_string(rmsq_status s);
 
@@ -226,6 +249,13 @@ const char *rmsq_last_error(void);
  * incomplete), RMSQ_ERR_BOUNDS if, in a library built with RMSQ_DEBUG, an
  * index check before a store failed (the store was skipped),
  * RMSQ_ERR_CUDA if the synchronisation failed, else RMSQ_OK.
+ *
+ * The word is one per device and per process, shared by every stream and
+ * host thread: a call reports (and clears) what any kernel of the library on
+ * this device recorded since the previous call, whichever stream launched
+ * it, and only `stream` is waited for. The bits read are cleared with an
+ * atomic operation enqueued on `stream`, so a bit that a kernel on another
+ * stream sets between the read and the clear is kept for the next call.
  */
 rmsq_status rmsq_sync_status(void *stream);
 
@@ -237,6 +267,15 @@ typedef enum rmsq_kernel {
     RMSQ_KERNEL_PERSISTENT = 2   /* grid of resident blocks looping over rows, x / residual
                                     rows double-buffered in shared memory by bulk copies */
 } rmsq_kernel;
+
+typedef enum rmsq_form {
+    RMSQ_FORM_AUTO = 0,          /* latency form when the row kernel's launch has at most one
+                                    block per SM, else the throughput form */
+    RMSQ_FORM_THROUGHPUT = 1,    /* gamma read as the row is normalised; the team's first warp
+                                    finalises inv_rms and broadcasts it (a second barrier) */
+    RMSQ_FORM_LATENCY = 2        /* gamma loaded together with the row; every warp finalises
+                                    inv_rms itself after the one barrier */
+} rmsq_form;
 
 /*
  * Optional launch control for the _ex entry points (NULL = defaults). Kernels
@@ -256,6 +295,11 @@ typedef enum rmsq_kernel {
  *   debug_skip_row  persistent kernel: the copy of this row is never issued,
  *                   so its wait runs out (test of the bounded wait); -1 = off
  *   wait_limit_ns   persistent kernel: limit of every wait, 0 = 2 s
+ *   form            row kernel: rmsq_form. Both forms give bit-identical
+ *                   outputs (same order of every addition); the latency form
+ *                   exists for the compiled team shapes (H = 7168, 8192, 5120,
+ *                   4096, 2048, 1536, 512 at their default vpt) and is
+ *                   ignored for other shapes.
  */
 typedef struct rmsq_launch_opts {
     int32_t kernel;
@@ -264,6 +308,7 @@ typedef struct rmsq_launch_opts {
     int32_t grid;
     int64_t debug_skip_row;
     int64_t wait_limit_ns;
+    int32_t form;
 } rmsq_launch_opts;
 
 rmsq_status rmsq_add_rmsnorm_quant_group_fp8_ex(

@@ -103,7 +103,7 @@ int pick_vpt(int64_t nvec, int gv, int forced, int &tpr)
 
 int default_rows_per_block(int tpr) { return tpr >= 256 ? 1 : 256 / tpr; }
 
-const rmsq_launch_opts kDefaultOpts = {RMSQ_KERNEL_AUTO, 0, 0, 0, -1, 0};
+const rmsq_launch_opts kDefaultOpts = {RMSQ_KERNEL_AUTO, 0, 0, 0, -1, 0, RMSQ_FORM_AUTO};
 
 // Checks shared by the single-tensor FP8 and MXFP4 calls.
 rmsq_status check_single(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
@@ -277,8 +277,15 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
         p.seg[0] = s;
         p.nseg = 1;
         const int ts = (static_shape(vpt, tpr) && vpt * tpr * 8 == s.H) ? tpr : 0;
-        cudaError_t e = mx ? launch_rows_mx(vpt, ts, p, (int)blocks, rpb * tpr, st)
-                           : launch_rows_fp8(vpt, ts, p, (int)blocks, rpb * tpr, st);
+        // The latency form (gamma loaded with the row, one barrier per row)
+        // when the launch is at most one block per SM: there the row's
+        // dependent chain, not bandwidth, sets the time.
+        if (o.form != RMSQ_FORM_AUTO && o.form != RMSQ_FORM_THROUGHPUT && o.form != RMSQ_FORM_LATENCY)
+            return fail(RMSQ_ERR_INVALID_ARG, "unknown kernel form %d", o.form);
+        const bool lat = ts && (o.form == RMSQ_FORM_LATENCY ||
+                                (o.form == RMSQ_FORM_AUTO && blocks <= (int64_t)sm_count()));
+        cudaError_t e = mx ? launch_rows_mx(vpt, ts, lat, p, (int)blocks, rpb * tpr, st)
+                           : launch_rows_fp8(vpt, ts, lat, p, (int)blocks, rpb * tpr, st);
         if (e != cudaSuccess)
             return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
         return ok();
@@ -335,6 +342,9 @@ __global__ void debug_bounds_selftest_kernel(unsigned int *flag, int64_t n)
         flag[0] |= 0u;
 }
 #endif
+
+// Clears the given bits of the status word (rmsq_sync_status).
+__global__ void clear_status_bits_kernel(unsigned int bits) { atomicAnd(&g_status_word, ~bits); }
 
 // ------------------------------------------------------- encoder kernels
 
@@ -609,10 +619,16 @@ rmsq_status rmsq_sync_status(void *stream)
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess)
         return fail(RMSQ_ERR_CUDA, "synchronize failed: %s", cudaGetErrorString(e));
-    unsigned int word = 0, zero = 0;
+    unsigned int word = 0;
     e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof word);
-    if (e == cudaSuccess && word)
-        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
+    if (e == cudaSuccess && word) {
+        // clear exactly the bits just read, atomically on the device, so that
+        // a bit another stream's kernel sets meanwhile is kept for the next read
+        clear_status_bits_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(word);
+        e = cudaGetLastError();
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize((cudaStream_t)stream);
+    }
     if (e != cudaSuccess)
         return fail(RMSQ_ERR_CUDA, "status word access failed: %s", cudaGetErrorString(e));
     if (word & 4u)

@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kMaxThreads) bulk_kernel(const __grid_constant
                     s.out_res[row * nv + v] = r[k];
             }
         }
-        row_finish<VPT, TPR, MX, true>(s, row, t, 0, it & 1, red, r, g_sm);
+        row_finish<VPT, TPR, MX, GAMMA_SHARED>(s, row, t, 0, it & 1, red, r, g_sm, r);   // r: unused gamma registers
     }
 }
 

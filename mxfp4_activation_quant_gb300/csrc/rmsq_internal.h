@@ -63,9 +63,11 @@ constexpr int kMaxThreads = 512;
 
 // Launchers (a switch over the instantiations each). tpr_static != 0 selects
 // a kernel compiled for that exact team size (see static_shape).
-cudaError_t launch_rows_fp8(int vpt, int tpr_static, const LaunchParams &p, int grid, int threads,
+// lat selects the latency form of a compiled team shape (gamma loaded with
+// the row, one barrier per row; bit-identical results).
+cudaError_t launch_rows_fp8(int vpt, int tpr_static, bool lat, const LaunchParams &p, int grid, int threads,
                             cudaStream_t st);
-cudaError_t launch_rows_mx(int vpt, int tpr_static, const LaunchParams &p, int grid, int threads,
+cudaError_t launch_rows_mx(int vpt, int tpr_static, bool lat, const LaunchParams &p, int grid, int threads,
                            cudaStream_t st);
 cudaError_t launch_dual(bool mx, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,
                         int threads, cudaStream_t st);

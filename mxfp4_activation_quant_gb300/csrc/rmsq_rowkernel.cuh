@@ -1,7 +1,9 @@
 // Register-resident row kernels: each team loads its row of x (and residual)
 // straight into registers with 16-byte streaming loads, adds, writes the
 // residual back, and finishes the row (rmsq_rows.cuh).
-//   rows_kernel<VPT, TPR, MX>       one tensor
+//   rows_kernel<VPT, TPR, MX, LAT>  one tensor; LAT: the latency form for
+//                                   launches of at most one block per SM
+//                                   (gamma loaded with the row, one barrier)
 //   dual_kernel<V0, T0, V1, T1, MX> two tensors (the MLA q_a / kv_a pair),
 //                                   blocks [0, seg[0].blocks) on the first
 // TPR / T0 / T1 = 0 means the team size is read at run time.
@@ -11,7 +13,7 @@
 
 namespace rmsq {
 
-template <int VPT, int TPR, bool MX>
+template <int VPT, int TPR, bool MX, bool LAT = false>
 __device__ __forceinline__ void block_rows(const Seg &s, int b, RedSmem &red)
 {
     const int tpr = TPR ? TPR : s.tpr;
@@ -37,14 +39,14 @@ __device__ __forceinline__ void block_rows(const Seg &s, int b, RedSmem &red)
                              : "memory");
         }
     }
-    row_from_global<VPT, TPR, MX>(s, row, t, team, 0, red);
+    row_from_global<VPT, TPR, MX, LAT>(s, row, t, team, 0, red);
 }
 
-template <int VPT, int TPR, bool MX>
+template <int VPT, int TPR, bool MX, bool LAT>
 __global__ void __launch_bounds__(kMaxThreads) rows_kernel(const __grid_constant__ LaunchParams p)
 {
     __shared__ RedSmem red;
-    block_rows<VPT, TPR, MX>(p.seg[0], blockIdx.x, red);
+    block_rows<VPT, TPR, MX, LAT>(p.seg[0], blockIdx.x, red);
 }
 
 template <int V0, int T0, int V1, int T1, bool MX>
@@ -68,29 +70,34 @@ __global__ void __launch_bounds__(kMaxThreads, 2) dual_kernel(const __grid_const
     X(3, 64)  /* H = 1536 */  \
     X(4, 16)  /* H = 512  */
 
+// The latency form exists for the compiled team shapes only; `lat` is
+// ignored for runtime team sizes.
 template <bool MX>
-cudaError_t launch_rows_impl(int vpt, int tpr_static, const LaunchParams &p, int grid, int threads,
-                             cudaStream_t st)
+cudaError_t launch_rows_impl(int vpt, int tpr_static, bool lat, const LaunchParams &p, int grid,
+                             int threads, cudaStream_t st)
 {
     if (tpr_static) {
-#define RMSQ_LAUNCH_STATIC(V, T)                                    \
-        if (vpt == V && tpr_static == T) {                          \
-            rows_kernel<V, T, MX><<<grid, threads, 0, st>>>(p);     \
-            return cudaGetLastError();                              \
+#define RMSQ_LAUNCH_STATIC(V, T)                                            \
+        if (vpt == V && tpr_static == T) {                                  \
+            if (lat)                                                        \
+                rows_kernel<V, T, MX, true><<<grid, threads, 0, st>>>(p);   \
+            else                                                            \
+                rows_kernel<V, T, MX, false><<<grid, threads, 0, st>>>(p);  \
+            return cudaGetLastError();                                      \
         }
         RMSQ_STATIC_SHAPES(RMSQ_LAUNCH_STATIC)
 #undef RMSQ_LAUNCH_STATIC
         return cudaErrorInvalidValue;
     }
     switch (vpt) {
-    case 1: rows_kernel<1, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 2: rows_kernel<2, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 3: rows_kernel<3, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 4: rows_kernel<4, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 5: rows_kernel<5, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 6: rows_kernel<6, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 7: rows_kernel<7, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 8: rows_kernel<8, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 1: rows_kernel<1, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
+    case 2: rows_kernel<2, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
+    case 3: rows_kernel<3, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
+    case 4: rows_kernel<4, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
+    case 5: rows_kernel<5, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
+    case 6: rows_kernel<6, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
+    case 7: rows_kernel<7, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
+    case 8: rows_kernel<8, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

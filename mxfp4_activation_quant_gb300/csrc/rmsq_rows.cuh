@@ -33,7 +33,7 @@ namespace rmsq {
 struct RedSmem {
     float2 part[2][32];   // per-warp double-float partials, two parity sets
     float inv[2][16];     // per-team inv_rms (NaN: take the fp64 path), two parity sets
-    double dpart[32];     // per-warp fp64 partials for the wide-range path
+    double dpart[32][2];  // per-warp double-double partials for the wide-range path
 };
 
 __device__ __forceinline__ unsigned team_lane_mask(int tpr, int lane)
@@ -65,37 +65,75 @@ __device__ __forceinline__ int64_t mma_scale_offset(int64_t row, int64_t g, int6
 
 // Team-wide fp64 sum of squares and fp64 finalisation, for rows whose sum
 // lies outside the fp32 range in which the double-float path is exact.
+//
+// The squares of bf16 values are exact in fp64 (8-bit significands, and
+// exponents from 2^-266 to 2^256 are all normal fp64). They are summed as a
+// double-double: Knuth's TwoSum keeps each addition's rounding error in a
+// second fp64 word, and the lane butterfly and the cross-warp step add
+// double-doubles the same way. Before its one rounding to fp64 the sum is
+// within n^2 * 2^-106 (relative; below 2^-76 for the widest row) of the exact
+// one, so the result is the correctly rounded sum that the oracle's
+// compensated summation gives, except in rows whose exact sum lies that close
+// to an fp64 rounding midpoint.
+__device__ __forceinline__ void two_sum_f64(double a, double b, double &s, double &e)
+{
+    s = __dadd_rn(a, b);
+    const double bb = __dsub_rn(s, a);
+    e = __dadd_rn(__dsub_rn(a, __dsub_rn(s, bb)), __dsub_rn(b, bb));
+}
+
+// (hi, lo) += (bhi, blo): the high words exactly, the errors into the low
+// word. Commutative bit for bit (TwoSum's error is the exact rounding error
+// of the sum, whichever operand comes first), so a butterfly leaves the same
+// value in every lane.
+__device__ __forceinline__ void dd_add(double &hi, double &lo, double bhi, double blo)
+{
+    double s, e;
+    two_sum_f64(hi, bhi, s, e);
+    hi = s;
+    lo = __dadd_rn(__dadd_rn(lo, blo), e);
+}
+
 template <int VPT>
 __device__ __forceinline__ float inv_rms_fp64_path(const uint4 (&r)[VPT], int H, float eps, int tpr,
                                                    int team, RedSmem &red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned tmask = team_lane_mask(tpr, lane);
-    double acc = 0.0;
+    double hi = 0.0, lo = 0.0;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const uint32_t w[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            double a = (double)bf_lo(w[j]), b = (double)bf_hi(w[j]);
-            acc = __fma_rn(a, a, acc);
-            acc = __fma_rn(b, b, acc);
+            const double a = (double)bf_lo(w[j]), b = (double)bf_hi(w[j]);
+            double s, e;
+            two_sum_f64(hi, __dmul_rn(a, a), s, e);
+            lo = __dadd_rn(lo, e);
+            two_sum_f64(s, __dmul_rn(b, b), hi, e);
+            lo = __dadd_rn(lo, e);
         }
     }
     const int wlim = tpr < 32 ? tpr : 32;
-    for (int off = 1; off < wlim; off <<= 1)
-        acc += __shfl_xor_sync(tmask, acc, off);
+    for (int off = 1; off < wlim; off <<= 1) {
+        const double ohi = __shfl_xor_sync(tmask, hi, off), olo = __shfl_xor_sync(tmask, lo, off);
+        dd_add(hi, lo, ohi, olo);
+    }
     if (tpr > 32) {
         const int nw = tpr >> 5, w0 = team * nw;
-        if (lane == 0)
-            red.dpart[warp] = acc;
+        if (lane == 0) {
+            red.dpart[warp][0] = hi;
+            red.dpart[warp][1] = lo;
+        }
         team_bar(team, tpr);
-        acc = red.dpart[w0];
+        hi = red.dpart[w0][0];
+        lo = red.dpart[w0][1];
         for (int i = 1; i < nw; ++i)
-            acc += red.dpart[w0 + i];
+            dd_add(hi, lo, red.dpart[w0 + i][0], red.dpart[w0 + i][1]);
         team_bar(team, tpr);
     }
-    return (float)(1.0 / sqrt(acc / (double)H + (double)eps));
+    const double S = __dadd_rn(hi, lo);
+    return (float)(1.0 / sqrt(S / (double)H + (double)eps));
 }
 
 // inv_rms of a team's row from the per-thread double-float partials of its
@@ -107,7 +145,14 @@ __device__ __forceinline__ float inv_rms_fp64_path(const uint4 (&r)[VPT], int H,
 // the shared slots between consecutive rows of a persistent team. A NaN
 // result means the sum left the double-float range: the caller takes the
 // fp64 path.
-template <int TPR>
+//
+// LAT (latency form, for launches of one row per SM or fewer): every warp of
+// the team reads all the partials after the one barrier and combines them
+// itself, in the same fixed butterfly, so the result is bit-identical to the
+// throughput form's and the second barrier and its shared-memory broadcast
+// leave the row's critical path. It needs no second slot set: a team's
+// slots are written once per launch (row kernel only).
+template <int TPR, bool LAT = false>
 __device__ __forceinline__ float team_inv_rms(DF S, const Seg &s, int tpr, int team, int parity,
                                               RedSmem &red, unsigned tmask)
 {
@@ -126,13 +171,18 @@ __device__ __forceinline__ float team_inv_rms(DF S, const Seg &s, int tpr, int t
     if (lane == 0)
         red.part[parity][warp] = make_float2(S.hi, S.lo);
     team_bar(team, tpr);
-    if (warp == w0) {
+    if (LAT || warp == w0) {
         const float2 p = lane < nw ? red.part[parity][w0 + lane] : make_float2(0.0f, 0.0f);
         DF T{p.x, p.y};
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1)
             if (off < nw)
                 T = df_add_lazy(T, shfl_xor_df(T, off, 0xffffffffu));
+        if (LAT) {                                // every lane holds the same T
+            if (!inv_rms_df(df_renorm(T), s.H, s.inv_h, s.eps, inv))
+                inv = __int_as_float(0x7fffffff);
+            return inv;
+        }
         if (lane == 0) {
             if (!inv_rms_df(df_renorm(T), s.H, s.inv_h, s.eps, inv))
                 inv = __int_as_float(0x7fffffff);
@@ -143,16 +193,22 @@ __device__ __forceinline__ float team_inv_rms(DF S, const Seg &s, int tpr, int t
     return red.inv[parity][team];
 }
 
+// Where row_finish takes gamma from: through the read-only cache when the
+// row is normalised, from shared memory (staged by the persistent kernel), or
+// from registers loaded together with the row (latency form).
+enum GammaFrom { GAMMA_GLOBAL = 0, GAMMA_SHARED = 1, GAMMA_REGS = 2 };
+
 // Everything after the row is loaded: r holds the thread's VPT vectors of
-// bf16 r (residual already added and written back by the caller). gamma is
-// read from shared memory (GAMMA_SHARED) or through the read-only cache.
-// TPR is the team size when known at compile time (the row is then an exact
-// fit, tpr * VPT * 8 == H), or 0 for a runtime team size with padding guards.
+// bf16 r (residual already added and written back by the caller). gamma
+// comes from gamma_src (GAMMA_GLOBAL, GAMMA_SHARED) or gpre (GAMMA_REGS, the
+// thread's own VPT vectors). TPR is the team size when known at compile time
+// (the row is then an exact fit, tpr * VPT * 8 == H), or 0 for a runtime
+// team size with padding guards. LAT selects team_inv_rms's latency form.
 // Elementwise arithmetic runs on packed fp32 pairs.
-template <int VPT, int TPR, bool MX, bool GAMMA_SHARED>
+template <int VPT, int TPR, bool MX, int GFROM, bool LAT = false>
 __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int team, int parity,
                                            RedSmem &red, const uint4 (&r)[VPT],
-                                           const uint4 *gamma_src)
+                                           const uint4 *gamma_src, const uint4 (&gpre)[VPT])
 {
     constexpr int GV = MX ? 4 : 16;   // 16-byte vectors per quant group
     constexpr bool GUARD = TPR == 0;
@@ -170,7 +226,7 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         acc_square2(unpack_bf16x2(r[k].z), hi, lo);
         acc_square2(unpack_bf16x2(r[k].w), hi, lo);
     }
-    float inv = team_inv_rms<TPR>(df_add_lazy(DF{hi.x, lo.x}, DF{hi.y, lo.y}), s, tpr, team, parity, red,
+    float inv = team_inv_rms<TPR, LAT>(df_add_lazy(DF{hi.x, lo.x}, DF{hi.y, lo.y}), s, tpr, team, parity, red,
                                   tmask);
     if (inv != inv)                                   // team-uniform: NaN asks for the fp64 path
         inv = inv_rms_fp64_path<VPT>(r, s.H, s.eps, tpr, team, red);
@@ -182,7 +238,8 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
     for (int k = 0; k < VPT; ++k) {
         const int vk = k * tpr + t;
         const uint4 g = (GUARD && vk >= nvec) ? make_uint4(0, 0, 0, 0)
-                        : GAMMA_SHARED ? gamma_src[vk] : ld_keep(gamma_src + vk);
+                        : GFROM == GAMMA_REGS ? gpre[k]
+                        : GFROM == GAMMA_SHARED ? gamma_src[vk] : ld_keep(gamma_src + vk);
         const uint32_t rw[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
         const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
         uint32_t yw[4];
@@ -272,14 +329,16 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
 }
 
 // Load (and add) one row from global memory, write the residual, finish it.
-template <int VPT, int TPR, bool MX>
+// LAT (latency form): gamma is loaded together with the row, so that its
+// load latency overlaps the row's instead of following the reduction.
+template <int VPT, int TPR, bool MX, bool LAT = false>
 __device__ __forceinline__ void row_from_global(const Seg &s, int64_t row, int t, int team, int parity,
                                                 RedSmem &red)
 {
     constexpr bool GUARD = TPR == 0;
     const int tpr = TPR ? TPR : s.tpr;
     const int nvec = TPR ? TPR * VPT : (s.H >> 3);
-    uint4 r[VPT];
+    uint4 r[VPT], g[VPT];
     const uint4 *xr = s.x + row * s.ldx_v + t;
     // vectors past the row end (padded team shapes) read as zero and are
     // never stored; they add nothing to the sum of squares
@@ -306,7 +365,14 @@ __device__ __forceinline__ void row_from_global(const Seg &s, int64_t row, int t
             r[k] = ok ? ld_stream(xr + k * tpr) : make_uint4(0, 0, 0, 0);
         }
     }
-    row_finish<VPT, TPR, MX, false>(s, row, t, team, parity, red, r, s.gamma);
+    if constexpr (LAT) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+            g[k] = (!GUARD || k * tpr + t < nvec) ? ld_keep(s.gamma + k * tpr + t) : make_uint4(0, 0, 0, 0);
+        row_finish<VPT, TPR, MX, GAMMA_REGS, true>(s, row, t, team, parity, red, r, s.gamma, g);
+    } else {
+        row_finish<VPT, TPR, MX, GAMMA_GLOBAL>(s, row, t, team, parity, red, r, s.gamma, g);
+    }
 }
 
 }  // namespace rmsq

@@ -12,6 +12,7 @@ all-reduce RMSNorm per-group quant for Qwen3.5 FP8" (Modifications):
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -26,6 +27,7 @@ RMSQ_OK = 0
 STATUS_NAMES = {0: "RMSQ_OK", 1: "RMSQ_ERR_INVALID_ARG", 2: "RMSQ_ERR_MISALIGNED",
                 3: "RMSQ_ERR_UNSUPPORTED", 4: "RMSQ_ERR_CUDA", 5: "RMSQ_ERR_TIMEOUT", 6: "RMSQ_ERR_BOUNDS"}
 KERNEL_AUTO, KERNEL_ROWS, KERNEL_PERSISTENT = 0, 1, 2
+FORM_AUTO, FORM_THROUGHPUT, FORM_LATENCY = 0, 1, 2
 SCALE_ROW_MAJOR, SCALE_COL_MAJOR, SCALE_COL_MAJOR_PAD4 = 0, 1, 2
 
 _p = ctypes.c_void_p
@@ -37,11 +39,11 @@ _f = ctypes.c_float
 class LaunchOpts(ctypes.Structure):
     """Mirror of ``rmsq_launch_opts``."""
     _fields_ = [("kernel", _i32), ("vpt", _i32), ("rows_per_block", _i32), ("grid", _i32),
-                ("debug_skip_row", _i64), ("wait_limit_ns", _i64)]
+                ("debug_skip_row", _i64), ("wait_limit_ns", _i64), ("form", _i32)]
 
     def __init__(self, kernel=KERNEL_AUTO, vpt=0, rows_per_block=0, grid=0, debug_skip_row=-1,
-                 wait_limit_ns=0):
-        super().__init__(kernel, vpt, rows_per_block, grid, debug_skip_row, wait_limit_ns)
+                 wait_limit_ns=0, form=FORM_AUTO):
+        super().__init__(kernel, vpt, rows_per_block, grid, debug_skip_row, wait_limit_ns, form)
 
 
 class GemmOpts(ctypes.Structure):
@@ -82,6 +84,7 @@ _SIGNATURES = {
     "rmsq_gemm_plan_for": [_i32, _i64, _i64, _i64, _p, _i32, _i32, _i32, _p],
     "rmsq_mx_scale_tiles": [_p, _i64, _i64, _i64, _p, ctypes.c_uint8, _p],
     "rmsq_sync_status": [_p],
+    "rmsq_copy": [_p, _p, _i64, _p],
     "rmsq_encode_e4m3": [_p, _p, _i64, _p],
     "rmsq_encode_e2m1": [_p, _p, _i64, _p],
     "rmsq_check_group_division": [_p, _p],
@@ -114,6 +117,35 @@ def _check(status: int) -> None:
         raise RmsqError(status, lib().rmsq_last_error().decode())
 
 
+def _current_index() -> int:
+    return torch.cuda.current_device()
+
+
+def _device_guard(index: int):
+    """Makes GPU `index` current for the library call (the C library launches
+    on the calling thread's current device); a no-op when it already is."""
+    if index == _current_index():
+        return contextlib.nullcontext()
+    return torch.cuda.device(index)
+
+
+def _device_index(*tensors) -> int:
+    """The one GPU all tensor arguments live on. Tensors on different GPUs are
+    refused: a kernel (or a TMA tensor map) given another GPU's address would
+    fault without peer access."""
+    found = sorted({t.device.index if t.device.index is not None else _current_index()
+                    for t in tensors if t is not None and getattr(t, "is_cuda", False)})
+    if len(found) > 1:
+        raise ValueError(f"all tensor arguments must be on the same GPU (got cuda:{found})")
+    return found[0] if found else _current_index()
+
+
+def _call(tensors, name: str, *args) -> None:
+    """Calls library entry point `name` on the GPU that holds `tensors`."""
+    with _device_guard(_device_index(*tensors)):
+        _check(getattr(lib(), name)(*args))
+
+
 def _ptr(t):
     """Device address of a tensor argument (None for an absent optional one).
     Host tensors are refused here: a kernel given a host address would fault."""
@@ -124,15 +156,26 @@ def _ptr(t):
     return t.data_ptr()
 
 
-def _buf(t, name: str, nbytes: int):
+# dtypes a buffer may have, by what the kernels store in it
+BF16 = (torch.bfloat16,)
+F32 = (torch.float32,)
+E4M3_CODES = (torch.uint8, torch.float8_e4m3fn)
+BYTES = (torch.uint8,) + tuple(getattr(torch, n) for n in ("float8_e8m0fnu",) if hasattr(torch, n))
+E2M1_CODES = (torch.uint8,) + tuple(getattr(torch, n) for n in ("float4_e2m1fn_x2",) if hasattr(torch, n))
+
+
+def _buf(t, name: str, nbytes: int, dtypes: tuple):
     """Address of a buffer the library addresses without a pitch (gamma, the
-    outputs, scale tiles): a contiguous CUDA tensor holding at least nbytes
-    bytes, or None when absent. The C calls see only pointers, so the sizes
-    are checked here."""
+    outputs, scale tiles): a contiguous CUDA tensor of one of `dtypes`
+    holding at least nbytes bytes, or None when absent. The C calls see only
+    pointers, so dtypes and sizes are checked here (an fp32 gamma, say, would
+    be read as pairs of bf16 halves)."""
     if t is None:
         return None
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must have dtype {' or '.join(str(d) for d in dtypes)} (got {t.dtype})")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     have = t.numel() * t.element_size()
@@ -209,12 +252,12 @@ def add_rmsnorm_quant_fp8(x: torch.Tensor, gamma: torch.Tensor, residual: torch.
     if residual is not None:
         res_out = out_residual if out_residual is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
-    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H, group, _ptr(q),
-            _ptr(scale), layout, _buf(res_out, "out_residual", 2 * M * H), _ptr(y), _stream(dev))
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H, BF16), eps, M, H, group, _ptr(q),
+            _ptr(scale), layout, _buf(res_out, "out_residual", 2 * M * H, BF16), _ptr(y), _stream(dev))
     if opts is None:
-        _check(lib().rmsq_add_rmsnorm_quant_group_fp8(*args))
+        _call((x, gamma, residual, out_residual), "rmsq_add_rmsnorm_quant_group_fp8", *args)
     else:
-        _check(lib().rmsq_add_rmsnorm_quant_group_fp8_ex(*args, ctypes.byref(opts)))
+        _call((x, gamma, residual, out_residual), "rmsq_add_rmsnorm_quant_group_fp8_ex", *args, ctypes.byref(opts))
     return ((y, q, scale) if keep_bf16 else (q, scale)), res_out
 
 
@@ -227,13 +270,13 @@ def add_rmsnorm_quant_fp8_into(x, gamma, residual, q, scale, res_out=None, y=Non
     ldr = _like_x(residual, "residual", M, H) if residual is not None else 0
     st = _stream(x.device) if stream is None else stream
     layout = _layout(scale_layout)
-    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H, group,
-            _buf(q, "q", M * H), _buf(scale, "scale", _scale_bytes(M, H, group, layout)), layout,
-            _buf(res_out, "res_out", 2 * M * H), _buf(y, "y", 2 * M * H), st)
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H, BF16), eps, M, H, group,
+            _buf(q, "q", M * H, E4M3_CODES), _buf(scale, "scale", _scale_bytes(M, H, group, layout), F32), layout,
+            _buf(res_out, "res_out", 2 * M * H, BF16), _buf(y, "y", 2 * M * H, BF16), st)
     if opts is None:
-        _check(lib().rmsq_add_rmsnorm_quant_group_fp8(*args))
+        _call((x, gamma, residual, q, scale, res_out, y), "rmsq_add_rmsnorm_quant_group_fp8", *args)
     else:
-        _check(lib().rmsq_add_rmsnorm_quant_group_fp8_ex(*args, ctypes.byref(opts)))
+        _call((x, gamma, residual, q, scale, res_out, y), "rmsq_add_rmsnorm_quant_group_fp8_ex", *args, ctypes.byref(opts))
 
 
 def add_rmsnorm_quant_mxfp4_into(x, gamma, residual, q, scale, res_out=None, y=None, eps: float = 1e-6,
@@ -243,13 +286,13 @@ def add_rmsnorm_quant_mxfp4_into(x, gamma, residual, q, scale, res_out=None, y=N
     M, H = x.shape
     ldr = _like_x(residual, "residual", M, H) if residual is not None else 0
     st = _stream(x.device) if stream is None else stream
-    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H,
-            _buf(q, "q", M * (H // 2)), _buf(scale, "scale", M * (H // 32)), _buf(res_out, "res_out", 2 * M * H),
-            _buf(y, "y", 2 * M * H), st)
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H, BF16), eps, M, H,
+            _buf(q, "q", M * (H // 2), E2M1_CODES), _buf(scale, "scale", M * (H // 32), BYTES), _buf(res_out, "res_out", 2 * M * H, BF16),
+            _buf(y, "y", 2 * M * H, BF16), st)
     if opts is None:
-        _check(lib().rmsq_add_rmsnorm_quant_mxfp4(*args))
+        _call((x, gamma, residual, q, scale, res_out, y), "rmsq_add_rmsnorm_quant_mxfp4", *args)
     else:
-        _check(lib().rmsq_add_rmsnorm_quant_mxfp4_ex(*args, ctypes.byref(opts)))
+        _call((x, gamma, residual, q, scale, res_out, y), "rmsq_add_rmsnorm_quant_mxfp4_ex", *args, ctypes.byref(opts))
 
 
 def qknorm_quant_fp8_into(q_a, kv_a, gamma_q, gamma_kv, qq, qs, kq, ks, qy=None, ky=None,
@@ -264,11 +307,11 @@ def qknorm_quant_fp8_into(q_a, kv_a, gamma_q, gamma_kv, qq, qs, kq, ks, qy=None,
         raise ValueError("q_a and kv_a must have the same number of rows")
     st = _stream(q_a.device) if stream is None else stream
     layout = _layout(scale_layout)
-    _check(lib().rmsq_qknorm_quant_fp8(
-        _ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq), _buf(gamma_kv, "gamma_kv", 2 * Hkv),
-        eps, M, Hq, Hkv, group, _buf(qq, "qq", M * Hq), _buf(qs, "qs", _scale_bytes(M, Hq, group, layout)),
-        _buf(kq, "kq", M * Hkv), _buf(ks, "ks", _scale_bytes(M, Hkv, group, layout)), layout,
-        _buf(qy, "qy", 2 * M * Hq), _buf(ky, "ky", 2 * M * Hkv), st))
+    _call((q_a, kv_a, gamma_q, gamma_kv, qq, qs, kq, ks, qy, ky), "rmsq_qknorm_quant_fp8",
+        _ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq, BF16), _buf(gamma_kv, "gamma_kv", 2 * Hkv, BF16),
+        eps, M, Hq, Hkv, group, _buf(qq, "qq", M * Hq, E4M3_CODES), _buf(qs, "qs", _scale_bytes(M, Hq, group, layout), F32),
+        _buf(kq, "kq", M * Hkv, E4M3_CODES), _buf(ks, "ks", _scale_bytes(M, Hkv, group, layout), F32), layout,
+        _buf(qy, "qy", 2 * M * Hq, BF16), _buf(ky, "ky", 2 * M * Hkv, BF16), st)
 
 
 def qknorm_quant_fp8(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Tensor,
@@ -294,9 +337,9 @@ def qknorm_quant_fp8(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Tenso
 
     qq, qs, qy = outs(Hq)
     kq, ks, ky = outs(Hkv)
-    _check(lib().rmsq_qknorm_quant_fp8(_ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq),
-                                       _buf(gamma_kv, "gamma_kv", 2 * Hkv), eps, M, Hq, Hkv, group, _ptr(qq), _ptr(qs), _ptr(kq), _ptr(ks),
-                                       layout, _ptr(qy), _ptr(ky), _stream(dev)))
+    _call((q_a, kv_a, gamma_q, gamma_kv), "rmsq_qknorm_quant_fp8", _ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq, BF16),
+                                       _buf(gamma_kv, "gamma_kv", 2 * Hkv, BF16), eps, M, Hq, Hkv, group, _ptr(qq), _ptr(qs), _ptr(kq), _ptr(ks),
+                                       layout, _ptr(qy), _ptr(ky), _stream(dev))
     if keep_bf16:
         return (qy, qq, qs), (ky, kq, ks)
     return (qq, qs), (kq, ks)
@@ -322,10 +365,10 @@ def qknorm_quant_mxfp4(q_a: torch.Tensor, kv_a: torch.Tensor, gamma_q: torch.Ten
 
     qq, qs, qy = outs(Hq)
     kq, ks, ky = outs(Hkv)
-    _check(lib().rmsq_qknorm_quant_mxfp4(_ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq),
-                                         _buf(gamma_kv, "gamma_kv", 2 * Hkv), eps,
+    _call((q_a, kv_a, gamma_q, gamma_kv), "rmsq_qknorm_quant_mxfp4", _ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq, BF16),
+                                         _buf(gamma_kv, "gamma_kv", 2 * Hkv, BF16), eps,
                                          M, Hq, Hkv, _ptr(qq), _ptr(qs), _ptr(kq), _ptr(ks), _ptr(qy),
-                                         _ptr(ky), _stream(dev)))
+                                         _ptr(ky), _stream(dev))
     if keep_bf16:
         return (qy, qq, qs), (ky, kq, ks)
     return (qq, qs), (kq, ks)
@@ -342,11 +385,11 @@ def qknorm_quant_mxfp4_into(q_a, kv_a, gamma_q, gamma_kv, qq, qs, kq, ks, qy=Non
     if Mk != M:
         raise ValueError("q_a and kv_a must have the same number of rows")
     st = _stream(q_a.device) if stream is None else stream
-    _check(lib().rmsq_qknorm_quant_mxfp4(
-        _ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq), _buf(gamma_kv, "gamma_kv", 2 * Hkv),
-        eps, M, Hq, Hkv, _buf(qq, "qq", M * (Hq // 2)), _buf(qs, "qs", M * (Hq // 32)),
-        _buf(kq, "kq", M * (Hkv // 2)), _buf(ks, "ks", M * (Hkv // 32)), _buf(qy, "qy", 2 * M * Hq),
-        _buf(ky, "ky", 2 * M * Hkv), st))
+    _call((q_a, kv_a, gamma_q, gamma_kv, qq, qs, kq, ks, qy, ky), "rmsq_qknorm_quant_mxfp4",
+        _ptr(q_a), ldq, _ptr(kv_a), ldk, _buf(gamma_q, "gamma_q", 2 * Hq, BF16), _buf(gamma_kv, "gamma_kv", 2 * Hkv, BF16),
+        eps, M, Hq, Hkv, _buf(qq, "qq", M * (Hq // 2), E2M1_CODES), _buf(qs, "qs", M * (Hq // 32), BYTES),
+        _buf(kq, "kq", M * (Hkv // 2), E2M1_CODES), _buf(ks, "ks", M * (Hkv // 32), BYTES), _buf(qy, "qy", 2 * M * Hq, BF16),
+        _buf(ky, "ky", 2 * M * Hkv, BF16), st)
 
 
 def add_rmsnorm_quant_mxfp4(x: torch.Tensor, gamma: torch.Tensor, residual: torch.Tensor | None = None,
@@ -364,12 +407,12 @@ def add_rmsnorm_quant_mxfp4(x: torch.Tensor, gamma: torch.Tensor, residual: torc
     if residual is not None:
         res_out = out_residual if out_residual is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
-    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H, _ptr(q), _ptr(scale),
-            _buf(res_out, "out_residual", 2 * M * H), _ptr(y), _stream(dev))
+    args = (_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H, BF16), eps, M, H, _ptr(q), _ptr(scale),
+            _buf(res_out, "out_residual", 2 * M * H, BF16), _ptr(y), _stream(dev))
     if opts is None:
-        _check(lib().rmsq_add_rmsnorm_quant_mxfp4(*args))
+        _call((x, gamma, residual, out_residual), "rmsq_add_rmsnorm_quant_mxfp4", *args)
     else:
-        _check(lib().rmsq_add_rmsnorm_quant_mxfp4_ex(*args, ctypes.byref(opts)))
+        _call((x, gamma, residual, out_residual), "rmsq_add_rmsnorm_quant_mxfp4_ex", *args, ctypes.byref(opts))
     return ((y, q, scale) if keep_bf16 else (q, scale)), res_out
 
 
@@ -388,10 +431,10 @@ def add_rmsnorm_quant_mxfp4_mma_scales(x: torch.Tensor, gamma: torch.Tensor,
                                                                 device=dev)
     res_out = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if residual is not None else None
     y = torch.empty((M, H), dtype=torch.bfloat16, device=dev) if keep_bf16 else None
-    _check(lib().rmsq_add_rmsnorm_quant_mxfp4_mma_scales(_ptr(x), ldx, _ptr(residual), ldr,
-                                                         _buf(gamma, "gamma", 2 * H), eps, M, H, _ptr(q),
-                                                         _buf(scale, "scale_out", mma_scale_bytes(M, H)),
-                                                         _ptr(res_out), _ptr(y), _stream(dev)))
+    _call((x, gamma, residual, scale_out), "rmsq_add_rmsnorm_quant_mxfp4_mma_scales", _ptr(x), ldx, _ptr(residual), ldr,
+                                                         _buf(gamma, "gamma", 2 * H, BF16), eps, M, H, _ptr(q),
+                                                         _buf(scale, "scale_out", mma_scale_bytes(M, H), BYTES),
+                                                         _ptr(res_out), _ptr(y), _stream(dev))
     return ((y, q, scale) if keep_bf16 else (q, scale)), res_out
 
 
@@ -409,8 +452,8 @@ def add_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, residual: torch.Tensor | N
     if residual is not None:
         res_out = out_residual if out_residual is not None else torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     st = _stream(dev) if stream is None else stream
-    _check(lib().rmsq_add_rmsnorm(_ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H,
-                                  _buf(res_out, "out_residual", 2 * M * H), _buf(y, "out", 2 * M * H), st))
+    _call((x, gamma, residual, out, out_residual), "rmsq_add_rmsnorm", _ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H, BF16), eps, M, H,
+                                  _buf(res_out, "out_residual", 2 * M * H, BF16), _buf(y, "out", 2 * M * H, BF16), st)
     return y, res_out
 
 
@@ -422,7 +465,7 @@ def mx_scale_tiles(scale: torch.Tensor, fill: int = 0, stream: int | None = None
     R, G = scale.shape
     out = torch.empty((R + 127) // 128 * ((G + 3) // 4) * 512, dtype=torch.uint8, device=scale.device)
     st = _stream(scale.device) if stream is None else stream
-    _check(lib().rmsq_mx_scale_tiles(_ptr(scale), scale.stride(0), R, G, _ptr(out), fill, st))
+    _call((scale,), "rmsq_mx_scale_tiles", _ptr(scale), scale.stride(0), R, G, _ptr(out), fill, st)
     return out
 
 
@@ -440,10 +483,23 @@ def _gemm_out(M, N, dev, out):
     return out
 
 
+def _gemm_check(check: bool, device) -> None:
+    """check=True: wait for the GEMM and raise if one of its bounded waits
+    gave up (D is then incomplete); otherwise the caller checks sync_status."""
+    if check:
+        with _device_guard(torch.device(device).index):
+            st = lib().rmsq_sync_status(_stream(device))
+        _check(st)
+
+
 def mxfp4_gemm(a_q: torch.Tensor, a_scale_tiles: torch.Tensor, b_q: torch.Tensor, b_scale_tiles: torch.Tensor,
-               out: torch.Tensor | None = None, opts: GemmOpts | None = None, stream: int | None = None):
+               out: torch.Tensor | None = None, opts: GemmOpts | None = None, stream: int | None = None,
+               check: bool = False):
     """D = A B^T (bf16 [M, N]) on the block-scaled tensor cores, A and B MXFP4:
-    codes [rows, K/2] uint8, scales in the MMA tile layout (flat uint8)."""
+    codes [rows, K/2] uint8, scales in the MMA tile layout (flat uint8).
+    With ``check`` the call waits for the GEMM and raises RmsqError if a
+    bounded wait inside it ran out (D incomplete); without it, call
+    ``sync_status`` before trusting D when the GPU may have been stalled."""
     lda, ldb = _codes_view(a_q, "a_q"), _codes_view(b_q, "b_q")
     M, K = a_q.shape[0], a_q.shape[1] * 2
     N = b_q.shape[0]
@@ -451,20 +507,23 @@ def mxfp4_gemm(a_q: torch.Tensor, a_scale_tiles: torch.Tensor, b_q: torch.Tensor
         raise ValueError("A and B have different K")
     d = _gemm_out(M, N, a_q.device, out)
     st = _stream(a_q.device) if stream is None else stream
-    args = (_ptr(a_q), lda, _buf(a_scale_tiles, "a_scale_tiles", mma_scale_bytes(M, K)), _ptr(b_q), ldb,
-            _buf(b_scale_tiles, "b_scale_tiles", mma_scale_bytes(N, K)), _ptr(d), d.stride(0),
+    args = (_ptr(a_q), lda, _buf(a_scale_tiles, "a_scale_tiles", mma_scale_bytes(M, K), BYTES), _ptr(b_q), ldb,
+            _buf(b_scale_tiles, "b_scale_tiles", mma_scale_bytes(N, K), BYTES), _ptr(d), d.stride(0),
             M, N, K, st)
     if opts is None:
-        _check(lib().rmsq_mxfp4_gemm(*args))
+        _call((a_q, a_scale_tiles, b_q, b_scale_tiles, out), "rmsq_mxfp4_gemm", *args)
     else:
-        _check(lib().rmsq_mxfp4_gemm_ex(*args, ctypes.byref(opts)))
+        _call((a_q, a_scale_tiles, b_q, b_scale_tiles, out), "rmsq_mxfp4_gemm_ex", *args, ctypes.byref(opts))
+    _gemm_check(check, a_q.device)
     return d
 
 
 def a16wfp4_gemm(a: torch.Tensor, b_q: torch.Tensor, b_scale_tiles: torch.Tensor,
-                 out: torch.Tensor | None = None, opts: GemmOpts | None = None, stream: int | None = None):
+                 out: torch.Tensor | None = None, opts: GemmOpts | None = None, stream: int | None = None,
+                 check: bool = False):
     """The prequant placement: A bf16 [M, K] is MXFP4-quantised inside the
-    GEMM (same rule as add_rmsnorm_quant_mxfp4), then D = A B^T (bf16 [M, N])."""
+    GEMM (same rule as add_rmsnorm_quant_mxfp4), then D = A B^T (bf16 [M, N]).
+    ``check`` as for mxfp4_gemm."""
     lda = _rows_view(a, "a")
     ldb = _codes_view(b_q, "b_q")
     M, K = a.shape
@@ -473,12 +532,13 @@ def a16wfp4_gemm(a: torch.Tensor, b_q: torch.Tensor, b_scale_tiles: torch.Tensor
         raise ValueError("A and B have different K")
     d = _gemm_out(M, N, a.device, out)
     st = _stream(a.device) if stream is None else stream
-    args = (_ptr(a), lda, _ptr(b_q), ldb, _buf(b_scale_tiles, "b_scale_tiles", mma_scale_bytes(N, K)), _ptr(d),
+    args = (_ptr(a), lda, _ptr(b_q), ldb, _buf(b_scale_tiles, "b_scale_tiles", mma_scale_bytes(N, K), BYTES), _ptr(d),
             d.stride(0), M, N, K, st)
     if opts is None:
-        _check(lib().rmsq_a16wfp4_gemm(*args))
+        _call((a, b_q, b_scale_tiles, out), "rmsq_a16wfp4_gemm", *args)
     else:
-        _check(lib().rmsq_a16wfp4_gemm_ex(*args, ctypes.byref(opts)))
+        _call((a, b_q, b_scale_tiles, out), "rmsq_a16wfp4_gemm_ex", *args, ctypes.byref(opts))
+    _gemm_check(check, a.device)
     return d
 
 
@@ -504,16 +564,33 @@ def add_rmsnorm_quant_mxfp4_mma_scales_into(x, gamma, residual, q, scale_tiles, 
     M, H = x.shape
     ldr = _like_x(residual, "residual", M, H) if residual is not None else 0
     st = _stream(x.device) if stream is None else stream
-    _check(lib().rmsq_add_rmsnorm_quant_mxfp4_mma_scales(
-        _ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H), eps, M, H, _buf(q, "q", M * (H // 2)),
-        _buf(scale_tiles, "scale_tiles", mma_scale_bytes(M, H)), _buf(res_out, "res_out", 2 * M * H),
-        _buf(y, "y", 2 * M * H), st))
+    _call((x, gamma, residual, q, scale_tiles, res_out, y), "rmsq_add_rmsnorm_quant_mxfp4_mma_scales",
+        _ptr(x), ldx, _ptr(residual), ldr, _buf(gamma, "gamma", 2 * H, BF16), eps, M, H, _buf(q, "q", M * (H // 2), E2M1_CODES),
+        _buf(scale_tiles, "scale_tiles", mma_scale_bytes(M, H), BYTES), _buf(res_out, "res_out", 2 * M * H, BF16),
+        _buf(y, "y", 2 * M * H, BF16), st)
+
+
+def copy_(dst: torch.Tensor, src: torch.Tensor, stream: int | None = None) -> None:
+    """dst <- src with the library's streaming copy kernel (both contiguous
+    CUDA tensors of the same byte size, a multiple of 16)."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src must have the same size in bytes")
+    for t, name in ((src, "src"), (dst, "dst")):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    st = _stream(src.device) if stream is None else stream
+    _call((src, dst), "rmsq_copy", _ptr(src), _ptr(dst), nbytes, st)
 
 
 def sync_status(device=None) -> int:
-    """Synchronises the current stream and returns the library status word's verdict."""
+    """Synchronises the device's current stream and returns the verdict of
+    the library's status word on that device (process-wide: it covers the
+    library's kernels on every stream of the device)."""
     dev = torch.device("cuda") if device is None else torch.device(device)
-    return lib().rmsq_sync_status(_stream(dev))
+    index = dev.index if dev.index is not None else _current_index()
+    with _device_guard(index):
+        return lib().rmsq_sync_status(_stream(dev))
 
 
 def encode_e4m3(v: torch.Tensor) -> torch.Tensor:
@@ -522,7 +599,7 @@ def encode_e4m3(v: torch.Tensor) -> torch.Tensor:
         raise ValueError("v must be float32")
     v = v.contiguous()
     out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
-    _check(lib().rmsq_encode_e4m3(_ptr(v), _ptr(out), v.numel(), _stream(v.device)))
+    _call((v,), "rmsq_encode_e4m3", _ptr(v), _ptr(out), v.numel(), _stream(v.device))
     return out
 
 
@@ -532,7 +609,7 @@ def encode_e2m1(v: torch.Tensor) -> torch.Tensor:
         raise ValueError("v must be float32")
     v = v.contiguous()
     out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
-    _check(lib().rmsq_encode_e2m1(_ptr(v), _ptr(out), v.numel(), _stream(v.device)))
+    _call((v,), "rmsq_encode_e2m1", _ptr(v), _ptr(out), v.numel(), _stream(v.device))
     return out
 
 

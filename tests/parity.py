@@ -68,57 +68,94 @@ def _boundary_rows(ref: dict, what: str) -> np.ndarray:
     return boundary
 
 
-def compare_fp8(got: dict, ref: dict, scale_layout: str = "row", what: str = "") -> dict:
-    """got/ref: dicts with q (codes [M,H]), scale, optional y, residual_out (bf16 bits)."""
-    boundary = _boundary_rows(ref, what)
-    stats = {"rows": int(len(boundary)), "boundary_rows": int(boundary.sum())}
+def _scale_array(s) -> np.ndarray:
+    return s.detach().cpu().numpy() if isinstance(s, torch.Tensor) else np.asarray(s)
+
+
+def fp8_stats(got: dict, ref: dict, scale_layout: str = "row") -> dict:
+    """Every figure of the parity bar for an FP8 call, without judging it.
+
+    got/ref: dicts with q (codes [M,H]), scale, optional y, residual_out (bf16
+    bits). Returns the rows, boundary rows, codes differing and their
+    fraction, the largest code distance in ULPs, the largest relative scale
+    error, and whether residual_out, y, codes and scales are bit-exact
+    outside boundary rows."""
+    boundary = ref["margin"] < BOUNDARY
     ok_rows = ~boundary
-    if "residual_out" in ref:
-        assert np.array_equal(u16(got["residual_out"]), ref["residual_out"]), f"{what}: residual_out differs"
+    st = {"rows": int(len(boundary)), "boundary_rows": int(boundary.sum())}
+    if "residual_out" in ref and got.get("residual_out") is not None:
+        st["residual_out_bit_exact"] = bool(np.array_equal(u16(got["residual_out"]), ref["residual_out"]))
     if got.get("y") is not None:
         gy, ry = u16(got["y"]), ref["y"]
-        assert np.array_equal(gy[ok_rows], ry[ok_rows]), f"{what}: bf16 y differs outside boundary rows"
-        assert np.all(np.abs(bf16_ordinal(gy) - bf16_ordinal(ry)) <= 1), f"{what}: bf16 y off by > 1 step"
+        st["y_bit_exact_outside_boundary"] = bool(np.array_equal(gy[ok_rows], ry[ok_rows]))
+        st["y_max_step"] = int(np.abs(bf16_ordinal(gy) - bf16_ordinal(ry)).max(initial=0))
     gq, rq = u8(got["q"]), ref["q"]
-    dist = np.abs(e4m3_ordinal(gq) - e4m3_ordinal(rq))
-    stats["codes_differing"] = int((gq != rq).sum())
-    stats["mismatch_fraction"] = stats["codes_differing"] / max(1, gq.size)
-    assert dist.max(initial=0) <= 1, f"{what}: a code is more than 1 ULP from the oracle"
-    assert stats["mismatch_fraction"] <= 1e-3, f"{what}: {stats['mismatch_fraction']:.2e} of codes differ"
-    assert np.array_equal(gq[ok_rows], rq[ok_rows]), f"{what}: codes differ outside boundary rows"
-    gs = got["scale"].detach().cpu().numpy() if isinstance(got["scale"], torch.Tensor) else got["scale"]
-    rs = ref["scale"]
-    assert gs.shape == rs.shape, f"{what}: scale shape {gs.shape} vs {rs.shape}"
-    rel = np.abs(gs.astype(np.float64) - rs) / np.maximum(np.abs(rs.astype(np.float64)), 1e-30)
-    assert rel.max(initial=0) <= 1e-5, f"{what}: scale relative error {rel.max():.3e}"
-    row_axis = 0 if scale_layout == "row" else 1
-    gs_rows = gs if row_axis == 0 else gs.T
-    rs_rows = rs if row_axis == 0 else rs.T
-    assert np.array_equal(gs_rows[ok_rows].view(np.uint32), rs_rows[ok_rows].view(np.uint32)), \
-        f"{what}: scales differ outside boundary rows"
-    return stats
+    st["codes_differing"] = int((gq != rq).sum())
+    st["mismatch_fraction"] = st["codes_differing"] / max(1, gq.size)
+    st["max_code_ulp"] = int(np.abs(e4m3_ordinal(gq) - e4m3_ordinal(rq)).max(initial=0))
+    st["codes_bit_exact_outside_boundary"] = bool(np.array_equal(gq[ok_rows], rq[ok_rows]))
+    gs, rs = _scale_array(got["scale"]), ref["scale"]
+    st["scale_shape_ok"] = gs.shape == rs.shape
+    if st["scale_shape_ok"]:
+        rel = np.abs(gs.astype(np.float64) - rs) / np.maximum(np.abs(rs.astype(np.float64)), 1e-30)
+        st["scale_max_rel"] = float(rel.max(initial=0))
+        gs_rows = gs if scale_layout == "row" else gs.T
+        rs_rows = rs if scale_layout == "row" else rs.T
+        st["scales_bit_exact_outside_boundary"] = bool(
+            np.array_equal(gs_rows[ok_rows].view(np.uint32), rs_rows[ok_rows].view(np.uint32)))
+    return st
+
+
+def compare_fp8(got: dict, ref: dict, scale_layout: str = "row", what: str = "") -> dict:
+    """got/ref: dicts with q (codes [M,H]), scale, optional y, residual_out (bf16 bits)."""
+    _boundary_rows(ref, what)
+    assert "residual_out" not in ref or got.get("residual_out") is not None, f"{what}: no residual_out"
+    st = fp8_stats(got, ref, scale_layout)
+    assert st.get("residual_out_bit_exact", True), f"{what}: residual_out differs"
+    assert st.get("y_bit_exact_outside_boundary", True), f"{what}: bf16 y differs outside boundary rows"
+    assert st.get("y_max_step", 0) <= 1, f"{what}: bf16 y off by > 1 step"
+    assert st["max_code_ulp"] <= 1, f"{what}: a code is more than 1 ULP from the oracle"
+    assert st["mismatch_fraction"] <= 1e-3, f"{what}: {st['mismatch_fraction']:.2e} of codes differ"
+    assert st["codes_bit_exact_outside_boundary"], f"{what}: codes differ outside boundary rows"
+    assert st["scale_shape_ok"], f"{what}: scale shape differs"
+    assert st["scale_max_rel"] <= 1e-5, f"{what}: scale relative error {st['scale_max_rel']:.3e}"
+    assert st["scales_bit_exact_outside_boundary"], f"{what}: scales differ outside boundary rows"
+    return st
+
+
+def mx_stats(got: dict, ref: dict) -> dict:
+    """Every figure of the parity bar for an MXFP4 call, without judging it
+    (codes compared per 4-bit element, E8M0 scales in exponent steps)."""
+    boundary = ref["margin"] < BOUNDARY
+    ok_rows = ~boundary
+    st = {"rows": int(len(boundary)), "boundary_rows": int(boundary.sum())}
+    if "residual_out" in ref and got.get("residual_out") is not None:
+        st["residual_out_bit_exact"] = bool(np.array_equal(u16(got["residual_out"]), ref["residual_out"]))
+    if got.get("y") is not None:
+        st["y_bit_exact_outside_boundary"] = bool(np.array_equal(u16(got["y"])[ok_rows], ref["y"][ok_rows]))
+    gq, rq = unpack_e2m1(u8(got["q"])), unpack_e2m1(ref["q"])
+    st["codes_differing"] = int((gq != rq).sum())
+    st["mismatch_fraction"] = st["codes_differing"] / max(1, gq.size)
+    st["max_code_ulp"] = int(np.abs(e2m1_ordinal(gq) - e2m1_ordinal(rq)).max(initial=0))
+    st["codes_bit_exact_outside_boundary"] = bool(np.array_equal(gq[ok_rows], rq[ok_rows]))
+    gs, rs = u8(got["scale"]), ref["scale"]
+    st["scales_bit_exact_outside_boundary"] = bool(np.array_equal(gs[ok_rows], rs[ok_rows]))
+    st["scale_max_step"] = int(np.abs(gs.astype(np.int32) - rs.astype(np.int32)).max(initial=0))
+    return st
 
 
 def compare_mx(got: dict, ref: dict, what: str = "") -> dict:
-    boundary = _boundary_rows(ref, what)
-    stats = {"rows": int(len(boundary)), "boundary_rows": int(boundary.sum())}
-    ok_rows = ~boundary
-    if "residual_out" in ref:
-        assert np.array_equal(u16(got["residual_out"]), ref["residual_out"]), f"{what}: residual_out differs"
-    if got.get("y") is not None:
-        gy, ry = u16(got["y"]), ref["y"]
-        assert np.array_equal(gy[ok_rows], ry[ok_rows]), f"{what}: bf16 y differs outside boundary rows"
-    gq, rq = unpack_e2m1(u8(got["q"])), unpack_e2m1(ref["q"])
-    dist = np.abs(e2m1_ordinal(gq) - e2m1_ordinal(rq))
-    stats["codes_differing"] = int((gq != rq).sum())
-    stats["mismatch_fraction"] = stats["codes_differing"] / max(1, gq.size)
-    assert dist.max(initial=0) <= 1, f"{what}: an E2M1 code is more than 1 ULP from the oracle"
-    assert stats["mismatch_fraction"] <= 1e-3, f"{what}: {stats['mismatch_fraction']:.2e} of codes differ"
-    assert np.array_equal(gq[ok_rows], rq[ok_rows]), f"{what}: codes differ outside boundary rows"
-    gs, rs = u8(got["scale"]), ref["scale"]
-    assert np.array_equal(gs[ok_rows], rs[ok_rows]), f"{what}: E8M0 scales differ outside boundary rows"
-    assert np.all(np.abs(gs.astype(np.int32) - rs.astype(np.int32)) <= 1), f"{what}: E8M0 off by > 1"
-    return stats
+    _boundary_rows(ref, what)
+    assert "residual_out" not in ref or got.get("residual_out") is not None, f"{what}: no residual_out"
+    st = mx_stats(got, ref)
+    assert st.get("residual_out_bit_exact", True), f"{what}: residual_out differs"
+    assert st.get("y_bit_exact_outside_boundary", True), f"{what}: bf16 y differs outside boundary rows"
+    assert st["max_code_ulp"] <= 1, f"{what}: an E2M1 code is more than 1 ULP from the oracle"
+    assert st["mismatch_fraction"] <= 1e-3, f"{what}: {st['mismatch_fraction']:.2e} of codes differ"
+    assert st["codes_bit_exact_outside_boundary"], f"{what}: codes differ outside boundary rows"
+    assert st["scales_bit_exact_outside_boundary"], f"{what}: E8M0 scales differ outside boundary rows"
+    assert st["scale_max_step"] <= 1, f"{what}: E8M0 off by > 1"
+    return st
 
 
 def compare_gemm(got, ref: dict, K: int, what: str = "") -> dict:

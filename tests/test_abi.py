@@ -156,9 +156,11 @@ def test_qknorm_rejects_bad_arguments(L):
 
 
 def test_launch_opts_layout_matches_header():
-    # int32 kernel, vpt, rows_per_block, grid; int64 debug_skip_row, wait_limit_ns
-    assert ctypes.sizeof(rmsq.LaunchOpts) == 32
+    # int32 kernel, vpt, rows_per_block, grid; int64 debug_skip_row, wait_limit_ns; int32 form
+    # (padded to the struct's 8-byte alignment)
+    assert ctypes.sizeof(rmsq.LaunchOpts) == 40
     assert rmsq.LaunchOpts.debug_skip_row.offset == 16
+    assert rmsq.LaunchOpts.form.offset == 32
 
 
 def test_host_tensors_are_refused():

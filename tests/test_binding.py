@@ -17,14 +17,15 @@ BF16, U8, F32, F8 = torch.bfloat16, torch.uint8, torch.float32, torch.float8_e4m
 
 
 class FakeCuda:
-    """What the binding reads of a CUDA tensor: shape, dtype, strides, size, address."""
+    """What the binding reads of a CUDA tensor: shape, dtype, strides, size,
+    address, device."""
     is_cuda = True
-    device = torch.device("cuda", 0)
     _next = 1 << 32
 
-    def __init__(self, shape, dtype, strides=None):
+    def __init__(self, shape, dtype, strides=None, device=0):
         self.shape = torch.Size(shape)
         self.dtype = dtype
+        self.device = torch.device("cuda", device)
         dense, acc = [], 1
         for n in reversed(self.shape):
             dense.insert(0, acc)
@@ -64,10 +65,25 @@ class FakeLib:
         return call
 
 
+class FakeGuard:
+    """Records which GPU the binding makes current around a library call."""
+    def __init__(self, lib, index):
+        self.lib, self.index = lib, index
+
+    def __enter__(self):
+        self.lib.devices.append(self.index)
+
+    def __exit__(self, *exc):
+        return False
+
+
 @pytest.fixture
 def fake(monkeypatch):
     lib = FakeLib()
+    lib.devices = []
     monkeypatch.setattr(rmsq, "lib", lambda: lib)
+    monkeypatch.setattr(rmsq, "_current_index", lambda: 0)
+    monkeypatch.setattr(rmsq, "_device_guard", lambda index: FakeGuard(lib, index))
     return lib
 
 
@@ -223,3 +239,53 @@ def test_encoders_want_float32(fake):
         rmsq.encode_e4m3(FakeCuda((4,), BF16))
     with pytest.raises(ValueError, match="float32"):
         rmsq.encode_e2m1(FakeCuda((4,), torch.float16))
+
+
+@pytest.mark.parametrize("call", sorted(CALLS))
+def test_tensors_on_two_gpus_are_refused(fake, call):
+    """One argument on another GPU: refused before the library sees an
+    address it cannot reach."""
+    run, make = CALLS[call]
+    args = make()
+    key = sorted(args)[-1]
+    t = args[key]
+    args[key] = FakeCuda(t.shape, t.dtype, device=1)
+    with pytest.raises(ValueError, match="same GPU"):
+        run(args)
+    assert not fake.calls
+
+
+@pytest.mark.parametrize("call", sorted(CALLS))
+def test_call_runs_on_the_tensors_gpu(fake, call):
+    """All arguments on cuda:1 while cuda:0 is current: the library call is
+    made with cuda:1 current (the C library launches on the current device)."""
+    run, make = CALLS[call]
+    args = {k: FakeCuda(t.shape, t.dtype, t.stride(), device=1) for k, t in make().items()}
+    run(args)
+    assert len(fake.calls) == 1
+    assert fake.devices == [1]
+
+
+@pytest.mark.parametrize("call,arg,dtype", [
+    ("fp8", "gamma", F32),              # read as pairs of bf16 halves
+    ("fp8", "y", F32),
+    ("fp8", "scale", torch.float16),
+    ("fp8", "q", torch.int8),
+    ("mxfp4", "scale", F32),
+    ("mxfp4", "q", BF16),
+    ("mma_scales", "scale_tiles", torch.int32),
+    ("qknorm", "gamma_kv", torch.float16),
+    ("norm", "out", F32),
+    ("gemm", "b_scale_tiles", torch.int8),
+])
+def test_wrong_dtypes_are_refused(fake, call, arg, dtype):
+    run, make = CALLS[call]
+    args = make()
+    t = args[arg]
+    # same byte size as the correct buffer, so only the dtype check can refuse it
+    nbytes = t.numel() * t.element_size()
+    esize = torch.empty((), dtype=dtype).element_size()
+    args[arg] = FakeCuda(((nbytes + esize - 1) // esize,), dtype)
+    with pytest.raises(ValueError, match=arg):
+        run(args)
+    assert not fake.calls

@@ -469,3 +469,31 @@ def test_strided_operands(oracle_mod):
     ref = oracle_mod.mxfp4_gemm(q, s, b_q.numpy(), b_s.numpy())
     parity.compare_gemm(pre, ref, K, what="strided bf16 A")
     assert rmsq.sync_status() == 0
+
+
+def test_default_wait_limit_is_far_above_the_runtime():
+    """Every wait inside the GEMM gives up after 2 s by default; the largest
+    shape the library is measured on (M = 16384 tokens, N = 2112, K = 7168,
+    both placements; the quantising GEMM is the slower, about a millisecond)
+    must finish in under a two-hundredth of that, so the limit only ever
+    trips on a stalled GPU. check=True raises if it did."""
+    M, N, K = 16384, 2112, 7168
+    a_q, a_s, b_q, b_s = operands(61, M, N, K)
+    ga, gb = a_q.to(DEV), b_q.to(DEV)
+    ta, tb = rmsq.mx_scale_tiles(a_s.to(DEV)), rmsq.mx_scale_tiles(b_s.to(DEV))
+    a_bf16 = torch.randn((M, K), device=DEV).to(torch.bfloat16)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    worst = 0.0
+    for fn in (lambda: rmsq.mxfp4_gemm(ga, ta, gb, tb, out=d, check=True),
+               lambda: rmsq.a16wfp4_gemm(a_bf16, gb, tb, out=d, check=True)):
+        fn()
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            worst = max(worst, e0.elapsed_time(e1) * 1e-3)
+    print(f"slowest launch {worst * 1e3:.3f} ms against the 2 s wait limit")
+    assert worst < 2.0 / 200
+    assert rmsq.sync_status() == 0

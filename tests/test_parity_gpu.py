@@ -529,3 +529,71 @@ def test_debug_build_bounds_check_fires():
     assert rmsq.lib().rmsq_debug_bounds_selftest(torch.cuda.current_stream().cuda_stream) == 0
     assert rmsq.sync_status() == 6                     # RMSQ_ERR_BOUNDS
     assert rmsq.sync_status() == 0
+
+
+# ------------------------------------------ column-major scales at prefill size
+
+@pytest.mark.parametrize("layout", ["col", "col_pad4"])
+def test_full_size_column_major_scales(oracle_mod, layout):
+    """The decode config's column-major scale layout at the prefill size
+    (M = 16384, H = 7168, keep_bf16), every row compared, default launch."""
+    w = synth.WORKLOADS["prefill"]
+    d = synth.make_inputs(w)
+    got = run_fp8(d, w.eps, layout=layout, keep=True)
+    ref = ref_fp8(oracle_mod, d, w.eps, layout=layout)
+    st = parity.compare_fp8(got, ref, "col", what=f"prefill {layout}")
+    print(layout, st)
+
+
+# ------------------------------------------------- rows outside fp32's range
+
+@pytest.mark.parametrize("H", [8192, 32768])
+def test_wide_range_rows_fp64_path(oracle_mod, H):
+    """Rows whose sum of squares leaves the double-float range (elements near
+    2^60 and near 2^-60, so sums near 2^133 and 2^-107), which take the fp64
+    path: 384 rows per width, eps = 0 so that the sum alone sets inv_rms, and
+    every output bit-exact against the oracle outside boundary rows."""
+    M = 384
+    base = synth.normals(40 + H, "x", M * H).reshape(M, H)
+    scale = np.where(np.arange(M)[:, None] % 2 == 0, 2.0 ** 60, 2.0 ** -60)
+    x = synth.to_bf16(base * scale, (M, H))
+    assert torch.isfinite(x.float()).all()
+    d = {"x": x, "gamma": synth.gaussian_bf16(41, "gamma", (H,), mean=1.0, var=0.1)}
+    ref = ref_fp8(oracle_mod, d, 0.0, residual=False)
+    st = parity.compare_fp8(run_fp8(d, 0.0, residual=False, keep=True), ref, what=f"wide range H={H}")
+    assert st["codes_differing"] == 0 or st["boundary_rows"] > 0
+    mref = oracle_mod.add_rmsnorm_quant_mxfp4(d["x"], None, d["gamma"], 0.0)
+    parity.compare_mx(run_mx(d, 0.0, residual=False, keep=True), mref, what=f"mx wide range H={H}")
+    print(H, st)
+
+
+# ------------------------------------------- latency form of the row kernel
+
+@pytest.mark.parametrize("name,M", [("decode", None), ("decode", 1), ("decode", 152), ("prefill", 2000),
+                                    ("mxfp4", 64)])
+def test_latency_form_is_bit_identical(oracle_mod, name, M):
+    """The latency form (gamma loaded with the row, every warp finalising
+    inv_rms) against the throughput form: every output bit-identical, and
+    both against the oracle."""
+    w = synth.WORKLOADS[name]
+    d = synth.make_inputs(w, M=M)
+    lat = rmsq.LaunchOpts(kernel=rmsq.KERNEL_ROWS, form=rmsq.FORM_LATENCY)
+    thr = rmsq.LaunchOpts(kernel=rmsq.KERNEL_ROWS, form=rmsq.FORM_THROUGHPUT)
+    if w.kind == "fp8":
+        a = run_fp8(d, w.eps, layout=w.scale_layout, keep=True, opts=lat)
+        b = run_fp8(d, w.eps, layout=w.scale_layout, keep=True, opts=thr)
+        parity.compare_fp8(a, ref_fp8(oracle_mod, d, w.eps, w.scale_layout), w.scale_layout, what="latency form")
+    else:
+        a = run_mx(d, w.eps, keep=True, opts=lat)
+        b = run_mx(d, w.eps, keep=True, opts=thr)
+        parity.compare_mx(a, oracle_mod.add_rmsnorm_quant_mxfp4(d["x"], d["residual"], d["gamma"], w.eps),
+                          what="mx latency form")
+    for k in ("q", "scale", "residual_out", "y"):
+        assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), k
+
+
+def test_unknown_form_is_refused():
+    w = synth.WORKLOADS["decode"]
+    g = _gpu(synth.make_inputs(w, M=4))
+    with pytest.raises(rmsq.RmsqError, match="form"):
+        rmsq.add_rmsnorm_quant_fp8(g["x"], g["gamma"], g["residual"], opts=rmsq.LaunchOpts(form=7))
