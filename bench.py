@@ -171,6 +171,75 @@ def recorded_traffic(kernel_name: str) -> float | None:
     return float(ent["dram_bytes_per_launch"])
 
 
+_NCU_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+              "ns": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6, "nsecond": 1}
+
+
+def ncu_launches(csv_path: str) -> list[dict]:
+    """Per-launch DRAM bytes and duration from an ncu --csv metrics log
+    (dram__bytes_read.sum, dram__bytes_write.sum, gpu__time_duration.sum)."""
+    import csv
+    with open(csv_path) as fh:
+        lines = [ln for ln in fh if ln.startswith('"')]
+    rows = list(csv.reader(lines))
+    head, body = rows[0], rows[1:]
+    col = {name: i for i, name in enumerate(head)}
+    launches: dict[str, dict] = {}
+    for r in body:
+        ent = launches.setdefault(r[col["ID"]], {"kernel": r[col["Kernel Name"]]})
+        value = float(r[col["Metric Value"]].replace(",", "")) * _NCU_UNITS[r[col["Metric Unit"]]]
+        ent[r[col["Metric Name"]]] = value
+    out = []
+    for ident in sorted(launches, key=int):
+        e = launches[ident]
+        out.append({"kernel": e["kernel"],
+                    "dram_bytes": int(e["dram__bytes_read.sum"] + e["dram__bytes_write.sum"]),
+                    "ns": e.get("gpu__time_duration.sum")})
+    return out
+
+
+def ingest_traffic(key: str, csv_path: str, bench_log: str, command: str) -> dict:
+    """Writes the steady-state DRAM traffic of one kernel into
+    profiles/traffic.json from a capture: the ncu metrics log of `command`
+    (which ran bench.py) and that bench.py run's own JSON line, whose
+    source_digest says which kernel sources ran. Refuses a capture taken on
+    sources other than the ones here."""
+    kind = "gemm" if key.startswith("consumer") else "rows"
+    with open(bench_log) as fh:
+        line = json.loads([ln for ln in fh if ln.startswith("{")][-1])
+    ran = line["source_digest"][kind]
+    if ran != kernel_source_digest(kind):
+        raise SystemExit(f"the capture ran {kind} sources {ran}, these are {kernel_source_digest(kind)}")
+    launches = ncu_launches(csv_path)
+    if not launches:
+        raise SystemExit("no launches in the capture")
+    per = [ln_["dram_bytes"] for ln_ in launches]
+    ent = {"kernel": launches[0]["kernel"], "kernel_source_digest": ran,
+           "captured_workload": line["config"]["workload"],
+           "dram_bytes_per_launch": int(round(statistics.mean(per))),
+           "dram_bytes_each_launch": per,
+           "ns_each_launch": [ln_["ns"] for ln_ in launches],
+           "algorithmic_bytes_per_launch": line["config"]["bytes_per_step"],
+           "command": command,
+           "reading": ("launches in their back-to-back state (--cache-control none): the previous launch's "
+                       "outputs still dirty in L2 are written back inside this one, as in the timed steps")}
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except (OSError, ValueError):
+        rec = {}
+    rec["about"] = ("DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch, steady state, from "
+                    "ncu metric captures on GB300 with --clock-control none, written by `bench.py "
+                    "--ingest-traffic` from the capture's CSV and the captured bench.py run's own line; valid "
+                    "only while the kernel family's sources hash to kernel_source_digest")
+    rec[key] = ent
+    with open(path, "w") as fh:
+        json.dump(rec, fh, indent=1)
+        fh.write("\n")
+    return ent
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -994,8 +1063,11 @@ def run_consumer(args) -> None:
         "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e2m1", "data": "synthetic",
+        "source_digest": {"rows": kernel_source_digest("rows"), "gemm": kernel_source_digest("gemm")},
         "config": {"workload": f"D[{M},{N}] = A[{M},{K}] B[{N},{K}]^T, A and B MXFP4 (E2M1, E8M0 per 32), "
                                "bf16 out; A from the fused norm + quant", "M": M, "N": N, "K": K,
+                   "bytes_per_step": (M + N) * K // 2 + rmsq.mma_scale_bytes(M, K) + rmsq.mma_scale_bytes(N, K)
+                   + 2 * M * N,
                    "l2": "L2 flushed (256 MB written) before each timed call",
                    "timing": "K calls, CUDA events around each, L2 flushed in between"},
         "warm_l2_graph": {"steps": 200, "ms_per_step": round(warm_ms / 200, 5),
@@ -1057,10 +1129,15 @@ def main() -> None:
                     help="replay the K timed steps from a CUDA graph (auto = on; off: back-to-back calls)")
     ap.add_argument("--rows", type=int, default=0,
                     help="rows of the batch (profiler captures only; the benchmark is M=16384)")
+    ap.add_argument("--ingest-traffic", nargs=4, metavar=("KEY", "NCU_CSV", "BENCH_LOG", "COMMAND"),
+                    help="record a steady-state DRAM traffic capture in profiles/traffic.json (no GPU needed)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.ingest_traffic:
+        key, csv_path, log_path, command = args.ingest_traffic
+        print(json.dumps(ingest_traffic(key, csv_path, log_path, command)))
+    elif args.impl == "reference":
         run_reference(args)
     elif args.workload == "consumer":
         run_consumer(args)

@@ -148,9 +148,10 @@ __device__ __forceinline__ float inv_rms_fp64_path(const uint4 (&r)[VPT], int H,
 //
 // LAT (latency form, for launches of one row per SM or fewer): every warp of
 // the team reads all the partials after the one barrier and combines them
-// itself, in the same fixed butterfly, so the result is bit-identical to the
-// throughput form's and the second barrier and its shared-memory broadcast
-// leave the row's critical path. It needs no second slot set: a team's
+// itself, in the same fixed butterfly (its lane 0 finalises and shuffles the
+// result to the warp), so the result is bit-identical to the throughput
+// form's and the second barrier and its shared-memory broadcast leave the
+// row's critical path. It needs no second slot set: a team's
 // slots are written once per launch (row kernel only).
 template <int TPR, bool LAT = false>
 __device__ __forceinline__ float team_inv_rms(DF S, const Seg &s, int tpr, int team, int parity,
@@ -178,10 +179,13 @@ __device__ __forceinline__ float team_inv_rms(DF S, const Seg &s, int tpr, int t
         for (int off = 1; off < 32; off <<= 1)
             if (off < nw)
                 T = df_add_lazy(T, shfl_xor_df(T, off, 0xffffffffu));
-        if (LAT) {                                // every lane holds the same T
+        if (LAT) {
+            // the butterfly spans the next power of two above nw lanes only:
+            // lane 0 holds the team's sum, so it finalises and every lane
+            // takes its value
             if (!inv_rms_df(df_renorm(T), s.H, s.inv_h, s.eps, inv))
                 inv = __int_as_float(0x7fffffff);
-            return inv;
+            return __shfl_sync(0xffffffffu, inv, 0);
         }
         if (lane == 0) {
             if (!inv_rms_df(df_renorm(T), s.H, s.inv_h, s.eps, inv))

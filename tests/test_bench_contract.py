@@ -150,3 +150,37 @@ def test_parity_verdict_applies_the_bar():
     assert not bench._verdict({**ok, "mismatch_fraction": 2e-3})["passes"]
     assert not bench._verdict({**ok, "residual_out_bit_exact": False})["passes"]
     assert not bench._verdict({**ok, "scale_max_rel": 1e-4})["passes"]
+
+
+def _ncu_csv(path, kernel, launches):
+    head = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",'
+            '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"')
+    rows = ["==PROF== Connected to process 1", head]
+    for i, (rd, wr, ns) in enumerate(launches):
+        for name, unit, v in (("dram__bytes_read.sum", "Mbyte", rd), ("dram__bytes_write.sum", "byte", wr),
+                              ("gpu__time_duration.sum", "ns", ns)):
+            rows.append(f'"{i}","1","python3","h","{kernel}","1","7","(224, 1, 1)","(16384, 1, 1)","0","10.3",'
+                        f'"Command line profiler metrics","{name}","{unit}","{v}"')
+    path.write_text("\n".join(rows) + "\n")
+
+
+def test_traffic_ingest_takes_the_digest_of_the_run(tmp_path, monkeypatch):
+    """A capture is recorded with the digest the captured bench.py run printed,
+    and only if that is the digest of the sources here."""
+    import json
+    import pytest
+    _fake_tree(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    _ncu_csv(tmp_path / "c.csv", "void rows_kernel<4, 224, 0, 0>(LaunchParams)",
+             [(470.5, 590000000, 158000), (471.5, 590000000, 158500)])
+    line = {"config": {"workload": "prefill", "bytes_per_step": 1060648960},
+            "source_digest": {"rows": bench.kernel_source_digest("rows"), "gemm": "x"}}
+    (tmp_path / "b.json").write_text("noise\n" + json.dumps(line) + "\n")
+    ent = bench.ingest_traffic("prefill:rows", str(tmp_path / "c.csv"), str(tmp_path / "b.json"), "ncu ...")
+    assert ent["dram_bytes_each_launch"] == [1060500000, 1061500000]
+    assert ent["dram_bytes_per_launch"] == 1061000000
+    assert bench.recorded_traffic("prefill:rows") == 1061000000
+    line["source_digest"]["rows"] = "0" * 16
+    (tmp_path / "b.json").write_text(json.dumps(line) + "\n")
+    with pytest.raises(SystemExit, match="sources"):
+        bench.ingest_traffic("prefill:rows", str(tmp_path / "c.csv"), str(tmp_path / "b.json"), "ncu ...")
