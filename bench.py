@@ -421,14 +421,29 @@ def time_launches(fn, steps: int, stream) -> tuple[float, list[float]]:
     return start.elapsed_time(end), [a.elapsed_time(b) for a, b in evs]
 
 
+class L2Flush:
+    """Evicts L2 between timed calls by reading a 256 MB buffer (twice L2). The
+    lines it leaves behind are clean, so the timed call that follows does not
+    pay for writing back the flush's own data, as it would after a flush that
+    writes (up to 129 MB of dirty lines)."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+        self()                      # the fill's dirty lines are written back here, untimed
+
+    def __call__(self):
+        self.total = self.buf.sum()
+
+
 def time_launches_cold(fn, steps: int, stream, flush) -> tuple[float, list[float]]:
-    """Each of `steps` calls timed alone (events on `stream`) after writing the
-    buffer `flush` (larger than L2) so that no input is L2-resident; returns
-    the sum of the calls' ms and each call's ms."""
+    """Each of `steps` calls timed alone (events on `stream`) after `flush()`
+    has evicted L2 so that no input is L2-resident; returns the sum of the
+    calls' ms and each call's ms."""
     import torch
     each = []
     for _ in range(steps):
-        flush.fill_(1)
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -465,12 +480,13 @@ def time_graph(fn, steps: int, stream) -> float:
 
 def _cold_us(fn, dev, calls: int = 50) -> float:
     """Median microseconds of `calls` calls, each timed alone (CUDA events)
-    after 256 MB (twice L2) have been written, so no input is L2-resident."""
+    after L2 has been evicted by reading 256 MB (L2Flush), so no input is
+    L2-resident."""
     import torch
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     each = []
     for _ in range(calls):
-        flush.fill_(1)
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
@@ -1010,9 +1026,9 @@ def run_consumer(args) -> None:
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    # The operands (37 MB) fit in L2: each timed call starts with L2 flushed
-    # (256 MB written between calls, outside the events).
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # The operands (37 MB) fit in L2: each timed call starts with L2 evicted
+    # (256 MB read between calls, outside the events).
+    flush = L2Flush(dev)
     total_ms, each = time_launches_cold(step, args.steps, stream, flush)
     del flush
     clocks = sampler.stop()
@@ -1068,8 +1084,8 @@ def run_consumer(args) -> None:
                                "bf16 out; A from the fused norm + quant", "M": M, "N": N, "K": K,
                    "bytes_per_step": (M + N) * K // 2 + rmsq.mma_scale_bytes(M, K) + rmsq.mma_scale_bytes(N, K)
                    + 2 * M * N,
-                   "l2": "L2 flushed (256 MB written) before each timed call",
-                   "timing": "K calls, CUDA events around each, L2 flushed in between"},
+                   "l2": "L2 evicted before each timed call by reading 256 MB (clean lines)",
+                   "timing": "K calls, CUDA events around each, L2 evicted in between"},
         "warm_l2_graph": {"steps": 200, "ms_per_step": round(warm_ms / 200, 5),
                           "value": round(flops * 200 / (warm_ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
                           "timing": "CUDA graph of 200 calls, operands L2-resident"},

@@ -454,6 +454,11 @@ rmsq_status qknorm_common(bool mx, const void *q_a, int64_t ld_q, const void *kv
     p.seg[0] = sq;
     p.seg[1] = sk;
     p.nseg = 2;
+    // L2 prefetch one resident wave ahead when the launch spans more than two
+    // waves (with fewer, the blocks that would be prefetched for are resident
+    // from the start)
+    const int64_t wave = (int64_t)dual_occupancy(mx, v0, t0s, v1, t1s, threads) * sm_count();
+    p.prefetch_blocks = (wave > 0 && bq + bk > 2 * wave) ? (int32_t)wave : 0;
     cudaError_t e = launch_dual(mx, v0, t0s, v1, t1s, p, (int)(bq + bk), threads, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));

@@ -40,6 +40,7 @@ struct Seg {
 struct LaunchParams {
     Seg seg[2];
     int32_t nseg;
+    int32_t prefetch_blocks;   // dual kernel: block b pulls the input rows of block b + this into L2 (0 = off)
 };
 
 // Persistent bulk-copy kernel: one segment, one row per team, rows strided
@@ -71,6 +72,8 @@ cudaError_t launch_rows_mx(int vpt, int tpr_static, bool lat, const LaunchParams
                            cudaStream_t st);
 cudaError_t launch_dual(bool mx, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,
                         int threads, cudaStream_t st);
+// Blocks of the dual kernel with this shape resident per SM (0 if the query fails).
+int dual_occupancy(bool mx, int v0, int t0, int v1, int t1, int threads);
 cudaError_t launch_bulk(bool mx, int vpt, int tpr_static, const BulkParams &p, int grid, int threads,
                         size_t smem, cudaStream_t st);
 int bulk_occupancy(bool mx, int vpt, int tpr_static, int threads, size_t smem);

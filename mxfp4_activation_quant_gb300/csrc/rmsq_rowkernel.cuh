@@ -49,10 +49,38 @@ __global__ void __launch_bounds__(kMaxThreads) rows_kernel(const __grid_constant
     block_rows<VPT, TPR, MX, LAT>(p.seg[0], blockIdx.x, red);
 }
 
+// Pulls the input rows of the dual kernel's block `b` into L2: one 1-D bulk
+// prefetch when its rows are contiguous, else one per row.
+__device__ __forceinline__ void prefetch_dual_block(const LaunchParams &p, int64_t b)
+{
+    const int si = b < p.seg[0].blocks ? 0 : 1;
+    const Seg &s = p.seg[si];
+    if (si == 1)
+        b -= p.seg[0].blocks;
+    if (b >= s.blocks)
+        return;
+    const int64_t r0 = b * s.rpb, r1 = min(r0 + s.rpb, s.M);
+    const uint32_t row_bytes = (uint32_t)s.H * 2;
+    if (s.ldx_v * 8 == s.H) {
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s.x + r0 * s.ldx_v),
+                     "r"((uint32_t)(r1 - r0) * row_bytes)
+                     : "memory");
+    } else {
+        for (int64_t r = r0; r < r1; ++r)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s.x + r * s.ldx_v), "r"(row_bytes)
+                         : "memory");
+    }
+}
+
 template <int V0, int T0, int V1, int T1, bool MX>
 __global__ void __launch_bounds__(kMaxThreads, 2) dual_kernel(const __grid_constant__ LaunchParams p)
 {
     __shared__ RedSmem red;
+    // Keep HBM busy while the resident blocks are in their (issue-bound)
+    // reduction and quantise phases: pull the rows of the block one resident
+    // wave later into L2, across the q_a / kv_a boundary.
+    if (p.prefetch_blocks && threadIdx.x == 0)
+        prefetch_dual_block(p, (int64_t)blockIdx.x + p.prefetch_blocks);
     if ((int)blockIdx.x < p.seg[0].blocks)
         block_rows<V0, T0, MX>(p.seg[0], blockIdx.x, red);
     else

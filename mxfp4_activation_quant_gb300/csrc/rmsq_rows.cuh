@@ -282,38 +282,62 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
 
     // ---- quantise and store
     const bool leader = (t & (GV - 1)) == 0;
+    if constexpr (!MX) {
+        // Every group's scale and divisor first, then the quotients of all
+        // vectors in one pass without control flow between them (the
+        // divisions of different vectors are independent and interleave):
+        // the direct IEEE division is kept for the rare groups whose scale
+        // is too small for the reciprocal method.
+        float scl[VPT];
+        GroupDivisor gd[VPT];
+        bool fast = true;
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int v = k * tpr + t;   // vector index in the row
-        if (GUARD && v >= nvec)
-            continue;                // padding of the team shape (whole groups)
-        const uint32_t yw[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
-        if constexpr (!MX) {
-            const float amax = __uint_as_float(am[k] << 16);
-            const float scale = div448(amax);
-            const float d = am[k] ? scale : 1.0f;   // all-zero group: codes of +-0
-            if (leader) {
-                const int64_t g = v >> 4, G = s.H >> 7;
-                float *sc = (float *)s.out_scale;
+        for (int k = 0; k < VPT; ++k) {
+            scl[k] = div448(__uint_as_float(am[k] << 16));
+            gd[k] = make_group_divisor(am[k] ? scl[k] : 1.0f);   // all-zero group: codes of +-0
+            fast = fast && gd[k].fast;
+        }
+        if (leader) {
+            const int64_t G = s.H >> 7;
+            float *sc = (float *)s.out_scale;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = k * tpr + t;
+                if (GUARD && v >= nvec)
+                    continue;                // padding of the team shape (whole groups)
+                const int64_t g = v >> 4;
                 const int64_t si = s.layout == 0 ? row * G + g : g * s.scale_ld + row;
                 if (RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && si < s.scale_elems))
-                    sc[si] = scale;
+                    sc[si] = scl[k];
             }
-            const GroupDivisor gd = make_group_divisor(d);
+        }
+        uint2 *qrow = reinterpret_cast<uint2 *>(s.out_q + row * (int64_t)s.H);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * tpr + t;   // vector index in the row
+            if (GUARD && v >= nvec)
+                continue;
+            const uint32_t yw[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
             float2 qv[4];
-            if (gd.fast) {
+            if (fast || gd[k].fast) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    qv[j] = div_fast_neg2(unpack_neg_bf16x2(yw[j]), gd);
+                    qv[j] = div_fast_neg2(unpack_neg_bf16x2(yw[j]), gd[k]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    qv[j] = make_float2(__fdiv_rn(bf_lo(yw[j]), d), __fdiv_rn(bf_hi(yw[j]), d));
+                    qv[j] = make_float2(__fdiv_rn(bf_lo(yw[j]), gd[k].d), __fdiv_rn(bf_hi(yw[j]), gd[k].d));
             }
-            const uint2 q = make_uint2(e4m3x4(qv[0], qv[1]), e4m3x4(qv[2], qv[3]));
             if (RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && v < nvec))
-                reinterpret_cast<uint2 *>(s.out_q + row * (int64_t)s.H)[v] = q;
-        } else {
+                qrow[v] = make_uint2(e4m3x4(qv[0], qv[1]), e4m3x4(qv[2], qv[3]));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * tpr + t;   // vector index in the row
+            if (GUARD && v >= nvec)
+                continue;                // padding of the team shape (whole groups)
+            const uint32_t yw[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
             const int X = mx_exponent_from_bits(am[k]);
             const float2 mult = f2(__uint_as_float((uint32_t)(127 - X) << 23));   // 2^-X
             if (leader) {
