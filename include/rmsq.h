@@ -300,6 +300,12 @@ typedef enum rmsq_form {
  *                   exists for the compiled team shapes (H = 7168, 8192, 5120,
  *                   4096, 2048, 1536, 512 at their default vpt) and is
  *                   ignored for other shapes.
+ *   split           latency form with one row per block: the blocks that
+ *                   share each row's outputs, 1, 2 or 4 (dividing vpt);
+ *                   each loads and reduces the whole row, so all compute the
+ *                   same inv_rms, and normalises, quantises and stores its
+ *                   part. 0 = auto: the largest of 4 and 2 that keeps the
+ *                   launch within one block per SM, else 1.
  */
 typedef struct rmsq_launch_opts {
     int32_t kernel;
@@ -309,6 +315,7 @@ typedef struct rmsq_launch_opts {
     int64_t debug_skip_row;
     int64_t wait_limit_ns;
     int32_t form;
+    int32_t split;
 } rmsq_launch_opts;
 
 rmsq_status rmsq_add_rmsnorm_quant_group_fp8_ex(

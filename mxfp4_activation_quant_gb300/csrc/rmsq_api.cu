@@ -103,7 +103,7 @@ int pick_vpt(int64_t nvec, int gv, int forced, int &tpr)
 
 int default_rows_per_block(int tpr) { return tpr >= 256 ? 1 : 256 / tpr; }
 
-const rmsq_launch_opts kDefaultOpts = {RMSQ_KERNEL_AUTO, 0, 0, 0, -1, 0, RMSQ_FORM_AUTO};
+const rmsq_launch_opts kDefaultOpts = {RMSQ_KERNEL_AUTO, 0, 0, 0, -1, 0, RMSQ_FORM_AUTO, 0};
 
 // Checks shared by the single-tensor FP8 and MXFP4 calls.
 rmsq_status check_single(const void *x, int64_t ld_x, const void *residual, int64_t ld_res,
@@ -279,13 +279,39 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
         const int ts = (static_shape(vpt, tpr) && vpt * tpr * 8 == s.H) ? tpr : 0;
         // The latency form (gamma loaded with the row, one barrier per row)
         // when the launch is at most one block per SM: there the row's
-        // dependent chain, not bandwidth, sets the time.
+        // dependent chain, not bandwidth, sets the time. With SMs to spare,
+        // each row's outputs are shared by 2 or 4 blocks on as many SMs: every
+        // one of them loads and reduces the whole row (the same inv_rms) and
+        // normalises, quantises and stores its part.
         if (o.form != RMSQ_FORM_AUTO && o.form != RMSQ_FORM_THROUGHPUT && o.form != RMSQ_FORM_LATENCY)
             return fail(RMSQ_ERR_INVALID_ARG, "unknown kernel form %d", o.form);
-        const bool lat = ts && (o.form == RMSQ_FORM_LATENCY ||
-                                (o.form == RMSQ_FORM_AUTO && blocks <= (int64_t)sm_count()));
-        cudaError_t e = mx ? launch_rows_mx(vpt, ts, lat, p, (int)blocks, rpb * tpr, st)
-                           : launch_rows_fp8(vpt, ts, lat, p, (int)blocks, rpb * tpr, st);
+        if (o.split != 0 && o.split != 1 && o.split != 2 && o.split != 4)
+            return fail(RMSQ_ERR_INVALID_ARG, "split must be 0, 1, 2 or 4 (got %d)", o.split);
+        const int64_t sms = sm_count();
+        const bool lat = ts && (o.form == RMSQ_FORM_LATENCY || (o.form == RMSQ_FORM_AUTO && blocks <= sms));
+        int split = 1;
+        if (lat && rpb == 1) {
+            if (o.split) {
+                split = o.split;
+            } else {
+                for (int c : {4, 2})
+                    if (vpt % c == 0 && s.M * c <= sms) {
+                        split = c;
+                        break;
+                    }
+            }
+            if (vpt % split)
+                return fail(RMSQ_ERR_UNSUPPORTED, "split %d does not divide %d vectors per thread", split, vpt);
+        } else if (o.split > 1) {
+            return fail(RMSQ_ERR_UNSUPPORTED, "split rows need the latency form of a compiled team shape "
+                                              "with one row per block");
+        }
+        const int64_t grid = blocks * split;   // split > 1 only with one row per block
+        if (grid > 0x7fffffff)
+            return fail(RMSQ_ERR_UNSUPPORTED, "M too large");
+        const int form = lat ? split : 0;
+        cudaError_t e = mx ? launch_rows_mx(vpt, ts, form, p, (int)grid, rpb * tpr, st)
+                           : launch_rows_fp8(vpt, ts, form, p, (int)grid, rpb * tpr, st);
         if (e != cudaSuccess)
             return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
         return ok();
@@ -454,11 +480,6 @@ rmsq_status qknorm_common(bool mx, const void *q_a, int64_t ld_q, const void *kv
     p.seg[0] = sq;
     p.seg[1] = sk;
     p.nseg = 2;
-    // L2 prefetch one resident wave ahead when the launch spans more than two
-    // waves (with fewer, the blocks that would be prefetched for are resident
-    // from the start)
-    const int64_t wave = (int64_t)dual_occupancy(mx, v0, t0s, v1, t1s, threads) * sm_count();
-    p.prefetch_blocks = (wave > 0 && bq + bk > 2 * wave) ? (int32_t)wave : 0;
     cudaError_t e = launch_dual(mx, v0, t0s, v1, t1s, p, (int)(bq + bk), threads, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));

@@ -1,6 +1,4 @@
 // Dual-tensor (MLA q_a / kv_a) kernel instantiations, FP8 1x128 and MXFP4.
-#include <atomic>
-
 #include "rmsq_rowkernel.cuh"
 
 namespace rmsq {
@@ -39,46 +37,6 @@ cudaError_t launch_dual_impl(int v0, int t0, int v1, int t1, const LaunchParams 
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
-}
-
-template <bool MX>
-const void *dual_fn(int v0, int t0, int v1, int t1)
-{
-    if (t0 || t1)
-        return static_dual_shape(v0, t0, v1, t1) ? (const void *)dual_kernel<6, 32, 4, 16, MX> : nullptr;
-    if (v0 != v1)
-        return nullptr;
-    switch (v0) {
-    case 1: return (const void *)dual_kernel<1, 0, 1, 0, MX>;
-    case 2: return (const void *)dual_kernel<2, 0, 2, 0, MX>;
-    case 3: return (const void *)dual_kernel<3, 0, 3, 0, MX>;
-    case 4: return (const void *)dual_kernel<4, 0, 4, 0, MX>;
-    case 5: return (const void *)dual_kernel<5, 0, 5, 0, MX>;
-    case 6: return (const void *)dual_kernel<6, 0, 6, 0, MX>;
-    case 7: return (const void *)dual_kernel<7, 0, 7, 0, MX>;
-    case 8: return (const void *)dual_kernel<8, 0, 8, 0, MX>;
-    }
-    return nullptr;
-}
-
-int dual_occupancy(bool mx, int v0, int t0, int v1, int t1, int threads)
-{
-    // the compiled MLA shape is queried once per device and quantiser
-    static std::atomic<int> cached[128][2];   // every thread stores the same value
-    int dev = 0;
-    const bool mla = static_dual_shape(v0, t0, v1, t1) && threads == 256;
-    if (mla && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 128) {
-        const int c = cached[dev][mx].load(std::memory_order_acquire);
-        if (c)
-            return c;
-    }
-    const void *fn = mx ? dual_fn<true>(v0, t0, v1, t1) : dual_fn<false>(v0, t0, v1, t1);
-    int n = 0;
-    if (!fn || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, 0) != cudaSuccess)
-        return 0;
-    if (mla && dev >= 0 && dev < 128)
-        cached[dev][mx].store(n, std::memory_order_release);
-    return n;
 }
 
 cudaError_t launch_dual(bool mx, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,

@@ -40,7 +40,6 @@ struct Seg {
 struct LaunchParams {
     Seg seg[2];
     int32_t nseg;
-    int32_t prefetch_blocks;   // dual kernel: block b pulls the input rows of block b + this into L2 (0 = off)
 };
 
 // Persistent bulk-copy kernel: one segment, one row per team, rows strided
@@ -64,16 +63,16 @@ constexpr int kMaxThreads = 512;
 
 // Launchers (a switch over the instantiations each). tpr_static != 0 selects
 // a kernel compiled for that exact team size (see static_shape).
-// lat selects the latency form of a compiled team shape (gamma loaded with
-// the row, one barrier per row; bit-identical results).
-cudaError_t launch_rows_fp8(int vpt, int tpr_static, bool lat, const LaunchParams &p, int grid, int threads,
+// lat > 0 selects the latency form of a compiled team shape (gamma loaded
+// with the row, one barrier per row; bit-identical results) with each row's
+// outputs shared by `lat` blocks (1, 2 or 4; block b holds row b / lat);
+// lat = 0 the throughput form.
+cudaError_t launch_rows_fp8(int vpt, int tpr_static, int lat, const LaunchParams &p, int grid, int threads,
                             cudaStream_t st);
-cudaError_t launch_rows_mx(int vpt, int tpr_static, bool lat, const LaunchParams &p, int grid, int threads,
+cudaError_t launch_rows_mx(int vpt, int tpr_static, int lat, const LaunchParams &p, int grid, int threads,
                            cudaStream_t st);
 cudaError_t launch_dual(bool mx, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,
                         int threads, cudaStream_t st);
-// Blocks of the dual kernel with this shape resident per SM (0 if the query fails).
-int dual_occupancy(bool mx, int v0, int t0, int v1, int t1, int threads);
 cudaError_t launch_bulk(bool mx, int vpt, int tpr_static, const BulkParams &p, int grid, int threads,
                         size_t smem, cudaStream_t st);
 int bulk_occupancy(bool mx, int vpt, int tpr_static, int threads, size_t smem);

@@ -1,9 +1,10 @@
 // Register-resident row kernels: each team loads its row of x (and residual)
 // straight into registers with 16-byte streaming loads, adds, writes the
 // residual back, and finishes the row (rmsq_rows.cuh).
-//   rows_kernel<VPT, TPR, MX, LAT>  one tensor; LAT: the latency form for
+//   rows_kernel<VPT, TPR, MX, LAT>  one tensor; LAT > 0: the latency form for
 //                                   launches of at most one block per SM
-//                                   (gamma loaded with the row, one barrier)
+//                                   (gamma loaded with the row, one barrier),
+//                                   each row's outputs shared by LAT blocks
 //   dual_kernel<V0, T0, V1, T1, MX> two tensors (the MLA q_a / kv_a pair),
 //                                   blocks [0, seg[0].blocks) on the first
 // TPR / T0 / T1 = 0 means the team size is read at run time.
@@ -13,15 +14,20 @@
 
 namespace rmsq {
 
-template <int VPT, int TPR, bool MX, bool LAT = false>
+// LAT = 0: the throughput form; LAT = 1, 2, 4: the latency form with the
+// outputs of each row shared by LAT blocks (block b: row b / LAT, part
+// b % LAT; one team per block).
+template <int VPT, int TPR, bool MX, int LAT = 0>
 __device__ __forceinline__ void block_rows(const Seg &s, int b, RedSmem &red)
 {
+    constexpr int SPLIT = LAT > 1 ? LAT : 1;
     const int tpr = TPR ? TPR : s.tpr;
     const int team = threadIdx.x / tpr;
     if (team >= s.rpb)
         return;                                   // idle team of a shared-size block
     const int t = threadIdx.x - team * tpr;
-    const int64_t row = (int64_t)b * s.rpb + team;
+    const int64_t row = SPLIT > 1 ? (int64_t)(b / SPLIT) : (int64_t)b * s.rpb + team;
+    const int part = SPLIT > 1 ? b % SPLIT : 0;
     if (row >= s.M)
         return;                                   // whole teams leave together
     if (s.prefetch_rows && t == 0) {
@@ -39,48 +45,20 @@ __device__ __forceinline__ void block_rows(const Seg &s, int b, RedSmem &red)
                              : "memory");
         }
     }
-    row_from_global<VPT, TPR, MX, LAT>(s, row, t, team, 0, red);
+    row_from_global<VPT, TPR, MX, (LAT > 0), SPLIT>(s, row, t, team, 0, red, part);
 }
 
-template <int VPT, int TPR, bool MX, bool LAT>
+template <int VPT, int TPR, bool MX, int LAT>
 __global__ void __launch_bounds__(kMaxThreads) rows_kernel(const __grid_constant__ LaunchParams p)
 {
     __shared__ RedSmem red;
     block_rows<VPT, TPR, MX, LAT>(p.seg[0], blockIdx.x, red);
 }
 
-// Pulls the input rows of the dual kernel's block `b` into L2: one 1-D bulk
-// prefetch when its rows are contiguous, else one per row.
-__device__ __forceinline__ void prefetch_dual_block(const LaunchParams &p, int64_t b)
-{
-    const int si = b < p.seg[0].blocks ? 0 : 1;
-    const Seg &s = p.seg[si];
-    if (si == 1)
-        b -= p.seg[0].blocks;
-    if (b >= s.blocks)
-        return;
-    const int64_t r0 = b * s.rpb, r1 = min(r0 + s.rpb, s.M);
-    const uint32_t row_bytes = (uint32_t)s.H * 2;
-    if (s.ldx_v * 8 == s.H) {
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s.x + r0 * s.ldx_v),
-                     "r"((uint32_t)(r1 - r0) * row_bytes)
-                     : "memory");
-    } else {
-        for (int64_t r = r0; r < r1; ++r)
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s.x + r * s.ldx_v), "r"(row_bytes)
-                         : "memory");
-    }
-}
-
 template <int V0, int T0, int V1, int T1, bool MX>
 __global__ void __launch_bounds__(kMaxThreads, 2) dual_kernel(const __grid_constant__ LaunchParams p)
 {
     __shared__ RedSmem red;
-    // Keep HBM busy while the resident blocks are in their (issue-bound)
-    // reduction and quantise phases: pull the rows of the block one resident
-    // wave later into L2, across the q_a / kv_a boundary.
-    if (p.prefetch_blocks && threadIdx.x == 0)
-        prefetch_dual_block(p, (int64_t)blockIdx.x + p.prefetch_blocks);
     if ((int)blockIdx.x < p.seg[0].blocks)
         block_rows<V0, T0, MX>(p.seg[0], blockIdx.x, red);
     else
@@ -98,34 +76,57 @@ __global__ void __launch_bounds__(kMaxThreads, 2) dual_kernel(const __grid_const
     X(3, 64)  /* H = 1536 */  \
     X(4, 16)  /* H = 512  */
 
-// The latency form exists for the compiled team shapes only; `lat` is
-// ignored for runtime team sizes.
+// One compiled team shape in the throughput form (lat 0) or the latency form
+// with each row's outputs shared by lat = 1, 2 or 4 blocks (a split that
+// divides V).
+template <int V, int T, bool MX>
+cudaError_t launch_static(int lat, const LaunchParams &p, int grid, int threads, cudaStream_t st)
+{
+    if (lat == 0)
+        rows_kernel<V, T, MX, 0><<<grid, threads, 0, st>>>(p);
+    else if (lat == 1)
+        rows_kernel<V, T, MX, 1><<<grid, threads, 0, st>>>(p);
+    else if constexpr (V % 2 == 0) {
+        if (lat == 2)
+            rows_kernel<V, T, MX, 2><<<grid, threads, 0, st>>>(p);
+        else if constexpr (V % 4 == 0) {
+            if (lat == 4)
+                rows_kernel<V, T, MX, 4><<<grid, threads, 0, st>>>(p);
+            else
+                return cudaErrorInvalidValue;
+        } else {
+            return cudaErrorInvalidValue;
+        }
+    } else {
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+// The latency form exists for the compiled team shapes only; `lat` (0 =
+// throughput form, else the latency form's split) is ignored for runtime
+// team sizes.
 template <bool MX>
-cudaError_t launch_rows_impl(int vpt, int tpr_static, bool lat, const LaunchParams &p, int grid,
+cudaError_t launch_rows_impl(int vpt, int tpr_static, int lat, const LaunchParams &p, int grid,
                              int threads, cudaStream_t st)
 {
     if (tpr_static) {
-#define RMSQ_LAUNCH_STATIC(V, T)                                            \
-        if (vpt == V && tpr_static == T) {                                  \
-            if (lat)                                                        \
-                rows_kernel<V, T, MX, true><<<grid, threads, 0, st>>>(p);   \
-            else                                                            \
-                rows_kernel<V, T, MX, false><<<grid, threads, 0, st>>>(p);  \
-            return cudaGetLastError();                                      \
-        }
+#define RMSQ_LAUNCH_STATIC(V, T)                                                \
+        if (vpt == V && tpr_static == T)                                        \
+            return launch_static<V, T, MX>(lat, p, grid, threads, st);
         RMSQ_STATIC_SHAPES(RMSQ_LAUNCH_STATIC)
 #undef RMSQ_LAUNCH_STATIC
         return cudaErrorInvalidValue;
     }
     switch (vpt) {
-    case 1: rows_kernel<1, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
-    case 2: rows_kernel<2, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
-    case 3: rows_kernel<3, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
-    case 4: rows_kernel<4, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
-    case 5: rows_kernel<5, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
-    case 6: rows_kernel<6, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
-    case 7: rows_kernel<7, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
-    case 8: rows_kernel<8, 0, MX, false><<<grid, threads, 0, st>>>(p); break;
+    case 1: rows_kernel<1, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
+    case 2: rows_kernel<2, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
+    case 3: rows_kernel<3, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
+    case 4: rows_kernel<4, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
+    case 5: rows_kernel<5, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
+    case 6: rows_kernel<6, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
+    case 7: rows_kernel<7, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
+    case 8: rows_kernel<8, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

@@ -202,24 +202,47 @@ __device__ __forceinline__ float team_inv_rms(DF S, const Seg &s, int tpr, int t
 // from registers loaded together with the row (latency form).
 enum GammaFrom { GAMMA_GLOBAL = 0, GAMMA_SHARED = 1, GAMMA_REGS = 2 };
 
+// Vector j of part `part` of a thread's VPT vectors cut into SPLIT parts of
+// VPT / SPLIT (k = part * VPT / SPLIT + j), chosen by selects so that the
+// array stays in registers (part is known only at run time).
+template <int SPLIT, int VPT>
+__device__ __forceinline__ uint4 part_vec(const uint4 (&a)[VPT], int part, int j)
+{
+    constexpr int NV = VPT / SPLIT;
+    uint4 v = a[j];
+#pragma unroll
+    for (int p = 1; p < SPLIT; ++p)
+        if (part == p)
+            v = a[p * NV + j];
+    return v;
+}
+
 // Everything after the row is loaded: r holds the thread's VPT vectors of
 // bf16 r (residual already added and written back by the caller). gamma
 // comes from gamma_src (GAMMA_GLOBAL, GAMMA_SHARED) or gpre (GAMMA_REGS, the
-// thread's own VPT vectors). TPR is the team size when known at compile time
-// (the row is then an exact fit, tpr * VPT * 8 == H), or 0 for a runtime
-// team size with padding guards. LAT selects team_inv_rms's latency form.
-// Elementwise arithmetic runs on packed fp32 pairs.
-template <int VPT, int TPR, bool MX, int GFROM, bool LAT = false>
+// thread's own vectors of this part). TPR is the team size when known at
+// compile time (the row is then an exact fit, tpr * VPT * 8 == H), or 0 for a
+// runtime team size with padding guards. LAT selects team_inv_rms's latency
+// form. SPLIT > 1 (latency form only): the row's outputs are shared by SPLIT
+// blocks; each reduces the whole row (the same sum in the same order, so the
+// same inv_rms) and normalises, quantises and stores only its part `part`,
+// vectors k = part * VPT / SPLIT .. of each thread. Elementwise arithmetic
+// runs on packed fp32 pairs.
+template <int VPT, int TPR, bool MX, int GFROM, bool LAT = false, int SPLIT = 1>
 __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int team, int parity,
                                            RedSmem &red, const uint4 (&r)[VPT],
-                                           const uint4 *gamma_src, const uint4 (&gpre)[VPT])
+                                           const uint4 *gamma_src, const uint4 (&gpre)[VPT / SPLIT],
+                                           int part = 0)
 {
     constexpr int GV = MX ? 4 : 16;   // 16-byte vectors per quant group
     constexpr bool GUARD = TPR == 0;
+    constexpr int NV = VPT / SPLIT;   // vectors of this block's part, per thread
+    static_assert(VPT % SPLIT == 0 && (SPLIT == 1 || (LAT && GFROM == GAMMA_REGS)), "split rows");
     const int tpr = TPR ? TPR : s.tpr;
     const int lane = threadIdx.x & 31;
     const unsigned tmask = team_lane_mask(tpr, lane);
     const int nvec = TPR ? TPR * VPT : (s.H >> 3);
+    const int kb = part * NV;         // first vector (k) of the part
 
     // ---- sum of squares: exact squares, two packed double-float accumulators
     float2 hi = f2(0.0f), lo = f2(0.0f);
@@ -236,15 +259,16 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         inv = inv_rms_fp64_path<VPT>(r, s.H, s.eps, tpr, team, red);
     const float2 inv2 = f2(inv);
 
-    // ---- normalise: y = bf16((r * inv) * gamma)
-    uint4 y[VPT];
+    // ---- normalise: y = bf16((r * inv) * gamma), this part's vectors
+    uint4 y[NV];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int vk = k * tpr + t;
+    for (int k = 0; k < NV; ++k) {
+        const int vk = (kb + k) * tpr + t;
         const uint4 g = (GUARD && vk >= nvec) ? make_uint4(0, 0, 0, 0)
                         : GFROM == GAMMA_REGS ? gpre[k]
                         : GFROM == GAMMA_SHARED ? gamma_src[vk] : ld_keep(gamma_src + vk);
-        const uint32_t rw[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
+        const uint4 rk = SPLIT == 1 ? r[k] : part_vec<SPLIT>(r, part, k);
+        const uint32_t rw[4] = {rk.x, rk.y, rk.z, rk.w};
         const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
         uint32_t yw[4];
 #pragma unroll
@@ -257,26 +281,28 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
     if (s.out_bf16) {
         uint4 *yrow = s.out_bf16 + row * nvec + t;
 #pragma unroll
-        for (int k = 0; k < VPT; ++k)
-            if ((!GUARD || k * tpr + t < nvec) && RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && k * tpr + t < nvec))
-                yrow[k * tpr] = y[k];
+        for (int k = 0; k < NV; ++k) {
+            const int vk = (kb + k) * tpr + t;
+            if ((!GUARD || vk < nvec) && RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && vk < nvec))
+                yrow[(kb + k) * tpr] = y[k];
+        }
     }
     if (!s.out_q)   // norm only (rmsq_add_rmsnorm)
         return;
 
     // ---- group amax over GV lanes (two vectors packed per shuffle)
-    uint32_t am[VPT];
+    uint32_t am[NV];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k)
+    for (int k = 0; k < NV; ++k)
         am[k] = amax_bits_bf16x8(y[k]);
 #pragma unroll
-    for (int k = 0; k < VPT; k += 2) {
-        uint32_t v = am[k] | ((k + 1 < VPT) ? (am[k + 1] << 16) : 0u);
+    for (int k = 0; k < NV; k += 2) {
+        uint32_t v = am[k] | ((k + 1 < NV) ? (am[k + 1] << 16) : 0u);
 #pragma unroll
         for (int off = 1; off < GV; off <<= 1)
             v = max_u16x2(v, __shfl_xor_sync(tmask, v, off));
         am[k] = v & 0xffffu;
-        if (k + 1 < VPT)
+        if (k + 1 < NV)
             am[k + 1] = v >> 16;
     }
 
@@ -288,11 +314,11 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         // divisions of different vectors are independent and interleave):
         // the direct IEEE division is kept for the rare groups whose scale
         // is too small for the reciprocal method.
-        float scl[VPT];
-        GroupDivisor gd[VPT];
+        float scl[NV];
+        GroupDivisor gd[NV];
         bool fast = true;
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
+        for (int k = 0; k < NV; ++k) {
             scl[k] = div448(__uint_as_float(am[k] << 16));
             gd[k] = make_group_divisor(am[k] ? scl[k] : 1.0f);   // all-zero group: codes of +-0
             fast = fast && gd[k].fast;
@@ -301,8 +327,8 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
             const int64_t G = s.H >> 7;
             float *sc = (float *)s.out_scale;
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = k * tpr + t;
+            for (int k = 0; k < NV; ++k) {
+                const int v = (kb + k) * tpr + t;
                 if (GUARD && v >= nvec)
                     continue;                // padding of the team shape (whole groups)
                 const int64_t g = v >> 4;
@@ -313,8 +339,8 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         }
         uint2 *qrow = reinterpret_cast<uint2 *>(s.out_q + row * (int64_t)s.H);
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * tpr + t;   // vector index in the row
+        for (int k = 0; k < NV; ++k) {
+            const int v = (kb + k) * tpr + t;   // vector index in the row
             if (GUARD && v >= nvec)
                 continue;
             const uint32_t yw[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
@@ -333,8 +359,8 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
         }
     } else {
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * tpr + t;   // vector index in the row
+        for (int k = 0; k < NV; ++k) {
+            const int v = (kb + k) * tpr + t;   // vector index in the row
             if (GUARD && v >= nvec)
                 continue;                // padding of the team shape (whole groups)
             const uint32_t yw[4] = {y[k].x, y[k].y, y[k].z, y[k].w};
@@ -358,15 +384,18 @@ __device__ __forceinline__ void row_finish(const Seg &s, int64_t row, int t, int
 
 // Load (and add) one row from global memory, write the residual, finish it.
 // LAT (latency form): gamma is loaded together with the row, so that its
-// load latency overlaps the row's instead of following the reduction.
-template <int VPT, int TPR, bool MX, bool LAT = false>
+// load latency overlaps the row's instead of following the reduction. SPLIT
+// (latency form only): this block owns part `part` of the row's outputs,
+// residual included, but loads and adds the whole row for its sum of squares.
+template <int VPT, int TPR, bool MX, bool LAT = false, int SPLIT = 1>
 __device__ __forceinline__ void row_from_global(const Seg &s, int64_t row, int t, int team, int parity,
-                                                RedSmem &red)
+                                                RedSmem &red, int part = 0)
 {
     constexpr bool GUARD = TPR == 0;
+    constexpr int NV = VPT / SPLIT;
     const int tpr = TPR ? TPR : s.tpr;
     const int nvec = TPR ? TPR * VPT : (s.H >> 3);
-    uint4 r[VPT], g[VPT];
+    uint4 r[VPT], g[NV];
     const uint4 *xr = s.x + row * s.ldx_v + t;
     // vectors past the row end (padded team shapes) read as zero and are
     // never stored; they add nothing to the sum of squares
@@ -383,7 +412,8 @@ __device__ __forceinline__ void row_from_global(const Seg &s, int64_t row, int t
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             r[k] = add_bf16x8(xv[k], rv[k]);
-            if ((!GUARD || k * tpr + t < nvec) && RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && k * tpr + t < nvec))
+            if ((SPLIT == 1 || k / NV == part) && (!GUARD || k * tpr + t < nvec) &&
+                RMSQ_IN_BOUNDS(s.debug_flag, row < s.M && k * tpr + t < nvec))
                 orow[k * tpr] = r[k];
         }
     } else {
@@ -395,10 +425,13 @@ __device__ __forceinline__ void row_from_global(const Seg &s, int64_t row, int t
     }
     if constexpr (LAT) {
 #pragma unroll
-        for (int k = 0; k < VPT; ++k)
-            g[k] = (!GUARD || k * tpr + t < nvec) ? ld_keep(s.gamma + k * tpr + t) : make_uint4(0, 0, 0, 0);
-        row_finish<VPT, TPR, MX, GAMMA_REGS, true>(s, row, t, team, parity, red, r, s.gamma, g);
+        for (int k = 0; k < NV; ++k) {
+            const int vk = (part * NV + k) * tpr + t;
+            g[k] = (!GUARD || vk < nvec) ? ld_keep(s.gamma + vk) : make_uint4(0, 0, 0, 0);
+        }
+        row_finish<VPT, TPR, MX, GAMMA_REGS, true, SPLIT>(s, row, t, team, parity, red, r, s.gamma, g, part);
     } else {
+        static_assert(SPLIT == 1, "split rows exist in the latency form only");
         row_finish<VPT, TPR, MX, GAMMA_GLOBAL>(s, row, t, team, parity, red, r, s.gamma, g);
     }
 }

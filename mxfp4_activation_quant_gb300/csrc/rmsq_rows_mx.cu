@@ -3,7 +3,7 @@
 
 namespace rmsq {
 
-cudaError_t launch_rows_mx(int vpt, int tpr_static, bool lat, const LaunchParams &p, int grid, int threads,
+cudaError_t launch_rows_mx(int vpt, int tpr_static, int lat, const LaunchParams &p, int grid, int threads,
                             cudaStream_t st)
 {
     return launch_rows_impl<true>(vpt, tpr_static, lat, p, grid, threads, st);

@@ -39,11 +39,11 @@ _f = ctypes.c_float
 class LaunchOpts(ctypes.Structure):
     """Mirror of ``rmsq_launch_opts``."""
     _fields_ = [("kernel", _i32), ("vpt", _i32), ("rows_per_block", _i32), ("grid", _i32),
-                ("debug_skip_row", _i64), ("wait_limit_ns", _i64), ("form", _i32)]
+                ("debug_skip_row", _i64), ("wait_limit_ns", _i64), ("form", _i32), ("split", _i32)]
 
     def __init__(self, kernel=KERNEL_AUTO, vpt=0, rows_per_block=0, grid=0, debug_skip_row=-1,
-                 wait_limit_ns=0, form=FORM_AUTO):
-        super().__init__(kernel, vpt, rows_per_block, grid, debug_skip_row, wait_limit_ns, form)
+                 wait_limit_ns=0, form=FORM_AUTO, split=0):
+        super().__init__(kernel, vpt, rows_per_block, grid, debug_skip_row, wait_limit_ns, form, split)
 
 
 class GemmOpts(ctypes.Structure):

@@ -156,11 +156,11 @@ def test_qknorm_rejects_bad_arguments(L):
 
 
 def test_launch_opts_layout_matches_header():
-    # int32 kernel, vpt, rows_per_block, grid; int64 debug_skip_row, wait_limit_ns; int32 form
-    # (padded to the struct's 8-byte alignment)
+    # int32 kernel, vpt, rows_per_block, grid; int64 debug_skip_row, wait_limit_ns; int32 form, split
     assert ctypes.sizeof(rmsq.LaunchOpts) == 40
     assert rmsq.LaunchOpts.debug_skip_row.offset == 16
     assert rmsq.LaunchOpts.form.offset == 32
+    assert rmsq.LaunchOpts.split.offset == 36
 
 
 def test_host_tensors_are_refused():

@@ -569,15 +569,18 @@ def test_wide_range_rows_fp64_path(oracle_mod, H):
 
 # ------------------------------------------- latency form of the row kernel
 
-@pytest.mark.parametrize("name,M", [("decode", None), ("decode", 1), ("decode", 152), ("prefill", 2000),
-                                    ("mxfp4", 64)])
-def test_latency_form_is_bit_identical(oracle_mod, name, M):
+@pytest.mark.parametrize("name,M,split", [("decode", None, 0), ("decode", None, 1), ("decode", None, 2),
+                                          ("decode", 1, 4), ("decode", 37, 4), ("decode", 152, 0),
+                                          ("prefill", 2000, 1), ("prefill", 300, 2), ("mxfp4", 64, 2),
+                                          ("mxfp4", 5, 4)])
+def test_latency_form_is_bit_identical(oracle_mod, name, M, split):
     """The latency form (gamma loaded with the row, every warp finalising
-    inv_rms) against the throughput form: every output bit-identical, and
-    both against the oracle."""
+    inv_rms; with split > 1 each row's outputs shared by that many blocks,
+    each reducing the whole row) against the throughput form: every output
+    bit-identical, and both against the oracle."""
     w = synth.WORKLOADS[name]
     d = synth.make_inputs(w, M=M)
-    lat = rmsq.LaunchOpts(kernel=rmsq.KERNEL_ROWS, form=rmsq.FORM_LATENCY)
+    lat = rmsq.LaunchOpts(kernel=rmsq.KERNEL_ROWS, form=rmsq.FORM_LATENCY, split=split)
     thr = rmsq.LaunchOpts(kernel=rmsq.KERNEL_ROWS, form=rmsq.FORM_THROUGHPUT)
     if w.kind == "fp8":
         a = run_fp8(d, w.eps, layout=w.scale_layout, keep=True, opts=lat)
@@ -592,8 +595,13 @@ def test_latency_form_is_bit_identical(oracle_mod, name, M):
         assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), k
 
 
-def test_unknown_form_is_refused():
+def test_unknown_form_and_bad_split_are_refused():
     w = synth.WORKLOADS["decode"]
     g = _gpu(synth.make_inputs(w, M=4))
     with pytest.raises(rmsq.RmsqError, match="form"):
         rmsq.add_rmsnorm_quant_fp8(g["x"], g["gamma"], g["residual"], opts=rmsq.LaunchOpts(form=7))
+    with pytest.raises(rmsq.RmsqError, match="split"):
+        rmsq.add_rmsnorm_quant_fp8(g["x"], g["gamma"], g["residual"], opts=rmsq.LaunchOpts(split=3))
+    with pytest.raises(rmsq.RmsqError, match="split"):     # the throughput form does not split rows
+        rmsq.add_rmsnorm_quant_fp8(g["x"], g["gamma"], g["residual"],
+                                   opts=rmsq.LaunchOpts(form=rmsq.FORM_THROUGHPUT, split=2))
