@@ -820,8 +820,8 @@ rmsq_status plan_gemm(bool prequant, int64_t M, int64_t N, int64_t K, const rmsq
     if (pair && !o.bn) {
         // Pair tile width: the one whose busiest pair does the least work,
         // counting a 192-wide tile as 0.75 of a 256-wide one and charging it
-        // 4 % for its lower efficiency per column (measured: 12.8 against
-        // 12.3 us per 256-column unit at N = 2112, K = 7168).
+        // 15 % for its lower efficiency per column (measured at N = 2112,
+        // K = 7168, 8192 tokens: 51.6 against 44.8 ns per column and pair).
         const int cap256 = pair_caps(256), cap192 = pair_caps(192);
         if (cap256 <= 0 || cap192 <= 0)
             return failf(caps_status,
@@ -829,7 +829,7 @@ rmsq_status plan_gemm(bool prequant, int64_t M, int64_t N, int64_t K, const rmsq
         const int64_t mt2 = (M + 255) / 256;
         const int64_t w256 = (mt2 * ((N + 255) / 256) + cap256 - 1) / cap256 * 256;
         const int64_t w192 = (mt2 * ((N + 191) / 192) + cap192 - 1) / cap192 * 192;
-        bn = w192 * 104 < w256 * 100 ? 192 : 256;
+        bn = w192 * 115 < w256 * 100 ? 192 : 256;
     }
     else if (o.schedule == 2) {
         if (prequant || ksplit != 1)

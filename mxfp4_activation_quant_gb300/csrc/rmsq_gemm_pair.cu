@@ -19,14 +19,23 @@ namespace gemm {
 // both. The MMA commits arrive on both CTAs' `empty` and `accum` barriers;
 // both epilogues (their own 128 rows, in their own tensor memory) arrive on
 // the even CTA's `tmem_empty`.
-// BN = 256: one accumulator, six ring stages. BN = 192: two accumulators
-// (the MMAs of the next tile run while the epilogue drains the last) and five
-// stages; 2 x 192 accumulator columns leave room for five stages' scale
-// factors. Each stage's scale factors keep their own tensor-memory slot, so
+// BN = 256: one accumulator. BN = 192: two accumulators (the MMAs of the
+// next tile run while the epilogue drains the last); 2 x 192 accumulator
+// columns leave room for five stages' scale factors. Both take five ring
+// stages: a sixth does not fit the shared memory next to the eight epilogue
+// warps' staging (and with half the staging per warp, six stages measured
+// 47.6 against 45.9 us). Each stage's scale factors keep their own tensor-memory slot, so
 // a slot is free again when the producer may refill the stage. (A separate
 // ring of five slots under seven stages, where the MMA warp waited for the
 // commit of stage g - 5 before reusing a slot, starved the tensor pipe:
 // 64.4 us at M = 8192 against 48.2 us.)
+// Eight epilogue warps (two per lane quarter of tensor memory, each with half
+// of the tile's columns) load all of their accumulator columns before their
+// first store and hand the accumulator back at once, so with a single
+// accumulator the next tile's MMAs wait only for those loads: at M = 8192,
+// N = 2112, K = 7168 the 256-wide tile went from 49.3 us (four epilogue warps,
+// release after the last of eight interleaved load/store rounds, six stages)
+// to 45.9 us, past the 192-wide tile's 48.2 us.
 // Stage shape measured on GB300 (BN = 256, N = 2112, K = 7168, M = 8192): one
 // span x six stages 50.7 us, one x five 51.6 us, two spans x three 56.2 us.
 template <int BN_>
@@ -37,12 +46,15 @@ struct PairCfg {
     static constexpr int kSpanB = kRowsB * kSpanBytes;
     static constexpr int kStage = kSpanA + kSpanB;     // one span of K per stage
     static constexpr int kSfbAtoms = 2;                // 128-row scale tiles of B a tile touches
-    static constexpr int kStages = BN == 256 ? 6 : 5;
+    static constexpr int kStages = 5;
     static constexpr int kAcc = BN == 256 ? 1 : 2;     // accumulators in tensor memory
     static constexpr int kOffSfa = kStages * kStage;
     static constexpr int kOffSfb = kOffSfa + kStages * 1024;
     static constexpr int kOffOut = kOffSfb + kStages * kSfbAtoms * 1024;
-    static constexpr int kOutBytes = 4 * 2048;         // each epilogue warp: 32 rows x 64 bytes of D
+    static constexpr int kEpiWarps = 8;                // warps 4..11
+    static constexpr int kThreads = 32 * (4 + kEpiWarps);
+    static constexpr int kChunks = BN / 64;            // 32-column chunks of D per epilogue warp
+    static constexpr int kOutBytes = kEpiWarps * 2048; // each epilogue warp: 32 rows x 64 bytes of D
     static constexpr int kOffBar = kOffOut + kOutBytes;
     static constexpr int kBarBytes = (2 * kStages + 2 * kAcc + 1) * 8 + 16;
     static constexpr size_t kSmem = 1024 + kOffBar + kBarBytes;
@@ -55,7 +67,7 @@ struct PairCfg {
 };
 
 template <int BN>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(PairCfg<BN>::kThreads, 1)
     mxfp4_gemm_pair_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap map_a,
                            const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_sfa,
                            const __grid_constant__ CUtensorMap map_sfb)
@@ -98,7 +110,8 @@ __global__ void __launch_bounds__(256, 1)
         }
         for (int a = 0; a < C::kAcc; ++a) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(accum + a)));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 8;" ::"r"(saddr(tmem_empty + a)));   // 4 warps x 2 CTAs
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(tmem_empty + a)),
+                         "r"(2 * C::kEpiWarps));   // the epilogue warps of both CTAs
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(drain)));
         *abort = 0;
@@ -212,11 +225,15 @@ __global__ void __launch_bounds__(256, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------- epilogue
-        // This CTA's 128 rows of the tile, 32 columns at a time, through
-        // shared memory so that each store instruction writes eight rows'
-        // whole 64-byte pieces (16-byte chunk j of row i at j ^ ((i/2) mod 4):
+        // Warp w reads tensor-memory lanes 32 (w % 4).. (32 of this CTA's
+        // rows) and column half (w - 4) / 4 of the tile: all of its chunks
+        // are loaded before the first store and the accumulator is handed
+        // back, then the chunks go to D through shared memory, 32 columns at
+        // a time, so that each store instruction writes eight rows' whole
+        // 64-byte pieces (16-byte piece j of row i at j ^ ((i / 2) mod 4):
         // conflict-free both ways).
-        const int q = warp & 3;
+        constexpr int NCH = C::kChunks;
+        const int q = warp & 3, half = (warp - 4) >> 2;
         uint8_t *const stage_w = smem + C::kOffOut + (warp - 4) * 2048;
         const int cj = lane & 3;
         int mt, nt;
@@ -226,18 +243,37 @@ __global__ void __launch_bounds__(256, 1)
                 break;
             tc_fence_after();
             const int64_t row0 = (int64_t)mt * 256 + kBM * (int)rank + q * 32, n0 = (int64_t)nt * BN;
-            const uint32_t trow = tmem + acc_slot * BN + ((uint32_t)(q * 32) << 16);
+            const int c_first = half * NCH;   // first 32-column chunk of this warp
+            const uint32_t trow = tmem + acc_slot * BN + ((uint32_t)(q * 32) << 16) + c_first * 32;
             const uint32_t tmem_empty_lead = cluster_addr(saddr(tmem_empty + acc_slot), 0);
-            // 32-column chunks of D this warp writes (warp-uniform; N is a multiple of 8)
-            const int nch = row0 < p.M ? (int)((min((int64_t)BN, p.N - n0) + 31) / 32) : 0;
-            auto store_chunk = [&](const uint32_t(&acc)[32], int c0) {
+            // chunks of this warp that hold columns < N (warp-uniform; N is a multiple of 8)
+            const int64_t cols_left = p.N - n0 - (int64_t)c_first * 32;
+            const int nch = row0 < p.M ? (int)max((int64_t)0, min((int64_t)NCH, (cols_left + 31) / 32)) : 0;
+            uint32_t acc[NCH][32];
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+                if (c < nch)
+                    tmem_ld32_issue(trow + c * 32, acc[c]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+                tmem_hold(acc[c]);
+            // the accumulator may now be overwritten by the next tile's MMAs
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(tmem_empty_lead);
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                if (c >= nch)
+                    continue;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     uint4 o;
-                    o.x = pack_bf16x2(__uint_as_float(acc[8 * j + 0]), __uint_as_float(acc[8 * j + 1]));
-                    o.y = pack_bf16x2(__uint_as_float(acc[8 * j + 2]), __uint_as_float(acc[8 * j + 3]));
-                    o.z = pack_bf16x2(__uint_as_float(acc[8 * j + 4]), __uint_as_float(acc[8 * j + 5]));
-                    o.w = pack_bf16x2(__uint_as_float(acc[8 * j + 6]), __uint_as_float(acc[8 * j + 7]));
+                    o.x = pack_bf16x2(__uint_as_float(acc[c][8 * j + 0]), __uint_as_float(acc[c][8 * j + 1]));
+                    o.y = pack_bf16x2(__uint_as_float(acc[c][8 * j + 2]), __uint_as_float(acc[c][8 * j + 3]));
+                    o.z = pack_bf16x2(__uint_as_float(acc[c][8 * j + 4]), __uint_as_float(acc[c][8 * j + 5]));
+                    o.w = pack_bf16x2(__uint_as_float(acc[c][8 * j + 6]), __uint_as_float(acc[c][8 * j + 7]));
                     *reinterpret_cast<uint4 *>(stage_w + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = o;
                 }
                 __syncwarp();
@@ -245,49 +281,11 @@ __global__ void __launch_bounds__(256, 1)
                 for (int it = 0; it < 4; ++it) {
                     const int rr = it * 8 + (lane >> 2);
                     const uint4 v = *reinterpret_cast<const uint4 *>(stage_w + rr * 64 + ((cj ^ ((rr >> 1) & 3)) << 4));
-                    const int64_t gm = row0 + rr, gn = n0 + c0 + cj * 8;
+                    const int64_t gm = row0 + rr, gn = n0 + (c_first + c) * 32 + cj * 8;
                     if (gm < p.M && gn < p.N && RMSQ_IN_BOUNDS(p.status, gn + 8 <= p.N))
                         *reinterpret_cast<uint4 *>(p.d + gm * p.ldd + gn) = v;
                 }
                 __syncwarp();
-            };
-            // the accumulator may be overwritten by the MMAs of a later tile
-            // once this warp's last tensor-memory load is complete
-            auto release = [&]() {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive_cluster(tmem_empty_lead);
-            };
-            // Chunk c + 1 is loaded from tensor memory while chunk c goes to D.
-            uint32_t a[32], b[32];
-            if (nch > 0) {
-                tmem_ld32_issue(trow, a);
-                tmem_ld_wait();
-                tmem_hold(a);
-            } else {
-                release();
-            }
-#pragma unroll 1
-            for (int c = 0; c < nch; c += 2) {
-                if (c + 1 < nch)
-                    tmem_ld32_issue(trow + (c + 1) * 32, b);
-                else
-                    release();
-                store_chunk(a, c * 32);
-                if (c + 1 < nch) {
-                    tmem_ld_wait();
-                    tmem_hold(b);
-                    if (c + 2 < nch)
-                        tmem_ld32_issue(trow + (c + 2) * 32, a);
-                    else
-                        release();
-                    store_chunk(b, (c + 1) * 32);
-                    if (c + 2 < nch) {
-                        tmem_ld_wait();
-                        tmem_hold(a);
-                    }
-                }
             }
         }
     }
@@ -331,7 +329,7 @@ int pair_capacity_t(int dev)
             return 0;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2, 1, 1);
-        cfg.blockDim = dim3(256, 1, 1);
+        cfg.blockDim = dim3(C::kThreads, 1, 1);
         cfg.dynamicSmemBytes = C::kSmem;
         cudaLaunchAttribute cl[1];
         cl[0].id = cudaLaunchAttributeClusterDimension;
@@ -386,7 +384,7 @@ cudaError_t launch_pair_t(const GemmLaunch &g, cudaStream_t st)
     const int pairs = (int)(tiles < cap ? tiles : cap);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute cl[1];

@@ -43,10 +43,12 @@ def raw_plan(L, M, n, k, opts, prequant=0, sms=SMS, pairs=(PAIRS, PAIRS)):
     # ... 128-row tiles from two row tiles of A on, K split to fill the SMs ...
     (False, 256, (128, 4, 1, 0)),
     (False, 512, (128, 2, 1, 0)),
-    # ... CTA pairs once 256-row tiles give half the SMs a tile: 256 x 256 at
-    # 2048 tokens, 256 x 192 at 8192 (fewer columns for the busiest pair)
+    # ... CTA pairs once 256-row tiles give half the SMs a tile, 256 x 256 tiles
+    # (the 192-wide tile's busiest pair has fewer columns at 8192 tokens, but
+    # not 15 % fewer)
     (False, 2048, (256, 1, 3, 0)),
-    (False, 8192, (192, 1, 3, 0)),
+    (False, 8192, (256, 1, 3, 0)),
+    (False, 16384, (256, 1, 3, 0)),
     # A in bf16 (quantised in the GEMM): 64-row tiles up to 16 tokens ...
     (True, 1, (64, 4, 1, 0)),
     (True, 16, (64, 4, 1, 0)),
@@ -78,10 +80,14 @@ def test_explicit_schedules(L):
 
 
 def test_pair_width_follows_the_capacity(L):
-    # the width is the one whose busiest pair does the least work: with room
-    # for 9 x 32 = 288 pairs of 256 x 256 at once, 256 wins at 8192 tokens
+    # the width is the one whose busiest pair does the least work, a 192-wide
+    # column charged 15 %: at 8192 tokens (9 x 32 = 288 tiles of 256 x 256,
+    # 11 x 32 = 352 of 256 x 192) 44 resident pairs give the busiest pair 7
+    # wide tiles (1792 columns) against 8 narrow ones (1536 x 1.15 = 1766)
+    assert plan(8192, pairs=(44, 44))[0] == 192
+    assert plan(8192, pairs=(48, 48))[0] == 256
     assert plan(8192, pairs=(288, 288))[0] == 256
-    assert plan(8192, pairs=(PAIRS, PAIRS))[0] == 192
+    assert plan(8192, pairs=(PAIRS, PAIRS))[0] == 256
 
 
 SHAPES_M = [1, 3, 16, 17, 100, 128, 129, 256, 257, 300, 1000, 2048, 8192, 16384]
