@@ -210,6 +210,17 @@ rmsq_status rmsq_mxfp4_gemm(
  * times the slowest launch measured on GB300 (the quantising GEMM at
  * M = 16384, N = 2112, K = 7168: about a millisecond; the GEMM on quantised
  * A: about 0.1 ms).
+ *
+ * Overlap with the norm + quant: the one-CTA-per-tile GEMM (the schedule the
+ * library picks below about 2048 tokens) is launched as a programmatic
+ * dependent of the kernel before it on the stream, and the norm + quant
+ * kernels let their dependents start early. Right after a norm + quant (or
+ * rmsq_add_rmsnorm) call on the same stream, the GEMM therefore sets up and
+ * loads B and its scale tiles while that call is still running, and waits
+ * for it to finish before it reads A (or the bf16 activation) and before it
+ * writes D. B and b_scale_tiles must not be outputs of that immediately
+ * preceding call. After any other kernel, the GEMM starts when that kernel
+ * has finished, as usual.
  */
 
 rmsq_status rmsq_a16wfp4_gemm(

@@ -277,6 +277,36 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                 atoms += (bt0 + t < p.b_row_tiles);
             const uint32_t span_tx = C::kSpanB + atoms * 1024u +
                                      (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kSpanBytes + C::kSfaSpan));
+            // B and its scales for stage j of this tile (one elected lane)
+            auto load_b = [&](int j, int s, int nsp, uint32_t fb) {
+                for (int sp = 0; sp < nsp; ++sp) {
+                    const int ks = ks0 + j * C::kSpans + sp;
+                    tma_2d(saddr(smem + s * C::kAB + sp * C::kSpanAB + C::kSpanA), &map_b, ks * kSpanBytes,
+                           (int)tn0, fb);
+                    for (int t = 0; t < C::kSfbAtoms; ++t)
+                        if (bt0 + t < p.b_row_tiles)
+                            bulk_g2s(saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan + t * 1024),
+                                     p.b_scale + ((int64_t)(bt0 + t) * (2 * KS) + 2 * ks) * 512, 1024, fb);
+                }
+            };
+            // The first tile's first stages are free from the start: their B
+            // loads (which do not depend on the kernel before this one) are
+            // issued before the wait for that kernel, their A loads after it.
+            int pre = 0;
+            if (!PREQUANT && ti == 0) {
+                pre = min(C::kStages, NST);
+                if (elect_one()) {
+                    for (int j = 0; j < pre; ++j) {
+                        if (j == p.debug_skip_stage)        // test hook: that stage never arrives
+                            continue;
+                        const int nsp = min(C::kSpans, KL - j * C::kSpans);
+                        mbar_arrive_tx(saddr(full + j), span_tx * nsp);
+                        load_b(j, j, nsp, saddr(full + j));
+                    }
+                }
+                __syncwarp();
+                grid_dep_wait();
+            }
             bool stop = false;
             for (int j = 0; j < NST; ++j, ++g) {
                 const int s = g % C::kStages;
@@ -288,21 +318,18 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                 if (g != p.debug_skip_stage && elect_one()) {   // test hook: that stage never arrives
                     const int nsp = min(C::kSpans, KL - j * C::kSpans);
                     const uint32_t fb = saddr(full + s);
-                    mbar_arrive_tx(fb, span_tx * nsp);
-                    for (int sp = 0; sp < nsp; ++sp) {
-                        const int ks = ks0 + j * C::kSpans + sp;
-                        uint8_t *a_dst = smem + s * C::kAB + sp * C::kSpanAB;
-                        if (!PREQUANT) {
-                            tma_2d(saddr(a_dst), &map_a, ks * kSpanBytes, (int)tm0, fb);
+                    if (j >= pre)
+                        mbar_arrive_tx(fb, span_tx * nsp);
+                    if (!PREQUANT) {
+                        for (int sp = 0; sp < nsp; ++sp) {
+                            const int ks = ks0 + j * C::kSpans + sp;
+                            tma_2d(saddr(smem + s * C::kAB + sp * C::kSpanAB), &map_a, ks * kSpanBytes, (int)tm0, fb);
                             bulk_g2s(saddr(smem + C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan),
                                      p.a_scale + ((int64_t)mt * (2 * KS) + 2 * ks) * 512, 1024, fb);
                         }
-                        tma_2d(saddr(a_dst + C::kSpanA), &map_b, ks * kSpanBytes, (int)tn0, fb);
-                        for (int t = 0; t < C::kSfbAtoms; ++t)
-                            if (bt0 + t < p.b_row_tiles)
-                                bulk_g2s(saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan + t * 1024),
-                                         p.b_scale + ((int64_t)(bt0 + t) * (2 * KS) + 2 * ks) * 512, 1024, fb);
                     }
+                    if (j >= pre)
+                        load_b(j, s, nsp, fb);
                 }
                 __syncwarp();
                 issued = g + 1;
@@ -382,6 +409,7 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
         const int c_lo = (PREQUANT && warp >= 8) ? BN / 2 : 0;
         const int c_hi = (PREQUANT && warp < 8) ? BN / 2 : BN;
         bool ok = true;
+        grid_dep_wait();    // before reading A (prequant) or writing D
         if (PREQUANT)
             ok = prequant_loop<BN>(p, m0, R, ks0, KL, smem, full, empty, abort);
         // ------------------------------------------------------- epilogue
@@ -482,6 +510,7 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
         // share of the tile's (row, 4-column) units over the cluster's
         // partials in rank order 0, 1, ... (deterministic), then rounds to bf16.
         cluster_sync();
+        grid_dep_wait();    // every thread of the CTA writes D here
         const int units = R * (BN / 4);
         const int u0 = (int)((int64_t)units * kz / p.ksplit), u1 = (int)((int64_t)units * (kz + 1) / p.ksplit);
         for (int u = u0 + (int)threadIdx.x; u < u1; u += (int)blockDim.x) {
@@ -584,28 +613,33 @@ cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUte
             return e;
         attr[dev].store(true, std::memory_order_release);
     }
-    if (p.persistent) {     // one CTA per SM walks the tiles
-        mxfp4_gemm_kernel<BN, PRE><<<dim3(persistent_ctas, 1, 1), gemm_threads<PRE>(), C::kSmem, st>>>(p, ma, mb);
-        return cudaGetLastError();
-    }
-    if (p.ksplit == 1) {
-        mxfp4_gemm_kernel<BN, PRE><<<dim3(n_tiles, m_tiles, 1), gemm_threads<PRE>(), C::kSmem, st>>>(p, ma, mb);
-        return cudaGetLastError();
-    }
-    // the CTAs that split one tile's K form a cluster (they exchange partial
-    // sums through distributed shared memory)
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: the CTAs may start, set up and load B while that kernel (the
+    // fused norm + quant) finishes; griddepcontrol.wait in the kernel holds
+    // back every read of A and write of D until it has.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_tiles, m_tiles, p.ksplit);
     cfg.blockDim = dim3(gemm_threads<PRE>(), 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
-    cudaLaunchAttribute cl[1];
-    cl[0].id = cudaLaunchAttributeClusterDimension;
-    cl[0].val.clusterDim.x = 1;
-    cl[0].val.clusterDim.y = 1;
-    cl[0].val.clusterDim.z = (unsigned)p.ksplit;
-    cfg.attrs = cl;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
     cfg.numAttrs = 1;
+    if (p.persistent) {     // one CTA per SM walks the tiles
+        cfg.gridDim = dim3(persistent_ctas, 1, 1);
+    } else if (p.ksplit == 1) {
+        cfg.gridDim = dim3(n_tiles, m_tiles, 1);
+    } else {
+        // the CTAs that split one tile's K form a cluster (they exchange
+        // partial sums through distributed shared memory)
+        cfg.gridDim = dim3(n_tiles, m_tiles, p.ksplit);
+        at[1].id = cudaLaunchAttributeClusterDimension;
+        at[1].val.clusterDim.x = 1;
+        at[1].val.clusterDim.y = 1;
+        at[1].val.clusterDim.z = (unsigned)p.ksplit;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, mxfp4_gemm_kernel<BN, PRE>, p, ma, mb);
 }
 

@@ -317,6 +317,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
     tmem_hold(r);
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// A GEMM launched as a programmatic dependent of the kernel before it in the
+// stream (the fused norm + quant) may start while that kernel still runs:
+// every thread waits here before its first read of memory the previous
+// kernel writes (A) and before its first write of D. Without the launch
+// attribute the previous kernel has finished and the wait returns at once.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------- cluster (split K)
 
 __device__ __forceinline__ void cluster_sync()

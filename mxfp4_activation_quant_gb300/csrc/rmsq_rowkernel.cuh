@@ -52,6 +52,10 @@ template <int VPT, int TPR, bool MX, int LAT>
 __global__ void __launch_bounds__(kMaxThreads) rows_kernel(const __grid_constant__ LaunchParams p)
 {
     __shared__ RedSmem red;
+    // A kernel launched after this one as a programmatic dependent (the
+    // consumer GEMM) may be scheduled from now on; it waits for this grid's
+    // completion before it reads what this grid writes.
+    asm volatile("griddepcontrol.launch_dependents;");
     block_rows<VPT, TPR, MX, LAT>(p.seg[0], blockIdx.x, red);
 }
 

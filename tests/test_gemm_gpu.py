@@ -497,3 +497,72 @@ def test_default_wait_limit_is_far_above_the_runtime():
     print(f"slowest launch {worst * 1e3:.3f} ms against the 2 s wait limit")
     assert worst < 2.0 / 200
     assert rmsq.sync_status() == 0
+
+
+@pytest.mark.parametrize("M,pre", [(4, False), (64, False), (300, False), (4, True), (64, True)])
+def test_gemm_after_the_quant_reads_its_output(M, pre):
+    """The single-CTA GEMM is launched as a programmatic dependent of the
+    kernel before it: right after the fused norm + quant (or the norm alone,
+    for the prequant GEMM) on the same stream, with no synchronisation, it
+    may start early but must read that call's activation, never what the
+    buffers held before. Six different activations through the same buffers,
+    back to back and inside a CUDA graph, each against a synchronised run."""
+    K, N = 7168, 2112
+    b_q, b_s = synth.mxfp4_weights(22, N, K)
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    ins = [_pipeline_inputs(M, K, 200 + i)[0] for i in range(6)]
+    x = torch.empty_like(ins[0]["x"])
+    res = torch.empty_like(ins[0]["residual"])
+    gamma = ins[0]["gamma"]
+    q = torch.empty((M, K // 2), dtype=torch.uint8, device=DEV)
+    t = torch.zeros(rmsq.mma_scale_bytes(M, K), dtype=torch.uint8, device=DEV)
+    y = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    ro = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+
+    def step():
+        if pre:
+            rmsq.add_rmsnorm(x, gamma, res, out=y, out_residual=ro)
+            rmsq.a16wfp4_gemm(y, gb, tb, out=d)
+        else:
+            rmsq.add_rmsnorm_quant_mxfp4_mma_scales_into(x, gamma, res, q, t, ro)
+            rmsq.mxfp4_gemm(q, t, gb, tb, out=d)
+
+    refs = []
+    for inp in ins:                      # synchronised between the two kernels
+        x.copy_(inp["x"])
+        res.copy_(inp["residual"])
+        if pre:
+            rmsq.add_rmsnorm(x, gamma, res, out=y, out_residual=ro)
+            torch.cuda.synchronize()
+            refs.append(rmsq.a16wfp4_gemm(y, gb, tb).clone())
+        else:
+            rmsq.add_rmsnorm_quant_mxfp4_mma_scales_into(x, gamma, res, q, t, ro)
+            torch.cuda.synchronize()
+            refs.append(rmsq.mxfp4_gemm(q, t, gb, tb).clone())
+        torch.cuda.synchronize()
+    outs = []
+    for inp in ins:                      # back to back on one stream
+        x.copy_(inp["x"])
+        res.copy_(inp["residual"])
+        step()
+        outs.append(d.clone())
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(zip(outs, refs)):
+        assert torch.equal(a, b), f"activation {i}, back to back"
+    side = torch.cuda.Stream(DEV)        # the same pair replayed from a CUDA graph
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            step()
+        for i, inp in enumerate(ins):
+            x.copy_(inp["x"])
+            res.copy_(inp["residual"])
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(d, refs[i]), f"activation {i}, graph replay"
+    torch.cuda.current_stream().wait_stream(side)
+    assert rmsq.sync_status() == 0
