@@ -605,3 +605,38 @@ def test_unknown_form_and_bad_split_are_refused():
     with pytest.raises(rmsq.RmsqError, match="split"):     # the throughput form does not split rows
         rmsq.add_rmsnorm_quant_fp8(g["x"], g["gamma"], g["residual"],
                                    opts=rmsq.LaunchOpts(form=rmsq.FORM_THROUGHPUT, split=2))
+
+
+# ------------------------------------- calls that read the previous call's outputs
+
+@pytest.mark.parametrize("M,kind", [(64, "fp8"), (8192, "fp8"), (37, "mx"), (3000, "mx")])
+def test_chained_calls_read_the_previous_outputs(M, kind):
+    """Each norm + quant call may start before the kernel ahead of it on the
+    stream has finished, and waits for it before touching memory. A chain of
+    six calls in which each reads what the previous one wrote -- the residual
+    updated in place, the next x being the previous y -- without
+    synchronisation must equal the same chain synchronised after every
+    call."""
+    H = 7168
+    x0 = synth.random_bf16(90 + M, (M, H)).to(DEV)
+    res0 = synth.random_bf16(91 + M, (M, H), var=4.0, tensor="residual").to(DEV)
+    gamma = synth.gaussian_bf16(92, "gamma", (H,), mean=1.0, var=0.1).to(DEV)
+
+    def chain(sync):
+        x, res, outs = x0, res0.clone(), []
+        for _ in range(6):
+            if kind == "fp8":
+                (y, q, s), _ = rmsq.add_rmsnorm_quant_fp8(x, gamma, res, keep_bf16=True, out_residual=res)
+            else:
+                (y, q, s), _ = rmsq.add_rmsnorm_quant_mxfp4(x, gamma, res, keep_bf16=True, out_residual=res)
+            if sync:
+                torch.cuda.synchronize()
+            outs.append((y, q, s, res.clone()))
+            x = y
+        torch.cuda.synchronize()
+        return outs
+
+    want, got = chain(True), chain(False)
+    for i, (a, b) in enumerate(zip(got, want)):
+        for u, v in zip(a, b):
+            assert torch.equal(u.view(torch.uint8), v.view(torch.uint8)), f"call {i}"
