@@ -450,7 +450,12 @@ class L2Flush:
         self.total = self.buf.sum()
         # then keep the GPU busy (~0.1 ms spin) while the host enqueues the
         # timed call, so that the call's events do not measure host latency
-        torch.cuda._sleep(200_000)
+        # (torch's private spin kernel; without it, a second read of the
+        # buffer does the same)
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(200_000)
+        else:
+            self.total = self.buf.sum()
 
 
 def time_launches_cold(fn, steps: int, stream, flush) -> tuple[float, list[float]]:
