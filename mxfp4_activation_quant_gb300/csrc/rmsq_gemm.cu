@@ -77,9 +77,13 @@ struct GemmCfg {
     static constexpr int kTmemCols = pow2_at_least(BN + kStages * kSfCols);
     static constexpr int kOffSfa = kStages * kAB;
     static constexpr int kOffSfb = kOffSfa + kStages * kSpans * kSfaSpan;
-    // plain GEMM: each epilogue warp stages 32 rows x 128 bytes of D here
+    // plain GEMM: each epilogue warp stages 32 rows x kStoreCols columns of D
+    // here. 64-row tiles stage 32 columns (64-byte pieces of rows), so that
+    // the CTA's shared memory leaves room on its SM for a block of the norm +
+    // quant kernel it is launched behind (both then run at once).
+    static constexpr int kStoreCols = BN == 64 ? 32 : 64;
     static constexpr int kOffOut = kOffSfb + kStages * kSpans * kSfbSpan;
-    static constexpr int kOutBytes = PRE ? 0 : 4 * 2 * 2048;
+    static constexpr int kOutBytes = PRE ? 0 : 4 * 32 * kStoreCols * 2;
     static constexpr int kOffBar = kOffOut + kOutBytes;
     static constexpr int kBarBytes = (2 * kStages + 3) * 8 + 16;
     static constexpr size_t kSmem = 1024 + kOffBar + kBarBytes;
@@ -414,7 +418,7 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
             ok = prequant_loop<BN>(p, m0, R, ks0, KL, smem, full, empty, abort);
         // ------------------------------------------------------- epilogue
         // plain GEMM: this warp's staging rows for the stores of D
-        uint8_t *const stage_w = smem + C::kOffOut + (warp - 4) * 4096;
+        uint8_t *const stage_w = smem + C::kOffOut + (warp - 4) * (32 * C::kStoreCols * 2);
         int mt, nt;
         for (int ti = 0; ok && tile_at(ti, mt, nt); ++ti) {
             if (!warp_wait(saddr(accum), (uint32_t)(ti & 1), abort, p))
@@ -429,36 +433,43 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
             // operand ring is free now), padded rows against bank conflicts
             float *red = (float *)smem + r * (BN + 4);
             if (!PREQUANT && p.ksplit == 1) {
-                // Stores of D, 64 columns at a time: each lane holds its row's
-                // 128 bytes; they pass through shared memory (16-byte chunk j
-                // of row i at j ^ (i mod 8): no bank conflicts either way) so
-                // that every store instruction writes four whole 128-byte
-                // lines of D (eight lanes per row) instead of 32 rows' pieces.
+                // Stores of D, SC columns at a time: each lane holds its row's
+                // SC * 2 bytes; they pass through shared memory (16-byte piece j
+                // of row i at j ^ swz(i): no bank conflicts either way) so that
+                // every store instruction writes whole pieces of 32 / V rows
+                // (four 128-byte lines, or eight rows' 64 bytes) instead of 32
+                // rows' 16 bytes.
+                constexpr int SC = C::kStoreCols;   // 64 or 32
+                constexpr int V = SC / 8;           // 16-byte pieces per staged row
+                constexpr int RPI = 32 / V;         // rows per store instruction
+                auto swz = [](int i) { return V == 8 ? (i & 7) : ((i >> 1) & 3); };
                 const int64_t row0 = tm0 + q * 32;
-                const int cj = lane & 7;
+                const int cj = lane % V;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN && row0 < p.M && tn0 + c0 < p.N; c0 += 64) {   // warp-uniform
+                for (int c0 = 0; c0 < BN && row0 < p.M && tn0 + c0 < p.N; c0 += SC) {   // warp-uniform
                     uint32_t lo[32], hi[32];
                     tmem_ld32_issue(trow + c0, lo);
-                    tmem_ld32_issue(trow + c0 + 32, hi);
+                    if (SC == 64)
+                        tmem_ld32_issue(trow + c0 + 32, hi);
                     tmem_ld_wait();
                     tmem_hold(lo);
-                    tmem_hold(hi);
+                    if (SC == 64)
+                        tmem_hold(hi);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < V; ++j) {
                         const uint32_t *a = j < 4 ? lo + 8 * j : hi + 8 * (j - 4);
                         uint4 o;
                         o.x = pack_bf16x2(__uint_as_float(a[0]), __uint_as_float(a[1]));
                         o.y = pack_bf16x2(__uint_as_float(a[2]), __uint_as_float(a[3]));
                         o.z = pack_bf16x2(__uint_as_float(a[4]), __uint_as_float(a[5]));
                         o.w = pack_bf16x2(__uint_as_float(a[6]), __uint_as_float(a[7]));
-                        *reinterpret_cast<uint4 *>(stage_w + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
+                        *reinterpret_cast<uint4 *>(stage_w + lane * (2 * SC) + ((j ^ swz(lane)) << 4)) = o;
                     }
                     __syncwarp();
 #pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int rr = it * 4 + (lane >> 3);
-                        const uint4 v = *reinterpret_cast<const uint4 *>(stage_w + rr * 128 + ((cj ^ (rr & 7)) << 4));
+                    for (int it = 0; it < V; ++it) {
+                        const int rr = it * RPI + lane / V;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(stage_w + rr * (2 * SC) + ((cj ^ swz(rr)) << 4));
                         const int64_t gm = row0 + rr, gn = tn0 + c0 + cj * 8;
                         if (gm < p.M && gn < p.N && RMSQ_IN_BOUNDS(p.status, gn + 8 <= p.N))
                             *reinterpret_cast<uint4 *>(p.d + gm * p.ldd + gn) = v;
@@ -466,33 +477,51 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                     __syncwarp();                // the rows are read before they are overwritten
                 }
             }
+            // split K / prequant: 32-column chunks, two per wait for the
+            // tensor-memory loads in the plain GEMM (the prequant kernel keeps
+            // to one, which holds its registers at 128 a thread: its CTA then
+            // fits on an SM beside a block of the norm kernel it follows)
+            constexpr int kStep = PREQUANT ? 32 : 64;
 #pragma unroll 1
-            for (int c0 = c_lo; c0 < c_hi && (PREQUANT || p.ksplit > 1); c0 += 32) {
-                uint32_t acc[32];
-                tmem_ld32(trow + c0, acc);
-                if (p.ksplit > 1) {
-                    if (r < tR) {
+            for (int c0 = c_lo; c0 < c_hi && (PREQUANT || p.ksplit > 1); c0 += kStep) {
+                const bool two = kStep == 64 && c0 + 32 < c_hi;   // warp-uniform
+                uint32_t acc2[2][32];
+                tmem_ld32_issue(trow + c0, acc2[0]);
+                if (two)
+                    tmem_ld32_issue(trow + c0 + 32, acc2[1]);
+                tmem_ld_wait();
+                tmem_hold(acc2[0]);
+                tmem_hold(acc2[1]);
 #pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            *reinterpret_cast<float4 *>(red + c0 + 4 * v) =
-                                make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
-                                            __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3]));
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && !two)
+                        continue;
+                    const int cc = c0 + 32 * h;
+                    const uint32_t(&acc)[32] = acc2[h];
+                    if (p.ksplit > 1) {
+                        if (r < tR) {
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                *reinterpret_cast<float4 *>(red + cc + 4 * v) =
+                                    make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
+                                                __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3]));
+                        }
+                        continue;
                     }
-                    continue;
-                }
-                const int64_t valid = p.N - (tn0 + c0);
-                if (r >= tR)
-                    continue;
+                    const int64_t valid = p.N - (tn0 + cc);
+                    if (r >= tR)
+                        continue;
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    if (valid >= 8 * (v + 1)) {
-                        uint4 o;
-                        o.x = pack_bf16x2(__uint_as_float(acc[8 * v + 0]), __uint_as_float(acc[8 * v + 1]));
-                        o.y = pack_bf16x2(__uint_as_float(acc[8 * v + 2]), __uint_as_float(acc[8 * v + 3]));
-                        o.z = pack_bf16x2(__uint_as_float(acc[8 * v + 4]), __uint_as_float(acc[8 * v + 5]));
-                        o.w = pack_bf16x2(__uint_as_float(acc[8 * v + 6]), __uint_as_float(acc[8 * v + 7]));
-                        if (RMSQ_IN_BOUNDS(p.status, m < p.M && tn0 + c0 + 8 * (v + 1) <= p.N))
-                            *reinterpret_cast<uint4 *>(drow + c0 + 8 * v) = o;
+                    for (int v = 0; v < 4; ++v) {
+                        if (valid >= 8 * (v + 1)) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(acc[8 * v + 0]), __uint_as_float(acc[8 * v + 1]));
+                            o.y = pack_bf16x2(__uint_as_float(acc[8 * v + 2]), __uint_as_float(acc[8 * v + 3]));
+                            o.z = pack_bf16x2(__uint_as_float(acc[8 * v + 4]), __uint_as_float(acc[8 * v + 5]));
+                            o.w = pack_bf16x2(__uint_as_float(acc[8 * v + 6]), __uint_as_float(acc[8 * v + 7]));
+                            if (RMSQ_IN_BOUNDS(p.status, m < p.M && tn0 + cc + 8 * (v + 1) <= p.N))
+                                *reinterpret_cast<uint4 *>(drow + cc + 8 * v) = o;
+                        }
                     }
                 }
             }
@@ -518,13 +547,21 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
             if (n0 + c >= p.N)
                 continue;
             const float *src = (const float *)smem + row * (BN + 4) + c;
-            float4 acc = ld_peer_f4(src, 0);
-            for (int z = 1; z < p.ksplit; ++z) {
-                const float4 v = ld_peer_f4(src, (uint32_t)z);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+            // all ranks' loads in flight before the first add (rank order kept)
+            float4 part[8];
+#pragma unroll
+            for (int z = 0; z < 8; ++z)
+                if (z < p.ksplit)
+                    part[z] = ld_peer_f4(src, (uint32_t)z);
+            float4 acc = part[0];
+#pragma unroll
+            for (int z = 1; z < 8; ++z) {
+                if (z < p.ksplit) {
+                    acc.x += part[z].x;
+                    acc.y += part[z].y;
+                    acc.z += part[z].z;
+                    acc.w += part[z].w;
+                }
             }
             if (RMSQ_IN_BOUNDS(p.status, m0 + row < p.M && n0 + c + 4 <= p.N))
                 *reinterpret_cast<uint2 *>(p.d + (m0 + row) * p.ldd + n0 + c) =

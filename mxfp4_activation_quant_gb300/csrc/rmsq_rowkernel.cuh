@@ -10,6 +10,8 @@
 // TPR / T0 / T1 = 0 means the team size is read at run time.
 #pragma once
 
+#include <atomic>
+
 #include "rmsq_rows.cuh"
 
 namespace rmsq {
@@ -80,31 +82,52 @@ __global__ void __launch_bounds__(kMaxThreads, 2) dual_kernel(const __grid_const
     X(3, 64)  /* H = 1536 */  \
     X(4, 16)  /* H = 512  */
 
+// The latency form: at most one block per SM, typically followed by a GEMM
+// launched as its programmatic dependent. The SMs its blocks occupy are asked
+// for the largest shared-memory carveout, so that the GEMM's CTAs (about
+// 220 KB of shared memory each) can start beside them instead of waiting for
+// the blocks to leave: an SM's carveout is set when an idle SM takes a block
+// and cannot grow while the block runs.
+template <int V, int T, bool MX, int LAT>
+cudaError_t launch_latency(const LaunchParams &p, int grid, int threads, cudaStream_t st)
+{
+    static std::atomic<uint64_t> carved{0};   // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 64 && !((carved.load(std::memory_order_acquire) >> dev) & 1u)) {
+        e = cudaFuncSetAttribute(rows_kernel<V, T, MX, LAT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return e;
+        carved.fetch_or(1ull << dev, std::memory_order_acq_rel);
+    }
+    rows_kernel<V, T, MX, LAT><<<grid, threads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
 // One compiled team shape in the throughput form (lat 0) or the latency form
 // with each row's outputs shared by lat = 1, 2 or 4 blocks (a split that
 // divides V).
 template <int V, int T, bool MX>
 cudaError_t launch_static(int lat, const LaunchParams &p, int grid, int threads, cudaStream_t st)
 {
-    if (lat == 0)
+    if (lat == 0) {
         rows_kernel<V, T, MX, 0><<<grid, threads, 0, st>>>(p);
-    else if (lat == 1)
-        rows_kernel<V, T, MX, 1><<<grid, threads, 0, st>>>(p);
-    else if constexpr (V % 2 == 0) {
-        if (lat == 2)
-            rows_kernel<V, T, MX, 2><<<grid, threads, 0, st>>>(p);
-        else if constexpr (V % 4 == 0) {
-            if (lat == 4)
-                rows_kernel<V, T, MX, 4><<<grid, threads, 0, st>>>(p);
-            else
-                return cudaErrorInvalidValue;
-        } else {
-            return cudaErrorInvalidValue;
-        }
-    } else {
-        return cudaErrorInvalidValue;
+        return cudaGetLastError();
     }
-    return cudaGetLastError();
+    if (lat == 1)
+        return launch_latency<V, T, MX, 1>(p, grid, threads, st);
+    if constexpr (V % 2 == 0) {
+        if (lat == 2)
+            return launch_latency<V, T, MX, 2>(p, grid, threads, st);
+    }
+    if constexpr (V % 4 == 0) {
+        if (lat == 4)
+            return launch_latency<V, T, MX, 4>(p, grid, threads, st);
+    }
+    return cudaErrorInvalidValue;
 }
 
 // The latency form exists for the compiled team shapes only; `lat` (0 =

@@ -79,20 +79,21 @@ def test_split_k_matches_oracle(oracle_mod, bn, ksplit):
 
 
 @pytest.mark.parametrize("bn,ksplit", [(64, 4), (64, 2), (256, 8), (128, 3)])
-def test_split_k_rows_independent_of_m(oracle_mod, bn, ksplit):
+@pytest.mark.parametrize("rows", [4, 33, 64])
+def test_split_k_rows_independent_of_m(oracle_mod, bn, ksplit, rows):
     """Split K adds the cluster's partial sums in rank order whatever the
-    tile's row count, so the rows a 4-token launch computes equal the same
-    rows of a 200-token launch bit for bit, and match the oracle."""
+    tile's row count, so the rows a 4-, 33- or 64-token launch computes equal
+    the same rows of a 200-token launch bit for bit, and match the oracle."""
     M, N, K = 200, 264, 2048
     a_q, a_s, b_q, b_s = operands(91, M, N, K)
     gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
     opts = rmsq.GemmOpts(bn=bn, ksplit=ksplit)
     full = rmsq.mxfp4_gemm(a_q.to(DEV), rmsq.mx_scale_tiles(a_s.to(DEV)), gb, tb, opts=opts)
-    few = rmsq.mxfp4_gemm(a_q[:4].to(DEV), rmsq.mx_scale_tiles(a_s[:4].to(DEV)), gb, tb, opts=opts)
+    few = rmsq.mxfp4_gemm(a_q[:rows].to(DEV), rmsq.mx_scale_tiles(a_s[:rows].to(DEV)), gb, tb, opts=opts)
     torch.cuda.synchronize()
-    assert torch.equal(few, full[:4])
-    ref = oracle_mod.mxfp4_gemm(a_q[:4].numpy(), a_s[:4].numpy(), b_q.numpy(), b_s.numpy())
-    parity.compare_gemm(few, ref, K, what=f"split K, 4 rows, bn={bn} ksplit={ksplit}")
+    assert torch.equal(few, full[:rows])
+    ref = oracle_mod.mxfp4_gemm(a_q[:rows].numpy(), a_s[:rows].numpy(), b_q.numpy(), b_s.numpy())
+    parity.compare_gemm(few, ref, K, what=f"split K, {rows} rows, bn={bn} ksplit={ksplit}")
     assert rmsq.sync_status() == 0
 
 
