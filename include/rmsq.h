@@ -316,7 +316,11 @@ typedef enum rmsq_form {
  *                   each loads and reduces the whole row, so all compute the
  *                   same inv_rms, and normalises, quantises and stores its
  *                   part. 0 = auto: the largest of 4 and 2 that keeps the
- *                   launch within one block per SM, else 1.
+ *                   launch within one block per SM, else 1. A residual
+ *                   updated in place (out_residual == residual) is never
+ *                   split: a block would write back its part while another
+ *                   block of the row may still be reading it. Auto then
+ *                   takes 1, and split > 1 is refused (RMSQ_ERR_UNSUPPORTED).
  */
 typedef struct rmsq_launch_opts {
     int32_t kernel;

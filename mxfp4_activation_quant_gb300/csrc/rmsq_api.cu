@@ -289,8 +289,15 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
             return fail(RMSQ_ERR_INVALID_ARG, "split must be 0, 1, 2 or 4 (got %d)", o.split);
         const int64_t sms = sm_count();
         const bool lat = ts && (o.form == RMSQ_FORM_LATENCY || (o.form == RMSQ_FORM_AUTO && blocks <= sms));
+        // Every block of a split row reads the whole residual row and writes
+        // back its own part, so a residual updated in place is not split: a
+        // part could be written before another block of the row has read it.
+        const bool in_place = s.res && (const void *)s.res == (const void *)s.out_res;
         int split = 1;
-        if (lat && rpb == 1) {
+        if (in_place && o.split > 1) {
+            return fail(RMSQ_ERR_UNSUPPORTED, "split rows need out_residual separate from residual "
+                                              "(an in-place residual update is not split)");
+        } else if (lat && rpb == 1 && !in_place) {
             if (o.split) {
                 split = o.split;
             } else {

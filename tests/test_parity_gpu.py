@@ -595,6 +595,33 @@ def test_latency_form_is_bit_identical(oracle_mod, name, M, split):
         assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), k
 
 
+@pytest.mark.parametrize("kind,M", [("fp8", 64), ("fp8", 37), ("fp8", 8), ("mx", 4), ("mx", 64)])
+def test_in_place_residual_is_not_split(kind, M):
+    """Split rows read the whole residual row in every block of the row and
+    write back one part each, which would race with an in-place residual
+    update: such calls take one block per row (auto) and refuse an explicit
+    split. Repeated in-place calls equal the out-of-place call (split rows)
+    bit for bit."""
+    H = 7168
+    x = synth.random_bf16(300 + M, (M, H)).to(DEV)
+    res = synth.random_bf16(301 + M, (M, H), var=4.0, tensor="residual").to(DEV)
+    gamma = synth.gaussian_bf16(302, "gamma", (H,), mean=1.0, var=0.1).to(DEV)
+    call = rmsq.add_rmsnorm_quant_fp8 if kind == "fp8" else rmsq.add_rmsnorm_quant_mxfp4
+    (y0, q0, s0), r0 = call(x, gamma, res, keep_bf16=True)     # out of place: split rows at these sizes
+    torch.cuda.synchronize()
+    copies = [res.clone() for _ in range(20)]
+    outs = [call(x, gamma, c, keep_bf16=True, out_residual=c) for c in copies]
+    torch.cuda.synchronize()
+    for i, ((y, q, sc), r) in enumerate(outs):
+        assert r.data_ptr() == copies[i].data_ptr()
+        for a, b in ((y, y0), (q, q0), (sc, s0), (r, r0)):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"call {i}"
+    c = res.clone()
+    with pytest.raises(rmsq.RmsqError, match="in-place"):
+        call(x, gamma, c, out_residual=c, opts=rmsq.LaunchOpts(form=rmsq.FORM_LATENCY, split=2))
+    assert rmsq.sync_status() == 0
+
+
 def test_unknown_form_and_bad_split_are_refused():
     w = synth.WORKLOADS["decode"]
     g = _gpu(synth.make_inputs(w, M=4))
@@ -611,12 +638,10 @@ def test_unknown_form_and_bad_split_are_refused():
 
 @pytest.mark.parametrize("M,kind", [(64, "fp8"), (8192, "fp8"), (37, "mx"), (3000, "mx")])
 def test_chained_calls_read_the_previous_outputs(M, kind):
-    """Each norm + quant call may start before the kernel ahead of it on the
-    stream has finished, and waits for it before touching memory. A chain of
-    six calls in which each reads what the previous one wrote -- the residual
-    updated in place, the next x being the previous y -- without
-    synchronisation must equal the same chain synchronised after every
-    call."""
+    """A chain of six calls in which each reads what the previous one wrote
+    -- the residual updated in place, the next x being the previous y --
+    launched back to back without synchronisation must equal the same chain
+    synchronised after every call."""
     H = 7168
     x0 = synth.random_bf16(90 + M, (M, H)).to(DEV)
     res0 = synth.random_bf16(91 + M, (M, H), var=4.0, tensor="residual").to(DEV)
