@@ -26,8 +26,8 @@
 // owns the tensor memory and issues tcgen05.cp (scale factors, shared ->
 // tensor memory) and tcgen05.mma (one elected lane each); warps 4-7 run the
 // epilogue (tcgen05.ld -> bf16 -> shared memory -> whole 128-byte lines of
-// D). The prequant kernel has 384 threads: warps 4-11 quantise A and then
-// share the epilogue.
+// D, or 64-byte pieces of rows for 64-row tiles). The prequant kernel has 384
+// threads: warps 4-11 quantise A and then share the epilogue.
 // Every mbarrier wait is bounded; a wait that runs out sets the status word,
 // makes the other roles stop, drains what is in flight and frees the tensor
 // memory before the CTA exits.
