@@ -61,6 +61,12 @@ namespace gemm {
 // prequant kernel's widest tile takes 2 x 2 (8.7 against 11.9 us at 4
 // tokens, equal at 64 and more). 64-row tiles: 4 spans x 2 stages (6.1
 // against 6.8 us at 4 tokens); 128-row tiles: 2 spans x 3 stages.
+// A stage's operands come in few copies, since issuing each costs the
+// producer time as well: A of all its spans in one 3-D box, B likewise, the
+// A scale tiles of its spans in one bulk copy and the B scale tiles in one
+// per 128-row scale tile (at 4 tokens the GEMM alone went from 6.1 to 5.8 us
+// against one box and one copy per span). The stage holds A's spans, then
+// B's spans; B's scale tiles by scale tile, then span.
 template <int BN, bool PRE = false>
 struct GemmCfg {
     static constexpr int kSpans = BN == 64 ? 4 : (BN == 128 ? 2 : (PRE ? 2 : 1));
@@ -68,8 +74,9 @@ struct GemmCfg {
     static constexpr int kSfbAtoms = BN >= 128 ? BN / 128 : 1;   // 128-row scale tiles of B per K chunk
     static constexpr int kSpanA = kBM * kSpanBytes;             // A codes of one span (16 KB)
     static constexpr int kSpanB = BN * kSpanBytes;
-    static constexpr int kSpanAB = kSpanA + kSpanB;
-    static constexpr int kAB = kSpans * kSpanAB;                  // operand bytes of a stage
+    // a stage: A of its spans, then B of its spans (each loaded by one 3-D box)
+    static constexpr int kAB = kSpans * (kSpanA + kSpanB);        // operand bytes of a stage
+    static constexpr int kStageA = kSpans * kSpanA;
     static constexpr int kSfaSpan = 2 * 512;                      // two 128-element K chunks
     static constexpr int kSfbSpan = kSfbAtoms * 2 * 512;
     static constexpr int kSfColsSpan = 8 + 8 * kSfbAtoms;        // scale-factor TMEM columns per span
@@ -166,7 +173,7 @@ __device__ __forceinline__ bool prequant_loop(const GemmParams &p, int64_t m0, i
             const uint32_t codes = e2m1x8(mul2(unpack_bf16x2(v.x), mult), mul2(unpack_bf16x2(v.y), mult),
                                           mul2(unpack_bf16x2(v.z), mult), mul2(unpack_bf16x2(v.w), mult));
             if (ok) {
-                uint8_t *sA = smem + s * C::kAB + sp * C::kSpanAB;
+                uint8_t *sA = smem + s * C::kAB + sp * C::kSpanA;
                 *reinterpret_cast<uint32_t *>(sA + row * kSpanBytes + ((g ^ (row & 7)) << 4) + (vec & 3) * 4) =
                     codes;
                 if ((vec & 3) == 0)            // scale tile g/4: (row % 32) * 16 + (row / 32) * 4 + g % 4
@@ -267,6 +274,7 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
     // Stages are counted over all of the CTA's tiles (g): the ring runs on
     // from one tile into the next.
     const int NST = (KL + C::kSpans - 1) / C::kSpans;            // stages per tile
+    const int a_pitch = PREQUANT ? C::kSpanA : p.a_box_rows * kSpanBytes;   // bytes between A's spans in a stage
     if (warp == 0) {
         // ---------------------------------------------------------- loads
         // The whole warp runs the loop (its values stay warp-uniform) and one
@@ -279,19 +287,24 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
             int atoms = 0;
             for (int t = 0; t < C::kSfbAtoms; ++t)
                 atoms += (bt0 + t < p.b_row_tiles);
-            const uint32_t span_tx = C::kSpanB + atoms * 1024u +
-                                     (PREQUANT ? 0u : (uint32_t)(p.a_box_rows * kSpanBytes + C::kSfaSpan));
-            // B and its scales for stage j of this tile (one elected lane)
+            // Bytes a stage of nsp spans brings: the 3-D boxes of A and B always
+            // carry kSpans spans (spans past the end of K read as zero, spans past
+            // this CTA's share of K are the next share's, which no MMA here
+            // reads), the scale copies exactly nsp.
+            auto stage_tx = [&](int nsp) -> uint32_t {
+                return (uint32_t)(C::kSpans * C::kSpanB + nsp * atoms * 1024) +
+                       (PREQUANT ? 0u : (uint32_t)(C::kSpans * p.a_box_rows * kSpanBytes + nsp * C::kSfaSpan));
+            };
+            // B and its scales for stage j of this tile (one elected lane): one
+            // 3-D box of all the stage's spans, one copy of their scale tiles per
+            // 128-row scale tile of B
             auto load_b = [&](int j, int s, int nsp, uint32_t fb) {
-                for (int sp = 0; sp < nsp; ++sp) {
-                    const int ks = ks0 + j * C::kSpans + sp;
-                    tma_2d(saddr(smem + s * C::kAB + sp * C::kSpanAB + C::kSpanA), &map_b, ks * kSpanBytes,
-                           (int)tn0, fb);
-                    for (int t = 0; t < C::kSfbAtoms; ++t)
-                        if (bt0 + t < p.b_row_tiles)
-                            bulk_g2s(saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan + t * 1024),
-                                     p.b_scale + ((int64_t)(bt0 + t) * (2 * KS) + 2 * ks) * 512, 1024, fb);
-                }
+                const int ks = ks0 + j * C::kSpans;
+                tma_3d(saddr(smem + s * C::kAB + C::kStageA), &map_b, 0, (int)tn0, ks, fb);
+                for (int t = 0; t < C::kSfbAtoms; ++t)
+                    if (bt0 + t < p.b_row_tiles)
+                        bulk_g2s(saddr(smem + C::kOffSfb + ((s * C::kSfbAtoms + t) * C::kSpans) * 1024),
+                                 p.b_scale + ((int64_t)(bt0 + t) * (2 * KS) + 2 * ks) * 512, 1024u * nsp, fb);
             };
             // The first tile's first stages are free from the start: their B
             // loads (which do not depend on the kernel before this one) are
@@ -304,7 +317,7 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                         if (j == p.debug_skip_stage)        // test hook: that stage never arrives
                             continue;
                         const int nsp = min(C::kSpans, KL - j * C::kSpans);
-                        mbar_arrive_tx(saddr(full + j), span_tx * nsp);
+                        mbar_arrive_tx(saddr(full + j), stage_tx(nsp));
                         load_b(j, j, nsp, saddr(full + j));
                     }
                 }
@@ -323,14 +336,12 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                     const int nsp = min(C::kSpans, KL - j * C::kSpans);
                     const uint32_t fb = saddr(full + s);
                     if (j >= pre)
-                        mbar_arrive_tx(fb, span_tx * nsp);
-                    if (!PREQUANT) {
-                        for (int sp = 0; sp < nsp; ++sp) {
-                            const int ks = ks0 + j * C::kSpans + sp;
-                            tma_2d(saddr(smem + s * C::kAB + sp * C::kSpanAB), &map_a, ks * kSpanBytes, (int)tm0, fb);
-                            bulk_g2s(saddr(smem + C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan),
-                                     p.a_scale + ((int64_t)mt * (2 * KS) + 2 * ks) * 512, 1024, fb);
-                        }
+                        mbar_arrive_tx(fb, stage_tx(nsp));
+                    if (!PREQUANT) {   // A of the stage's spans in one 3-D box, their scale tiles in one copy
+                        const int ks = ks0 + j * C::kSpans;
+                        tma_3d(saddr(smem + s * C::kAB), &map_a, 0, (int)tm0, ks, fb);
+                        bulk_g2s(saddr(smem + C::kOffSfa + s * C::kSpans * C::kSfaSpan),
+                                 p.a_scale + ((int64_t)mt * (2 * KS) + 2 * ks) * 512, (uint32_t)(C::kSfaSpan * nsp), fb);
                     }
                     if (j >= pre)
                         load_b(j, s, nsp, fb);
@@ -370,16 +381,18 @@ __global__ void __launch_bounds__(gemm_threads<PREQUANT>(), 1)
                         const uint32_t sfa_col = tmem_sf + s * C::kSfCols + sp * C::kSfColsSpan;
                         const uint32_t sfb_col = sfa_col + 8;
                         const uint32_t sfa_smem = saddr(smem + C::kOffSfa + (s * C::kSpans + sp) * C::kSfaSpan);
-                        const uint32_t sfb_smem = saddr(smem + C::kOffSfb + (s * C::kSpans + sp) * C::kSfbSpan);
-                        const uint32_t a_smem = saddr(smem + s * C::kAB + sp * C::kSpanAB),
-                                       b_smem = a_smem + C::kSpanA;
+                        // B scales: tile t's spans after tile t - 1's
+                        const uint32_t sfb_smem = saddr(smem + C::kOffSfb + (s * C::kSfbAtoms * C::kSpans + sp) * 1024);
+                        // A's spans lie a_box_rows rows apart as loaded (128 when quantised here)
+                        const uint32_t a_smem = saddr(smem + s * C::kAB + sp * a_pitch),
+                                       b_smem = saddr(smem + s * C::kAB + C::kStageA + sp * C::kSpanB);
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
                             cp_sf(sfa_col + 4 * c, desc_sf(sfa_smem + c * 512));
 #pragma unroll
                             for (int t = 0; t < C::kSfbAtoms; ++t)
                                 cp_sf(sfb_col + 4 * C::kSfbAtoms * c + 4 * t,
-                                      desc_sf(sfb_smem + t * 1024 + c * 512));
+                                      desc_sf(sfb_smem + t * C::kSpans * 1024 + c * 512));
                         }
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
@@ -631,6 +644,25 @@ bool make_code_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over the codes seen as (128 bytes of a K span, row, span): rows ld
+// bytes apart, spans 128 bytes apart, 128-byte swizzle; a box covers box_rows
+// rows of box_spans spans and lands span after span, each span laid out as
+// the 2-D box; rows and spans past the end read as zero codes.
+bool make_code_map3(CUtensorMap *map, const void *base, int64_t rows, int64_t spans, int64_t ld, int box_rows,
+                    int box_spans)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kSpanBytes, (cuuint64_t)rows, (cuuint64_t)spans};
+    cuuint64_t strides[2] = {(cuuint64_t)ld, (cuuint64_t)kSpanBytes};
+    cuuint32_t box[3] = {(cuuint32_t)kSpanBytes, (cuuint32_t)box_rows, (cuuint32_t)box_spans};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, bool PRE>
 cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUtensorMap &mb, int m_tiles,
                           int n_tiles, int persistent_ctas, cudaStream_t st)
@@ -682,6 +714,17 @@ cudaError_t launch_gemm_t(const GemmParams &p, const CUtensorMap &ma, const CUte
 
 bool pre_of(const GemmLaunch &g) { return g.a_bf16 != nullptr; }
 
+// K spans per ring stage of the one-CTA kernel (0 for a width it lacks)
+int stage_spans(int bn, bool pre)
+{
+    switch (bn) {
+    case 64: return pre ? GemmCfg<64, true>::kSpans : GemmCfg<64, false>::kSpans;
+    case 128: return pre ? GemmCfg<128, true>::kSpans : GemmCfg<128, false>::kSpans;
+    case 256: return pre ? GemmCfg<256, true>::kSpans : GemmCfg<256, false>::kSpans;
+    }
+    return 0;
+}
+
 // 2-D map over a scale-tile array viewed as rows of 256 bytes (one K span of
 // a 128-row tile is four such rows, 1 KB); rows past the end read as zero.
 bool make_scale_map(CUtensorMap *map, const void *base, int64_t rows)
@@ -714,8 +757,11 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
     p.k_spans = (int32_t)(g.K / kSpanK);
     p.b_row_tiles = (int32_t)((g.N + 127) / 128);
     // Rows of the A tile past M are never stored, so with fewer than 128
-    // rows only those (rounded up to a swizzle atom of 8) are loaded; the
-    // rest of the tile keeps whatever it held and feeds only discarded rows.
+    // rows only those (rounded up to a swizzle atom of 8) are loaded. A 3-D
+    // box lands its spans a_box_rows * 128 bytes apart; the MMA reads each
+    // span there, and its rows past a_box_rows -- later bytes of the same
+    // stage's A area, which its own copies have filled or an earlier stage
+    // left -- feed only discarded rows of D.
     p.a_box_rows = g.M >= kBM ? kBM : (int32_t)((g.M + 7) / 8 * 8);
     p.ksplit = g.ksplit;
     p.debug_skip_stage = g.debug_skip_stage;
@@ -724,12 +770,17 @@ cudaError_t launch_mxfp4_gemm(const GemmLaunch &g, cudaStream_t st)
         return cudaErrorInvalidValue;
     p.wait_limit_ns = g.wait_limit_ns;
     p.status = g.status;
+    // 3-D boxes of a ring stage's spans (the stage's span count depends on the
+    // tile width and the kernel)
+    const int sps = stage_spans(g.bn, g.a_bf16 != nullptr);
+    if (!sps)
+        return cudaErrorInvalidValue;
     CUtensorMap ma, mb;
-    if (!make_code_map(&mb, g.b_q, g.N, g.K / 2, g.ldb, g.bn))
+    if (!make_code_map3(&mb, g.b_q, g.N, p.k_spans, g.ldb, g.bn, sps))
         return cudaErrorInvalidValue;
     if (g.a_bf16) {
         ma = mb;   // unused by the prequant kernel
-    } else if (!make_code_map(&ma, g.a_q, g.M, g.K / 2, g.lda, p.a_box_rows)) {
+    } else if (!make_code_map3(&ma, g.a_q, g.M, p.k_spans, g.lda, p.a_box_rows, sps)) {
         return cudaErrorInvalidValue;
     }
     const int m_tiles = (int)((g.M + kBM - 1) / kBM), n_tiles = (int)((g.N + g.bn - 1) / g.bn);

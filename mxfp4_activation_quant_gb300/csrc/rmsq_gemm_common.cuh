@@ -64,7 +64,7 @@ struct GemmParams {
     int64_t M, N;
     int32_t k_spans;            // K / 256: spans of K (a ring stage holds one or more)
     int32_t b_row_tiles;        // ceil(N / 128): 128-row scale tiles that exist for B
-    int32_t a_box_rows;         // rows of A per TMA box: 128, or M rounded up to 8 when M < 128
+    int32_t a_box_rows;         // rows of A per TMA box (128; rows past M read as zero)
     int32_t ksplit;             // CTAs of a cluster that split K (1 = no split)
     int32_t persistent;         // 1: a grid of gridDim.x CTAs walks the m_tiles x n_tiles tiles
     int32_t m_tiles, n_tiles;   // tiles of the launch (the pair kernel: 256-row tiles of A and B)
@@ -165,6 +165,15 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// A 3-D box (coordinates x, y, z innermost first) whose bytes count on `bar`.
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
 }
 
@@ -359,6 +368,11 @@ __device__ __forceinline__ float4 ld_peer_f4(const float *local, uint32_t rank)
 // 2-D map over `rows` rows of `row_bytes` code bytes (leading dimension `ld`
 // bytes), boxes of 128 bytes x box_rows rows, 128-byte swizzle.
 bool make_code_map(CUtensorMap *map, const void *base, int64_t rows, int64_t row_bytes, int64_t ld, int box_rows);
+// 3-D map over the same codes seen as (128 bytes of a K span, row, span):
+// rows ld bytes apart, spans 128 bytes apart; a box of box_rows rows and
+// box_spans spans lands span after span, each span laid out as the 2-D box.
+bool make_code_map3(CUtensorMap *map, const void *base, int64_t rows, int64_t spans, int64_t ld, int box_rows,
+                    int box_spans);
 // 2-D map over a scale-tile array viewed as rows of 256 bytes.
 bool make_scale_map(CUtensorMap *map, const void *base, int64_t rows);
 // CTA-pair kernel (rmsq_gemm_pair.cu): pairs resident at once for tile width
