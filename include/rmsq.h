@@ -259,7 +259,9 @@ const char *rmsq_last_error(void);
  * since the last read gave up a bounded wait (its outputs are then
  * incomplete), RMSQ_ERR_BOUNDS if, in a library built with RMSQ_DEBUG, an
  * index check before a store failed (the store was skipped),
- * RMSQ_ERR_CUDA if the synchronisation failed, else RMSQ_OK.
+ * RMSQ_ERR_CUDA if the synchronisation failed or a GEMM kernel found its
+ * shared memory not 1024-byte aligned (it then wrote nothing; its layout
+ * relies on the alignment the hardware gives), else RMSQ_OK.
  *
  * The word is one per device and per process, shared by every stream and
  * host thread: a call reports (and clears) what any kernel of the library on

@@ -666,6 +666,9 @@ rmsq_status rmsq_sync_status(void *stream)
         return fail(RMSQ_ERR_CUDA, "status word access failed: %s", cudaGetErrorString(e));
     if (word & 4u)
         return fail(RMSQ_ERR_BOUNDS, "a debug-build bounds check failed, the store was skipped (status 0x%x)", word);
+    if (word & 8u)
+        return fail(RMSQ_ERR_CUDA, "a GEMM kernel found its shared memory not 1024-byte aligned and wrote nothing "
+                                   "(status 0x%x)", word);
     if (word)
         return fail(RMSQ_ERR_TIMEOUT, "a bounded wait gave up (status 0x%x)", word);
     return ok();
