@@ -80,7 +80,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2) dual_kernel(const __grid_const
     X(4, 128) /* H = 4096 */  \
     X(4, 64)  /* H = 2048 */  \
     X(3, 64)  /* H = 1536 */  \
-    X(4, 16)  /* H = 512  */
+    X(4, 16)  /* H = 512  */  \
+    X(2, 16)  /* H = 256  */
 
 // The latency form: at most one block per SM, typically followed by a GEMM
 // launched as its programmatic dependent. The SMs its blocks occupy are asked
