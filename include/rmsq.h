@@ -311,7 +311,7 @@ typedef enum rmsq_form {
  *   form            row kernel: rmsq_form. Both forms give bit-identical
  *                   outputs (same order of every addition); the latency form
  *                   exists for the compiled team shapes (H = 7168, 8192, 5120,
- *                   4096, 2048, 1536, 512 at their default vpt) and is
+ *                   4096, 2048, 1536, 512, 256 at their default vpt) and is
  *                   ignored for other shapes.
  *   split           latency form with one row per block: the blocks that
  *                   share each row's outputs, 1, 2 or 4 (dividing vpt);
