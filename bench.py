@@ -605,6 +605,21 @@ def other_workloads(dev, stream, peak: float) -> tuple[dict, dict]:
                            "GBps_cold_l2": round(nb / cold / 1e3, 1),
                            "frac_of_hbm_peak_cold_l2": round(nb / cold / 1e3 / peak, 4) if peak else None}
 
+    # the same pair at the decode config's 64 tokens (latency form of the pair)
+    Md = synth.WORKLOADS["decode"].M
+    dd = {k: v[:Md].contiguous() for k, v in d.items() if k in ("q_a", "kv_a")}
+    dq, dqs = qq[:Md].contiguous(), qs[:Md].contiguous()
+    dk, dks = kq[:Md].contiguous(), ks[:Md].contiguous()
+
+    def qk_decode():
+        rmsq.qknorm_quant_fp8_into(dd["q_a"], dd["kv_a"], d["gamma_q"], d["gamma_kv"], dq, dqs, dk, dks, eps=w.eps)
+    for _ in range(10):
+        qk_decode()
+    torch.cuda.synchronize()
+    us = _graph_us(qk_decode, 200)
+    out["qknorm_m64"] = {"us_per_call_graph_warm_l2": round(us, 3), "GBps_graph_warm": round(qk_bytes(Md, w.Hq, w.Hkv) / us / 1e3, 1),
+                         "form": "latency (one block per SM or fewer)"}
+
     # MXFP4, M=8192, H=7168
     w = synth.WORKLOADS["mxfp4"]
     dc = synth.make_inputs(w)

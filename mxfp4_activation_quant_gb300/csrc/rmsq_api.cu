@@ -487,7 +487,9 @@ rmsq_status qknorm_common(bool mx, const void *q_a, int64_t ld_q, const void *kv
     p.seg[0] = sq;
     p.seg[1] = sk;
     p.nseg = 2;
-    cudaError_t e = launch_dual(mx, v0, t0s, v1, t1s, p, (int)(bq + bk), threads, (cudaStream_t)stream);
+    // at most one block per SM: the compiled pair shape's latency form
+    const bool lat = t0s && bq + bk <= sm_count();
+    cudaError_t e = launch_dual(mx, lat, v0, t0s, v1, t1s, p, (int)(bq + bk), threads, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     return ok();

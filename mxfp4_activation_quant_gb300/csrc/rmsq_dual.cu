@@ -6,21 +6,24 @@ namespace rmsq {
 // The MLA latent pair (q_a 1536, kv_a 512): one warp per q_a row with six
 // vectors per thread (no cross-warp step: 14.73 against 15.59 us for the
 // FP8 pair at M = 8192 with a two-warp team of three vectors each), and
-// 16-thread teams of four vectors for kv_a.
+// 16-thread teams of four vectors for kv_a. Launches of at most one block per
+// SM take the pair's latency form (gamma loaded with each row).
 bool static_dual_shape(int v0, int t0, int v1, int t1)
 {
     return v0 == 6 && t0 == 32 && v1 == 4 && t1 == 16;
 }
 
 template <bool MX>
-cudaError_t launch_dual_impl(int v0, int t0, int v1, int t1, const LaunchParams &p, int grid, int threads,
-                             cudaStream_t st)
+cudaError_t launch_dual_impl(bool lat, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,
+                             int threads, cudaStream_t st)
 {
     if (t0 || t1) {
-        if (static_dual_shape(v0, t0, v1, t1))
-            dual_kernel<6, 32, 4, 16, MX><<<grid, threads, 0, st>>>(p);
-        else
+        if (!static_dual_shape(v0, t0, v1, t1))
             return cudaErrorInvalidValue;
+        if (lat)
+            dual_kernel_lat<6, 32, 4, 16, MX><<<grid, threads, 0, st>>>(p);
+        else
+            dual_kernel<6, 32, 4, 16, MX><<<grid, threads, 0, st>>>(p);
         return cudaGetLastError();
     }
     if (v0 != v1)
@@ -39,11 +42,11 @@ cudaError_t launch_dual_impl(int v0, int t0, int v1, int t1, const LaunchParams 
     return cudaGetLastError();
 }
 
-cudaError_t launch_dual(bool mx, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,
+cudaError_t launch_dual(bool mx, bool lat, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,
                         int threads, cudaStream_t st)
 {
-    return mx ? launch_dual_impl<true>(v0, t0, v1, t1, p, grid, threads, st)
-              : launch_dual_impl<false>(v0, t0, v1, t1, p, grid, threads, st);
+    return mx ? launch_dual_impl<true>(lat, v0, t0, v1, t1, p, grid, threads, st)
+              : launch_dual_impl<false>(lat, v0, t0, v1, t1, p, grid, threads, st);
 }
 
 }  // namespace rmsq

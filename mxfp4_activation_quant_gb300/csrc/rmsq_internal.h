@@ -71,7 +71,8 @@ cudaError_t launch_rows_fp8(int vpt, int tpr_static, int lat, const LaunchParams
                             cudaStream_t st);
 cudaError_t launch_rows_mx(int vpt, int tpr_static, int lat, const LaunchParams &p, int grid, int threads,
                            cudaStream_t st);
-cudaError_t launch_dual(bool mx, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,
+// lat: the latency form of the compiled MLA pair shape (ignored for others)
+cudaError_t launch_dual(bool mx, bool lat, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,
                         int threads, cudaStream_t st);
 cudaError_t launch_bulk(bool mx, int vpt, int tpr_static, const BulkParams &p, int grid, int threads,
                         size_t smem, cudaStream_t st);

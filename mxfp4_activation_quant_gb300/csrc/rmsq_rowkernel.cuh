@@ -71,6 +71,19 @@ __global__ void __launch_bounds__(kMaxThreads, 2) dual_kernel(const __grid_const
         block_rows<V1, T1, MX>(p.seg[1], blockIdx.x - p.seg[0].blocks, red);
 }
 
+// The latency form of the pair, for launches of at most one block per SM
+// (decode sizes): gamma is loaded with each row; with so few blocks the
+// registers need no cap for occupancy.
+template <int V0, int T0, int V1, int T1, bool MX>
+__global__ void __launch_bounds__(kMaxThreads, 1) dual_kernel_lat(const __grid_constant__ LaunchParams p)
+{
+    __shared__ RedSmem red;
+    if ((int)blockIdx.x < p.seg[0].blocks)
+        block_rows<V0, T0, MX, 1>(p.seg[0], blockIdx.x, red);
+    else
+        block_rows<V1, T1, MX, 1>(p.seg[1], blockIdx.x - p.seg[0].blocks, red);
+}
+
 // Team shapes compiled with a fixed team size: exact fits of common hidden
 // sizes (vectors per thread x threads x 8 = H).
 #define RMSQ_STATIC_SHAPES(X) \

@@ -622,6 +622,30 @@ def test_in_place_residual_is_not_split(kind, M):
     assert rmsq.sync_status() == 0
 
 
+@pytest.mark.parametrize("mx", [False, True])
+@pytest.mark.parametrize("M", [1, 5, 64, 76, 1300])
+def test_qknorm_pair_latency_form(oracle_mod, M, mx):
+    """The MLA pair (q_a 1536, kv_a 512) at decode sizes takes the pair's
+    latency form (gamma loaded with each row; at most one block per SM, so
+    up to 1216 tokens); 1300 tokens take the throughput form. Both against
+    the oracle, every row."""
+    Hq, Hkv = 1536, 512
+    q_a = synth.random_bf16(500 + M, (M, Hq), tensor="q_a")
+    kv_a = synth.random_bf16(501 + M, (M, Hkv), var=2.0, tensor="kv_a")
+    gq = synth.gaussian_bf16(502, "gamma_q", (Hq,), mean=1.0, var=0.1)
+    gk = synth.gaussian_bf16(503, "gamma_kv", (Hkv,), mean=1.0, var=0.1)
+    fn = rmsq.qknorm_quant_mxfp4 if mx else rmsq.qknorm_quant_fp8
+    outq, outk = fn(q_a.to(DEV), kv_a.to(DEV), gq.to(DEV), gk.to(DEV), keep_bf16=True)
+    torch.cuda.synchronize()
+    for out, x, g in ((outq, q_a, gq), (outk, kv_a, gk)):
+        got = {"q": out[-2], "scale": out[-1], "y": out[0]}
+        if mx:
+            parity.compare_mx(got, oracle_mod.add_rmsnorm_quant_mxfp4(x, None, g), what=f"pair M={M}")
+        else:
+            parity.compare_fp8(got, oracle_mod.add_rmsnorm_quant_fp8(x, None, g), "row", what=f"pair M={M}")
+    assert rmsq.sync_status() == 0
+
+
 def test_unknown_form_and_bad_split_are_refused():
     w = synth.WORKLOADS["decode"]
     g = _gpu(synth.make_inputs(w, M=4))
