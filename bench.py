@@ -519,22 +519,32 @@ def _cold_us(fn, dev, calls: int = 50) -> float:
     return statistics.median(each)
 
 
-def _graph_us(fn, reps: int) -> float:
+def _graph_us(fn, reps: int, timed: int = 7, warm_ms: float = 30.0) -> float:
     """Microseconds per call of fn() replayed from a CUDA graph of `reps` calls
-    captured on torch's capture stream (warm L2 across calls)."""
+    captured on torch's capture stream (warm L2 across calls): the graph is
+    replayed for at least `warm_ms` first (the host-side capture leaves the GPU
+    idle long enough for its clocks to drop), then the median of `timed`
+    replays, each timed with events on the replay stream."""
     import torch
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         for _ in range(reps):
             fn()
-    g.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    g.replay()
-    b.record()
-    torch.cuda.synchronize()
-    return a.elapsed_time(b) * 1e3 / reps
+    t0 = time.perf_counter()
+    while True:
+        g.replay()
+        torch.cuda.synchronize()
+        if (time.perf_counter() - t0) * 1e3 >= warm_ms:
+            break
+    us = []
+    for _ in range(timed):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us.append(a.elapsed_time(b) * 1e3 / reps)
+    return statistics.median(us)
 
 
 def other_workloads(dev, stream, peak: float) -> tuple[dict, dict]:
