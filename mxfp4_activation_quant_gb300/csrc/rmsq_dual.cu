@@ -20,26 +20,22 @@ cudaError_t launch_dual_impl(bool lat, int v0, int t0, int v1, int t1, const Lau
     if (t0 || t1) {
         if (!static_dual_shape(v0, t0, v1, t1))
             return cudaErrorInvalidValue;
-        if (lat)
-            dual_kernel_lat<6, 32, 4, 16, MX><<<grid, threads, 0, st>>>(p);
-        else
-            dual_kernel<6, 32, 4, 16, MX><<<grid, threads, 0, st>>>(p);
-        return cudaGetLastError();
+        return lat ? launch_pdl(dual_kernel_lat<6, 32, 4, 16, MX>, grid, threads, st, p)
+                   : launch_pdl(dual_kernel<6, 32, 4, 16, MX>, grid, threads, st, p);
     }
     if (v0 != v1)
         return cudaErrorInvalidValue;
     switch (v0) {
-    case 1: dual_kernel<1, 0, 1, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 2: dual_kernel<2, 0, 2, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 3: dual_kernel<3, 0, 3, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 4: dual_kernel<4, 0, 4, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 5: dual_kernel<5, 0, 5, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 6: dual_kernel<6, 0, 6, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 7: dual_kernel<7, 0, 7, 0, MX><<<grid, threads, 0, st>>>(p); break;
-    case 8: dual_kernel<8, 0, 8, 0, MX><<<grid, threads, 0, st>>>(p); break;
+    case 1: return launch_pdl(dual_kernel<1, 0, 1, 0, MX>, grid, threads, st, p);
+    case 2: return launch_pdl(dual_kernel<2, 0, 2, 0, MX>, grid, threads, st, p);
+    case 3: return launch_pdl(dual_kernel<3, 0, 3, 0, MX>, grid, threads, st, p);
+    case 4: return launch_pdl(dual_kernel<4, 0, 4, 0, MX>, grid, threads, st, p);
+    case 5: return launch_pdl(dual_kernel<5, 0, 5, 0, MX>, grid, threads, st, p);
+    case 6: return launch_pdl(dual_kernel<6, 0, 6, 0, MX>, grid, threads, st, p);
+    case 7: return launch_pdl(dual_kernel<7, 0, 7, 0, MX>, grid, threads, st, p);
+    case 8: return launch_pdl(dual_kernel<8, 0, 8, 0, MX>, grid, threads, st, p);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_dual(bool mx, bool lat, int v0, int t0, int v1, int t1, const LaunchParams &p, int grid,

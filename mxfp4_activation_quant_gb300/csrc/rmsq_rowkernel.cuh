@@ -8,6 +8,15 @@
 //   dual_kernel<V0, T0, V1, T1, MX> two tensors (the MLA q_a / kv_a pair),
 //                                   blocks [0, seg[0].blocks) on the first
 // TPR / T0 / T1 = 0 means the team size is read at run time.
+//
+// Every one of them is launched as a programmatic dependent of the previous
+// kernel in its stream (launch_pdl): its blocks may be scheduled while that
+// kernel finishes, and griddepcontrol.wait holds them back, before their first
+// access to global memory, until it has completed and its writes are visible.
+// Only after that wait does a block let the grid's own dependents (a following
+// GEMM or norm) launch: a trigger before the wait lets a chain of calls pile up
+// waiting blocks on the SMs (64-token decode measured 2.49 -> 4.57 us per call
+// that way, against 2.31 us with the trigger after the wait).
 #pragma once
 
 #include <atomic>
@@ -50,14 +59,38 @@ __device__ __forceinline__ void block_rows(const Seg &s, int b, RedSmem &red)
     row_from_global<VPT, TPR, MX, (LAT > 0), SPLIT>(s, row, t, team, 0, red, part);
 }
 
+// Start of every row and pair kernel: wait for the kernel this one depends on
+// (a no-op when launched without the programmatic attribute), then allow the
+// next kernel in the stream to be scheduled; it waits in turn for this grid's
+// completion before it reads or overwrites what this grid touches.
+__device__ __forceinline__ void grid_dep_sync()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
+// Launch a row or pair kernel as a programmatic dependent of the previous
+// kernel in the stream (static shared memory only).
+template <typename Kernel>
+cudaError_t launch_pdl(Kernel k, int grid, int threads, cudaStream_t st, const LaunchParams &p)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, p);
+}
+
 template <int VPT, int TPR, bool MX, int LAT>
 __global__ void __launch_bounds__(kMaxThreads) rows_kernel(const __grid_constant__ LaunchParams p)
 {
     __shared__ RedSmem red;
-    // A kernel launched after this one as a programmatic dependent (the
-    // consumer GEMM) may be scheduled from now on; it waits for this grid's
-    // completion before it reads what this grid writes.
-    asm volatile("griddepcontrol.launch_dependents;");
+    grid_dep_sync();
     block_rows<VPT, TPR, MX, LAT>(p.seg[0], blockIdx.x, red);
 }
 
@@ -65,6 +98,7 @@ template <int V0, int T0, int V1, int T1, bool MX>
 __global__ void __launch_bounds__(kMaxThreads, 2) dual_kernel(const __grid_constant__ LaunchParams p)
 {
     __shared__ RedSmem red;
+    grid_dep_sync();
     if ((int)blockIdx.x < p.seg[0].blocks)
         block_rows<V0, T0, MX>(p.seg[0], blockIdx.x, red);
     else
@@ -78,6 +112,7 @@ template <int V0, int T0, int V1, int T1, bool MX>
 __global__ void __launch_bounds__(kMaxThreads, 1) dual_kernel_lat(const __grid_constant__ LaunchParams p)
 {
     __shared__ RedSmem red;
+    grid_dep_sync();
     if ((int)blockIdx.x < p.seg[0].blocks)
         block_rows<V0, T0, MX, 1>(p.seg[0], blockIdx.x, red);
     else
@@ -117,8 +152,7 @@ cudaError_t launch_latency(const LaunchParams &p, int grid, int threads, cudaStr
             return e;
         carved.fetch_or(1ull << dev, std::memory_order_acq_rel);
     }
-    rows_kernel<V, T, MX, LAT><<<grid, threads, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(rows_kernel<V, T, MX, LAT>, grid, threads, st, p);
 }
 
 // One compiled team shape in the throughput form (lat 0) or the latency form
@@ -127,10 +161,8 @@ cudaError_t launch_latency(const LaunchParams &p, int grid, int threads, cudaStr
 template <int V, int T, bool MX>
 cudaError_t launch_static(int lat, const LaunchParams &p, int grid, int threads, cudaStream_t st)
 {
-    if (lat == 0) {
-        rows_kernel<V, T, MX, 0><<<grid, threads, 0, st>>>(p);
-        return cudaGetLastError();
-    }
+    if (lat == 0)
+        return launch_pdl(rows_kernel<V, T, MX, 0>, grid, threads, st, p);
     if (lat == 1)
         return launch_latency<V, T, MX, 1>(p, grid, threads, st);
     if constexpr (V % 2 == 0) {
@@ -160,17 +192,16 @@ cudaError_t launch_rows_impl(int vpt, int tpr_static, int lat, const LaunchParam
         return cudaErrorInvalidValue;
     }
     switch (vpt) {
-    case 1: rows_kernel<1, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
-    case 2: rows_kernel<2, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
-    case 3: rows_kernel<3, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
-    case 4: rows_kernel<4, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
-    case 5: rows_kernel<5, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
-    case 6: rows_kernel<6, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
-    case 7: rows_kernel<7, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
-    case 8: rows_kernel<8, 0, MX, 0><<<grid, threads, 0, st>>>(p); break;
+    case 1: return launch_pdl(rows_kernel<1, 0, MX, 0>, grid, threads, st, p);
+    case 2: return launch_pdl(rows_kernel<2, 0, MX, 0>, grid, threads, st, p);
+    case 3: return launch_pdl(rows_kernel<3, 0, MX, 0>, grid, threads, st, p);
+    case 4: return launch_pdl(rows_kernel<4, 0, MX, 0>, grid, threads, st, p);
+    case 5: return launch_pdl(rows_kernel<5, 0, MX, 0>, grid, threads, st, p);
+    case 6: return launch_pdl(rows_kernel<6, 0, MX, 0>, grid, threads, st, p);
+    case 7: return launch_pdl(rows_kernel<7, 0, MX, 0>, grid, threads, st, p);
+    case 8: return launch_pdl(rows_kernel<8, 0, MX, 0>, grid, threads, st, p);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace rmsq

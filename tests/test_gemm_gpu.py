@@ -567,3 +567,60 @@ def test_gemm_after_the_quant_reads_its_output(M, pre):
             assert torch.equal(d, refs[i]), f"activation {i}, graph replay"
     torch.cuda.current_stream().wait_stream(side)
     assert rmsq.sync_status() == 0
+
+
+@pytest.mark.parametrize("M,pre", [(4, False), (64, False), (8192, False), (64, True)])
+def test_quant_gemm_chain_with_no_kernel_between(M, pre):
+    """Norm (+ quant) and GEMM alternate on one stream with nothing between
+    them: each norm is a programmatic dependent of the GEMM before it and
+    overwrites the activation that GEMM reads, each GEMM a dependent of the
+    norm before it. Five activations staged in their own buffers beforehand,
+    five outputs; back to back and replayed from a CUDA graph, each must
+    equal the same step run alone and synchronised."""
+    K, N = 7168, 2112
+    b_q, b_s = synth.mxfp4_weights(23, N, K)
+    gb, tb = b_q.to(DEV), rmsq.mx_scale_tiles(b_s.to(DEV))
+    ins = [_pipeline_inputs(M, K, 300 + i)[0] for i in range(5)]
+    gamma = ins[0]["gamma"]
+    q = torch.empty((M, K // 2), dtype=torch.uint8, device=DEV)
+    t = torch.zeros(rmsq.mma_scale_bytes(M, K), dtype=torch.uint8, device=DEV)
+    y = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    ro = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    ds = [torch.empty((M, N), dtype=torch.bfloat16, device=DEV) for _ in ins]
+
+    def step(i):
+        if pre:
+            rmsq.add_rmsnorm(ins[i]["x"], gamma, ins[i]["residual"], out=y, out_residual=ro)
+            rmsq.a16wfp4_gemm(y, gb, tb, out=ds[i])
+        else:
+            rmsq.add_rmsnorm_quant_mxfp4_mma_scales_into(ins[i]["x"], gamma, ins[i]["residual"], q, t, ro)
+            rmsq.mxfp4_gemm(q, t, gb, tb, out=ds[i])
+
+    refs = []
+    for i in range(len(ins)):
+        step(i)
+        torch.cuda.synchronize()
+        refs.append(ds[i].clone())
+    for d in ds:
+        d.zero_()
+    torch.cuda.synchronize()
+    for i in range(len(ins)):            # back to back
+        step(i)
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(zip(ds, refs)):
+        assert torch.equal(a, b), f"activation {i}, back to back"
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(len(ins)):
+                step(i)
+        for d in ds:
+            d.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+    for i, (a, b) in enumerate(zip(ds, refs)):
+        assert torch.equal(a, b), f"activation {i}, graph replay"
+    torch.cuda.current_stream().wait_stream(side)
+    assert rmsq.sync_status() == 0

@@ -660,6 +660,113 @@ def test_unknown_form_and_bad_split_are_refused():
 
 # ------------------------------------- calls that read the previous call's outputs
 
+@pytest.mark.parametrize("M,kind,in_place", [(4, "fp8", True), (64, "fp8", False), (64, "fp8", True),
+                                              (16384, "fp8", True), (64, "mx", False), (8192, "mx", True)])
+def test_dependent_launches_with_no_kernel_between(M, kind, in_place):
+    """Eight calls with nothing between them on the stream, each reading the
+    previous call's y as its x and its residual output as its residual (in
+    place, or alternating between two buffers), every output in a buffer of
+    its own: each call is launched as a programmatic dependent of the one
+    before and must still read what that one wrote. Back to back and from a
+    CUDA graph, against the same chain synchronised after every call."""
+    H, n = 7168, 8
+    x0 = synth.random_bf16(70 + M, (M, H)).to(DEV)
+    res0 = synth.random_bf16(71 + M, (M, H), var=4.0, tensor="residual").to(DEV)
+    gamma = synth.gaussian_bf16(72, "gamma", (H,), mean=1.0, var=0.1).to(DEV)
+    mx = kind == "mx"
+    ys = [torch.empty((M, H), dtype=torch.bfloat16, device=DEV) for _ in range(n)]
+    qs = [torch.empty((M, H // 2 if mx else H), dtype=torch.uint8, device=DEV) for _ in range(n)]
+    ss = [torch.empty((M, H // 32), dtype=torch.uint8, device=DEV) if mx else
+          torch.empty((M, H // 128), dtype=torch.float32, device=DEV) for _ in range(n)]
+    res = [res0.clone(), torch.empty_like(res0)]
+
+    def chain(sync):
+        res[0].copy_(res0)
+        torch.cuda.synchronize()
+        x = x0
+        for i in range(n):
+            r_in = res[0] if in_place else res[i % 2]
+            r_out = res[0] if in_place else res[(i + 1) % 2]
+            if mx:
+                rmsq.add_rmsnorm_quant_mxfp4_into(x, gamma, r_in, qs[i], ss[i], r_out, ys[i])
+            else:
+                rmsq.add_rmsnorm_quant_fp8_into(x, gamma, r_in, qs[i], ss[i], r_out, ys[i])
+            if sync:
+                torch.cuda.synchronize()
+            x = ys[i]
+
+    chain(True)
+    want = [t.clone() for t in ys + qs + ss + [res[0] if in_place else res[n % 2]]]
+    for t in ys + qs + ss:
+        t.zero_()
+    chain(False)
+    torch.cuda.synchronize()
+    got = ys + qs + ss + [res[0] if in_place else res[n % 2]]
+    for i, (a, b) in enumerate(zip(got, want)):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"tensor {i}, back to back"
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            x = x0
+            for i in range(n):
+                r_in = res[0] if in_place else res[i % 2]
+                r_out = res[0] if in_place else res[(i + 1) % 2]
+                if mx:
+                    rmsq.add_rmsnorm_quant_mxfp4_into(x, gamma, r_in, qs[i], ss[i], r_out, ys[i],
+                                                      stream=side.cuda_stream)
+                else:
+                    rmsq.add_rmsnorm_quant_fp8_into(x, gamma, r_in, qs[i], ss[i], r_out, ys[i],
+                                                    stream=side.cuda_stream)
+                x = ys[i]
+        res[0].copy_(res0)
+        for t in ys + qs + ss:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+    torch.cuda.current_stream().wait_stream(side)
+    for i, (a, b) in enumerate(zip(got, want)):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"tensor {i}, graph replay"
+    assert rmsq.sync_status() == 0
+
+
+@pytest.mark.parametrize("M", [4, 64, 8192])
+def test_pair_calls_with_no_kernel_between(M):
+    """The MLA pair called four times with nothing between them, each call
+    normalising the previous call's bf16 outputs: back to back must equal the
+    chain synchronised after every call."""
+    q_a = synth.random_bf16(81, (M, 1536), tensor="q_a").to(DEV)
+    kv_a = synth.random_bf16(82, (M, 512), tensor="kv_a").to(DEV)
+    gq = synth.gaussian_bf16(83, "gamma_q", (1536,), mean=1.0).to(DEV)
+    gk = synth.gaussian_bf16(84, "gamma_kv", (512,), mean=1.0).to(DEV)
+    n = 4
+    outs = [[torch.empty((M, 1536), dtype=torch.uint8, device=DEV), torch.empty((M, 12), dtype=torch.float32, device=DEV),
+             torch.empty((M, 512), dtype=torch.uint8, device=DEV), torch.empty((M, 4), dtype=torch.float32, device=DEV),
+             torch.empty((M, 1536), dtype=torch.bfloat16, device=DEV), torch.empty((M, 512), dtype=torch.bfloat16, device=DEV)]
+            for _ in range(n)]
+
+    def chain(sync):
+        a, b = q_a, kv_a
+        for o in outs:
+            rmsq.qknorm_quant_fp8_into(a, b, gq, gk, o[0], o[1], o[2], o[3], qy=o[4], ky=o[5])
+            if sync:
+                torch.cuda.synchronize()
+            a, b = o[4], o[5]
+        torch.cuda.synchronize()
+
+    chain(True)
+    want = [t.clone() for o in outs for t in o]
+    for o in outs:
+        for t in o:
+            t.zero_()
+    chain(False)
+    got = [t for o in outs for t in o]
+    for i, (u, v) in enumerate(zip(got, want)):
+        assert torch.equal(u.view(torch.uint8), v.view(torch.uint8)), f"tensor {i}"
+    assert rmsq.sync_status() == 0
+
+
 @pytest.mark.parametrize("M,kind", [(64, "fp8"), (8192, "fp8"), (37, "mx"), (3000, "mx")])
 def test_chained_calls_read_the_previous_outputs(M, kind):
     """A chain of six calls in which each reads what the previous one wrote
