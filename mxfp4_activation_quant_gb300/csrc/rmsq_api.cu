@@ -2,6 +2,7 @@
 // kernel and team shape, launch, and status reporting. Nothing here
 // allocates device memory; the only device state is the status word that
 // bounded waits report through.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -289,6 +290,19 @@ rmsq_status launch_single(Seg s, bool mx, const rmsq_launch_opts &o, cudaStream_
             return fail(RMSQ_ERR_INVALID_ARG, "split must be 0, 1, 2 or 4 (got %d)", o.split);
         const int64_t sms = sm_count();
         const bool lat = ts && (o.form == RMSQ_FORM_LATENCY || (o.form == RMSQ_FORM_AUTO && blocks <= sms));
+        if (lat && o.rows_per_block <= 0) {
+            // Latency form, rows per block chosen here: as few rows per block
+            // (whole warps) as keep the launch within one block per SM, so
+            // that the rows spread over as many SMs as there are.
+            const int64_t spread = std::max<int64_t>((s.M + sms - 1) / sms, (32 + tpr - 1) / tpr);
+            if (spread < rpb) {
+                rpb = (int)spread;
+                blocks = (s.M + rpb - 1) / rpb;
+                s.rpb = rpb;
+                s.blocks = (int32_t)blocks;
+                p.seg[0] = s;
+            }
+        }
         // Every block of a split row reads the whole residual row and writes
         // back its own part, so a residual updated in place is not split: a
         // part could be written before another block of the row has read it.
@@ -472,6 +486,21 @@ rmsq_status qknorm_common(bool mx, const void *q_a, int64_t ld_q, const void *kv
     int tk_threads = default_rows_per_block(tk) * tk;
     if (tk_threads > threads)
         threads = tk_threads;
+    // The latency form of the compiled pair shape when the launch can have at
+    // most one block per SM: the smallest block (32 .. 256 threads) for which
+    // it does, so that the rows spread over as many SMs as there are (64 tokens
+    // in 96 blocks of one q_a row and two kv_a rows: 2.69 -> 2.24 us per call).
+    bool lat = false;
+    if (t0s) {
+        for (int th = 32; th <= threads; th *= 2) {
+            const int64_t nq = (M + th / tq - 1) / (th / tq), nk = (M + th / tk - 1) / (th / tk);
+            if (nq + nk <= sm_count()) {
+                threads = th;
+                lat = true;
+                break;
+            }
+        }
+    }
     sq.tpr = tq;
     sk.tpr = tk;
     sq.rpb = threads / tq;
@@ -487,8 +516,6 @@ rmsq_status qknorm_common(bool mx, const void *q_a, int64_t ld_q, const void *kv
     p.seg[0] = sq;
     p.seg[1] = sk;
     p.nseg = 2;
-    // at most one block per SM: the compiled pair shape's latency form
-    const bool lat = t0s && bq + bk <= sm_count();
     cudaError_t e = launch_dual(mx, lat, v0, t0s, v1, t1s, p, (int)(bq + bk), threads, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return fail(RMSQ_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));

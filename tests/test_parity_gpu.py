@@ -595,6 +595,31 @@ def test_latency_form_is_bit_identical(oracle_mod, name, M, split):
         assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), k
 
 
+
+@pytest.mark.parametrize("H", [256, 512, 1536, 2048, 4096, 5120, 8192])
+@pytest.mark.parametrize("M", [1, 4, 37, 64, 150, 300])
+def test_latency_form_across_compiled_shapes(oracle_mod, H, M):
+    """At every compiled team shape the automatic choice at decode sizes --
+    the latency form, its rows spread over as many blocks as keep one block
+    per SM, rows split between blocks where SMs remain -- gives outputs
+    bit-identical to the throughput form, FP8 and MXFP4, and meets the bar
+    against the oracle."""
+    d = {"x": synth.random_bf16(110 + H, (M, H)),
+         "residual": synth.random_bf16(120 + H, (M, H), var=4.0, tensor="residual"),
+         "gamma": synth.gaussian_bf16(130 + H, "gamma", (H,), mean=1.0, var=0.1)}
+    thr = rmsq.LaunchOpts(kernel=rmsq.KERNEL_ROWS, form=rmsq.FORM_THROUGHPUT)
+    a = run_fp8(d, 1e-6, keep=True)
+    b = run_fp8(d, 1e-6, keep=True, opts=thr)
+    parity.compare_fp8(a, ref_fp8(oracle_mod, d, 1e-6), what=f"latency form H={H} M={M}")
+    for k in ("q", "scale", "residual_out", "y"):
+        assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), k
+    a = run_mx(d, 1e-6, keep=True)
+    b = run_mx(d, 1e-6, keep=True, opts=thr)
+    parity.compare_mx(a, oracle_mod.add_rmsnorm_quant_mxfp4(d["x"], d["residual"], d["gamma"], 1e-6),
+                      what=f"mx latency form H={H} M={M}")
+    for k in ("q", "scale", "residual_out", "y"):
+        assert torch.equal(a[k].view(torch.uint8), b[k].view(torch.uint8)), k
+
 @pytest.mark.parametrize("kind,M", [("fp8", 64), ("fp8", 37), ("fp8", 8), ("mx", 4), ("mx", 64)])
 def test_in_place_residual_is_not_split(kind, M):
     """Split rows read the whole residual row in every block of the row and
@@ -623,12 +648,14 @@ def test_in_place_residual_is_not_split(kind, M):
 
 
 @pytest.mark.parametrize("mx", [False, True])
-@pytest.mark.parametrize("M", [1, 5, 64, 76, 1300])
+@pytest.mark.parametrize("M", [1, 5, 64, 76, 101, 102, 128, 300, 700, 808, 809, 1300])
 def test_qknorm_pair_latency_form(oracle_mod, M, mx):
     """The MLA pair (q_a 1536, kv_a 512) at decode sizes takes the pair's
-    latency form (gamma loaded with each row; at most one block per SM, so
-    up to 1216 tokens); 1300 tokens take the throughput form. Both against
-    the oracle, every row."""
+    latency form (gamma loaded with each row) in the smallest block that keeps
+    the launch within one block per SM: 32 threads (one q_a row, two kv_a
+    rows) up to 101 tokens, then 64, 128 and 256 threads up to 808 tokens;
+    809 and 1300 tokens take the throughput form. Each against the oracle,
+    every row."""
     Hq, Hkv = 1536, 512
     q_a = synth.random_bf16(500 + M, (M, Hq), tensor="q_a")
     kv_a = synth.random_bf16(501 + M, (M, Hkv), var=2.0, tensor="kv_a")
