@@ -41,6 +41,15 @@
  *  - The work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream) and the call returns without waiting. A launch failure
  *    returns RMSQ_ERR_CUDA; rmsq_last_error() then holds the CUDA message.
+ *  - Stream order is kept. The norm + quant kernels are launched as
+ *    programmatic dependents of the kernel before them on the stream: their
+ *    blocks may be scheduled while it finishes, but every block waits
+ *    (griddepcontrol.wait) for it to complete, and its writes to be visible,
+ *    before reading or writing any global memory. Only then does the kernel
+ *    allow the next kernel on the stream to be scheduled early, if that one
+ *    is itself launched as a programmatic dependent (the GEMMs below are);
+ *    such a kernel must wait in the same way before it reads these outputs.
+ *    Kernels launched without the attribute are unaffected.
  */
 #ifndef RMSQ_H
 #define RMSQ_H
@@ -303,7 +312,9 @@ typedef enum rmsq_form {
  *                   multiple of the group's vector count up to 32 or a
  *                   multiple of 32, at most 512; vectors past the row end
  *                   are idle (whole groups).
- *   rows_per_block  0 = auto
+ *   rows_per_block  0 = auto: 256 threads' worth of teams, or in the latency
+ *                   form as few rows per block (whole warps) as keep the
+ *                   launch within one block per SM
  *   grid            persistent kernel: number of blocks, 0 = auto
  *   debug_skip_row  persistent kernel: the copy of this row is never issued,
  *                   so its wait runs out (test of the bounded wait); -1 = off
